@@ -1,0 +1,296 @@
+"""Benchmark of the routed MoE layer on GB300 (one JSON line on stdout).
+
+Default workload: BF16 forward, T=2560 tokens, H=7168, I=2048, E=32 experts,
+top-k=8 (Kimi-2.5-shaped experts), uniform routing. One step = one whole
+layer: route + top-k + layout, pull-dispatch, grouped gate/up GEMM with fused
+SwiGLU, grouped down GEMM with push-combine, fixed-order weighted sum.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl mok|reference]
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; L2 is flushed (a 256 MiB write) before every timed
+step. Multi-GPU (torchrun, N > 1): every rank runs an independent replica of
+the layer (the layer does not shard on one node without expert parallelism);
+rank 0 reports the aggregate over ranks with the max time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_router_top_expert_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (fwd, fwd+bwd) at H7168/I2048; grouped-GEMM % TC peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d.get("hbm_gbs", 6800.0), bf16=d.get("bf16_tflops", 1900.0),
+                    bf16_sus=d.get("bf16_tflops_sustained", 1700.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mok_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_baseline(inp, wl, n_tokens=48):
+    """The oracle as it stands on a bounded sample of the workload's tokens."""
+    import oracle
+    dt = oracle.MODE_MXFP8 if wl.dtype == "mxfp8" else oracle.MODE_BF16
+    t0 = time.perf_counter()
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    toks = np.arange(min(n_tokens, wl.T), dtype=np.int32)
+    oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=dt, tokens=toks, shared=inp.shared)
+    dt_s = time.perf_counter() - t0
+    return {"value": len(toks) / dt_s, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"routing of all {wl.T} tokens + layer output of the first {len(toks)} tokens "
+                      f"({len(toks) * wl.k} routed rows), fp64, {dt_s:.1f} s"}
+
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = synth.make_inputs(wl)
+    import oracle
+    oracle.build()
+    n_tok = 16
+    for _ in range(args.warmup):
+        pass  # the oracle has nothing to warm
+    times = []
+    for _ in range(args.steps):
+        cb = cpu_baseline(inp, wl, n_tokens=n_tok)
+        times.append(n_tok / cb["value"])
+    v = n_tok * len(times) / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                                            "k": wl.k, "operands": wl.dtype},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "value": v, "unit": "tokens/s",
+                             "sample": f"per step: routing of all tokens + output of {n_tok} tokens"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from combine_router_top_expert_gb300 import mok
+    from combine_router_top_expert_gb300.layer import MoELayer, to_dev_bf16
+
+    dtype = mok.MXFP8 if wl.dtype == "mxfp8" else mok.BF16
+    inp = synth.make_inputs(wl)
+    layer = MoELayer(inp.W_r, inp.Wg, inp.Wu, inp.Wd, wl.k, dtype=dtype, bias=inp.bias, shared=inp.shared,
+                     device=dev, keep_unpacked=wl.backward)
+    T, H = wl.T, wl.H
+    x = to_dev_bf16(inp.x, dev)
+    p = layer.problem(T)
+    b = layer.buffers(T)
+    rt = b["routing"]
+    rows = mok.padded_rows_max(T, wl.E, wl.k)
+    eb = 1 if dtype == mok.MXFP8 else 2
+    A = mok.alloc_bytes(rows * H * eb, dev)
+    A_sf = mok.alloc_bytes(rows * H // 32, dev) if dtype == mok.MXFP8 else None
+    h = mok.alloc_bytes(rows * wl.I * eb, dev)
+    h_sf = mok.alloc_bytes(rows * wl.I // 32, dev) if dtype == mok.MXFP8 else None
+    part = torch.empty((T * wl.k, H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    status_ws = b["ws"]
+
+    def step(ev=None):
+        # one layer: route/layout, dispatch, grouped GEMMs, combine (7 launches)
+        layer.route(x, stream=stream)
+        mok.dispatch(p, x, rt, A, A_sf, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, status_ws, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mok.combine(p, part, rt["topk_w"], out, stream=stream)
+
+    launches_per_step = 7
+    if wl.shared_I:
+        raise SystemExit("the stage-split bench step covers routed experts only; use the layer test for shared")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = mok.device_status(status_ws)
+    if st[0] != mok.OK:
+        raise SystemExit(f"device status after warm-up: {st}")
+
+    clocks = ClockSampler(local)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        s0, s1, g0, g1 = evs[i]
+        s0.record(stream)
+        step((g0, g1))
+        s1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    gemm_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_ms = sum(step_ms)
+    st = mok.device_status(status_ws)
+    if st[0] != mok.OK:
+        raise SystemExit(f"device status after timed steps: {st}")
+
+    # end to end through the public API with host buffers: pinned x in,
+    # route + forward (mok_moe_forward), out back to pinned host memory
+    x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    x_dev2 = torch.empty_like(x)
+    for _ in range(2):
+        x_dev2.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev2, stream=stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for i in range(max(3, args.steps // 2)):
+        flush.zero_()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        x_dev2.copy_(x_host, non_blocking=True)
+        y = layer.forward(x_dev2, stream=stream)
+        out_host.copy_(y, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(a0.elapsed_time(a1))
+
+    # aggregate over ranks: total tokens / max time
+    t_max = total_ms
+    e2e_max = sum(e2e_ms)
+    if ws > 1:
+        tt = torch.tensor([total_ms, e2e_max], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max, e2e_max = tt.tolist()
+    if rank != 0:
+        return
+    value = ws * T * args.steps / (t_max / 1000.0)
+    e2e_val = ws * T * len(e2e_ms) / (e2e_max / 1000.0)
+    peaks = load_peaks()
+    fl = 6.0 * H * wl.I * T * wl.k
+    g_ms = statistics.mean(gemm_ms)
+    achieved = fl / (g_ms / 1000.0) / 1e12
+    peak = peaks["bf16"] * (2.0 if dtype == mok.MXFP8 else 1.0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == mok.BF16 else "mxfp8",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "operands": wl.dtype, "routing": "zipf s=1.2 bias" if wl.zipf_s else "uniform",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "flushed before every timed step (256 MiB write); per-step CUDA events",
+                   "step": "route+topk+layout, dispatch, grouped gate/up+SwiGLU, grouped down+push, combine"},
+        "roofline": {"kernel": "grouped expert GEMMs (gate/up+SwiGLU, down+push; 2 launches)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
+                     "flops_per_launch_pair": fl, "ms_per_launch_pair": g_ms, "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "api": "mok_route_layout + mok_moe_forward"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "stage_ms": {"step_median": statistics.median(step_ms), "grouped_gemm_median": statistics.median(gemm_ms)},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, wl)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,382 @@
+// api.cu - the C ABI declared in include/mok.h.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "moves.cuh"
+
+using namespace mok;
+
+namespace {
+
+constexpr int kDefaultTimeoutMs = 4000;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Gate/up columns interleaved per this many columns in the packed weights
+// (half the N-tile of the gate/up GEMM).
+int gu_interleave(int I, int dtype) {
+    if (dtype == MOK_MXFP8) return 64;
+    return 2 * I >= 256 ? 128 : 64;
+}
+
+bool dims_ok(int E, int H, int I, int dtype) {
+    if (E < 1 || E > kMaxE || H <= 0 || I <= 0) return false;
+    if (H % 128 || H > 65536) return false;
+    if (dtype == MOK_BF16) return I == 64 || I % 128 == 0;
+    if (dtype == MOK_MXFP8) return I % 128 == 0;
+    return false;
+}
+
+bool problem_ok(const mok_problem* p) {
+    if (!p) return false;
+    if (p->T < 0 || p->k < 1 || p->k > p->E) return false;
+    if (!dims_ok(p->E, p->H, p->I, p->dtype)) return false;
+    if (p->I_shared < 0 || (p->I_shared > 0 && !(p->I_shared == 64 || p->I_shared % 128 == 0))) return false;
+    if ((int64_t)p->T * p->k >= (int64_t)1 << 30) return false;
+    return true;
+}
+
+struct PackedLayout {
+    size_t gu, gu_sf, dn, dn_sf, total;
+};
+
+PackedLayout packed_layout(int E, int H, int I, int dtype) {
+    PackedLayout L{};
+    const int64_t eb = dtype == MOK_MXFP8 ? 1 : 2;
+    size_t o = 0;
+    L.gu = o; o += align_up((int64_t)E * 2 * I * H * eb, 1024);
+    L.gu_sf = o; if (dtype == MOK_MXFP8) o += align_up((int64_t)E * 2 * I * H / 32, 1024);
+    L.dn = o; o += align_up((int64_t)E * H * I * eb, 1024);
+    L.dn_sf = o; if (dtype == MOK_MXFP8) o += align_up((int64_t)E * H * I / 32, 1024);
+    L.total = o;
+    return L;
+}
+
+// Forward buffers. When `saved` is given (BF16 training), A, GU, h and the
+// partials live there so the backward can read them.
+struct FwdLayout {
+    size_t A, A_sf, h, h_sf, partials, shared, hs, total;   // workspace offsets
+    size_t sA, sGU, sh, spart, saved_total;                  // saved offsets
+};
+
+FwdLayout fwd_layout(const mok_problem* p, bool training) {
+    FwdLayout L{};
+    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
+    const int64_t eb = p->dtype == MOK_MXFP8 ? 1 : 2;
+    size_t o = kStatusBytes;
+    if (!training) { L.A = o; o += align_up(rows * p->H * eb, 1024); }
+    L.A_sf = o; if (p->dtype == MOK_MXFP8) o += align_up(rows * p->H / 32, 1024);
+    if (!training) { L.h = o; o += align_up(rows * p->I * eb, 1024); }
+    L.h_sf = o; if (p->dtype == MOK_MXFP8) o += align_up(rows * p->I / 32, 1024);
+    if (!training) { L.partials = o; o += align_up((int64_t)p->T * p->k * p->H * 2, 1024); }
+    if (p->I_shared > 0) {
+        L.shared = o; o += align_up((int64_t)p->T * p->H * 4, 1024);
+        L.hs = o; o += align_up((int64_t)p->T * p->I_shared * 2, 1024);
+    }
+    L.total = o;
+    size_t q = 0;
+    L.sA = q; q += align_up(rows * p->H * 2, 1024);
+    L.sGU = q; q += align_up(rows * 2 * p->I * 2, 1024);
+    L.sh = q; q += align_up(rows * p->I * 2, 1024);
+    L.spart = q; q += align_up((int64_t)p->T * p->k * p->H * 2, 1024);
+    L.saved_total = q;
+    return L;
+}
+
+struct BwdLayout {
+    size_t dy, dgu, da, gw, dl, dl_full, part, wrt, total;
+};
+
+BwdLayout bwd_layout(const mok_problem* p) {
+    BwdLayout L{};
+    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
+    size_t o = kStatusBytes;
+    L.dy = o; o += align_up(rows * p->H * 2, 1024);
+    L.dgu = o; o += align_up(rows * 2 * p->I * 2, 1024);
+    L.da = o; o += align_up((int64_t)p->T * p->k * p->H * 2, 1024);
+    L.gw = o; o += align_up((int64_t)p->T * p->k * 4, 1024);
+    L.dl = o; o += align_up((int64_t)p->T * p->k * 4, 1024);
+    L.dl_full = o; o += align_up((int64_t)p->T * p->E * 4, 1024);
+    L.part = o; o += align_up(dwr_partial_floats(p->H, p->E) * 4, 1024);
+    L.wrt = o; o += align_up((int64_t)p->E * p->H * 4, 1024);
+    L.total = o;
+    return L;
+}
+
+mok_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
+
+GemmCommon make_common(void* ws, const mok_config* cfg) {
+    GemmCommon c{};
+    c.status = static_cast<StatusBlock*>(ws);
+    int ms = (cfg && cfg->timeout_ms > 0) ? cfg->timeout_ms : kDefaultTimeoutMs;
+    c.timeout_ns = (unsigned long long)ms * 1000000ull;
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (cfg && cfg->num_sms > 0) n = std::min(n, (int)cfg->num_sms);
+    c.num_sms = n > 0 ? n : 1;
+    return c;
+}
+
+bool routing_ok(const mok_routing* r) {
+    return r && r->topk_idx && r->topk_w && r->counts && r->offsets && r->row_src && r->slot_row;
+}
+
+// Requires an sm_103-class device for the tensor-core kernels.
+bool device_ok() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return major == 10 && minor == 3;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mok_version(void) { return "mok-gb300 0.1 (sm_103a)"; }
+
+const char* mok_status_string(mok_status s) {
+    switch (s) {
+        case MOK_OK: return "ok";
+        case MOK_ERR_INVALID: return "invalid argument";
+        case MOK_ERR_CUDA: return "CUDA error";
+        case MOK_ERR_TIMEOUT: return "device wait timed out";
+        case MOK_ERR_CAPACITY: return "ring buffer smaller than one minibatch";
+        case MOK_ERR_UNSUPPORTED: return "unsupported";
+    }
+    return "unknown status";
+}
+
+size_t mok_route_workspace_size(int32_t T, int32_t H, int32_t E, int32_t k) {
+    if (T < 0 || H <= 0 || E < 1 || E > kMaxE || k < 1 || k > E) return 0;
+    return route_workspace_bytes(T, H, E, k);
+}
+
+mok_status mok_route_layout(const void* x, const float* W_r, const float* bias, int32_t T, int32_t H, int32_t E,
+                            int32_t k, int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                            int32_t* row_src, int32_t* slot_row, void* workspace, size_t ws_bytes,
+                            mok_stream_t stream) {
+    if (T < 0 || H <= 0 || H % 8 || E < 1 || E > kMaxE || k < 1 || k > E) return MOK_ERR_INVALID;
+    if ((int64_t)T * k >= (int64_t)1 << 30) return MOK_ERR_INVALID;
+    if (!counts || !offsets || !workspace || !W_r) return MOK_ERR_INVALID;
+    if (T > 0 && (!x || !topk_idx || !topk_w || !row_src || !slot_row)) return MOK_ERR_INVALID;
+    if (ws_bytes < route_workspace_bytes(T, H, E, k) || !aligned(workspace, 256) || !aligned(x, 16))
+        return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(launch_route_layout(x, W_r, bias, T, H, E, k, topk_idx, topk_w, counts, offsets, row_src,
+                                           slot_row, workspace, (cudaStream_t)stream));
+}
+
+size_t mok_packed_weights_size(int32_t E, int32_t H, int32_t I, int32_t dtype) {
+    if (!dims_ok(E, H, I, dtype)) return 0;
+    return packed_layout(E, H, I, dtype).total;
+}
+
+mok_status mok_pack_weights(int32_t E, int32_t H, int32_t I, int32_t dtype, const void* W_gate, const void* W_up,
+                            const void* W_down, void* packed, size_t packed_bytes, mok_stream_t stream) {
+    if (!dims_ok(E, H, I, dtype) || !W_gate || !W_up || !W_down || !packed) return MOK_ERR_INVALID;
+    PackedLayout L = packed_layout(E, H, I, dtype);
+    if (packed_bytes < L.total || !aligned(packed, 256)) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* b = static_cast<char*>(packed);
+    const bool mx = dtype == MOK_MXFP8;
+    cudaError_t e = launch_pack(mx, W_gate, W_up, E, H, I, gu_interleave(I, dtype), b + L.gu,
+                                mx ? reinterpret_cast<uint8_t*>(b + L.gu_sf) : nullptr, s);
+    if (e == cudaSuccess)
+        e = launch_pack(mx, W_down, nullptr, E, I, H, 0, b + L.dn, mx ? reinterpret_cast<uint8_t*>(b + L.dn_sf) : nullptr,
+                        s);
+    return cuda_status(e);
+}
+
+int64_t mok_padded_rows_max(int32_t T, int32_t E, int32_t k) { return padded_rows_max(T, E, k); }
+
+size_t mok_saved_size(const mok_problem* p) {
+    if (!problem_ok(p)) return 0;
+    return fwd_layout(p, true).saved_total;
+}
+
+size_t mok_workspace_size(const mok_problem* p, const mok_config* cfg) {
+    (void)cfg;
+    if (!problem_ok(p)) return 0;
+    size_t f = fwd_layout(p, false).total;
+    size_t b = p->dtype == MOK_BF16 ? bwd_layout(p).total : 0;
+    return std::max(f, b);
+}
+
+mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
+                        mok_stream_t stream) {
+    if (!problem_ok(p) || !routing_ok(r) || !A || (p->T > 0 && !x)) return MOK_ERR_INVALID;
+    if (p->dtype == MOK_MXFP8 && !A_sf) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(launch_dispatch(p->dtype == MOK_MXFP8, x, p->T, p->H, p->E, p->k, r->counts, r->offsets,
+                                       r->row_src, A, static_cast<uint8_t*>(A_sf), nullptr, nullptr,
+                                       (cudaStream_t)stream));
+}
+
+mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf, const void* packed,
+                          const mok_routing* r, void* h, void* h_sf, void* partials, const mok_config* cfg,
+                          void* workspace, mok_stream_t stream) {
+    if (!problem_ok(p) || !routing_ok(r) || !A || !packed || !h || !partials || !workspace) return MOK_ERR_INVALID;
+    const bool mx = p->dtype == MOK_MXFP8;
+    if (mx && (!A_sf || !h_sf)) return MOK_ERR_INVALID;
+    if (!aligned(A, 1024) || !aligned(h, 1024) || !aligned(packed, 256) || !aligned(workspace, 256))
+        return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaMemsetAsync(workspace, 0, kStatusBytes, s);
+    if (p->T == 0) return MOK_OK;
+    GemmCommon c = make_common(workspace, cfg);
+    PackedLayout L = packed_layout(p->E, p->H, p->I, p->dtype);
+    const char* pk = static_cast<const char*>(packed);
+    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
+    cudaError_t e = gemm_gateup(mx, A, static_cast<const uint8_t*>(A_sf), pk + L.gu,
+                                reinterpret_cast<const uint8_t*>(pk + L.gu_sf), p->E, p->H, p->I, r->counts, 0, rows,
+                                h, static_cast<uint8_t*>(h_sf), nullptr, c, s);
+    if (e == cudaSuccess)
+        e = gemm_down(mx, h, static_cast<const uint8_t*>(h_sf), pk + L.dn, reinterpret_cast<const uint8_t*>(pk + L.dn_sf),
+                      p->E, p->H, p->I, r->counts, r->offsets, r->row_src, 0, rows, partials, c, s);
+    return cuda_status(e);
+}
+
+mok_status mok_combine(const mok_problem* p, const void* partials, const float* topk_w, const float* shared,
+                       void* out, mok_stream_t stream) {
+    if (!problem_ok(p) || (p->T > 0 && (!partials || !topk_w || !out))) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(launch_combine(partials, topk_w, shared, out, p->T, p->H, p->k, (cudaStream_t)stream));
+}
+
+mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mok_config* cfg,
+                           mok_stream_t stream) {
+    if (!problem_ok(p) || !a || !routing_ok(&a->routing) || !a->packed || !a->out || !a->workspace)
+        return MOK_ERR_INVALID;
+    if (p->T > 0 && !a->x) return MOK_ERR_INVALID;
+    if ((p->I_shared > 0) != (a->packed_shared != nullptr)) return MOK_ERR_INVALID;
+    const bool training = a->saved != nullptr;
+    const bool mx = p->dtype == MOK_MXFP8;
+    if (training && mx) return MOK_ERR_UNSUPPORTED;
+    if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->packed, 256) ||
+        !aligned(a->x, 16) || !aligned(a->out, 16) || (training && !aligned(a->saved, 1024)))
+        return MOK_ERR_INVALID;
+    if (p->I_shared > 0 && !aligned(a->packed_shared, 256)) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = static_cast<char*>(a->workspace);
+    char* sv = static_cast<char*>(a->saved);
+    FwdLayout L = fwd_layout(p, training);
+    void* A = training ? sv + L.sA : ws + L.A;
+    void* h = training ? sv + L.sh : ws + L.h;
+    void* partials = training ? sv + L.spart : ws + L.partials;
+    void* gu = training ? sv + L.sGU : nullptr;
+    uint8_t* A_sf = mx ? reinterpret_cast<uint8_t*>(ws + L.A_sf) : nullptr;
+    uint8_t* h_sf = mx ? reinterpret_cast<uint8_t*>(ws + L.h_sf) : nullptr;
+    const mok_routing& r = a->routing;
+
+    cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+    if (p->T == 0) return cuda_status(e);
+    GemmCommon c = make_common(ws, cfg);
+    PackedLayout PL = packed_layout(p->E, p->H, p->I, p->dtype);
+    const char* pk = static_cast<const char*>(a->packed);
+    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
+    if (e == cudaSuccess)
+        e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
+                            nullptr, s);
+    if (e == cudaSuccess)
+        e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H, p->I,
+                        r.counts, 0, rows, h, h_sf, gu, c, s);
+    if (e == cudaSuccess)
+        e = gemm_down(mx, h, h_sf, pk + PL.dn, reinterpret_cast<const uint8_t*>(pk + PL.dn_sf), p->E, p->H, p->I,
+                      r.counts, r.offsets, r.row_src, 0, rows, partials, c, s);
+    float* shared = nullptr;
+    if (e == cudaSuccess && p->I_shared > 0) {
+        PackedLayout SL = packed_layout(1, p->H, p->I_shared, MOK_BF16);
+        const char* sp = static_cast<const char*>(a->packed_shared);
+        shared = reinterpret_cast<float*>(ws + L.shared);
+        void* hs = ws + L.hs;
+        e = gemm_gateup(false, a->x, nullptr, sp + SL.gu, nullptr, 1, p->H, p->I_shared, nullptr, p->T, p->T, hs,
+                        nullptr, nullptr, c, s);
+        if (e == cudaSuccess)
+            e = gemm_down(false, hs, nullptr, sp + SL.dn, nullptr, 1, p->H, p->I_shared, nullptr, nullptr, nullptr,
+                          p->T, p->T, shared, c, s);
+    }
+    if (e == cudaSuccess) e = launch_combine(partials, r.topk_w, shared, a->out, p->T, p->H, p->k, s);
+    return cuda_status(e);
+}
+
+mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const mok_config* cfg,
+                            mok_stream_t stream) {
+    if (!problem_ok(p) || !a || !routing_ok(&a->routing)) return MOK_ERR_INVALID;
+    if (p->dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
+    if (p->I_shared > 0) return MOK_ERR_UNSUPPORTED;
+    if (!a->x || !a->W_r || !a->W_gate || !a->W_up || !a->W_down || !a->dY || !a->saved || !a->dX ||
+        !a->dW_gate || !a->dW_up || !a->dW_down || !a->dW_r || !a->workspace)
+        return MOK_ERR_INVALID;
+    if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->saved, 1024))
+        return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = static_cast<char*>(a->workspace);
+    const char* sv = static_cast<const char*>(a->saved);
+    FwdLayout FL = fwd_layout(p, true);
+    BwdLayout L = bwd_layout(p);
+    const mok_routing& r = a->routing;
+    const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k;
+    const int64_t rows = padded_rows_max(T, E, k);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+    if (T == 0) {
+        // no tokens: every gradient is zero
+        if (e == cudaSuccess) e = cudaMemsetAsync(a->dW_gate, 0, (size_t)E * H * I * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a->dW_up, 0, (size_t)E * H * I * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a->dW_down, 0, (size_t)E * H * I * 2, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a->dW_r, 0, (size_t)E * H * 4, s);
+        return cuda_status(e);
+    }
+    GemmCommon c = make_common(ws, cfg);
+    void* dy = ws + L.dy;
+    void* dgu = ws + L.dgu;
+    void* da = ws + L.da;
+    float* gw = reinterpret_cast<float*>(ws + L.gw);
+    float* dl = reinterpret_cast<float*>(ws + L.dl);
+    float* dl_full = reinterpret_cast<float*>(ws + L.dl_full);
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    float* WrT = reinterpret_cast<float*>(ws + L.wrt);
+    // reverse-combine (pull): dy rows in expert order, gate gradients
+    if (e == cudaSuccess) e = launch_transpose_wr(a->W_r, WrT, H, E, s);
+    if (e == cudaSuccess)
+        e = launch_dispatch(false, a->dY, T, H, E, k, r.counts, r.offsets, r.row_src, dy, nullptr, a->dY, r.topk_w, s);
+    if (e == cudaSuccess)
+        e = launch_bwd_small(a->dY, sv + FL.spart, r.topk_w, r.topk_idx, a->x, WrT, da, T, H, E, k, gw, dl, dl_full,
+                             part, a->dX, a->dW_r, 0, s);
+    // expert dgrad
+    if (e == cudaSuccess) e = gemm_dgrad_h(dy, a->W_down, E, H, I, r.counts, rows, sv + FL.sGU, dgu, c, s);
+    if (e == cudaSuccess)
+        e = gemm_dgrad_a(dgu, a->W_gate, a->W_up, E, H, I, r.counts, r.offsets, r.row_src, rows, da, c, s);
+    // expert wgrad (each expert's rows, in row order)
+    if (e == cudaSuccess) e = gemm_wgrad(sv + FL.sA, H, dgu, 2 * I, E, r.counts, rows, a->dW_gate, a->dW_up, I, c, s);
+    if (e == cudaSuccess) e = gemm_wgrad(sv + FL.sh, I, dy, H, E, r.counts, rows, a->dW_down, nullptr, H, c, s);
+    // reverse-dispatch (push) + reduce, router gradient
+    if (e == cudaSuccess)
+        e = launch_bwd_small(a->dY, sv + FL.spart, r.topk_w, r.topk_idx, a->x, WrT, da, T, H, E, k, gw, dl, dl_full,
+                             part, a->dX, a->dW_r, 1, s);
+    return cuda_status(e);
+}
+
+mok_status mok_device_status(const void* workspace, mok_stream_t stream, int32_t* detail, int32_t reset) {
+    if (!workspace) return MOK_ERR_INVALID;
+    StatusBlock hb{};
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&hb, workspace, sizeof(hb), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOK_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOK_ERR_CUDA;
+    if (reset) {
+        if (cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(hb), s) != cudaSuccess) return MOK_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOK_ERR_CUDA;
+    }
+    if (detail) *detail = hb.detail;
+    return (mok_status)hb.code;
+}
+
+}  // extern "C"

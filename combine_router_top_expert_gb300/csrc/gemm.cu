@@ -1,0 +1,214 @@
+// gemm.cu - host launchers of the grouped tcgen05 GEMM: tensor maps, tile
+// shapes per call site, persistent grid sizing.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "gemm.cuh"
+#include "moves.cuh"
+
+namespace mok {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major [rows, cols] tensor; box = box_cols x box_rows with a
+// 128-byte swizzle (box_cols * elem_bytes == 128). Out-of-range rows read 0.
+bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
+               int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * elem_bytes)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+void ensure_smem_attr(const void* func, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void*>> done;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> g(mu);
+    auto key = std::make_pair(dev, func);
+    if (done.count(key)) return;
+    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    done.insert(key);
+}
+
+template <int BN, bool MX, bool MN, int EPI, int S, int ACC>
+cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
+                int64_t tiles_ub, int num_sms, cudaStream_t s) {
+    using C = GemmCfg<BN, MX, MN, EPI, S, ACC>;
+    auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC>;
+    ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
+    int grid = (int)std::min<int64_t>(tiles_ub, num_sms);
+    if (grid < 1) return cudaSuccess;
+    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(a, b, b2, p);
+    return cudaGetLastError();
+}
+
+GemmParams base_params(const GemmCommon& c) {
+    GemmParams p{};
+    p.b_split_kb = 1 << 30;
+    p.status = c.status;
+    p.timeout_ns = c.timeout_ns;
+    return p;
+}
+
+// Upper bound on 128-row tiles of a grouped layout with `rows` routed rows.
+int64_t mtiles_ub(int64_t rows, int E) { return (rows + kTileM - 1) / kTileM + E; }
+
+}  // namespace
+
+cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
+                        int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows, void* h,
+                        uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s) {
+    const int BN = (2 * I) >= 256 ? 256 : 128;
+    const int eb = mx ? 1 : 2;
+    const int bk = 128 / eb;
+    GemmParams p = base_params(c);
+    p.E = identity_rows > 0 ? 1 : E;
+    p.counts = counts;
+    p.identity_rows = identity_rows;
+    p.num_kb = H / bk;
+    p.b_rows_per_expert = 2 * I;
+    p.out0 = h;
+    p.out_sf = h_sf;
+    p.gu = gu_save;
+    p.split_col = I;
+    p.a_sf = A_sf;
+    p.b_sf = Bgu_sf;
+    p.sf_kchunks = H / 128;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, a_rows, H, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, mx ? 128 : BN)) return cudaErrorInvalidValue;
+    const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
+    if (mx) {
+        // MXFP8: 128-wide tiles (gate 64 | up 64), double-buffered accumulator
+        p.n_tiles = 2 * I / 128;
+        return run<128, true, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    }
+    p.n_tiles = 2 * I / BN;
+    if (BN == 256) return run<256, false, false, kEpiSwiGLU, 4, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    return run<128, false, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+}
+
+cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* Bdn, const uint8_t* Bdn_sf, int E,
+                      int H, int I, const int32_t* counts, const int32_t* offsets, const int32_t* row_src,
+                      int identity_rows, int64_t a_rows, void* out, const GemmCommon& c, cudaStream_t s) {
+    const int eb = mx ? 1 : 2;
+    const int bk = 128 / eb;
+    GemmParams p = base_params(c);
+    p.E = identity_rows > 0 ? 1 : E;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.row_src = row_src;
+    p.identity_rows = identity_rows;
+    p.num_kb = I / bk;
+    p.b_rows_per_expert = H;
+    p.out0 = out;
+    p.ldo = H;
+    p.out_f32 = identity_rows > 0 ? 1 : 0;
+    p.a_sf = h_sf;
+    p.b_sf = Bdn_sf;
+    p.sf_kchunks = I / 128;
+    const int BN = (H % 256 == 0 && !mx) ? 256 : 128;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, h, a_rows, I, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Bdn, (int64_t)p.E * H, I, eb, bk, BN)) return cudaErrorInvalidValue;
+    const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
+    p.n_tiles = H / BN;
+    if (mx) return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+}
+
+cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I, const int32_t* counts,
+                         int64_t a_rows, const void* gu, void* dgu, const GemmCommon& c, cudaStream_t s) {
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.num_kb = H / 64;
+    p.b_rows_per_expert = I;
+    p.out0 = dgu;
+    p.gu = const_cast<void*>(gu);
+    p.split_col = I;
+    const int BN = I % 256 == 0 ? 256 : (I % 128 == 0 ? 128 : 64);
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, dy, a_rows, H, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, BN)) return cudaErrorInvalidValue;
+    p.n_tiles = I / BN;
+    const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    if (BN == 256) return run<256, false, false, kEpiDSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    if (BN == 128) return run<128, false, false, kEpiDSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    return run<64, false, false, kEpiDSwiGLU, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+}
+
+cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, int E, int H, int I,
+                         const int32_t* counts, const int32_t* offsets, const int32_t* row_src, int64_t a_rows,
+                         void* da, const GemmCommon& c, cudaStream_t s) {
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.row_src = row_src;
+    p.num_kb = 2 * I / 64;
+    p.b_split_kb = I / 64;
+    p.b_rows_per_expert = H;
+    p.out0 = da;
+    p.ldo = H;
+    const int BN = H % 256 == 0 ? 256 : 128;
+    CUtensorMap ta, tb, tb2;
+    if (!make_tmap(&ta, dgu, a_rows, 2 * I, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, W_gate, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb2, W_up, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
+    p.n_tiles = H / BN;
+    const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+    return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+}
+
+cudaError_t gemm_wgrad(const void* Aact, int M, const void* B, int N, int E, const int32_t* counts, int64_t a_rows,
+                       void* out0, void* out1, int split_col, const GemmCommon& c, cudaStream_t s) {
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.m_fixed = M;
+    p.out0 = out0;
+    p.out1 = out1;
+    p.split_col = split_col;
+    p.ldo = split_col < N ? split_col : N;
+    const int BN = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, Aact, a_rows, M, 2, 64, 64)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, B, a_rows, N, 2, 64, 64)) return cudaErrorInvalidValue;
+    p.n_tiles = N / BN;
+    const int64_t tub = (int64_t)E * ((M + kTileM - 1) / kTileM) * p.n_tiles;
+    if (BN == 256) return run<256, false, true, kEpiDense, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    if (BN == 128) return run<128, false, true, kEpiDense, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    return run<64, false, true, kEpiDense, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+}
+
+}  // namespace mok

@@ -1,0 +1,499 @@
+// gemm.cuh - persistent grouped GEMM on tcgen05 tensor cores (sm_103a).
+//
+// One kernel template serves every expert GEMM of the layer ("grouped GEMM"
+// over each expert's contiguous token segment, as the KuCoin article on MoK
+// describes in section 01): the forward gate/up GEMM with the SwiGLU epilogue,
+// the forward down GEMM whose epilogue pushes each row to its (token, slot)
+// partial, the backward dgrad GEMMs, and the backward wgrad GEMMs that reduce
+// over each expert's rows.
+//
+// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0     TMA producer: streams A and B K-blocks into a ring of smem
+//              stages (and, for MXFP8, the 512-byte scale chunks)
+//   warp 1     allocates tensor memory; one lane issues tcgen05.mma into a
+//              double-buffered fp32 accumulator in TMEM
+//   warps 2-5  epilogue: tcgen05.ld the accumulator (one row per thread) and
+//              apply the fused epilogue, then release the accumulator
+// Every wait is bounded (StatusBlock); nothing traps.
+#pragma once
+
+#include "tc.cuh"
+
+namespace mok {
+
+enum EpiKind : int {
+    kEpiSwiGLU = 0,   // h = silu(G) * U (bf16 or MXFP8), optional G/U save
+    kEpiScatter = 1,  // row -> slot (or identity) store, bf16 or f32
+    kEpiDSwiGLU = 2,  // dh -> dG, dU using saved G, U
+    kEpiDense = 3,    // dense tile store (wgrad), column split into two outputs
+};
+
+struct GemmParams {
+    int E;
+    int n_tiles;            // output tiles along N per expert
+    int num_kb;             // K-blocks for grouped-M kinds
+    int b_rows_per_expert;  // B row stride between experts (K-major B)
+    int b_split_kb;         // K-blocks >= this read from tmB2 (dgrad2); large = never
+    // row groups
+    const int32_t* counts;  // [E] routed rows per expert (grouped kinds)
+    int identity_rows;      // > 0: a single group of this many rows, no padding
+    int m_fixed;            // wgrad: output rows per expert; 0 otherwise
+    // epilogue
+    void* out0;
+    void* out1;
+    int ldo;                // leading dimension (elements) of out0/out1
+    int split_col;          // dense: columns >= split go to out1; SwiGLU/DSwiGLU: I
+    uint8_t* out_sf;        // MXFP8 h scales (SwiGLU)
+    void* gu;               // SwiGLU: G/U save target; DSwiGLU: G/U source ([rows, 2I] bf16)
+    const int32_t* offsets; // scatter: unpadded offsets [E+1]
+    const int32_t* row_src; // scatter: row -> slot
+    int out_f32;            // scatter: store fp32 instead of bf16
+    // MXFP8 scales of A and B (tile-ordered chunks)
+    const uint8_t* a_sf;
+    const uint8_t* b_sf;
+    int sf_kchunks;         // 128-wide K chunks per row tile (= K / 128)
+    StatusBlock* status;
+    unsigned long long timeout_ns;
+};
+
+template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES>
+struct GemmCfg {
+    static constexpr int kThreads = 192;
+    static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
+    static constexpr int kBytesB = BN * 128;
+    static constexpr int kStageBytes = kBytesA + kBytesB;
+    static constexpr int kSfaBytes = MX ? 512 : 0;
+    static constexpr int kSfbBytes = MX ? (BN / 128) * 512 : 0;
+    static constexpr int kSfStage = kSfaBytes + kSfbBytes;
+    static constexpr int kBK = MX ? 128 : 64;           // K elements per stage (128 bytes)
+    static constexpr int kUmmaK = MX ? 32 : 16;
+    static constexpr int kMmasPerStage = kBK / kUmmaK;  // 4
+    static constexpr int kAccCols = BN * ACC_STAGES;
+    static constexpr int kSfCols = MX ? 4 + 4 * (BN / 128) : 0;
+    static constexpr int kTmemNeed = kAccCols + STAGES * kSfCols;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                   : kTmemNeed <= 256 ? 256 : 512;
+    static constexpr int kBarOffset = STAGES * (kStageBytes + kSfStage);
+    static constexpr int kSmemBytes = 1024 /*align slack*/ + kBarOffset + 256;
+    static_assert(kTmemNeed <= 512, "tensor memory budget");
+    static_assert(BN % 64 == 0 && BN <= 256, "BN");
+    static_assert(!MX || (BN % 128 == 0), "MXFP8 tiles need whole 128-row scale chunks");
+    static_assert(!(MX && MN_MAJOR), "MXFP8 operands are K-major");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+struct TileInfo {
+    int e, m, n;
+    int a_row0;      // K-major: first A row; MN-major: first K row of the expert segment
+    int num_kb;
+    int row_base;    // first padded row of the tile (output row space of A rows)
+    int local_row0;  // first expert-local row of the tile
+    int valid;       // 0: skip
+};
+
+// Per-CTA copy of the group schedule.
+struct Sched {
+    int poff[kMaxE + 1];   // padded row offset of each expert segment
+    int toff[kMaxE + 1];   // first tile of each expert
+};
+
+template <int BN, bool MN_MAJOR>
+__device__ __forceinline__ void build_sched(const GemmParams& p, Sched& s) {
+    if (threadIdx.x == 0) {
+        int rows = 0, tiles = 0;
+        for (int e = 0; e < p.E; ++e) {
+            int cnt = p.identity_rows > 0 ? p.identity_rows : p.counts[e];
+            int mt = ceil_div(cnt, kTileM);
+            s.poff[e] = rows;
+            s.toff[e] = tiles;
+            rows += p.identity_rows > 0 ? cnt : mt * kTileM;
+            tiles += p.m_fixed > 0 ? ceil_div(p.m_fixed, kTileM) * p.n_tiles : mt * p.n_tiles;
+        }
+        s.poff[p.E] = rows;
+        s.toff[p.E] = tiles;
+    }
+}
+
+template <int BN, bool MN_MAJOR, int BK>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched& s, int g) {
+    TileInfo ti;
+    int lo = 0, hi = p.E - 1;  // last e with toff[e] <= g
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s.toff[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    int e = lo;
+    int local = g - s.toff[e];
+    ti.e = e;
+    if (p.m_fixed > 0) {
+        int mt = ceil_div(p.m_fixed, kTileM);
+        ti.n = local / mt;
+        ti.m = local % mt;
+        int cnt = p.counts[e];
+        ti.a_row0 = s.poff[e];
+        ti.num_kb = (ceil_div(cnt, kTileM) * kTileM) / BK;
+        ti.row_base = ti.m * kTileM;
+        ti.local_row0 = ti.m * kTileM;
+    } else {
+        int cnt = p.identity_rows > 0 ? p.identity_rows : p.counts[e];
+        int mt = ceil_div(cnt, kTileM);
+        ti.n = local / mt;
+        ti.m = local % mt;
+        ti.a_row0 = s.poff[e] + ti.m * kTileM;
+        ti.num_kb = p.num_kb;
+        ti.row_base = ti.a_row0;
+        ti.local_row0 = ti.m * kTileM;
+    }
+    ti.valid = 1;
+    return ti;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES>
+__global__ void __launch_bounds__(192, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+    using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ Sched sched;
+    __shared__ uint32_t s_tmem_base;
+
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = tc::smem_u32(smem);
+    const uint32_t bar_base = smem_base + C::kBarOffset;
+    auto full_bar = [&](int s) { return bar_base + 8u * s; };
+    auto empty_bar = [&](int s) { return bar_base + 8u * (STAGES + s); };
+    auto accf_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + a); };
+    auto acce_bar = [&](int a) { return bar_base + 8u * (2 * STAGES + ACC_STAGES + a); };
+    const uint32_t drain_bar = bar_base + 8u * (2 * STAGES + 2 * ACC_STAGES);
+    auto a_tile = [&](int s) { return smem_base + s * C::kStageBytes; };
+    auto b_tile = [&](int s) { return smem_base + s * C::kStageBytes + C::kBytesA; };
+    auto sf_tile = [&](int s) { return smem_base + STAGES * C::kStageBytes + s * C::kSfStage; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    StatusBlock* st = p.status;
+    const uint64_t tmo = p.timeout_ns;
+
+    build_sched<BN, MN_MAJOR>(p, sched);
+    if (threadIdx.x == 32) {
+        for (int s = 0; s < STAGES; ++s) {
+            tc::mbar_init(full_bar(s), 1);
+            tc::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < ACC_STAGES; ++a) {
+            tc::mbar_init(accf_bar(a), 1);
+            tc::mbar_init(acce_bar(a), 128);
+        }
+        tc::mbar_init(drain_bar, 1);
+        tc::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tc::prefetch_tmap(&tmA);
+        tc::prefetch_tmap(&tmB);
+        tc::prefetch_tmap(&tmB2);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tc::smem_u32(&s_tmem_base), C::kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem_base;
+    const int total_tiles = sched.toff[p.E];
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int last_par[STAGES];
+            for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
+            bool ok = true;
+            for (int g = blockIdx.x; g < total_tiles && ok; g += gridDim.x) {
+                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
+                    tc::mbar_expect_tx(full_bar(stage), C::kStageBytes + C::kSfStage);
+                    if constexpr (MN_MAJOR) {
+                        const int krow = ti.a_row0 + kb * 64;
+                        const int m0 = ti.m * kTileM;
+                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), m0, krow);
+                        tc::tma_load_2d(a_tile(stage) + 8192, &tmA, full_bar(stage), m0 + 64, krow);
+#pragma unroll
+                        for (int j = 0; j < BN / 64; ++j)
+                            tc::tma_load_2d(b_tile(stage) + 8192 * j, &tmB, full_bar(stage), ti.n * BN + 64 * j, krow);
+                    } else {
+                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
+                        const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
+                        if (kb < p.b_split_kb)
+                            tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kb * C::kBK, brow);
+                        else
+                            tc::tma_load_2d(b_tile(stage), &tmB2, full_bar(stage), (kb - p.b_split_kb) * C::kBK, brow);
+                        if constexpr (MX) {
+                            const int art = ti.a_row0 / kTileM;
+                            tc::bulk_load(sf_tile(stage), p.a_sf + ((int64_t)art * p.sf_kchunks + kb) * 512, 512,
+                                          full_bar(stage));
+#pragma unroll
+                            for (int j = 0; j < BN / 128; ++j) {
+                                const int brt = brow / kTileM + j;
+                                tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
+                                              p.b_sf + ((int64_t)brt * p.sf_kchunks + kb) * 512, 512, full_bar(stage));
+                            }
+                        }
+                    }
+                    last_par[stage] = (int)ph;
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (last_par[s] >= 0) tc::mbar_wait(full_bar(s), (uint32_t)last_par[s], st, tmo, kSiteDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t acc_ph = 0;
+            bool ok = true, issued = false;
+            for (int g = blockIdx.x; g < total_tiles && ok; g += gridDim.x) {
+                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+                if (ti.num_kb == 0) continue;
+                if (!tc::mbar_wait(acce_bar(acc), acc_ph ^ 1u, st, tmo, kSiteMmaAccEmpty)) { ok = false; break; }
+                tc::fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    if (!tc::mbar_wait(full_bar(stage), ph, st, tmo, kSiteMmaFull)) { ok = false; break; }
+                    tc::fence_after_sync();
+                    uint32_t sfa_t = 0, sfb_t = 0;
+                    if constexpr (MX) {
+                        sfa_t = tmem + (uint32_t)(C::kAccCols + stage * C::kSfCols);
+                        sfb_t = sfa_t + 4;
+                        tc::tmem_cp_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
+#pragma unroll
+                        for (int j = 0; j < BN / 128; ++j)
+                            tc::tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                                       tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
+                        uint64_t ad, bd;
+                        if constexpr (MN_MAJOR) {
+                            ad = tc::make_sdesc(a_tile(stage) + kk * 2048, 8192, 1024, tc::kLayoutSW128);
+                            bd = tc::make_sdesc(b_tile(stage) + kk * 2048, 8192, 1024, tc::kLayoutSW128);
+                        } else {
+                            ad = tc::make_sdesc(a_tile(stage) + kk * 32, 16, 1024, tc::kLayoutSW128);
+                            bd = tc::make_sdesc(b_tile(stage) + kk * 32, 16, 1024, tc::kLayoutSW128);
+                        }
+                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (MX) {
+                            tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
+                        } else {
+                            tc::mma_bf16(d, ad, bd, tc::idesc_bf16(128, BN, MN_MAJOR, MN_MAJOR), accum);
+                        }
+                    }
+                    issued = true;
+                    tc::mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                tc::mma_commit(accf_bar(acc));
+                if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+            }
+            if (!ok && issued) {
+                // every MMA issued so far must finish before tensor memory is freed
+                tc::mma_commit(drain_bar);
+                tc::mbar_wait(drain_bar, 0, st, tmo, kSiteDrain);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;          // TMEM lane quadrant of this warp
+        const int row = q * 32 + lane;   // tile row owned by this thread
+        int acc = 0;
+        uint32_t acc_ph = 0;
+        for (int g = blockIdx.x; g < total_tiles; g += gridDim.x) {
+            TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+            const bool has_acc = ti.num_kb > 0;
+            if (has_acc) {
+                if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
+                tc::fence_after_sync();
+            }
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+
+            if constexpr (EPI == kEpiSwiGLU) {
+                const int I = p.split_col;
+                const int64_t prow = ti.row_base + row;
+                const bool live = p.identity_rows > 0 ? (prow < p.identity_rows) : true;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+                    uint32_t gr[32], ur[32];
+                    tc::tmem_ld_32x32b_x32(tbase + c0, gr);
+                    tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c0, ur);
+                    tc::tmem_ld_wait();
+                    const int hc = ti.n * (BN / 2) + c0;
+                    float hv[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float gv = __uint_as_float(gr[i]), uv = __uint_as_float(ur[i]);
+                        hv[i] = silu_f(gv) * uv;
+                    }
+                    if (!live) continue;
+                    if constexpr (MX) {
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+                        const uint32_t code = e8m0_code(amax);
+                        const float inv = e8m0_inv_scale(code);
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            uint32_t lo = f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv);
+                            uint32_t hi = f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
+                            w[i] = lo | (hi << 16);
+                        }
+                        uint8_t* dst = static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc;
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc / 128;
+                        p.out_sf[chunk * 512 + sf_chunk_offset((int)(prow % kTileM), (hc / 32) & 3)] = (uint8_t)code;
+                    } else {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)I + hc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                    if (p.gu != nullptr) {
+                        uint32_t wg[16], wu[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            wg[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
+                            wu[i] = pack_bf16x2(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
+                        }
+                        __nv_bfloat16* gb = static_cast<__nv_bfloat16*>(p.gu) + prow * (int64_t)(2 * I);
+                        uint4* dg = reinterpret_cast<uint4*>(gb + hc);
+                        uint4* du = reinterpret_cast<uint4*>(gb + I + hc);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            dg[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
+                            du[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
+                        }
+                    }
+                }
+            } else if constexpr (EPI == kEpiScatter) {
+                int64_t dest = -1;
+                const int lrow = ti.local_row0 + row;
+                if (p.identity_rows > 0) {
+                    if (lrow < p.identity_rows) dest = lrow;
+                } else if (lrow < p.counts[ti.e]) {
+                    dest = p.row_src[p.offsets[ti.e] + lrow];
+                }
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(tbase + c0, r);
+                    tc::tmem_ld_wait();
+                    if (dest < 0) continue;
+                    const int col = ti.n * BN + c0;
+                    if (p.out_f32) {
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.out0) + dest * p.ldo + col);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                    } else {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + dest * p.ldo + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
+                }
+            } else if constexpr (EPI == kEpiDSwiGLU) {
+                const int I = p.split_col;
+                const int64_t prow = ti.row_base + row;
+                const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.gu) + prow * (int64_t)(2 * I);
+                __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)(2 * I);
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t r[32];
+                    tc::tmem_ld_32x32b_x32(tbase + c0, r);
+                    tc::tmem_ld_wait();
+                    const int col = ti.n * BN + c0;
+                    uint32_t gw[16], uw[16], dgw[16], duw[16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 a = reinterpret_cast<const uint4*>(gb + col)[i];
+                        uint4 b = reinterpret_cast<const uint4*>(gb + I + col)[i];
+                        gw[4 * i] = a.x; gw[4 * i + 1] = a.y; gw[4 * i + 2] = a.z; gw[4 * i + 3] = a.w;
+                        uw[4 * i] = b.x; uw[4 * i + 1] = b.y; uw[4 * i + 2] = b.z; uw[4 * i + 3] = b.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float dg2[2], du2[2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float G = h ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
+                            float U = h ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
+                            float dh = __uint_as_float(r[2 * i + h]);
+                            float sg = 1.0f / (1.0f + expf(-G));
+                            dg2[h] = dh * U * (sg * (1.0f + G * (1.0f - sg)));
+                            du2[h] = dh * (G * sg);
+                        }
+                        dgw[i] = pack_bf16x2(dg2[0], dg2[1]);
+                        duw[i] = pack_bf16x2(du2[0], du2[1]);
+                    }
+                    uint4* dg = reinterpret_cast<uint4*>(ob + col);
+                    uint4* du = reinterpret_cast<uint4*>(ob + I + col);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        dg[i] = make_uint4(dgw[4 * i], dgw[4 * i + 1], dgw[4 * i + 2], dgw[4 * i + 3]);
+                        du[i] = make_uint4(duw[4 * i], duw[4 * i + 1], duw[4 * i + 2], duw[4 * i + 3]);
+                    }
+                }
+            } else {  // kEpiDense
+                const bool live = ti.row_base + row < p.m_fixed;
+                const int64_t mrow = (int64_t)ti.e * p.m_fixed + ti.row_base + row;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    uint32_t r[32];
+                    if (has_acc) {
+                        tc::tmem_ld_32x32b_x32(tbase + c0, r);
+                        tc::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = 0u;
+                    }
+                    if (!live) continue;
+                    const int col = ti.n * BN + c0;
+                    __nv_bfloat16* ob;
+                    if (col < p.split_col) ob = static_cast<__nv_bfloat16*>(p.out0) + mrow * p.ldo + col;
+                    else ob = static_cast<__nv_bfloat16*>(p.out1) + mrow * p.ldo + (col - p.split_col);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                    uint4* dst = reinterpret_cast<uint4*>(ob);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (has_acc) {
+                tc::fence_before_sync();
+                tc::mbar_arrive(acce_bar(acc));
+                if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+            }
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+}  // namespace mok

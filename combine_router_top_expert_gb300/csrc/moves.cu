@@ -1,0 +1,407 @@
+// moves.cu - the layer's memory-bound kernels: pull-dispatch (gather, with
+// MXFP8 quantisation fused in), the fixed-order combine, weight packing, and
+// the backward's reverse-combine and reverse-dispatch / router-gradient pass.
+//
+// Pages (KuCoin article on Cursor's MoK, section 02): the expert side pulls
+// the tokens it needs ("pull dispatch") and results are pushed back to the
+// tokens they belong to ("push combine"); in the backward the directions are
+// pull on reverse-combine and push on reverse-dispatch. MXFP8 quantisation of
+// activations is fused into the dispatch path instead of a separate kernel.
+// The layer ends with a weighted sum (section 03) in a fixed floating-point
+// order (RuntimeWire, "Rebuilding the MoE layer around communication").
+#include <algorithm>
+
+#include "common.cuh"
+#include "moves.cuh"
+
+namespace mok {
+
+// Padded segment offsets (each expert starts on a 128-row boundary).
+__device__ __forceinline__ void padded_offsets(const int32_t* counts, int E, int32_t* poff) {
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int e = 0; e < E; ++e) {
+            poff[e] = s;
+            s += ceil_div(counts[e], kTileM) * kTileM;
+        }
+        poff[E] = s;
+    }
+    __syncthreads();
+}
+
+// expert owning padded row pr: last e with poff[e] <= pr (skips empty experts)
+__device__ __forceinline__ int find_expert(const int32_t* poff, int E, int pr) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (poff[mid] <= pr) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Pull-dispatch: one warp per padded row.
+// ---------------------------------------------------------------------------
+template <bool MX>
+__global__ void __launch_bounds__(256)
+dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
+                const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_src, void* __restrict__ A,
+                uint8_t* __restrict__ A_sf, const __nv_bfloat16* __restrict__ scale_src, const float* __restrict__ wslot) {
+    __shared__ int32_t poff[kMaxE + 1];
+    padded_offsets(counts, E, poff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = poff[E];
+    for (int pr = blockIdx.x * 8 + warp; pr < total; pr += gridDim.x * 8) {
+        const int e = find_expert(poff, E, pr);
+        const int local = pr - poff[e];
+        const __nv_bfloat16* src = nullptr;
+        float wmul = 1.f;
+        if (local < counts[e]) {
+            const int slot = row_src[offsets[e] + local];
+            src = (scale_src ? scale_src : x) + (int64_t)(slot / k) * H;
+            if (wslot) wmul = wslot[slot];
+        }
+        if constexpr (!MX) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(A) + (int64_t)pr * H);
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+            const int n = H / 8;
+            if (!src) {
+                for (int c = lane; c < n; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+            } else if (!wslot) {
+                for (int c = lane; c < n; c += 32) dst[c] = __ldg(s4 + c);
+            } else {
+                // reverse-combine: dy = w[t,j] * dY[t], rounded to bf16
+                for (int c = lane; c < n; c += 32) {
+                    uint4 v = __ldg(s4 + c);
+                    uint4 o;
+                    o.x = pack_bf16x2(wmul * bf16_lo(v.x), wmul * bf16_hi(v.x));
+                    o.y = pack_bf16x2(wmul * bf16_lo(v.y), wmul * bf16_hi(v.y));
+                    o.z = pack_bf16x2(wmul * bf16_lo(v.z), wmul * bf16_hi(v.z));
+                    o.w = pack_bf16x2(wmul * bf16_lo(v.w), wmul * bf16_hi(v.w));
+                    dst[c] = o;
+                }
+            }
+        } else {
+            uint8_t* dst = static_cast<uint8_t*>(A) + (int64_t)pr * H;
+            const int nb = H / 32;
+            const int rt = pr / kTileM, r = pr % kTileM;
+            for (int b = lane; b < nb; b += 32) {
+                uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+                uint32_t code = 0;
+                if (src) {
+                    const uint4* s4 = reinterpret_cast<const uint4*>(src + b * 32);
+                    uint4 v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) v[i] = __ldg(s4 + i);
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        f[8 * i + 0] = bf16_lo(v[i].x); f[8 * i + 1] = bf16_hi(v[i].x);
+                        f[8 * i + 2] = bf16_lo(v[i].y); f[8 * i + 3] = bf16_hi(v[i].y);
+                        f[8 * i + 4] = bf16_lo(v[i].z); f[8 * i + 5] = bf16_hi(v[i].z);
+                        f[8 * i + 6] = bf16_lo(v[i].w); f[8 * i + 7] = bf16_hi(v[i].w);
+                    }
+                    float amax = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                    code = e8m0_code(amax);
+                    const float inv = e8m0_inv_scale(code);
+                    uint32_t w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+                               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+                    o0 = make_uint4(w[0], w[1], w[2], w[3]);
+                    o1 = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                reinterpret_cast<uint4*>(dst + b * 32)[0] = o0;
+                reinterpret_cast<uint4*>(dst + b * 32)[1] = o1;
+                A_sf[((int64_t)rt * (H / 128) + b / 4) * 512 + sf_chunk_offset(r, b & 3)] = (uint8_t)code;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-order combine: out[t] = bf16(sum_j w[t,j] * y[t,j] (+ shared[t])).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+combine_kernel(const __nv_bfloat16* __restrict__ partials, const float* __restrict__ w,
+               const float* __restrict__ shared, __nv_bfloat16* __restrict__ out, int H, int k) {
+    const int t = blockIdx.x;
+    const int n = H / 8;
+    for (int c = threadIdx.x; c < n; c += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const float wj = __ldg(w + (int64_t)t * k + j);
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(partials + ((int64_t)t * k + j) * H) + c);
+            acc[0] = fmaf(wj, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wj, bf16_hi(v.x), acc[1]);
+            acc[2] = fmaf(wj, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wj, bf16_hi(v.y), acc[3]);
+            acc[4] = fmaf(wj, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wj, bf16_hi(v.z), acc[5]);
+            acc[6] = fmaf(wj, bf16_lo(v.w), acc[6]); acc[7] = fmaf(wj, bf16_hi(v.w), acc[7]);
+        }
+        if (shared) {
+            const float4* s = reinterpret_cast<const float4*>(shared + (int64_t)t * H) + 2 * c;
+            float4 a = __ldg(s), b = __ldg(s + 1);
+            acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+            acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(out + (int64_t)t * H)[c] = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Weight packing: src [E][K][Nsrc] (row-major, K = reduction dim) ->
+// dst rows [E][Ndst][K] (K-major). With src1 != NULL the destination
+// interleaves the two sources per group of `il` columns:
+//   dst row q*2il + r  = src0 column q*il + r       (r <  il)
+//                      = src1 column q*il + r - il  (r >= il)
+// One thread = one destination row x 32 K values.
+// ---------------------------------------------------------------------------
+template <bool MX>
+__global__ void __launch_bounds__(256)
+pack_kernel(const __nv_bfloat16* __restrict__ src0, const __nv_bfloat16* __restrict__ src1, int K, int Nsrc,
+            int il, void* __restrict__ dst, uint8_t* __restrict__ dst_sf) {
+    const int Ndst = src1 ? 2 * Nsrc : Nsrc;
+    const int e = blockIdx.z;
+    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+    const int kb = blockIdx.y;  // 32-wide K block
+    if (n >= Ndst) return;
+    const __nv_bfloat16* src;
+    int col;
+    if (src1) {
+        const int q = n / (2 * il), r = n % (2 * il);
+        src = r < il ? src0 : src1;
+        col = q * il + (r < il ? r : r - il);
+    } else {
+        src = src0;
+        col = n;
+    }
+    const __nv_bfloat16* s = src + (int64_t)e * K * Nsrc + (int64_t)(kb * 32) * Nsrc + col;
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __bfloat162float(s[(int64_t)i * Nsrc]);
+    const int64_t grow = (int64_t)e * Ndst + n;
+    if constexpr (!MX) {
+        uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(dst) + grow * K + kb * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d[i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
+                              pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
+    } else {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        const uint32_t code = e8m0_code(amax);
+        const float inv = e8m0_inv_scale(code);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+                   (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+        uint4* d = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + grow * K + kb * 32);
+        d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        const int64_t rt = grow / kTileM;
+        dst_sf[(rt * (K / 128) + kb / 4) * 512 + sf_chunk_offset((int)(grow % kTileM), kb & 3)] = (uint8_t)code;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward helpers
+// ---------------------------------------------------------------------------
+// gw[t*k+j] = <dY[t], y[t,j]> (fp32, fixed order: lane-strided partial sums
+// then a butterfly). One warp per slot.
+__global__ void __launch_bounds__(256)
+gate_grad_kernel(const __nv_bfloat16* __restrict__ dY, const __nv_bfloat16* __restrict__ partials, int T, int H,
+                 int k, float* __restrict__ gw) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = blockIdx.x * 8 + warp;
+    if (slot >= T * k) return;
+    const int t = slot / k;
+    const uint4* a = reinterpret_cast<const uint4*>(dY + (int64_t)t * H);
+    const uint4* b = reinterpret_cast<const uint4*>(partials + (int64_t)slot * H);
+    float s = 0.f;
+    for (int c = lane; c < H / 8; c += 32) {
+        uint4 u = __ldg(a + c), v = __ldg(b + c);
+        s = fmaf(bf16_lo(u.x), bf16_lo(v.x), s); s = fmaf(bf16_hi(u.x), bf16_hi(v.x), s);
+        s = fmaf(bf16_lo(u.y), bf16_lo(v.y), s); s = fmaf(bf16_hi(u.y), bf16_hi(v.y), s);
+        s = fmaf(bf16_lo(u.z), bf16_lo(v.z), s); s = fmaf(bf16_hi(u.z), bf16_hi(v.z), s);
+        s = fmaf(bf16_lo(u.w), bf16_lo(v.w), s); s = fmaf(bf16_hi(u.w), bf16_hi(v.w), s);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s = s + __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) gw[slot] = s;
+}
+
+// dl[t,j] = w_j (gw_j - sum_i w_i gw_i), i ascending.
+__global__ void router_dlogit_kernel(const float* __restrict__ w, const float* __restrict__ gw, int T, int k,
+                                     float* __restrict__ dl) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    float m = 0.f;
+    for (int j = 0; j < k; ++j) m = fmaf(w[(int64_t)t * k + j], gw[(int64_t)t * k + j], m);
+    for (int j = 0; j < k; ++j) dl[(int64_t)t * k + j] = w[(int64_t)t * k + j] * (gw[(int64_t)t * k + j] - m);
+}
+
+// Reverse-dispatch push + reduce: dX[t] = bf16( sum_j da[t,j] + sum_j dl[t,j] W_r[:, e_j] ),
+// j ascending in both sums, the expert term first.
+__global__ void __launch_bounds__(128)
+dx_kernel(const __nv_bfloat16* __restrict__ da, const float* __restrict__ dl, const int32_t* __restrict__ idx,
+          const float* __restrict__ WrT, int H, int k, __nv_bfloat16* __restrict__ dX) {
+    const int t = blockIdx.x;
+    for (int c = threadIdx.x; c < H / 8; c += blockDim.x) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int j = 0; j < k; ++j) {
+            uint4 v = __ldg(reinterpret_cast<const uint4*>(da + ((int64_t)t * k + j) * H) + c);
+            acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+            acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+        }
+        for (int j = 0; j < k; ++j) {
+            const float d = dl[(int64_t)t * k + j];
+            const float4* wr = reinterpret_cast<const float4*>(WrT + (int64_t)idx[(int64_t)t * k + j] * H) + 2 * c;
+            float4 a = __ldg(wr), b = __ldg(wr + 1);
+            acc[0] = fmaf(d, a.x, acc[0]); acc[1] = fmaf(d, a.y, acc[1]);
+            acc[2] = fmaf(d, a.z, acc[2]); acc[3] = fmaf(d, a.w, acc[3]);
+            acc[4] = fmaf(d, b.x, acc[4]); acc[5] = fmaf(d, b.y, acc[5]);
+            acc[6] = fmaf(d, b.z, acc[6]); acc[7] = fmaf(d, b.w, acc[7]);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]); o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(dX + (int64_t)t * H)[c] = o;
+    }
+}
+
+// dl_full[t, e] = dl[t, j] where idx[t, j] == e, else 0.
+__global__ void dl_scatter_kernel(const float* __restrict__ dl, const int32_t* __restrict__ idx, int T, int E,
+                                  int k, float* __restrict__ dl_full) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    for (int e = 0; e < E; ++e) dl_full[(int64_t)t * E + e] = 0.f;
+    for (int j = 0; j < k; ++j) dl_full[(int64_t)t * E + idx[(int64_t)t * k + j]] = dl[(int64_t)t * k + j];
+}
+
+// dW_r partial sums over a token range: part[split][h][e] = sum_{t in split}
+// x[t,h] dl_full[t,e], t ascending. One thread per h, 32 experts per pass.
+constexpr int kDwrSplits = 8;
+__global__ void __launch_bounds__(256)
+dwr_partial_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ dl_full, int T, int H, int E,
+                   float* __restrict__ part) {
+    __shared__ float dls[64][32];
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    const int split = blockIdx.y;
+    const int per = ceil_div(T, kDwrSplits);
+    const int ts = split * per, te = min(T, ts + per);
+    for (int eg = 0; eg < E; eg += 32) {
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        for (int t0 = ts; t0 < te; t0 += 64) {
+            const int nt = min(64, te - t0);
+            __syncthreads();
+            for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
+                const int tt = i / 32, e = eg + i % 32;
+                dls[tt][i % 32] = (tt < nt && e < E) ? dl_full[(int64_t)(t0 + tt) * E + e] : 0.f;
+            }
+            __syncthreads();
+            if (h < H)
+                for (int tt = 0; tt < nt; ++tt) {
+                    const float xv = __bfloat162float(x[(int64_t)(t0 + tt) * H + h]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = fmaf(xv, dls[tt][e], acc[e]);
+                }
+        }
+        if (h < H)
+            for (int e = 0; e < 32 && eg + e < E; ++e) part[((int64_t)split * H + h) * E + eg + e] = acc[e];
+    }
+}
+
+// dW_r[h, e] = sum over splits in ascending order.
+__global__ void dwr_reduce_kernel(const float* __restrict__ part, int H, int E, float* __restrict__ dWr) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)H * E) return;
+    float s = 0.f;
+    for (int sp = 0; sp < kDwrSplits; ++sp) s += part[(int64_t)sp * H * E + i];
+    dWr[i] = s;
+}
+
+// ---------------------------------------------------------------------------
+// Launchers
+// ---------------------------------------------------------------------------
+static int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
+                            const void* scale_src, const float* wslot, cudaStream_t s) {
+    int64_t rows = padded_rows_max(T, E, k);
+    int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
+    if (blocks < 1) blocks = 1;
+    if (mx)
+        dispatch_kernel<true><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts, offsets,
+                                                     row_src, A, A_sf, nullptr, nullptr);
+    else
+        dispatch_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts,
+                                                      offsets, row_src, A, nullptr,
+                                                      static_cast<const __nv_bfloat16*>(scale_src), wslot);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* partials, const float* w, const float* shared, void* out, int T, int H,
+                           int k, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    combine_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(partials), w, shared,
+                                     static_cast<__nv_bfloat16*>(out), H, k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(bool mx, const void* src0, const void* src1, int E, int K, int Nsrc, int il, void* dst,
+                        uint8_t* dst_sf, cudaStream_t s) {
+    const int Ndst = src1 ? 2 * Nsrc : Nsrc;
+    dim3 grid(ceil_div(Ndst, 128), K / 32, E);
+    if (mx)
+        pack_kernel<true><<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src0),
+                                               static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf);
+    else
+        pack_kernel<false><<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src0),
+                                                static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf);
+    return cudaGetLastError();
+}
+
+int64_t dwr_partial_floats(int H, int E) { return (int64_t)kDwrSplits * H * E; }
+
+cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* w, const int32_t* idx,
+                             const void* x, const float* WrT, const void* da, int T, int H, int E, int k, float* gw,
+                             float* dl, float* dl_full, float* part, void* dX, float* dWr, int stage,
+                             cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    if (stage == 0) {
+        gate_grad_kernel<<<ceil_div(T * k, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dY),
+                                                            static_cast<const __nv_bfloat16*>(partials), T, H, k, gw);
+        router_dlogit_kernel<<<ceil_div(T, 128), 128, 0, s>>>(w, gw, T, k, dl);
+    } else {
+        dx_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(da), dl, idx, WrT, H, k,
+                                    static_cast<__nv_bfloat16*>(dX));
+        dl_scatter_kernel<<<ceil_div(T, 128), 128, 0, s>>>(dl, idx, T, E, k, dl_full);
+        dwr_partial_kernel<<<dim3(ceil_div(H, 256), kDwrSplits), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                                                                               dl_full, T, H, E, part);
+        dwr_reduce_kernel<<<ceil_div(H * E, 256), 256, 0, s>>>(part, H, E, dWr);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mok

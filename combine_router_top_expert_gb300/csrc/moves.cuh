@@ -1,0 +1,60 @@
+// moves.cuh - host launchers of the routing, data-movement and GEMM kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace mok {
+
+// route.cu
+size_t route_workspace_bytes(int T, int H, int E, int k);
+cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,
+                                int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
+                                int32_t* row_src, int32_t* slot_row, void* ws, cudaStream_t s);
+cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, cudaStream_t s);
+
+// moves.cu
+// Gather rows into the padded expert-contiguous layout. BF16 with `wslot`:
+// the rows are scale_src[t] * wslot[t*k+j] (reverse-combine of the backward).
+cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
+                            const void* scale_src, const float* wslot, cudaStream_t s);
+cudaError_t launch_combine(const void* partials, const float* w, const float* shared, void* out, int T, int H,
+                           int k, cudaStream_t s);
+cudaError_t launch_pack(bool mx, const void* src0, const void* src1, int E, int K, int Nsrc, int il, void* dst,
+                        uint8_t* dst_sf, cudaStream_t s);
+// stage 0: gw, dl; stage 1: dX, dW_r
+cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* w, const int32_t* idx,
+                             const void* x, const float* WrT, const void* da, int T, int H, int E, int k, float* gw,
+                             float* dl, float* dl_full, float* dwr_part, void* dX, float* dWr, int stage,
+                             cudaStream_t s);
+int64_t dwr_partial_floats(int H, int E);
+
+// gemm.cu
+struct GemmCommon {
+    StatusBlock* status;
+    unsigned long long timeout_ns;
+    int num_sms;
+};
+// Forward gate/up GEMM + SwiGLU. A: [rows, H] (bf16 or E4M3 + tile scales);
+// packed B: [E * 2I, H] (interleaved gate/up per il = BN/2 columns).
+// identity_rows > 0: A is a plain [identity_rows, H] matrix (shared expert).
+cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
+                        int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows,
+                        void* h, uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s);
+// Forward down GEMM; rows pushed to out[row_src[...]] (bf16) or, for
+// identity_rows > 0, out[row] as f32.
+cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* Bdn, const uint8_t* Bdn_sf, int E,
+                      int H, int I, const int32_t* counts, const int32_t* offsets, const int32_t* row_src,
+                      int identity_rows, int64_t a_rows, void* out, const GemmCommon& c, cudaStream_t s);
+// dh = dy W_down^T with the dSwiGLU epilogue -> dGU [rows, 2I].
+cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I, const int32_t* counts,
+                         int64_t a_rows, const void* gu, void* dgu, const GemmCommon& c, cudaStream_t s);
+// da = dG W_gate^T + dU W_up^T, rows pushed to da[row_src[...]].
+cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, int E, int H, int I,
+                         const int32_t* counts, const int32_t* offsets, const int32_t* row_src, int64_t a_rows,
+                         void* da, const GemmCommon& c, cudaStream_t s);
+// out[e] = Aact_e^T B_e over each expert's padded rows; Aact [rows, M], B [rows, N].
+cudaError_t gemm_wgrad(const void* Aact, int M, const void* B, int N, int E, const int32_t* counts, int64_t a_rows,
+                       void* out0, void* out1, int split_col, const GemmCommon& c, cudaStream_t s);
+
+}  // namespace mok

@@ -1,0 +1,268 @@
+"""Python binding of libmok.so (the C ABI in include/mok.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+Tensors are torch CUDA tensors; PyTorch supplies device memory and streams.
+If the library or a CUDA device is missing, calls raise - there is no CPU
+fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmok.so")
+
+BF16, MXFP8 = 0, 1
+OK, ERR_INVALID, ERR_CUDA, ERR_TIMEOUT, ERR_CAPACITY, ERR_UNSUPPORTED = range(6)
+STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID", 2: "MOK_ERR_CUDA", 3: "MOK_ERR_TIMEOUT",
+                4: "MOK_ERR_CAPACITY", 5: "MOK_ERR_UNSUPPORTED"}
+
+# every function declared in include/mok.h
+EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_size", "mok_pack_weights",
+           "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
+           "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
+           "mok_version"]
+
+
+class MokError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("dtype", ctypes.c_int32), ("I_shared", ctypes.c_int32)]
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int32), ("timeout_ms", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
+
+
+class Routing(ctypes.Structure):
+    _fields_ = [("topk_idx", ctypes.c_void_p), ("topk_w", ctypes.c_void_p), ("counts", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("row_src", ctypes.c_void_p), ("slot_row", ctypes.c_void_p)]
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("packed", ctypes.c_void_p), ("packed_shared", ctypes.c_void_p),
+                ("routing", Routing), ("out", ctypes.c_void_p), ("saved", ctypes.c_void_p),
+                ("workspace", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("W_r", ctypes.c_void_p), ("W_gate", ctypes.c_void_p),
+                ("W_up", ctypes.c_void_p), ("W_down", ctypes.c_void_p), ("packed", ctypes.c_void_p),
+                ("dY", ctypes.c_void_p), ("routing", Routing), ("saved", ctypes.c_void_p),
+                ("dX", ctypes.c_void_p), ("dW_gate", ctypes.c_void_p), ("dW_up", ctypes.c_void_p),
+                ("dW_down", ctypes.c_void_p), ("dW_r", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libmok.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libmok.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            PP = ctypes.POINTER(Problem)
+            PC = ctypes.POINTER(Config)
+            PR = ctypes.POINTER(Routing)
+            L.mok_route_workspace_size.argtypes = [I32] * 4
+            L.mok_route_workspace_size.restype = SZ
+            L.mok_route_layout.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P]
+            L.mok_packed_weights_size.argtypes = [I32] * 4
+            L.mok_packed_weights_size.restype = SZ
+            L.mok_pack_weights.argtypes = [I32, I32, I32, I32, P, P, P, P, SZ, P]
+            L.mok_workspace_size.argtypes = [PP, PC]
+            L.mok_workspace_size.restype = SZ
+            L.mok_saved_size.argtypes = [PP]
+            L.mok_saved_size.restype = SZ
+            L.mok_moe_forward.argtypes = [PP, ctypes.POINTER(FwdArgs), PC, P]
+            L.mok_padded_rows_max.argtypes = [I32, I32, I32]
+            L.mok_padded_rows_max.restype = ctypes.c_int64
+            L.mok_dispatch.argtypes = [PP, P, PR, P, P, P]
+            L.mok_expert_ffn.argtypes = [PP, P, P, P, PR, P, P, P, PC, P, P]
+            L.mok_combine.argtypes = [PP, P, P, P, P, P]
+            L.mok_moe_backward.argtypes = [PP, ctypes.POINTER(BwdArgs), PC, P]
+            L.mok_device_status.argtypes = [P, P, ctypes.POINTER(I32), I32]
+            L.mok_status_string.argtypes = [I32]
+            L.mok_status_string.restype = ctypes.c_char_p
+            L.mok_version.restype = ctypes.c_char_p
+            for name in ("mok_route_layout", "mok_pack_weights", "mok_moe_forward", "mok_dispatch",
+                         "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc, what):
+    if rc != OK:
+        raise MokError(rc, what)
+
+
+def _bf16(t):
+    assert t.dtype == torch.bfloat16 and t.is_cuda and t.is_contiguous(), "bf16 contiguous CUDA tensor expected"
+    return t
+
+
+def make_problem(T, H, I, E, k, dtype=BF16, I_shared=0) -> Problem:
+    return Problem(T, H, I, E, k, dtype, I_shared)
+
+
+def make_config(num_sms=0, timeout_ms=0, flags=0) -> Config:
+    return Config(num_sms, timeout_ms, flags)
+
+
+# --------------------------------------------------------------------------- sizes
+
+def route_workspace_size(T, H, E, k) -> int:
+    return int(lib().mok_route_workspace_size(T, H, E, k))
+
+
+def packed_weights_size(E, H, I, dtype) -> int:
+    return int(lib().mok_packed_weights_size(E, H, I, dtype))
+
+
+def workspace_size(p: Problem, cfg: Config | None = None) -> int:
+    return int(lib().mok_workspace_size(ctypes.byref(p), ctypes.byref(cfg) if cfg else None))
+
+
+def saved_size(p: Problem) -> int:
+    return int(lib().mok_saved_size(ctypes.byref(p)))
+
+
+def padded_rows_max(T, E, k) -> int:
+    return int(lib().mok_padded_rows_max(T, E, k))
+
+
+def version() -> str:
+    return lib().mok_version().decode()
+
+
+# --------------------------------------------------------------------------- calls
+
+def alloc_bytes(n, device="cuda"):
+    """Device buffer of n bytes, 1024-byte aligned (torch's caching allocator
+    returns 512-byte aligned blocks; one extra KiB is sliced off the front)."""
+    raw = torch.empty(max(int(n), 1) + 1024, dtype=torch.uint8, device=device)
+    off = (-raw.data_ptr()) % 1024
+    return raw[off:off + max(int(n), 1)]
+
+
+def route_layout(x, W_r, k, bias=None, out=None, workspace=None, stream=None):
+    """Router + top-k + layout. Returns a dict of device tensors."""
+    _bf16(x)
+    T, H = x.shape
+    E = W_r.shape[1]
+    dev = x.device
+    if out is None:
+        out = dict(topk_idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+                   topk_w=torch.empty((T, k), dtype=torch.float32, device=dev),
+                   counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   row_src=torch.empty(T * k, dtype=torch.int32, device=dev),
+                   slot_row=torch.empty(T * k, dtype=torch.int32, device=dev))
+    if workspace is None:
+        workspace = alloc_bytes(route_workspace_size(T, H, E, k), dev)
+    rc = lib().mok_route_layout(_ptr(x), _ptr(W_r), _ptr(bias), T, H, E, k, _ptr(out["topk_idx"]),
+                                _ptr(out["topk_w"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                _ptr(out["row_src"]), _ptr(out["slot_row"]), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(rc, "mok_route_layout")
+    return out
+
+
+def routing_struct(r) -> Routing:
+    return Routing(r["topk_idx"].data_ptr(), r["topk_w"].data_ptr(), r["counts"].data_ptr(),
+                   r["offsets"].data_ptr(), r["row_src"].data_ptr(), r["slot_row"].data_ptr())
+
+
+def pack_weights(Wg, Wu, Wd, dtype, packed=None, stream=None):
+    E, H, I = Wg.shape
+    n = packed_weights_size(E, H, I, dtype)
+    if n == 0:
+        raise MokError(ERR_INVALID, "mok_packed_weights_size")
+    if packed is None:
+        packed = alloc_bytes(n, Wg.device)
+    rc = lib().mok_pack_weights(E, H, I, dtype, _ptr(_bf16(Wg)), _ptr(_bf16(Wu)), _ptr(_bf16(Wd)), _ptr(packed),
+                                packed.numel(), _stream(stream))
+    _check(rc, "mok_pack_weights")
+    return packed
+
+
+def moe_forward(p: Problem, x, packed, routing, out, workspace, saved=None, packed_shared=None,
+                cfg: Config | None = None, stream=None):
+    a = FwdArgs(x.data_ptr(), packed.data_ptr(), packed_shared.data_ptr() if packed_shared is not None else None,
+                routing_struct(routing), out.data_ptr(), saved.data_ptr() if saved is not None else None,
+                workspace.data_ptr(), workspace.numel())
+    rc = lib().mok_moe_forward(ctypes.byref(p), ctypes.byref(a), ctypes.byref(cfg) if cfg else None, _stream(stream))
+    _check(rc, "mok_moe_forward")
+    return out
+
+
+def moe_backward(p: Problem, x, W_r, Wg, Wu, Wd, packed, dY, routing, saved, grads, workspace,
+                 cfg: Config | None = None, stream=None):
+    """grads: dict with dX, dW_gate, dW_up, dW_down, dW_r (preallocated)."""
+    a = BwdArgs(x.data_ptr(), W_r.data_ptr(), Wg.data_ptr(), Wu.data_ptr(), Wd.data_ptr(), packed.data_ptr(),
+                dY.data_ptr(), routing_struct(routing), saved.data_ptr(), grads["dX"].data_ptr(),
+                grads["dW_gate"].data_ptr(), grads["dW_up"].data_ptr(), grads["dW_down"].data_ptr(),
+                grads["dW_r"].data_ptr(), workspace.data_ptr(), workspace.numel())
+    rc = lib().mok_moe_backward(ctypes.byref(p), ctypes.byref(a), ctypes.byref(cfg) if cfg else None,
+                                _stream(stream))
+    _check(rc, "mok_moe_backward")
+    return grads
+
+
+def dispatch(p: Problem, x, routing, A, A_sf=None, stream=None):
+    rs = routing_struct(routing)
+    rc = lib().mok_dispatch(ctypes.byref(p), _ptr(x), ctypes.byref(rs), _ptr(A), _ptr(A_sf), _stream(stream))
+    _check(rc, "mok_dispatch")
+
+
+def expert_ffn(p: Problem, A, A_sf, packed, routing, h, h_sf, partials, workspace, cfg: Config | None = None,
+               stream=None):
+    rs = routing_struct(routing)
+    rc = lib().mok_expert_ffn(ctypes.byref(p), _ptr(A), _ptr(A_sf), _ptr(packed), ctypes.byref(rs), _ptr(h),
+                              _ptr(h_sf), _ptr(partials), ctypes.byref(cfg) if cfg else None, _ptr(workspace),
+                              _stream(stream))
+    _check(rc, "mok_expert_ffn")
+
+
+def combine(p: Problem, partials, topk_w, out, shared=None, stream=None):
+    rc = lib().mok_combine(ctypes.byref(p), _ptr(partials), _ptr(topk_w), _ptr(shared), _ptr(out), _stream(stream))
+    _check(rc, "mok_combine")
+
+
+def device_status(workspace, reset=False, stream=None):
+    """(status code, detail) recorded on the device by the last call."""
+    d = ctypes.c_int32(0)
+    rc = lib().mok_device_status(_ptr(workspace), _stream(stream), ctypes.byref(d), int(reset))
+    return int(rc), int(d.value)
+
+
+def check_device_status(workspace, what="device", stream=None):
+    rc, d = device_status(workspace, stream=stream)
+    if rc != OK:
+        raise MokError(rc, f"{what} (detail {d})")

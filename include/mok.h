@@ -1,0 +1,254 @@
+/*
+ * mok.h - C ABI of the GB300 (sm_103a) routed MoE layer library, libmok.so.
+ *
+ * The layer follows the pages on Cursor's "Mixture-of-Kittens" (MoK):
+ *   [K-ja]  KuCoin (ja) "Cursor's MoK achieves 2.37x performance boost on
+ *           NVIDIA GB300 NVL72", sections 01, 02, 03 (and the Filipino copy).
+ *   [RW]    RuntimeWire "Cursor open-sources MoK MoE training kernel",
+ *           "Rebuilding the MoE layer around communication".
+ * A router picks k experts per token; per-expert counts and an
+ * expert-contiguous placement feed a grouped GEMM ([K-ja] 01); tokens are
+ * pulled to their experts, each expert runs a SwiGLU FFN, results are pushed
+ * back to their tokens and summed with the routing weights ([K-ja] 02, 03), in
+ * a fixed floating-point order so repeated runs are bitwise identical ([RW]).
+ * On one GPU the pull-dispatch is a gather from local HBM.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated; the caller owns
+ *     and allocates every buffer (inputs, outputs, packed weights, workspace,
+ *     saved context). The library never allocates device memory.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and never synchronise the host, except
+ *     mok_device_status and the *_host entry points, which say so.
+ *   - Row-major layouts. BF16 tensors are raw IEEE bfloat16 (2 bytes).
+ *   - Argument errors are detected on the host before any launch and return
+ *     MOK_ERR_INVALID (nothing is enqueued). CUDA launch errors return
+ *     MOK_ERR_CUDA. Problems found on the device (a bounded wait that ran out,
+ *     a ring too small for one minibatch) are written to a status word in the
+ *     workspace; read it with mok_device_status after the stream work ends.
+ *   - No CPU fallback: without an sm_103a device every compute call returns
+ *     MOK_ERR_CUDA.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* mok_stream_t; /* cudaStream_t */
+
+typedef enum { MOK_BF16 = 0, MOK_MXFP8 = 1 } mok_dtype;
+
+typedef enum {
+    MOK_OK = 0,
+    MOK_ERR_INVALID = 1,     /* bad argument (host check) */
+    MOK_ERR_CUDA = 2,        /* CUDA runtime/driver error */
+    MOK_ERR_TIMEOUT = 3,     /* a device-side bounded wait gave up */
+    MOK_ERR_CAPACITY = 4,    /* ring buffer smaller than one minibatch */
+    MOK_ERR_UNSUPPORTED = 5  /* valid but not built (e.g. MXFP8 backward) */
+} mok_status;
+
+/* Shapes of one layer. T tokens, hidden H, expert intermediate I, E routed
+ * experts, top-k. dtype: operand type of the routed experts (MOK_BF16 or
+ * MOK_MXFP8, E4M3 elements + one E8M0 scale per 32 elements along each GEMM's
+ * reduction dimension). I_shared > 0 adds one BF16 shared expert (SwiGLU, I =
+ * I_shared) applied to every token with weight 1 ([RW]: shared experts stay
+ * BF16). Limits: 1 <= k <= E <= 256; H % 128 == 0; I % 128 == 0 or I == 64
+ * (BF16); I % 128 == 0 (MXFP8); I_shared likewise; T >= 0, T*k < 2^30. */
+typedef struct {
+    int32_t T, H, I, E, k;
+    int32_t dtype;
+    int32_t I_shared;
+} mok_problem;
+
+/* Execution knobs. Zero-initialise for defaults. */
+typedef struct {
+    int32_t num_sms;         /* SMs the persistent kernels may use; 0 = all */
+    int32_t timeout_ms;      /* limit of every device-side wait; 0 = 4000 */
+    int32_t flags;           /* MOK_FLAG_* */
+    int32_t reserved[5];
+} mok_config;
+
+/* ------------------------------------------------------------------------- */
+/* Router, top-k and layout ([K-ja] 01: count each expert's tokens, place each */
+/* token, keep each expert's tokens adjacent for the grouped GEMM).           */
+/* ------------------------------------------------------------------------- */
+
+/* Workspace bytes mok_route_layout needs (device memory, any content). */
+size_t mok_route_workspace_size(int32_t T, int32_t H, int32_t E, int32_t k);
+
+/* logits[t,e] = sum_h x[t,h] * W_r[h,e] (+ bias[e]) in binary32, in this fixed
+ * order: 32 partial fma chains, chain c over h = 256*i + 8*c + m (i = 0,1,..,
+ * m = 0..7, h < H), combined by butterfly adds with offsets 16,8,4,2,1, then
+ * the bias add. Top-k by (logit descending, expert ascending); slot j is the
+ * j-th ranked expert; topk_w[t,j] = exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ * (the softmax over E renormalised over the selected experts).
+ * counts[e] = routed rows of expert e; offsets = exclusive prefix sum (E+1
+ * entries, unpadded); rows are ordered by (expert, token); row_src[row] =
+ * t*k + j; slot_row[t*k + j] = row.
+ *   x [T,H] bf16, W_r [H,E] f32, bias [E] f32 or NULL;
+ *   outputs topk_idx [T,k] i32, topk_w [T,k] f32, counts [E] i32,
+ *   offsets [E+1] i32, row_src [T*k] i32, slot_row [T*k] i32.
+ * Logits must be finite (non-finite inputs give unspecified routing). */
+mok_status mok_route_layout(const void* x, const float* W_r, const float* bias,
+                            int32_t T, int32_t H, int32_t E, int32_t k,
+                            int32_t* topk_idx, float* topk_w, int32_t* counts,
+                            int32_t* offsets, int32_t* row_src, int32_t* slot_row,
+                            void* workspace, size_t ws_bytes, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Expert weights                                                              */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of the packed form of E experts' weights (dtype MOK_BF16/MOK_MXFP8). */
+size_t mok_packed_weights_size(int32_t E, int32_t H, int32_t I, int32_t dtype);
+
+/* One-time repacking of W_gate [E,H,I], W_up [E,H,I], W_down [E,I,H] (bf16,
+ * device) into the K-major tile layout the tensor-core GEMMs read, with gate
+ * and up columns interleaved per output tile (so one tile holds matching gate
+ * and up columns for the fused SwiGLU), and for MXFP8 quantised to E4M3 with
+ * E8M0 scales per 32 elements along H (gate/up) and along I (down). Runs on
+ * `stream`; `packed` must hold mok_packed_weights_size bytes, 256-B aligned.
+ * For the shared expert pass E = 1 and dtype MOK_BF16. */
+mok_status mok_pack_weights(int32_t E, int32_t H, int32_t I, int32_t dtype,
+                            const void* W_gate, const void* W_up, const void* W_down,
+                            void* packed, size_t packed_bytes, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Forward                                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* Routing produced by mok_route_layout (device pointers). */
+typedef struct {
+    const int32_t* topk_idx;  /* [T,k] */
+    const float* topk_w;      /* [T,k] */
+    const int32_t* counts;    /* [E] */
+    const int32_t* offsets;   /* [E+1] */
+    const int32_t* row_src;   /* [T*k] */
+    const int32_t* slot_row;  /* [T*k] */
+} mok_routing;
+
+typedef struct {
+    const void* x;             /* [T,H] bf16 */
+    const void* packed;        /* routed experts, from mok_pack_weights */
+    const void* packed_shared; /* shared expert (E=1, BF16) or NULL; needs I_shared > 0 */
+    mok_routing routing;
+    void* out;                 /* [T,H] bf16 */
+    void* saved;               /* NULL (inference) or mok_saved_size bytes kept for backward */
+    void* workspace;           /* mok_workspace_size bytes, 256-B aligned */
+    size_t ws_bytes;
+} mok_fwd_args;
+
+/* Workspace bytes of mok_moe_forward / mok_moe_backward for this problem. */
+size_t mok_workspace_size(const mok_problem* p, const mok_config* cfg);
+/* Bytes of the saved context (BF16 training forward only). */
+size_t mok_saved_size(const mok_problem* p);
+
+/* The layer forward: pull-gather (+MXFP8 quantisation) of each routed row
+ * into expert-contiguous order, grouped gate/up GEMM with fused SwiGLU
+ * (+MXFP8 quantisation of h), grouped down GEMM whose epilogue pushes each
+ * row to its (token, slot) partial, then out[t] = bf16(sum_{j=0..k-1}
+ * w[t,j] * y[t,j] (+ shared[t])) in fp32 with j ascending. Bitwise
+ * deterministic. `saved` != NULL keeps the activations the backward needs
+ * (BF16 only; MOK_ERR_UNSUPPORTED for MXFP8). */
+mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a,
+                           const mok_config* cfg, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* The forward's stages as separate calls (same kernels), for tests and for   */
+/* callers that interleave their own work.                                    */
+/* ------------------------------------------------------------------------- */
+
+/* Rows of the padded expert-contiguous layout the stages use: each expert's
+ * segment starts on a multiple of 128 rows; pad rows hold zeros. */
+int64_t mok_padded_rows_max(int32_t T, int32_t E, int32_t k);
+
+/* Pull-dispatch: for every padded row of expert e at local index r < counts[e],
+ * A[row] = Q(x[t]) with t*k+j = row_src[offsets[e]+r]; pad rows are zero.
+ * BF16: A is [rows_max, H] bf16 and A_sf is unused (NULL).
+ * MXFP8: A is [rows_max, H] E4M3 bytes and A_sf receives the E8M0 scales in
+ * the tensor-core tile order: for row-tile rt (128 rows) and 128-column block
+ * kc, a 512-byte chunk at ((rt * (H/128)) + kc) * 512 whose byte
+ * (r % 32) * 16 + (r / 32) * 4 + (c / 32) % 4 holds the scale of row 128*rt+r,
+ * 32-column block c/32 (c within the 128-column block). */
+mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* r,
+                        void* A, void* A_sf, mok_stream_t stream);
+
+/* Grouped expert FFN on the dispatched rows: h = SwiGLU(A W_gate[e], A W_up[e])
+ * (BF16 or MXFP8 as dtype), y = h W_down[e], y row pushed to partials[t*k+j]
+ * ([T*k, H] bf16, unweighted). h/h_sf are caller scratch of
+ * [rows_max, I] (bf16 or E4M3; h_sf uses the same tile order as A_sf with I
+ * in place of H; MXFP8 only). A and h must be 1024-B aligned. `workspace`
+ * supplies the 256-byte device status block (its first 256 bytes). */
+mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf,
+                          const void* packed, const mok_routing* r, void* h, void* h_sf,
+                          void* partials, const mok_config* cfg, void* workspace,
+                          mok_stream_t stream);
+
+/* Fixed-order weighted sum: out[t] = bf16(sum_j topk_w[t,j] * partials[t*k+j]
+ * (+ shared[t])), fp32, j ascending. shared: [T,H] f32 or NULL. */
+mok_status mok_combine(const mok_problem* p, const void* partials, const float* topk_w,
+                       const float* shared, void* out, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Backward (BF16)                                                              */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const void* x;          /* [T,H] bf16 (forward input) */
+    const float* W_r;       /* [H,E] f32 */
+    const void* W_gate;     /* [E,H,I] bf16, original layout */
+    const void* W_up;       /* [E,H,I] bf16 */
+    const void* W_down;     /* [E,I,H] bf16 */
+    const void* packed;     /* the forward's packed weights */
+    const void* dY;         /* [T,H] bf16 upstream gradient */
+    mok_routing routing;
+    const void* saved;      /* filled by the training forward */
+    void* dX;               /* [T,H] bf16 */
+    void* dW_gate;          /* [E,H,I] bf16 */
+    void* dW_up;            /* [E,H,I] bf16 */
+    void* dW_down;          /* [E,I,H] bf16 */
+    float* dW_r;            /* [H,E] f32 */
+    void* workspace;
+    size_t ws_bytes;
+} mok_bwd_args;
+
+/* Backward of the layer ([K-ja] 02: pull on reverse-combine, push on
+ * reverse-dispatch). Reverse-combine pulls dy[row] = w[t,j] * dY[t] into
+ * expert order and gw[t,j] = <dY[t], y[t,j]>; grouped dgrad GEMMs give
+ * dh = dy W_down^T, dG = dh*U*silu'(G), dU = dh*silu(G),
+ * da = dG W_gate^T + dU W_up^T, each da row pushed to its slot; grouped wgrad
+ * GEMMs reduce over each expert's rows in row order (no split, no atomics):
+ * dW_gate = A^T dG, dW_up = A^T dU, dW_down = h^T dy; router: dl_j =
+ * w_j (gw_j - sum_i w_i gw_i), dW_r = x^T dl, and dX[t] = sum_j da[t,j] +
+ * sum_j dl_j W_r[:, e_j] in fixed order. The bias gets no gradient.
+ * Bitwise deterministic. */
+mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
+                            const mok_config* cfg, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Device status                                                               */
+/* ------------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then returns the status the last forward/backward
+ * using `workspace` recorded on the device (MOK_OK, MOK_ERR_TIMEOUT or
+ * MOK_ERR_CAPACITY); *detail (if not NULL) receives a code naming the wait
+ * that gave up. reset != 0 clears the word afterwards. */
+mok_status mok_device_status(const void* workspace, mok_stream_t stream, int32_t* detail,
+                             int32_t reset);
+
+/* Human-readable name of a status code (static string). */
+const char* mok_status_string(mok_status s);
+
+/* Library version string. */
+const char* mok_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H */

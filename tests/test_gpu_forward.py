@@ -1,0 +1,152 @@
+"""Forward layer on the GPU against the oracle (small and medium shapes)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_router_top_expert_gb300 import mok, synth
+from helpers import (TOL, assert_close, dtype_of, host_bf16_f64, layer_for, to_dev_bf16, untile_sf)
+
+FWD_CASES = [
+    # tiny layer of the pages' shape family, BF16
+    synth.small("tiny", T=64, H=128, I=64, E=8, k=2),
+    # several 128-row tiles per expert with ragged tails, BF16
+    synth.small("ragged_bf16", T=1000, H=512, I=256, E=4, k=2),
+    # wide expert (I=2048) at small H, skewed routing, BF16
+    synth.small("skew_bf16", T=300, H=256, I=2048, E=8, k=2, zipf_s=1.2),
+    # MXFP8 operands, skewed routing
+    synth.small("ragged_mx", T=600, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
+    synth.small("mx_k8", T=200, H=1024, I=512, E=32, k=8, dtype="mxfp8"),
+    # BF16 shared expert added to MXFP8 routed experts
+    synth.small("mx_shared", T=300, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2, shared_I=256),
+    # one token; one expert with k=1 (dense SwiGLU)
+    synth.small("one_token", T=1, H=256, I=128, E=16, k=4),
+    synth.small("dense", T=130, H=256, I=128, E=1, k=1),
+    # more experts than tokens can fill: several experts get zero rows
+    synth.small("sparse", T=8, H=256, I=128, E=64, k=1),
+]
+
+
+def _oracle_mode(dtype):
+    return oracle.MODE_MXFP8 if dtype == mok.MXFP8 else oracle.MODE_BF16
+
+
+def _run_case(wl, seed=0):
+    inp = synth.make_inputs(wl, seed=seed)
+    dt = dtype_of(wl)
+    layer = layer_for(inp, dt)
+    x = to_dev_bf16(inp.x)
+    out = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    assert layer.status(wl.T) == (mok.OK, 0)
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=_oracle_mode(dt), shared=inp.shared)
+    return inp, layer, x, out, ref
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", FWD_CASES, ids=[w.name for w in FWD_CASES])
+def test_forward_matches_oracle(wl):
+    inp, layer, x, out, ref = _run_case(wl)
+    assert_close(host_bf16_f64(out), ref, TOL[dtype_of(wl)], wl.name)
+
+
+@pytest.mark.gpu
+def test_forward_bitwise_deterministic():
+    wl = synth.small("det", T=700, H=512, I=256, E=8, k=4, zipf_s=1.2)
+    inp = synth.make_inputs(wl, seed=3)
+    for dt in (mok.BF16, mok.MXFP8):
+        layer = layer_for(inp, dt)
+        x = to_dev_bf16(inp.x)
+        first = layer.forward(x).clone()
+        for _ in range(9):
+            again = layer.forward(x)
+            assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dt", [mok.BF16, mok.MXFP8])
+def test_dispatch_bytes(dt):
+    """The gather reproduces x rows (BF16) or the oracle's MXFP8 bytes and
+    scales (MXFP8) bit for bit; pad rows are zero."""
+    wl = synth.small("disp", T=333, H=1024, I=128, E=8, k=3, zipf_s=1.2)
+    inp = synth.make_inputs(wl, seed=1)
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    layer = layer_for(inp, dt)
+    x = to_dev_bf16(inp.x)
+    rt = layer.route(x)
+    p = layer.problem(wl.T)
+    rows = mok.padded_rows_max(wl.T, wl.E, wl.k)
+    if dt == mok.BF16:
+        A = mok.alloc_bytes(rows * wl.H * 2).view(torch.bfloat16).view(rows, wl.H)
+        mok.dispatch(p, x, rt, A)
+    else:
+        A = mok.alloc_bytes(rows * wl.H).view(rows, wl.H)
+        A_sf = mok.alloc_bytes(rows * wl.H // 32)
+        mok.dispatch(p, x, rt, A, A_sf)
+    torch.cuda.synchronize()
+    counts = r["counts"]
+    poff = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    src_rows = np.full(poff[-1], -1)
+    for e in range(wl.E):
+        src_rows[poff[e]:poff[e] + counts[e]] = r["row_src"][r["offsets"][e]:r["offsets"][e + 1]] // wl.k
+    live = src_rows >= 0
+    if dt == mok.BF16:
+        got = A[:poff[-1]].view(torch.int16).cpu().numpy().view(np.uint16)
+        assert np.array_equal(got[live], inp.x[src_rows[live]])
+        assert np.all(got[~live] == 0)
+    else:
+        codes, scales = oracle.mx_quantize_bf16_rows(inp.x)
+        got = A[:poff[-1]].cpu().numpy()
+        assert np.array_equal(got[live], codes[src_rows[live]])
+        assert np.all(got[~live] == 0)
+        sf = untile_sf(A_sf.cpu().numpy(), poff[-1], wl.H)
+        assert np.array_equal(sf[live], scales[src_rows[live]])
+        assert np.all(sf[~live] == 0)
+
+
+@pytest.mark.gpu
+def test_stages_compose_to_forward():
+    """dispatch -> expert_ffn -> combine gives the same bits as moe_forward."""
+    wl = synth.small("stages", T=256, H=512, I=256, E=8, k=2, dtype="mxfp8")
+    inp = synth.make_inputs(wl, seed=4)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    full = layer.forward(x).clone()
+    rt = layer.buffers(wl.T)["routing"]
+    p = layer.problem(wl.T)
+    rows = mok.padded_rows_max(wl.T, wl.E, wl.k)
+    A = mok.alloc_bytes(rows * wl.H)
+    A_sf = mok.alloc_bytes(rows * wl.H // 32)
+    h = mok.alloc_bytes(rows * wl.I)
+    h_sf = mok.alloc_bytes(rows * wl.I // 32)
+    part = torch.empty((wl.T * wl.k, wl.H), dtype=torch.bfloat16, device="cuda")
+    ws = mok.alloc_bytes(256)
+    out = torch.empty_like(full)
+    mok.dispatch(p, x, rt, A, A_sf)
+    mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, ws)
+    mok.combine(p, part, rt["topk_w"], out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), full.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_invalid_arguments_rejected_on_host():
+    wl = synth.small("inv", T=16, H=256, I=128, E=4, k=2)
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    b = layer.buffers(wl.T)
+    p = mok.make_problem(wl.T, wl.H, wl.I, wl.E, 9, mok.BF16)  # k > E
+    with pytest.raises(mok.MokError) as ei:
+        mok.moe_forward(p, x, layer.packed, b["routing"], b["out"], b["ws"])
+    assert ei.value.code == mok.ERR_INVALID
+    small_ws = b["ws"][:1024]
+    with pytest.raises(mok.MokError) as ei:
+        mok.moe_forward(layer.problem(wl.T), x, layer.packed, b["routing"], b["out"], small_ws)
+    assert ei.value.code == mok.ERR_INVALID
+    p_mx = mok.make_problem(wl.T, wl.H, wl.I, wl.E, wl.k, mok.MXFP8)
+    with pytest.raises(mok.MokError) as ei:
+        mok.moe_forward(p_mx, x, layer.packed, b["routing"], b["out"], b["ws"], saved=b["ws"])
+    assert ei.value.code == mok.ERR_UNSUPPORTED
