@@ -77,7 +77,7 @@ FwdLayout fwd_layout(const mok_problem* p, bool training) {
     L.total = o;
     size_t q = 0;
     L.sA = q; q += align_up(rows * p->H * 2, 1024);
-    L.sGU = q; q += align_up(rows * 2 * p->I * 2, 1024);
+    L.sGU = q; q += align_up(rows * 2 * p->I * 4, 1024);   // fp32 G | U
     L.sh = q; q += align_up(rows * p->I * 2, 1024);
     L.spart = q; q += align_up((int64_t)p->T * p->k * p->H * 2, 1024);
     L.saved_total = q;

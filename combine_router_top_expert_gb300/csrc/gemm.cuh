@@ -22,7 +22,7 @@
 namespace mok {
 
 enum EpiKind : int {
-    kEpiSwiGLU = 0,   // h = silu(G) * U (bf16 or MXFP8), optional G/U save
+    kEpiSwiGLU = 0,   // h = silu(G) * U (bf16 or MXFP8), optional fp32 G/U save
     kEpiScatter = 1,  // row -> slot (or identity) store, bf16 or f32
     kEpiDSwiGLU = 2,  // dh -> dG, dU using saved G, U
     kEpiDense = 3,    // dense tile store (wgrad), column split into two outputs
@@ -44,7 +44,7 @@ struct GemmParams {
     int ldo;                // leading dimension (elements) of out0/out1
     int split_col;          // dense: columns >= split go to out1; SwiGLU/DSwiGLU: I
     uint8_t* out_sf;        // MXFP8 h scales (SwiGLU)
-    void* gu;               // SwiGLU: G/U save target; DSwiGLU: G/U source ([rows, 2I] bf16)
+    void* gu;               // SwiGLU: G/U save target; DSwiGLU: G/U source ([rows, 2I] fp32)
     const int32_t* offsets; // scatter: unpadded offsets [E+1]
     const int32_t* row_src; // scatter: row -> slot
     int out_f32;            // scatter: store fp32 instead of bf16
@@ -371,19 +371,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
                     if (p.gu != nullptr) {
-                        uint32_t wg[16], wu[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            wg[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
-                            wu[i] = pack_bf16x2(__uint_as_float(ur[2 * i]), __uint_as_float(ur[2 * i + 1]));
-                        }
-                        __nv_bfloat16* gb = static_cast<__nv_bfloat16*>(p.gu) + prow * (int64_t)(2 * I);
+                        // pre-activations kept in fp32 for the backward's dSwiGLU
+                        float* gb = static_cast<float*>(p.gu) + prow * (int64_t)(2 * I);
                         uint4* dg = reinterpret_cast<uint4*>(gb + hc);
                         uint4* du = reinterpret_cast<uint4*>(gb + I + hc);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            dg[i] = make_uint4(wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
-                            du[i] = make_uint4(wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
+                        for (int i = 0; i < 8; ++i) {
+                            dg[i] = make_uint4(gr[4 * i], gr[4 * i + 1], gr[4 * i + 2], gr[4 * i + 3]);
+                            du[i] = make_uint4(ur[4 * i], ur[4 * i + 1], ur[4 * i + 2], ur[4 * i + 3]);
                         }
                     }
                 }
@@ -418,7 +413,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else if constexpr (EPI == kEpiDSwiGLU) {
                 const int I = p.split_col;
                 const int64_t prow = ti.row_base + row;
-                const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(p.gu) + prow * (int64_t)(2 * I);
+                const float* gb = static_cast<const float*>(p.gu) + prow * (int64_t)(2 * I);
                 __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)(2 * I);
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -426,28 +421,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc::tmem_ld_32x32b_x32(tbase + c0, r);
                     tc::tmem_ld_wait();
                     const int col = ti.n * BN + c0;
-                    uint32_t gw[16], uw[16], dgw[16], duw[16];
+                    uint32_t dgw[16], duw[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 a = reinterpret_cast<const uint4*>(gb + col)[i];
-                        uint4 b = reinterpret_cast<const uint4*>(gb + I + col)[i];
-                        gw[4 * i] = a.x; gw[4 * i + 1] = a.y; gw[4 * i + 2] = a.z; gw[4 * i + 3] = a.w;
-                        uw[4 * i] = b.x; uw[4 * i + 1] = b.y; uw[4 * i + 2] = b.z; uw[4 * i + 3] = b.w;
-                    }
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 g4 = reinterpret_cast<const float4*>(gb + col)[i];
+                        const float4 u4 = reinterpret_cast<const float4*>(gb + I + col)[i];
+                        const float Gv[4] = {g4.x, g4.y, g4.z, g4.w};
+                        const float Uv[4] = {u4.x, u4.y, u4.z, u4.w};
+                        float dg4[4], du4[4];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float dg2[2], du2[2];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            float G = h ? bf16_hi(gw[i]) : bf16_lo(gw[i]);
-                            float U = h ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
-                            float dh = __uint_as_float(r[2 * i + h]);
-                            float sg = 1.0f / (1.0f + expf(-G));
-                            dg2[h] = dh * U * (sg * (1.0f + G * (1.0f - sg)));
-                            du2[h] = dh * (G * sg);
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            const float G = Gv[q2], U = Uv[q2];
+                            const float dh = __uint_as_float(r[4 * i + q2]);
+                            const float sg = 1.0f / (1.0f + expf(-G));
+                            dg4[q2] = dh * U * (sg * (1.0f + G * (1.0f - sg)));
+                            du4[q2] = dh * (G * sg);
                         }
-                        dgw[i] = pack_bf16x2(dg2[0], dg2[1]);
-                        duw[i] = pack_bf16x2(du2[0], du2[1]);
+                        dgw[2 * i] = pack_bf16x2(dg4[0], dg4[1]);
+                        dgw[2 * i + 1] = pack_bf16x2(dg4[2], dg4[3]);
+                        duw[2 * i] = pack_bf16x2(du4[0], du4[1]);
+                        duw[2 * i + 1] = pack_bf16x2(du4[2], du4[3]);
                     }
                     uint4* dg = reinterpret_cast<uint4*>(ob + col);
                     uint4* du = reinterpret_cast<uint4*>(ob + I + col);

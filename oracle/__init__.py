@@ -56,6 +56,8 @@ def lib():
                                           P, P, P, I, P, P]
             L.orc_moe_backward.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, I,
                                            P, P, P, P, P]
+            L.orc_moe_backward_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, I, P, I, P, P, I,
+                                                   P, P, P, P]
             L.orc_mx_quantize_rows.argtypes = [P, I64, I64, P, P]
             L.orc_mx_quantize_bf16_rows.argtypes = [P, I64, I64, P, P]
             L.orc_e4m3_value.argtypes = [ctypes.c_uint8]
@@ -253,3 +255,29 @@ def moe_backward(x, W_r, Wg, Wu, Wd, dY, routing, mode=MODE_BF16, f64=False):
                                 _p(dX), _p(dWg), _p(dWu), _p(dWd), _p(dWr))
     _check(rc, "moe_backward")
     return dX, dWg, dWu, dWd, dWr
+
+
+def moe_backward_sampled(x, W_r, Wg, Wu, Wd, dY, routing, tokens, cols, mode=MODE_BF16):
+    """Selected backward outputs: dX rows of `tokens` [n, H]; for each (e, i)
+    in `cols`: dW_gate[e][:, i], dW_up[e][:, i], dW_down[e][i, :] (each [n_col, H])."""
+    x, Wg, Wu, Wd, dY = _inputs([x, Wg, Wu, Wd, dY], False)
+    W_r = np.ascontiguousarray(W_r, dtype=np.float32)
+    T, H = x.shape
+    E, _, I = Wg.shape
+    k = routing["idx"].shape[1]
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    ce = np.ascontiguousarray([c[0] for c in cols], dtype=np.int32)
+    ci = np.ascontiguousarray([c[1] for c in cols], dtype=np.int32)
+    dX = np.empty((len(tok), H))
+    dWg = np.empty((len(cols), H))
+    dWu = np.empty((len(cols), H))
+    dWd = np.empty((len(cols), H))
+    rc = lib().orc_moe_backward_sampled(
+        _p(x), _p(W_r), _p(Wg), _p(Wu), _p(Wd), _p(dY), T, H, I, E, k,
+        _p(np.ascontiguousarray(routing["idx"], dtype=np.int32)),
+        _p(np.ascontiguousarray(routing["w"], dtype=np.float64)),
+        _p(np.ascontiguousarray(routing["offsets"], dtype=np.int32)),
+        _p(np.ascontiguousarray(routing["row_src"], dtype=np.int32)), mode,
+        _p(tok), len(tok), _p(ce), _p(ci), len(cols), _p(dX), _p(dWg), _p(dWu), _p(dWd))
+    _check(rc, "moe_backward_sampled")
+    return dX, dWg, dWu, dWd

@@ -695,6 +695,164 @@ int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void*
     return ORC_OK;
 }
 
+/* Selected outputs of the backward above, computed one by one (for inputs
+ * too large for the full backward): the same formulas restricted to
+ *   dX rows of the tokens in `tok` (n_tok),
+ *   dW_gate[e][:, i] and dW_up[e][:, i] columns for the (e, i) pairs in
+ *   `col_e`/`col_i` (n_col), and dW_down[e][i][:] rows for the same pairs.
+ * Inputs as in orc_moe_backward (BF16 bits, mode 0 rounds the operands the GPU
+ * stores in BF16). Outputs: dX_s [n_tok, H], dWg_s/dWu_s [n_col, H],
+ * dWd_s [n_col, H]. The router term of dX needs gw for the token's own slots
+ * only, so no other token is touched. */
+static void row_fwd_cols(const double* a, const uint16_t* Wg, const uint16_t* Wu, long base, int H, int I,
+                         int i, double* G, double* U) {
+    double g = 0.0, u = 0.0;
+    for (int hh = 0; hh < H; ++hh) {
+        g += a[hh] * bf16_to_f64(Wg[base + (long)hh * I + i]);
+        u += a[hh] * bf16_to_f64(Wu[base + (long)hh * I + i]);
+    }
+    *G = g;
+    *U = u;
+}
+
+int orc_moe_backward_sampled(const uint16_t* x, const float* W_r, const uint16_t* Wg, const uint16_t* Wu,
+                             const uint16_t* Wd, const uint16_t* dY, int T, int H, int I, int E, int k,
+                             const int32_t* idx, const double* w, const int32_t* offsets, const int32_t* row_src,
+                             int mode, const int32_t* tok, int n_tok, const int32_t* col_e, const int32_t* col_i,
+                             int n_col, double* dX_s, double* dWg_s, double* dWu_s, double* dWd_s) {
+    if (mode != ORC_BF16 && mode != ORC_EXACT) return ORC_ERR;
+    long HI = (long)H * I;
+    /* ---- dX rows */
+    for (int q = 0; q < n_tok; ++q) {
+        int t = tok[q];
+        if (t < 0 || t >= T) return ORC_ERR;
+        double* o = dX_s + (long)q * H;
+        double* gwv = (double*)calloc((size_t)k, sizeof(double));
+        double* a = (double*)malloc(sizeof(double) * H);
+        double* da = (double*)calloc((size_t)k * H, sizeof(double));
+        if (!gwv || !a || !da) return ORC_ERR;
+        for (int h = 0; h < H; ++h) a[h] = bf16_to_f64(x[(long)t * H + h]);
+        for (int j = 0; j < k; ++j) {
+            int e = idx[(long)t * k + j];
+            long base = (long)e * HI;
+            double wj = w[(long)t * k + j];
+            double* G = (double*)malloc(sizeof(double) * I);
+            double* U = (double*)malloc(sizeof(double) * I);
+            double* hb = (double*)malloc(sizeof(double) * I);
+            double* dyr = (double*)malloc(sizeof(double) * H);
+            double* DG = (double*)malloc(sizeof(double) * I);
+            double* DU = (double*)malloc(sizeof(double) * I);
+#pragma omp parallel for schedule(static)
+            for (int i = 0; i < I; ++i) row_fwd_cols(a, Wg, Wu, base, H, I, i, &G[i], &U[i]);
+            for (int i = 0; i < I; ++i) {
+                hb[i] = silu(G[i]) * U[i];
+                if (mode == ORC_BF16) hb[i] = orc_round_bf16(hb[i]);
+            }
+            /* y and gw */
+            double g = 0.0;
+            for (int c = 0; c < H; ++c) {
+                double y = 0.0;
+                for (int i = 0; i < I; ++i) y += hb[i] * bf16_to_f64(Wd[base + (long)i * H + c]);
+                double dYv = bf16_to_f64(dY[(long)t * H + c]);
+                g += dYv * y;
+                dyr[c] = wj * dYv;
+                if (mode == ORC_BF16) dyr[c] = orc_round_bf16(dyr[c]);
+            }
+            gwv[j] = g;
+#pragma omp parallel for schedule(static)
+            for (int i = 0; i < I; ++i) {
+                double dh = 0.0;
+                for (int c = 0; c < H; ++c) dh += dyr[c] * bf16_to_f64(Wd[base + (long)i * H + c]);
+                double sg = 1.0 / (1.0 + exp(-G[i]));
+                double dgv = dh * U[i] * sg * (1.0 + G[i] * (1.0 - sg));
+                double duv = dh * G[i] * sg;
+                if (mode == ORC_BF16) { dgv = orc_round_bf16(dgv); duv = orc_round_bf16(duv); }
+                DG[i] = dgv;
+                DU[i] = duv;
+            }
+#pragma omp parallel for schedule(static)
+            for (int c = 0; c < H; ++c) {
+                double s = 0.0;
+                for (int i = 0; i < I; ++i)
+                    s += DG[i] * bf16_to_f64(Wg[base + (long)c * I + i]) + DU[i] * bf16_to_f64(Wu[base + (long)c * I + i]);
+                da[(long)j * H + c] = s;
+            }
+            free(G); free(U); free(hb); free(dyr); free(DG); free(DU);
+        }
+        double m = 0.0;
+        for (int j = 0; j < k; ++j) m += w[(long)t * k + j] * gwv[j];
+        for (int c = 0; c < H; ++c) {
+            double s = 0.0;
+            for (int j = 0; j < k; ++j) s += da[(long)j * H + c];
+            for (int j = 0; j < k; ++j) {
+                double dl = w[(long)t * k + j] * (gwv[j] - m);
+                s += dl * (double)W_r[(long)c * E + idx[(long)t * k + j]];
+            }
+            o[c] = s;
+        }
+        free(gwv); free(a); free(da);
+    }
+    /* ---- weight-gradient columns / rows */
+    for (int q = 0; q < n_col; ++q) {
+        int e = col_e[q], i = col_i[q];
+        if (e < 0 || e >= E || i < 0 || i >= I) return ORC_ERR;
+        long base = (long)e * HI;
+        int r0 = offsets[e], r1 = offsets[e + 1];
+        double* og = dWg_s + (long)q * H;
+        double* ou = dWu_s + (long)q * H;
+        double* od = dWd_s + (long)q * H;
+        for (int c = 0; c < H; ++c) { og[c] = 0.0; ou[c] = 0.0; od[c] = 0.0; }
+        int nr = r1 - r0;
+        double* DGc = (double*)malloc(sizeof(double) * (nr > 0 ? nr : 1));
+        double* DUc = (double*)malloc(sizeof(double) * (nr > 0 ? nr : 1));
+        double* Hc = (double*)malloc(sizeof(double) * (nr > 0 ? nr : 1));
+        if (!DGc || !DUc || !Hc) return ORC_ERR;
+#pragma omp parallel
+        {
+            double* a = (double*)malloc(sizeof(double) * H);
+#pragma omp for schedule(static)
+            for (int rr = 0; rr < nr; ++rr) {
+                int slot = row_src[r0 + rr];
+                int t = slot / k;
+                for (int h = 0; h < H; ++h) a[h] = bf16_to_f64(x[(long)t * H + h]);
+                double G, U;
+                row_fwd_cols(a, Wg, Wu, base, H, I, i, &G, &U);
+                double hv = silu(G) * U;
+                if (mode == ORC_BF16) hv = orc_round_bf16(hv);
+                double dh = 0.0;
+                for (int c = 0; c < H; ++c) {
+                    double dyv = w[slot] * bf16_to_f64(dY[(long)t * H + c]);
+                    if (mode == ORC_BF16) dyv = orc_round_bf16(dyv);
+                    dh += dyv * bf16_to_f64(Wd[base + (long)i * H + c]);
+                }
+                double sg = 1.0 / (1.0 + exp(-G));
+                double dgv = dh * U * sg * (1.0 + G * (1.0 - sg));
+                double duv = dh * G * sg;
+                if (mode == ORC_BF16) { dgv = orc_round_bf16(dgv); duv = orc_round_bf16(duv); }
+                DGc[rr] = dgv;
+                DUc[rr] = duv;
+                Hc[rr] = hv;
+            }
+            free(a);
+        }
+        /* sums over the expert's rows, row order */
+        for (int rr = 0; rr < nr; ++rr) {
+            int slot = row_src[r0 + rr];
+            int t = slot / k;
+            for (int c = 0; c < H; ++c) {
+                double av = bf16_to_f64(x[(long)t * H + c]);
+                double dyv = w[slot] * bf16_to_f64(dY[(long)t * H + c]);
+                if (mode == ORC_BF16) dyv = orc_round_bf16(dyv);
+                og[c] += av * DGc[rr];
+                ou[c] += av * DUc[rr];
+                od[c] += Hc[rr] * dyv;
+            }
+        }
+        free(DGc); free(DUc); free(Hc);
+    }
+    return ORC_OK;
+}
+
 /* Number of threads the OpenMP runtime will use. */
 int orc_num_threads(void) {
 #ifdef _OPENMP

@@ -443,3 +443,19 @@ def test_backward_matches_torch_autograd():
     (out * torch.tensor(dY)).sum().backward()
     for mine, ref in zip(got, (tx.grad, tWg.grad, tWu.grad, tWd.grad, tWr.grad)):
         assert np.allclose(mine, ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_sampled_backward_equals_full_backward():
+    """The one-by-one backward gives the same numbers as the full backward."""
+    wl = synth.small("t", T=40, H=64, I=32, E=4, k=2, backward=True)
+    inp = synth.make_inputs(wl, seed=31)
+    r = oracle.route(inp.x, inp.W_r, 2)
+    dX, dWg, dWu, dWd, dWr = oracle.moe_backward(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r)
+    toks = [0, 17, 39]
+    cols = [(0, 3), (3, 31), (1, 0)]
+    sX, sG, sU, sD = oracle.moe_backward_sampled(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, toks, cols)
+    assert np.allclose(sX, dX[toks], rtol=1e-12, atol=1e-15)
+    for q, (e, i) in enumerate(cols):
+        assert np.allclose(sG[q], dWg[e][:, i], rtol=1e-12, atol=1e-15)
+        assert np.allclose(sU[q], dWu[e][:, i], rtol=1e-12, atol=1e-15)
+        assert np.allclose(sD[q], dWd[e][i, :], rtol=1e-12, atol=1e-15)
