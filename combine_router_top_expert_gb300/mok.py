@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID", 2: "MOK_ERR_CUDA", 3: "MOK_ER
 EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_size", "mok_pack_weights",
            "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
-           "mok_version"]
+           "mok_version", "mok_route_layout_static"]
 
 
 class MokError(RuntimeError):
@@ -83,6 +83,7 @@ def lib():
             L.mok_route_workspace_size.argtypes = [I32] * 4
             L.mok_route_workspace_size.restype = SZ
             L.mok_route_layout.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P]
+            L.mok_route_layout_static.argtypes = [P, P, P, I32, I32, I32, I32, P, P, P, P, P, P, P]
             L.mok_packed_weights_size.argtypes = [I32] * 4
             L.mok_packed_weights_size.restype = SZ
             L.mok_pack_weights.argtypes = [I32, I32, I32, I32, P, P, P, P, SZ, P]
@@ -101,7 +102,7 @@ def lib():
             L.mok_status_string.argtypes = [I32]
             L.mok_status_string.restype = ctypes.c_char_p
             L.mok_version.restype = ctypes.c_char_p
-            for name in ("mok_route_layout", "mok_pack_weights", "mok_moe_forward", "mok_dispatch",
+            for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward", "mok_dispatch",
                          "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -191,6 +192,30 @@ def route_layout(x, W_r, k, bias=None, out=None, workspace=None, stream=None):
                                 _ptr(out["row_src"]), _ptr(out["slot_row"]), _ptr(workspace),
                                 workspace.numel(), _stream(stream))
     _check(rc, "mok_route_layout")
+    return out
+
+
+ROUTE_STATIC_SCRATCH_BYTES = 8 << 20  # MOK_ROUTE_STATIC_SCRATCH_BYTES
+
+
+def route_layout_static(x, W_r, k, bias=None, out=None, stream=None):
+    """Routing with the library's own scratch array: no workspace argument,
+    nothing allocated by the library (the outputs are still the caller's)."""
+    _bf16(x)
+    T, H = x.shape
+    E = W_r.shape[1]
+    dev = x.device
+    if out is None:
+        out = dict(topk_idx=torch.empty((T, k), dtype=torch.int32, device=dev),
+                   topk_w=torch.empty((T, k), dtype=torch.float32, device=dev),
+                   counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   row_src=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev),
+                   slot_row=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev))
+    rc = lib().mok_route_layout_static(_ptr(x), _ptr(W_r), _ptr(bias), T, H, E, k, _ptr(out["topk_idx"]),
+                                       _ptr(out["topk_w"]), _ptr(out["counts"]), _ptr(out["offsets"]),
+                                       _ptr(out["row_src"]), _ptr(out["slot_row"]), _stream(stream))
+    _check(rc, "mok_route_layout_static")
     return out
 
 

@@ -231,6 +231,41 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
                             const mok_config* cfg, mok_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* Routing without a caller workspace. The pages have no counterpart: this    */
+/* entry point exists for callers of this library that cannot allocate.       */
+/* ------------------------------------------------------------------------- */
+
+/* Size of the device scratch array owned by the library (8 MiB). Every GPU
+ * that loads libmok.so holds one such array until the process exits. */
+#define MOK_ROUTE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* Same computation, arguments and outputs as mok_route_layout, minus the
+ * workspace: the scratch (transposed router weights and per-block expert
+ * histograms, mok_route_workspace_size bytes) lives in a file-scope device
+ * array of MOK_ROUTE_STATIC_SCRATCH_BYTES inside the library. For callers that
+ * cannot allocate device memory themselves - e.g. code that must route every
+ * allocation through a host framework's allocator it cannot reach, plugins in
+ * processes whose device memory is already fully reserved, or hot paths where
+ * allocating is not allowed. It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Problems whose scratch exceeds the array (mok_route_workspace_size(T, H,
+ *     E, k) > MOK_ROUTE_STATIC_SCRATCH_BYTES; e.g. E*H*4 bytes of transposed
+ *     router weights must fit) return MOK_ERR_INVALID; nothing is enqueued.
+ *   - All calls on a device share that device's array, which keeps the last
+ *     call's contents; the kernels overwrite every byte they read, so nothing
+ *     needs clearing, but calls that overlap on the same GPU (e.g. issued on
+ *     different streams without ordering) race on the array: order them on
+ *     one stream or with events. */
+mok_status mok_route_layout_static(const void* x, const float* W_r, const float* bias,
+                                   int32_t T, int32_t H, int32_t E, int32_t k,
+                                   int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                   int32_t* offsets, int32_t* row_src, int32_t* slot_row,
+                                   mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Device status                                                               */
 /* ------------------------------------------------------------------------- */
 
