@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -45,18 +46,6 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
     return r == CUDA_SUCCESS;
 }
 
-void ensure_smem_attr(const void* func, int bytes) {
-    static std::mutex mu;
-    static std::set<std::pair<int, const void*>> done;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> g(mu);
-    auto key = std::make_pair(dev, func);
-    if (done.count(key)) return;
-    cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    done.insert(key);
-}
-
 template <int BN, bool MX, bool MN, int EPI, int S, int ACC>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
                 int64_t tiles_ub, int num_sms, cudaStream_t s) {
@@ -81,6 +70,21 @@ GemmParams base_params(const GemmCommon& c) {
 int64_t mtiles_ub(int64_t rows, int E) { return (rows + kTileM - 1) / kTileM + E; }
 
 }  // namespace
+
+void ensure_smem_attr(const void* func, int bytes) {
+    // The limit is raised whenever a launch needs more than any earlier one
+    // (kernels whose shared memory depends on the problem, e.g. the router).
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> limit;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> g(mu);
+    auto key = std::make_pair(dev, func);
+    auto it = limit.find(key);
+    if (it != limit.end() && it->second >= bytes) return;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess)
+        limit[key] = bytes;
+}
 
 cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
                         int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows, void* h,

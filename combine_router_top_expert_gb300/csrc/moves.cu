@@ -392,13 +392,21 @@ cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* 
     if (stage == 0) {
         gate_grad_kernel<<<ceil_div(T * k, 8), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dY),
                                                             static_cast<const __nv_bfloat16*>(partials), T, H, k, gw);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         router_dlogit_kernel<<<ceil_div(T, 128), 128, 0, s>>>(w, gw, T, k, dl);
     } else {
         dx_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(da), dl, idx, WrT, H, k,
                                     static_cast<__nv_bfloat16*>(dX));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         dl_scatter_kernel<<<ceil_div(T, 128), 128, 0, s>>>(dl, idx, T, E, k, dl_full);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         dwr_partial_kernel<<<dim3(ceil_div(H, 256), kDwrSplits), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
                                                                                dl_full, T, H, E, part);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         dwr_reduce_kernel<<<ceil_div(H * E, 256), 256, 0, s>>>(part, H, E, dWr);
     }
     return cudaGetLastError();

@@ -30,6 +30,9 @@ cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* 
 int64_t dwr_partial_floats(int H, int E);
 
 // gemm.cu
+// Raise a kernel's dynamic shared memory limit (per device) to at least `bytes`.
+void ensure_smem_attr(const void* func, int bytes);
+
 struct GemmCommon {
     StatusBlock* status;
     unsigned long long timeout_ns;

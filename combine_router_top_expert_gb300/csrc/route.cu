@@ -11,8 +11,6 @@
 //                       per-block expert histogram
 //   route_layout_kernel counts, offsets, and the stable (expert, token)
 //                       permutation row_src / slot_row
-#include <mutex>
-
 #include "common.cuh"
 #include "moves.cuh"
 
@@ -42,10 +40,22 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
     return va > vb || (va == vb && ea < eb);
 }
 
+// 16-byte global -> shared copy that bypasses L1; `bytes` = 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // One CTA = kRouteTT tokens x all experts. Warp w owns experts
 // eg + 4w .. eg + 4w + 3 of each 32-expert group eg; lane c owns summation
-// chain c (h = 256*i + 8*c + m). Dynamic shared memory:
-//   xs [kRouteTT][256] bf16 | ws [32][256] f32 | lg [kRouteTT][E] f32 |
+// chain c (h = 256*i + 8*c + m). The x and router-weight chunks of 256 h
+// values stream through a double-buffered shared-memory pipeline (cp.async),
+// so chunk i+1 is in flight while chunk i is multiplied. Dynamic shared
+// memory:
+//   xs [2][kRouteTT][256] bf16 | ws [2][32][256] f32 | lg [kRouteTT][E] f32 |
 //   slog [kRouteTT][k] f32 | cnt [E] i32
 __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ WrT,
@@ -53,16 +63,37 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist) {
     extern __shared__ __align__(16) unsigned char route_smem[];
     __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(route_smem);
-    float* ws = reinterpret_cast<float*>(route_smem + kRouteTT * kRouteChunk * 2);
-    float* lg = ws + 32 * kRouteChunk;
+    float* ws = reinterpret_cast<float*>(route_smem + 2 * kRouteTT * kRouteChunk * 2);
+    float* lg = ws + 2 * 32 * kRouteChunk;
     float* slog = lg + kRouteTT * E;
     int32_t* cnt = reinterpret_cast<int32_t*>(slog + kRouteTT * k);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * kRouteTT;
     const int ntok = min(kRouteTT, T - t0);
+    const int nchunks = ceil_div(H, kRouteChunk);
 
     for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+
+    // issue the copies of chunk c (expert group eg) into buffer b
+    auto load_chunk = [&](int eg, int c, int b) {
+        const int h0 = c * kRouteChunk;
+        __nv_bfloat16* xb = xs + b * kRouteTT * kRouteChunk;
+        float* wb = ws + b * 32 * kRouteChunk;
+        for (int v = tid; v < kRouteTT * (kRouteChunk / 8); v += kRouteThreads) {
+            const int t = v / (kRouteChunk / 8), c8 = (v % (kRouteChunk / 8)) * 8;
+            const bool ok = t < ntok && h0 + c8 < H;
+            const __nv_bfloat16* src = ok ? x + (int64_t)(t0 + t) * H + h0 + c8 : x;
+            cp_async16(xb + t * kRouteChunk + c8, src, ok ? 16 : 0);
+        }
+        for (int v = tid; v < 32 * (kRouteChunk / 4); v += kRouteThreads) {
+            const int e = v / (kRouteChunk / 4), c4 = (v % (kRouteChunk / 4)) * 4;
+            const bool ok = eg + e < E && h0 + c4 < H;
+            const float* src = ok ? WrT + (int64_t)(eg + e) * H + h0 + c4 : WrT;
+            cp_async16(wb + e * kRouteChunk + c4, src, ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
 
     for (int eg = 0; eg < E; eg += 32) {
         float acc[kRouteTT][4];
@@ -71,37 +102,31 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
 
-        for (int h0 = 0; h0 < H; h0 += kRouteChunk) {
-            __syncthreads();
-            // x chunk: kRouteTT rows x 256 bf16, 16-byte vectors (H % 8 == 0)
-            for (int v = tid; v < kRouteTT * (kRouteChunk / 8); v += kRouteThreads) {
-                int t = v / (kRouteChunk / 8), c8 = (v % (kRouteChunk / 8)) * 8;
-                uint4 val = make_uint4(0, 0, 0, 0);
-                if (t < ntok && h0 + c8 < H)
-                    val = *reinterpret_cast<const uint4*>(x + (int64_t)(t0 + t) * H + h0 + c8);
-                *reinterpret_cast<uint4*>(xs + t * kRouteChunk + c8) = val;
-            }
-            // router weight chunk: 32 experts x 256 floats
-            for (int v = tid; v < 32 * (kRouteChunk / 4); v += kRouteThreads) {
-                int e = v / (kRouteChunk / 4), c4 = (v % (kRouteChunk / 4)) * 4;
-                float4 val = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (eg + e < E && h0 + c4 < H)
-                    val = *reinterpret_cast<const float4*>(WrT + (int64_t)(eg + e) * H + h0 + c4);
-                *reinterpret_cast<float4*>(ws + e * kRouteChunk + c4) = val;
+        __syncthreads();  // buffers free (previous expert group done)
+        load_chunk(eg, 0, 0);
+        for (int c = 0; c < nchunks; ++c) {
+            if (c + 1 < nchunks) {
+                load_chunk(eg, c + 1, (c + 1) & 1);
+                cp_async_wait<1>();
+            } else {
+                cp_async_wait<0>();
             }
             __syncthreads();
+            const int h0 = c * kRouteChunk;
+            const __nv_bfloat16* xb = xs + (c & 1) * kRouteTT * kRouteChunk;
+            const float* wb = ws + (c & 1) * 32 * kRouteChunk;
             if (h0 + 8 * lane < H) {
                 float wv[4][8];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float4 a = *reinterpret_cast<const float4*>(ws + (4 * warp + q) * kRouteChunk + 8 * lane);
-                    float4 b = *reinterpret_cast<const float4*>(ws + (4 * warp + q) * kRouteChunk + 8 * lane + 4);
+                    float4 a = *reinterpret_cast<const float4*>(wb + (4 * warp + q) * kRouteChunk + 8 * lane);
+                    float4 b = *reinterpret_cast<const float4*>(wb + (4 * warp + q) * kRouteChunk + 8 * lane + 4);
                     wv[q][0] = a.x; wv[q][1] = a.y; wv[q][2] = a.z; wv[q][3] = a.w;
                     wv[q][4] = b.x; wv[q][5] = b.y; wv[q][6] = b.z; wv[q][7] = b.w;
                 }
 #pragma unroll
                 for (int t = 0; t < kRouteTT; ++t) {
-                    uint4 xv = *reinterpret_cast<const uint4*>(xs + t * kRouteChunk + 8 * lane);
+                    uint4 xv = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * lane);
                     float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
                                    bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
@@ -110,6 +135,7 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
                         for (int m = 0; m < 8; ++m) acc[t][q] = fmaf(xf[m], wv[q][m], acc[t][q]);
                 }
             }
+            __syncthreads();  // buffer (c & 1) may be refilled by the next iteration
         }
         // butterfly across the 32 chains, then the bias
 #pragma unroll
@@ -173,7 +199,7 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 }
 
 size_t route_topk_smem_bytes(int E, int k) {
-    return (size_t)kRouteTT * kRouteChunk * 2 + 32 * kRouteChunk * 4 + (size_t)kRouteTT * E * 4 +
+    return (size_t)2 * kRouteTT * kRouteChunk * 2 + 2 * 32 * kRouteChunk * 4 + (size_t)kRouteTT * E * 4 +
            (size_t)kRouteTT * k * 4 + (size_t)E * 4;
 }
 
@@ -232,12 +258,14 @@ route_layout_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     }
     for (int i = tid; i < ntok * k; i += kRouteThreads) {
         int t = i / k;
-        sel[t][topk_idx[(int64_t)t0 * k + i]] = 1;
+        const int e = topk_idx[(int64_t)t0 * k + i];
+        if ((unsigned)e < (unsigned)E) sel[t][e] = 1;
     }
     __syncthreads();
     for (int i = tid; i < ntok * k; i += kRouteThreads) {
         int t = i / k;
         int e = topk_idx[(int64_t)t0 * k + i];
+        if ((unsigned)e >= (unsigned)E) continue;   // never produced by the top-k kernel
         int rank = 0;
         for (int tt = 0; tt < t; ++tt) rank += sel[tt][e];
         int row = off[e] + pre[e] + rank;
@@ -270,11 +298,15 @@ cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bi
         return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
     }
     transpose_wr_kernel<<<dim3(ceil_div(H, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(W_r, WrT, H, E);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     size_t smem = route_topk_smem_bytes(E, k);
-    if (smem > 48 * 1024)
-        cudaFuncSetAttribute(route_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(route_topk_kernel), (int)smem);
     route_topk_kernel<<<nblocks, kRouteThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(x), WrT, bias, T, H, E,
                                                         k, topk_idx, topk_w, hist);
+    // the layout kernel must never run on top-k results that were not produced
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
     route_layout_kernel<<<nblocks, kRouteThreads, 0, s>>>(topk_idx, hist, T, E, k, nblocks, counts, offsets,
                                                           row_src, slot_row);
     return cudaGetLastError();
