@@ -4,6 +4,7 @@
 
 #include "common.cuh"
 #include "moves.cuh"
+#include "plan.cuh"
 
 using namespace mok;
 
@@ -106,6 +107,39 @@ BwdLayout bwd_layout(const mok_problem* p) {
 
 mok_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
 
+constexpr int kDefaultMovers = 8;
+
+// Megakernel tile width: both GEMMs use the same N-tile (BF16 256, MXFP8 128).
+bool mega_supported(const mok_problem* p) {
+    const int BN = p->dtype == MOK_MXFP8 ? 128 : 256;
+    return p->H % BN == 0 && (2 * p->I) % BN == 0;
+}
+
+int mega_region_rows(const mok_problem* p, const mok_config* cfg) {
+    if (cfg && cfg->ring_rows > 0) return (cfg->ring_rows / 2) / kTileM * kTileM;
+    return (int)align_up(padded_rows_max(p->T, p->E, p->k), kTileM);
+}
+
+struct MegaLayout {
+    size_t scratch, partials, shared, hs, total;
+};
+
+MegaLayout mega_layout(const mok_problem* p, int nbatch, const mok_config* cfg) {
+    MegaLayout L{};
+    size_t o = kStatusBytes;
+    L.scratch = o;
+    o += align_up(mega_scratch_bytes(nbatch, p->T, p->H, p->I, p->E, p->k, mega_region_rows(p, cfg),
+                                     p->dtype == MOK_MXFP8), 1024);
+    L.partials = o;
+    o += (size_t)nbatch * align_up((int64_t)p->T * p->k * p->H * 2, 1024);
+    L.shared = o;
+    if (p->I_shared > 0) o += (size_t)nbatch * align_up((int64_t)p->T * p->H * 4, 1024);
+    L.hs = o;
+    if (p->I_shared > 0) o += align_up((int64_t)p->T * p->I_shared * 2, 1024);
+    L.total = o;
+    return L;
+}
+
 GemmCommon make_common(void* ws, const mok_config* cfg) {
     GemmCommon c{};
     c.status = static_cast<StatusBlock*>(ws);
@@ -201,11 +235,16 @@ size_t mok_saved_size(const mok_problem* p) {
 }
 
 size_t mok_workspace_size(const mok_problem* p, const mok_config* cfg) {
-    (void)cfg;
     if (!problem_ok(p)) return 0;
     size_t f = fwd_layout(p, false).total;
     size_t b = p->dtype == MOK_BF16 ? bwd_layout(p).total : 0;
-    return std::max(f, b);
+    size_t m = mega_supported(p) ? mega_layout(p, 1, cfg).total : 0;
+    return std::max(std::max(f, b), m);
+}
+
+size_t mok_workspace_size_batches(const mok_problem* p, int32_t nbatch, const mok_config* cfg) {
+    if (!problem_ok(p) || nbatch < 1 || nbatch > kMaxBatches || !mega_supported(p)) return 0;
+    return mega_layout(p, nbatch, cfg).total;
 }
 
 mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
@@ -250,6 +289,80 @@ mok_status mok_combine(const mok_problem* p, const void* partials, const float* 
     return cuda_status(launch_combine(partials, topk_w, shared, out, p->T, p->H, p->k, (cudaStream_t)stream));
 }
 
+static mok_status forward_mega(const mok_problem* p, int32_t nbatch, const mok_fwd_args* a,
+                               const mok_config* cfg, mok_stream_t stream) {
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool mx = p->dtype == MOK_MXFP8;
+    char* ws = static_cast<char*>(a[0].workspace);
+    MegaLayout ML = mega_layout(p, nbatch, cfg);
+    cudaError_t e = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+    if (p->T == 0 || e != cudaSuccess) return cuda_status(e);
+    GemmCommon c = make_common(ws, cfg);
+    const int movers = (cfg && cfg->mover_ctas > 0) ? cfg->mover_ctas : kDefaultMovers;
+    if (movers >= c.num_sms) return MOK_ERR_INVALID;
+    // shared expert first (BF16 tensor-core GEMMs over every token)
+    const float* shared[kMaxBatches] = {};
+    if (p->I_shared > 0) {
+        PackedLayout SL = packed_layout(1, p->H, p->I_shared, MOK_BF16);
+        const char* sp = static_cast<const char*>(a[0].packed_shared);
+        void* hs = ws + ML.hs;
+        for (int b = 0; b < nbatch && e == cudaSuccess; ++b) {
+            float* sh = reinterpret_cast<float*>(ws + ML.shared + (size_t)b * align_up((int64_t)p->T * p->H * 4, 1024));
+            shared[b] = sh;
+            e = gemm_gateup(false, a[b].x, nullptr, sp + SL.gu, nullptr, 1, p->H, p->I_shared, nullptr, p->T, p->T, hs,
+                            nullptr, nullptr, c, s);
+            if (e == cudaSuccess)
+                e = gemm_down(false, hs, nullptr, sp + SL.dn, nullptr, 1, p->H, p->I_shared, nullptr, nullptr,
+                              nullptr, p->T, p->T, sh, c, s);
+        }
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    PackedLayout PL = packed_layout(p->E, p->H, p->I, p->dtype);
+    const char* pk = static_cast<const char*>(a[0].packed);
+    MegaLaunch L{};
+    L.mx = mx;
+    L.E = p->E; L.H = p->H; L.I = p->I; L.k = p->k; L.T = p->T; L.nbatch = nbatch;
+    for (int b = 0; b < nbatch; ++b) {
+        L.x[b] = a[b].x;
+        L.offsets[b] = a[b].routing.offsets;
+        L.row_src[b] = a[b].routing.row_src;
+        L.topk_w[b] = a[b].routing.topk_w;
+        L.partials[b] = ws + ML.partials + (size_t)b * align_up((int64_t)p->T * p->k * p->H * 2, 1024);
+        L.shared[b] = shared[b];
+        L.out[b] = a[b].out;
+    }
+    L.gu = pk + PL.gu;
+    L.dn = pk + PL.dn;
+    L.gu_sf = mx ? reinterpret_cast<const uint8_t*>(pk + PL.gu_sf) : nullptr;
+    L.dn_sf = mx ? reinterpret_cast<const uint8_t*>(pk + PL.dn_sf) : nullptr;
+    L.scratch = ws + ML.scratch;
+    L.region_rows = mega_region_rows(p, cfg);
+    L.max_tokens = (cfg && cfg->minibatch_tokens > 0) ? cfg->minibatch_tokens : p->T;
+    L.n_movers = movers;
+    L.grid = c.num_sms;
+    L.test_flags = cfg ? cfg->flags : 0;
+    L.status = c.status;
+    L.timeout_ns = c.timeout_ns;
+    return cuda_status(launch_mega(L, s));
+}
+
+mok_status mok_moe_forward_batches(const mok_problem* p, int32_t nbatch, const mok_fwd_args* a,
+                                   const mok_config* cfg, mok_stream_t stream) {
+    if (!problem_ok(p) || !a || nbatch < 1 || nbatch > kMaxBatches || !mega_supported(p)) return MOK_ERR_INVALID;
+    if (!a[0].packed || !a[0].workspace || (p->I_shared > 0) != (a[0].packed_shared != nullptr))
+        return MOK_ERR_INVALID;
+    if (a[0].ws_bytes < mok_workspace_size_batches(p, nbatch, cfg) || !aligned(a[0].workspace, 1024) ||
+        !aligned(a[0].packed, 256))
+        return MOK_ERR_INVALID;
+    for (int b = 0; b < nbatch; ++b) {
+        if (!routing_ok(&a[b].routing) || !a[b].out || a[b].saved) return MOK_ERR_INVALID;
+        if (p->T > 0 && (!a[b].x || !aligned(a[b].x, 16) || !aligned(a[b].out, 16))) return MOK_ERR_INVALID;
+    }
+    if (mega_region_rows(p, cfg) < kTileM) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return forward_mega(p, nbatch, a, cfg, stream);
+}
+
 mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mok_config* cfg,
                            mok_stream_t stream) {
     if (!problem_ok(p) || !a || !routing_ok(&a->routing) || !a->packed || !a->out || !a->workspace)
@@ -264,6 +377,10 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
         return MOK_ERR_INVALID;
     if (p->I_shared > 0 && !aligned(a->packed_shared, 256)) return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;
+    if (!training && !(cfg && (cfg->flags & MOK_FLAG_STAGED)) && mega_supported(p)) {
+        if (mega_region_rows(p, cfg) < kTileM) return MOK_ERR_INVALID;
+        return forward_mega(p, 1, a, cfg, stream);
+    }
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = static_cast<char*>(a->workspace);
     char* sv = static_cast<char*>(a->saved);

@@ -43,7 +43,7 @@ class MoELayer:
     def problem(self, T) -> mok.Problem:
         return mok.make_problem(T, self.H, self.I, self.E, self.k, self.dtype, self.I_shared)
 
-    def buffers(self, T, training=False):
+    def buffers(self, T, training=False, cfg=None):
         key = (T, training)
         if key not in self._bufs:
             p = self.problem(T)
@@ -55,7 +55,7 @@ class MoELayer:
                              offsets=torch.empty(self.E + 1, dtype=torch.int32, device=self.device),
                              row_src=torch.empty(max(T * self.k, 1), dtype=torch.int32, device=self.device),
                              slot_row=torch.empty(max(T * self.k, 1), dtype=torch.int32, device=self.device)),
-                ws=mok.alloc_bytes(mok.workspace_size(p), self.device),
+                ws=mok.alloc_bytes(mok.workspace_size(p, cfg), self.device),
                 out=torch.empty((max(T, 1), self.H), dtype=torch.bfloat16, device=self.device),
             )
             if training:
@@ -69,9 +69,11 @@ class MoELayer:
                                 stream=stream)
 
     def forward(self, x, training=False, cfg=None, stream=None, route=True):
-        """out [T, H] bf16 (a view of a reused buffer)."""
+        """out [T, H] bf16 (a view of a reused buffer). Inference runs the
+        megakernel unless cfg has FLAG_STAGED (or the shape needs the staged
+        path); training runs the staged kernels and keeps activations."""
         T = x.shape[0]
-        b = self.buffers(T, training)
+        b = self.buffers(T, training, cfg)
         if route:
             self.route(x, training, stream)
         mok.moe_forward(self.problem(T), x, self.packed, b["routing"], b["out"], b["ws"],

@@ -25,7 +25,10 @@ STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID", 2: "MOK_ERR_CUDA", 3: "MOK_ER
 EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_size", "mok_pack_weights",
            "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
-           "mok_version", "mok_route_layout_static"]
+           "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches"]
+
+FLAG_STAGED = 1
+FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 
 class MokError(RuntimeError):
@@ -41,7 +44,8 @@ class Problem(ctypes.Structure):
 
 class Config(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("timeout_ms", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("mover_ctas", ctypes.c_int32), ("minibatch_tokens", ctypes.c_int32), ("ring_rows", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class Routing(ctypes.Structure):
@@ -92,6 +96,9 @@ def lib():
             L.mok_saved_size.argtypes = [PP]
             L.mok_saved_size.restype = SZ
             L.mok_moe_forward.argtypes = [PP, ctypes.POINTER(FwdArgs), PC, P]
+            L.mok_moe_forward_batches.argtypes = [PP, I32, ctypes.POINTER(FwdArgs), PC, P]
+            L.mok_workspace_size_batches.argtypes = [PP, I32, PC]
+            L.mok_workspace_size_batches.restype = SZ
             L.mok_padded_rows_max.argtypes = [I32, I32, I32]
             L.mok_padded_rows_max.restype = ctypes.c_int64
             L.mok_dispatch.argtypes = [PP, P, PR, P, P, P]
@@ -102,7 +109,8 @@ def lib():
             L.mok_status_string.argtypes = [I32]
             L.mok_status_string.restype = ctypes.c_char_p
             L.mok_version.restype = ctypes.c_char_p
-            for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward", "mok_dispatch",
+            for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
+                         "mok_moe_forward_batches", "mok_dispatch",
                          "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -132,8 +140,8 @@ def make_problem(T, H, I, E, k, dtype=BF16, I_shared=0) -> Problem:
     return Problem(T, H, I, E, k, dtype, I_shared)
 
 
-def make_config(num_sms=0, timeout_ms=0, flags=0) -> Config:
-    return Config(num_sms, timeout_ms, flags)
+def make_config(num_sms=0, timeout_ms=0, flags=0, mover_ctas=0, minibatch_tokens=0, ring_rows=0) -> Config:
+    return Config(num_sms, timeout_ms, flags, mover_ctas, minibatch_tokens, ring_rows)
 
 
 # --------------------------------------------------------------------------- sizes
@@ -148,6 +156,10 @@ def packed_weights_size(E, H, I, dtype) -> int:
 
 def workspace_size(p: Problem, cfg: Config | None = None) -> int:
     return int(lib().mok_workspace_size(ctypes.byref(p), ctypes.byref(cfg) if cfg else None))
+
+
+def workspace_size_batches(p: Problem, nbatch: int, cfg: Config | None = None) -> int:
+    return int(lib().mok_workspace_size_batches(ctypes.byref(p), nbatch, ctypes.byref(cfg) if cfg else None))
 
 
 def saved_size(p: Problem) -> int:
@@ -245,6 +257,21 @@ def moe_forward(p: Problem, x, packed, routing, out, workspace, saved=None, pack
     rc = lib().mok_moe_forward(ctypes.byref(p), ctypes.byref(a), ctypes.byref(cfg) if cfg else None, _stream(stream))
     _check(rc, "mok_moe_forward")
     return out
+
+
+def moe_forward_batches(p: Problem, xs, packed, routings, outs, workspace, packed_shared=None,
+                        cfg: Config | None = None, stream=None):
+    """One megakernel launch over len(xs) macro-batches (same weights)."""
+    n = len(xs)
+    arr = (FwdArgs * n)()
+    for b in range(n):
+        arr[b] = FwdArgs(xs[b].data_ptr(), packed.data_ptr(),
+                         packed_shared.data_ptr() if packed_shared is not None else None,
+                         routing_struct(routings[b]), outs[b].data_ptr(), None, workspace.data_ptr(),
+                         workspace.numel())
+    rc = lib().mok_moe_forward_batches(ctypes.byref(p), n, arr, ctypes.byref(cfg) if cfg else None, _stream(stream))
+    _check(rc, "mok_moe_forward_batches")
+    return outs
 
 
 def moe_backward(p: Problem, x, W_r, Wg, Wu, Wd, packed, dY, routing, saved, grads, workspace,

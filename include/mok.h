@@ -65,13 +65,28 @@ typedef struct {
     int32_t I_shared;
 } mok_problem;
 
-/* Execution knobs. Zero-initialise for defaults. */
+/* Execution knobs. Zero-initialise for defaults. The megakernel's SM split,
+ * minibatch size and ring size are explicit parameters, as the pages set
+ * them per shape ([K-ja] 02 and 03). */
 typedef struct {
-    int32_t num_sms;         /* SMs the persistent kernels may use; 0 = all */
-    int32_t timeout_ms;      /* limit of every device-side wait; 0 = 4000 */
-    int32_t flags;           /* MOK_FLAG_* */
-    int32_t reserved[5];
+    int32_t num_sms;          /* SMs the persistent kernels may use; 0 = all */
+    int32_t timeout_ms;       /* limit of every device-side wait; 0 = 4000 */
+    int32_t flags;            /* MOK_FLAG_* */
+    int32_t mover_ctas;       /* megakernel: SMs that move tokens; 0 = 8 */
+    int32_t minibatch_tokens; /* megakernel: most tokens per minibatch; 0 = as many as a ring region holds */
+    int32_t ring_rows;        /* megakernel: ring token buffer rows, split in two regions;
+                                 0 = two regions of mok_padded_rows_max rows each */
+    int32_t reserved[2];
 } mok_config;
+
+/* Run the forward as separate stage kernels (dispatch, grouped GEMMs,
+ * combine) instead of the persistent megakernel. */
+#define MOK_FLAG_STAGED 1
+/* Test hook: a mover withholds the publish of the last 8-row chunk of the
+ * first minibatch, so the tiles waiting for it give up after timeout_ms and
+ * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use
+ * in production). */
+#define MOK_FLAG_TEST_WITHHOLD_PUBLISH 256
 
 /* ------------------------------------------------------------------------- */
 /* Router, top-k and layout ([K-ja] 01: count each expert's tokens, place each */
@@ -143,8 +158,11 @@ typedef struct {
     size_t ws_bytes;
 } mok_fwd_args;
 
-/* Workspace bytes of mok_moe_forward / mok_moe_backward for this problem. */
+/* Workspace bytes of mok_moe_forward / mok_moe_backward for this problem
+ * (either forward path, one batch). */
 size_t mok_workspace_size(const mok_problem* p, const mok_config* cfg);
+/* Workspace bytes of mok_moe_forward_batches for nbatch macro-batches. */
+size_t mok_workspace_size_batches(const mok_problem* p, int32_t nbatch, const mok_config* cfg);
 /* Bytes of the saved context (BF16 training forward only). */
 size_t mok_saved_size(const mok_problem* p);
 
@@ -153,10 +171,31 @@ size_t mok_saved_size(const mok_problem* p);
  * (+MXFP8 quantisation of h), grouped down GEMM whose epilogue pushes each
  * row to its (token, slot) partial, then out[t] = bf16(sum_{j=0..k-1}
  * w[t,j] * y[t,j] (+ shared[t])) in fp32 with j ascending. Bitwise
- * deterministic. `saved` != NULL keeps the activations the backward needs
- * (BF16 only; MOK_ERR_UNSUPPORTED for MXFP8). */
+ * deterministic, and the same bits on either path.
+ * Inference (saved == NULL) runs the persistent megakernel ([K-ja] 02): one
+ * cooperative launch whose first cfg->mover_ctas CTAs gather minibatches into
+ * a two-region ring while the other CTAs run the tensor-core tiles; the two
+ * sides synchronise through GPU-local counters only. It needs every SM of the
+ * device (the launch fails with MOK_ERR_CUDA if they cannot all be resident)
+ * and tile widths that divide H and 2I (256 for BF16, 128 for MXFP8); other
+ * shapes use the staged path. MOK_FLAG_STAGED, or `saved` != NULL (training:
+ * keeps the activations the backward needs; BF16 only, MOK_ERR_UNSUPPORTED
+ * for MXFP8), runs the stage kernels in sequence instead. The device status
+ * reports MOK_ERR_CAPACITY if a ring region cannot hold the padded rows of
+ * 16 tokens. */
 mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a,
                            const mok_config* cfg, mok_stream_t stream);
+
+/* Macro-batch streaming ([K-ja] 02, ring token buffer): nbatch <= 32
+ * independent batches of p->T tokens each (a[b].x, a[b].routing, a[b].out),
+ * the same weights (a[0].packed / packed_shared) and one workspace
+ * (a[0].workspace, mok_workspace_size_batches bytes), through ONE megakernel
+ * launch: minibatches of consecutive batches flow through the same ring, so
+ * the weighted sums of batch b overlap the dispatch of batch b+1. The shared
+ * expert (if any) runs as tensor-core GEMMs before the megakernel, for all
+ * batches. Inference only (a[b].saved must be NULL). */
+mok_status mok_moe_forward_batches(const mok_problem* p, int32_t nbatch, const mok_fwd_args* a,
+                                   const mok_config* cfg, mok_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* The forward's stages as separate calls (same kernels), for tests and for   */

@@ -1,0 +1,149 @@
+"""The persistent forward megakernel (mover / compute SM split, GPU-local
+counters, minibatches through a two-region ring).
+
+It runs the same tile shapes and the same arithmetic as the staged kernels,
+so its output must be bit-identical to theirs for every minibatch size, ring
+size and mover count (the result must not depend on how the work is cut),
+and within tolerance of the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_router_top_expert_gb300 import mok, synth
+from helpers import TOL, assert_close, dtype_of, host_bf16_f64, layer_for, to_dev_bf16
+
+CASES = [
+    synth.small("mega_bf16", T=1000, H=512, I=256, E=8, k=2),
+    synth.small("mega_bf16_skew", T=600, H=256, I=2048, E=8, k=4, zipf_s=1.2),
+    synth.small("mega_mx", T=1000, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
+    synth.small("mega_mx_k8", T=300, H=1024, I=512, E=32, k=8, dtype="mxfp8"),
+]
+
+
+def _forward(layer, x, cfg, T):
+    p = layer.problem(T)
+    b = layer.buffers(T)
+    ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
+    out = torch.empty((T, layer.H), dtype=torch.bfloat16, device="cuda")
+    mok.moe_forward(p, x, layer.packed, b["routing"], out, ws, packed_shared=layer.packed_shared, cfg=cfg)
+    torch.cuda.synchronize()
+    return out, mok.device_status(ws)
+
+
+def _staged(layer, x, T):
+    return _forward(layer, x, mok.make_config(flags=mok.FLAG_STAGED), T)[0]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", CASES, ids=[w.name for w in CASES])
+def test_megakernel_matches_staged_bitwise_and_oracle(wl):
+    inp = synth.make_inputs(wl)
+    dt = dtype_of(wl)
+    layer = layer_for(inp, dt)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    ref = _staged(layer, x, wl.T)
+    out, st = _forward(layer, x, mok.make_config(), wl.T)
+    assert st == (mok.OK, 0)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    mode = oracle.MODE_MXFP8 if dt == mok.MXFP8 else oracle.MODE_BF16
+    o = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=mode)
+    assert_close(host_bf16_f64(out), o, TOL[dt], wl.name)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", [CASES[0], CASES[2]], ids=["bf16", "mxfp8"])
+def test_megakernel_independent_of_minibatch_ring_and_movers(wl):
+    inp = synth.make_inputs(wl, seed=7)
+    layer = layer_for(inp, dtype_of(wl))
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    ref = _staged(layer, x, wl.T)
+    configs = [
+        mok.make_config(minibatch_tokens=64),                        # many minibatches, both regions reused
+        mok.make_config(minibatch_tokens=160, ring_rows=2 * 1536),   # ring forces the cut
+        mok.make_config(mover_ctas=1),
+        mok.make_config(mover_ctas=24, minibatch_tokens=300),
+    ]
+    for cfg in configs:
+        out, st = _forward(layer, x, cfg, wl.T)
+        assert st == (mok.OK, 0), (cfg.minibatch_tokens, cfg.ring_rows, cfg.mover_ctas, st)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (cfg.minibatch_tokens, cfg.mover_ctas)
+
+
+@pytest.mark.gpu
+def test_megakernel_bitwise_reruns():
+    wl = CASES[2]
+    inp = synth.make_inputs(wl, seed=9)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    cfg = mok.make_config(minibatch_tokens=128)
+    first, _ = _forward(layer, x, cfg, wl.T)
+    for _ in range(9):
+        again, st = _forward(layer, x, cfg, wl.T)
+        assert st == (mok.OK, 0)
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_macro_batches_through_one_ring_with_shared_expert():
+    """Several macro-batches (own tokens, same weights) stream through one
+    launch and a small ring; each output equals that batch's staged forward,
+    shared BF16 expert included."""
+    wl = synth.small("stream", T=400, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2, shared_I=256,
+                     batches=3)
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.MXFP8)
+    xs = [to_dev_bf16(x) for x in inp.xs]
+    routings, refs = [], []
+    for x in xs:
+        r = layer.route(x)
+        routings.append({n: v.clone() for n, v in r.items()})
+        refs.append(_staged(layer, x, wl.T).clone())
+    p = layer.problem(wl.T)
+    cfg = mok.make_config(ring_rows=2 * 1024, minibatch_tokens=128)
+    ws = mok.alloc_bytes(mok.workspace_size_batches(p, len(xs), cfg))
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda") for _ in xs]
+    mok.moe_forward_batches(p, xs, layer.packed, routings, outs, ws, packed_shared=layer.packed_shared, cfg=cfg)
+    torch.cuda.synchronize()
+    assert mok.device_status(ws) == (mok.OK, 0)
+    for b in range(len(xs)):
+        assert torch.equal(outs[b].view(torch.int16), refs[b].view(torch.int16)), b
+    r = oracle.route(inp.xs[1], inp.W_r, wl.k, inp.bias)
+    o = oracle.moe_forward(inp.xs[1], inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_MXFP8, shared=inp.shared)
+    assert_close(host_bf16_f64(outs[1]), o, TOL[mok.MXFP8], "batch 1")
+
+
+@pytest.mark.gpu
+def test_ring_smaller_than_one_token_block_reports_capacity():
+    wl = CASES[0]
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    out, st = _forward(layer, x, mok.make_config(ring_rows=2 * 128), wl.T)
+    assert st[0] == mok.ERR_CAPACITY
+    ref = _staged(layer, x, wl.T)       # the device is still usable
+    out, st = _forward(layer, x, mok.make_config(), wl.T)
+    assert st == (mok.OK, 0) and torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_withheld_publish_times_out_cleanly():
+    """A mover that never publishes one chunk: the waiting tiles give up
+    after timeout_ms, the call reports MOK_ERR_TIMEOUT, nothing hangs, and the
+    next call works."""
+    wl = CASES[0]
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    cfg = mok.make_config(timeout_ms=300, flags=mok.FLAG_TEST_WITHHOLD_PUBLISH)
+    out, st = _forward(layer, x, cfg, wl.T)
+    assert st[0] == mok.ERR_TIMEOUT
+    ref = _staged(layer, x, wl.T)
+    out, st = _forward(layer, x, mok.make_config(), wl.T)
+    assert st == (mok.OK, 0) and torch.equal(out.view(torch.int16), ref.view(torch.int16))
