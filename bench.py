@@ -144,6 +144,9 @@ def main():
     ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--staged", action="store_true", help="time the stage kernels instead of the megakernel")
+    ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
+    ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -165,36 +168,95 @@ def main():
     layer = MoELayer(inp.W_r, inp.Wg, inp.Wu, inp.Wd, wl.k, dtype=dtype, bias=inp.bias, shared=inp.shared,
                      device=dev, keep_unpacked=wl.backward)
     T, H = wl.T, wl.H
-    x = to_dev_bf16(inp.x, dev)
+    xs = [to_dev_bf16(xb, dev) for xb in inp.xs]
+    x = xs[0]
     p = layer.problem(T)
-    b = layer.buffers(T)
-    rt = b["routing"]
-    rows = mok.padded_rows_max(T, wl.E, wl.k)
-    eb = 1 if dtype == mok.MXFP8 else 2
-    A = mok.alloc_bytes(rows * H * eb, dev)
-    A_sf = mok.alloc_bytes(rows * H // 32, dev) if dtype == mok.MXFP8 else None
-    h = mok.alloc_bytes(rows * wl.I * eb, dev)
-    h_sf = mok.alloc_bytes(rows * wl.I // 32, dev) if dtype == mok.MXFP8 else None
-    part = torch.empty((T * wl.k, H), dtype=torch.bfloat16, device=dev)
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    status_ws = b["ws"]
+    staged = args.staged or wl.backward
+    cfg = mok.make_config(flags=mok.FLAG_STAGED if staged else 0, ring_rows=wl.ring_rows,
+                          mover_ctas=args.movers, minibatch_tokens=args.minibatch)
+    b = layer.buffers(T, training=wl.backward, cfg=cfg)
+    rt = b["routing"]
+    mode = ("fwd+bwd (staged)" if wl.backward else
+            f"{len(xs)} macro-batches, megakernel" if len(xs) > 1 else
+            "staged kernels" if staged else "megakernel")
 
-    def step(ev=None):
-        # one layer: route/layout, dispatch, grouped GEMMs, combine (7 launches)
-        layer.route(x, stream=stream)
-        mok.dispatch(p, x, rt, A, A_sf, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, status_ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        mok.combine(p, part, rt["topk_w"], out, stream=stream)
+    if wl.backward:
+        dY = to_dev_bf16(inp.dY, dev)
 
-    launches_per_step = 7
-    if wl.shared_I:
-        raise SystemExit("the stage-split bench step covers routed experts only; use the layer test for shared")
+        def step(ev=None):
+            # route + training forward (saves activations) + backward
+            layer.route(x, training=True, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            layer.forward(x, training=True, cfg=cfg, stream=stream, route=False)
+            layer.backward(x, dY, cfg=cfg, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+        # route 3, training forward 4 (dispatch, 2 GEMMs, combine), backward 12
+        launches_per_step = 3 + 4 + 12
+        status_ws = b["ws"]
+        flops = 18.0 * H * wl.I * T * wl.k
+        kern = "layer GEMMs fwd+bwd (staged; 2 fwd + 4 bwd grouped GEMM launches)"
+    elif len(xs) > 1:
+        routings = [{n: v.clone() for n, v in rt.items()} for _ in xs]
+        outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs]
+        ws_b = mok.alloc_bytes(mok.workspace_size_batches(p, len(xs), cfg), dev)
+        route_ws = b["route_ws"]
+
+        def step(ev=None):
+            for xb, rb in zip(xs, routings):
+                mok.route_layout(xb, layer.W_r, wl.k, layer.bias, out=rb, workspace=route_ws, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            mok.moe_forward_batches(p, xs, layer.packed, routings, outs, ws_b, packed_shared=layer.packed_shared,
+                                    cfg=cfg, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+        # per batch: route 3 (+ 2 shared-expert GEMMs); then plan 2 + megakernel 1
+        launches_per_step = 3 * len(xs) + (2 * len(xs) if wl.shared_I else 0) + 3
+        status_ws = ws_b
+        flops = wl.fwd_flops()
+        kern = "shared-expert GEMMs + forward megakernel (one launch for all macro-batches)"
+    elif staged:
+        rows = mok.padded_rows_max(T, wl.E, wl.k)
+        eb = 1 if dtype == mok.MXFP8 else 2
+        A = mok.alloc_bytes(rows * H * eb, dev)
+        A_sf = mok.alloc_bytes(rows * H // 32, dev) if dtype == mok.MXFP8 else None
+        h = mok.alloc_bytes(rows * wl.I * eb, dev)
+        h_sf = mok.alloc_bytes(rows * wl.I // 32, dev) if dtype == mok.MXFP8 else None
+        part = torch.empty((T * wl.k, H), dtype=torch.bfloat16, device=dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        status_ws = b["ws"]
+
+        def step(ev=None):
+            # route/layout, dispatch, grouped GEMMs, combine (7 launches)
+            layer.route(x, stream=stream)
+            mok.dispatch(p, x, rt, A, A_sf, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, status_ws, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            mok.combine(p, part, rt["topk_w"], out, stream=stream)
+        launches_per_step = 7
+        flops = 6.0 * H * wl.I * T * wl.k
+        kern = "grouped expert GEMMs (gate/up+SwiGLU, down+push; 2 launches)"
+    else:
+        status_ws = b["ws"]
+
+        def step(ev=None):
+            # route/layout (3 launches), plan (2), megakernel (1)
+            layer.route(x, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            layer.forward(x, cfg=cfg, stream=stream, route=False)
+            if ev is not None:
+                ev[1].record(stream)
+        launches_per_step = 6
+        flops = 6.0 * H * wl.I * T * wl.k
+        kern = "forward megakernel (dispatch + grouped GEMMs + combine, one launch; plus 2 plan launches)"
 
     for _ in range(args.warmup):
         step()
@@ -226,24 +288,45 @@ def main():
     st = mok.device_status(status_ws)
     if st[0] != mok.OK:
         raise SystemExit(f"device status after timed steps: {st}")
+    tokens_per_step = T * len(xs)
 
-    # end to end through the public API with host buffers: pinned x in,
-    # route + forward (mok_moe_forward), out back to pinned host memory
-    x_host = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    out_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
-    x_dev2 = torch.empty_like(x)
+    # end to end through the public API with host buffers: pinned inputs in,
+    # route + forward (+ backward), result back to pinned host memory
+    x_host = [torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory() for xb in inp.xs]
+    if wl.backward:
+        dY_host = torch.from_numpy(inp.dY.view(np.int16)).view(torch.bfloat16).pin_memory()
+        dY_dev2 = torch.empty_like(dY)
+    out_host = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    x_dev2 = [torch.empty_like(xb) for xb in xs]
+
+    def e2e_step():
+        for xh, xd in zip(x_host, x_dev2):
+            xd.copy_(xh, non_blocking=True)
+        if wl.backward:
+            dY_dev2.copy_(dY_host, non_blocking=True)
+            layer.forward(x_dev2[0], training=True, cfg=cfg, stream=stream)
+            g = layer.backward(x_dev2[0], dY_dev2, cfg=cfg, stream=stream)
+            out_host[0].copy_(g["dX"], non_blocking=True)
+        elif len(xs) > 1:
+            for xd, rb in zip(x_dev2, routings):
+                mok.route_layout(xd, layer.W_r, wl.k, layer.bias, out=rb, workspace=b["route_ws"], stream=stream)
+            mok.moe_forward_batches(p, x_dev2, layer.packed, routings, outs, ws_b,
+                                    packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
+            for o, oh in zip(outs, out_host):
+                oh.copy_(o, non_blocking=True)
+        else:
+            y = layer.forward(x_dev2[0], cfg=cfg, stream=stream)
+            out_host[0].copy_(y, non_blocking=True)
+
     for _ in range(2):
-        x_dev2.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev2, stream=stream)
+        e2e_step()
     torch.cuda.synchronize(dev)
     e2e_ms = []
     for i in range(max(3, args.steps // 2)):
         flush.zero_()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        x_dev2.copy_(x_host, non_blocking=True)
-        y = layer.forward(x_dev2, stream=stream)
-        out_host.copy_(y, non_blocking=True)
+        e2e_step()
         a1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms.append(a0.elapsed_time(a1))
@@ -257,13 +340,14 @@ def main():
         t_max, e2e_max = tt.tolist()
     if rank != 0:
         return
-    value = ws * T * args.steps / (t_max / 1000.0)
-    e2e_val = ws * T * len(e2e_ms) / (e2e_max / 1000.0)
+    value = ws * tokens_per_step * args.steps / (t_max / 1000.0)
+    e2e_val = ws * tokens_per_step * len(e2e_ms) / (e2e_max / 1000.0)
     peaks = load_peaks()
-    fl = 6.0 * H * wl.I * T * wl.k
+    fl = flops
     g_ms = statistics.mean(gemm_ms)
     achieved = fl / (g_ms / 1000.0) / 1e12
-    peak = peaks["bf16"] * (2.0 if dtype == mok.MXFP8 else 1.0)
+    long_region = total_ms > 1000.0
+    peak = (peaks["bf16_sus"] if long_region else peaks["bf16"]) * (2.0 if dtype == mok.MXFP8 else 1.0)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -271,19 +355,24 @@ def main():
         "data": "synthetic",
         "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "k": wl.k,
                    "operands": wl.dtype, "routing": "zipf s=1.2 bias" if wl.zipf_s else "uniform",
+                   "macro_batches": len(xs), "shared_expert_I": wl.shared_I, "ring_rows": wl.ring_rows or "default",
+                   "mover_ctas": args.movers or 8, "path": mode,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "flushed before every timed step (256 MiB write); per-step CUDA events",
-                   "step": "route+topk+layout, dispatch, grouped gate/up+SwiGLU, grouped down+push, combine"},
-        "roofline": {"kernel": "grouped expert GEMMs (gate/up+SwiGLU, down+push; 2 launches)",
+                   "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
+        "roofline": {"kernel": kern,
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "peak_source": f"{peaks['source']} bf16 burst" + (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
-                     "flops_per_launch_pair": fl, "ms_per_launch_pair": g_ms, "traffic": None},
-        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-                "d2h_bytes_per_step": T * H * 2, "api": "mok_route_layout + mok_moe_forward"},
+                     "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
+                                    (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
+                     "flops_per_step": fl, "ms_per_step": g_ms, "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "tokens/s",
+                "h2d_bytes_per_step": tokens_per_step * H * 2 * (2 if wl.backward else 1),
+                "d2h_bytes_per_step": tokens_per_step * H * 2,
+                "api": "mok_route_layout + " + ("mok_moe_forward(training) + mok_moe_backward" if wl.backward else
+                                                "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward")},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
-        "stage_ms": {"step_median": statistics.median(step_ms), "grouped_gemm_median": statistics.median(gemm_ms)},
+        "stage_ms": {"step_median": statistics.median(step_ms), "timed_kernels_median": statistics.median(gemm_ms)},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, wl)
