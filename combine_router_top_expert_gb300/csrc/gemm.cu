@@ -46,15 +46,41 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool MX, bool MN, int EPI, int S, int ACC>
+template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
                 int64_t tiles_ub, int num_sms, cudaStream_t s) {
     using C = GemmCfg<BN, MX, MN, EPI, S, ACC>;
-    auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC>;
+    auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC, CLN>;
     ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
-    int grid = (int)std::min<int64_t>(tiles_ub, num_sms);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = s;
+    int grid;
+    if constexpr (CLN == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // persistent: as many CTA pairs as can be resident at once
+        cfg.gridDim = dim3(2 * ((num_sms + 1) / 2));
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            clusters = num_sms / 2;
+        }
+        clusters = std::min(clusters, num_sms / 2);
+        grid = 2 * (int)std::min<int64_t>((tiles_ub + 1) / 2, clusters);
+    } else {
+        grid = (int)std::min<int64_t>(tiles_ub, num_sms);
+    }
     if (grid < 1) return cudaSuccess;
-    kern<<<grid, C::kThreads, C::kSmemBytes, s>>>(a, b, b2, p);
+    cfg.gridDim = dim3(grid);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, b2, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -105,18 +131,23 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.a_sf = A_sf;
     p.b_sf = Bgu_sf;
     p.sf_kchunks = H / 128;
+    p.n_tiles = 2 * I / (mx ? 128 : BN);
+    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, A, a_rows, H, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, A, a_rows, H, eb, bk, cl ? 64 : 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, mx ? 128 : BN)) return cudaErrorInvalidValue;
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
+    const int64_t tub = mt * p.n_tiles;
     if (mx) {
         // MXFP8: 128-wide tiles (gate 64 | up 64), double-buffered accumulator
-        p.n_tiles = 2 * I / 128;
-        return run<128, true, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+        if (cl) return run<128, true, false, kEpiSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        return run<128, true, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
-    p.n_tiles = 2 * I / BN;
-    if (BN == 256) return run<256, false, false, kEpiSwiGLU, 4, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
-    return run<128, false, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    if (BN == 256) {
+        if (cl) return run<256, false, false, kEpiSwiGLU, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        return run<256, false, false, kEpiSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    }
+    return run<128, false, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
 }
 
 cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* Bdn, const uint8_t* Bdn_sf, int E,
@@ -139,14 +170,22 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     p.b_sf = Bdn_sf;
     p.sf_kchunks = I / 128;
     const int BN = (H % 256 == 0 && !mx) ? 256 : 128;
+    p.n_tiles = H / BN;
+    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, h, a_rows, I, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, h, a_rows, I, eb, bk, cl ? 64 : 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, Bdn, (int64_t)p.E * H, I, eb, bk, BN)) return cudaErrorInvalidValue;
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
-    p.n_tiles = H / BN;
-    if (mx) return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
-    if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
-    return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, mt * p.n_tiles, c.num_sms, s);
+    const int64_t tub = mt * p.n_tiles;
+    if (mx) {
+        if (cl) return run<128, true, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    }
+    if (BN == 256) {
+        if (cl) return run<256, false, false, kEpiScatter, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    }
+    return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
 }
 
 cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I, const int32_t* counts,
@@ -160,11 +199,13 @@ cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I
     p.gu = const_cast<void*>(gu);
     p.split_col = I;
     const int BN = I % 256 == 0 ? 256 : (I % 128 == 0 ? 128 : 64);
-    CUtensorMap ta, tb;
-    if (!make_tmap(&ta, dy, a_rows, H, 2, 64, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, BN)) return cudaErrorInvalidValue;
     p.n_tiles = I / BN;
+    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0 && BN == 256;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, dy, a_rows, H, 2, 64, cl ? 64 : 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, BN)) return cudaErrorInvalidValue;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    if (cl) return run<256, false, false, kEpiDSwiGLU, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, false, kEpiDSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     if (BN == 128) return run<128, false, false, kEpiDSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     return run<64, false, false, kEpiDSwiGLU, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -184,12 +225,14 @@ cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, 
     p.out0 = da;
     p.ldo = H;
     const int BN = H % 256 == 0 ? 256 : 128;
+    p.n_tiles = H / BN;
+    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0 && BN == 256;
     CUtensorMap ta, tb, tb2;
-    if (!make_tmap(&ta, dgu, a_rows, 2 * I, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, dgu, a_rows, 2 * I, 2, 64, cl ? 64 : 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, W_gate, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb2, W_up, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
-    p.n_tiles = H / BN;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    if (cl) return run<256, false, false, kEpiScatter, 4, 2, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
 }

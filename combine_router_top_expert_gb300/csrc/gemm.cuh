@@ -150,11 +150,30 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES>
+// Cluster pairs: pair index gp covers the two N-neighbour tiles (2n', 2n'+1)
+// of one (expert, m-tile); rank picks the CTA's own tile. n_tiles is even.
+__device__ __forceinline__ int pair_tile(const GemmParams& p, const Sched& s, int gp, int rank) {
+    int lo = 0, hi = p.E - 1;  // last e with toff[e] / 2 <= gp
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s.toff[mid] / 2 <= gp) lo = mid; else hi = mid - 1;
+    }
+    const int mt = (s.toff[lo + 1] - s.toff[lo]) / p.n_tiles;
+    const int pl = gp - s.toff[lo] / 2;
+    const int np = pl / mt, m = pl % mt;
+    return s.toff[lo] + (2 * np + rank) * mt + m;
+}
+
+// CLN = 2: launched as clusters of two CTAs that compute N-neighbour tiles of
+// the same (expert, m-tile); each loads half of the shared A tile and
+// multicasts it to both, so per K-block each CTA fetches 40 KB instead of
+// 48 KB from L2 (BF16, BN=256) or 24 KB instead of 32 KB (MXFP8, BN=128).
+template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
     using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES>;
+    static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR), "cluster pairs share K-major A tiles");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Sched sched;
     __shared__ uint32_t s_tmem_base;
@@ -179,7 +198,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (threadIdx.x == 32) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
-            tc::mbar_init(empty_bar(s), 1);
+            tc::mbar_init(empty_bar(s), CLN);   // one MMA commit per CTA of the cluster
         }
         for (int a = 0; a < ACC_STAGES; ++a) {
             tc::mbar_init(accf_bar(a), 1);
@@ -200,8 +219,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if constexpr (CLN == 2) tc::cluster_sync();   // peers' barriers exist before any multicast
     const uint32_t tmem = s_tmem_base;
     const int total_tiles = sched.toff[p.E];
+    const int rank = CLN == 2 ? (int)tc::cluster_ctarank() : 0;
+    const int gstart = CLN == 2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+    const int gstep = CLN == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
+    const int gtotal = CLN == 2 ? total_tiles / 2 : total_tiles;
+    auto tile_of = [&](int gi) { return CLN == 2 ? pair_tile(p, sched, gi, rank) : gi; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -211,8 +236,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int last_par[STAGES];
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             bool ok = true;
-            for (int g = blockIdx.x; g < total_tiles && ok; g += gridDim.x) {
-                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+            for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
+                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
                     tc::mbar_expect_tx(full_bar(stage), C::kStageBytes + C::kSfStage);
@@ -225,7 +250,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int j = 0; j < BN / 64; ++j)
                             tc::tma_load_2d(b_tile(stage) + 8192 * j, &tmB, full_bar(stage), ti.n * BN + 64 * j, krow);
                     } else {
-                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
+                        if constexpr (CLN == 2)
+                            tc::tma_load_2d_multicast(a_tile(stage) + rank * 8192, &tmA, full_bar(stage), kb * C::kBK,
+                                                      ti.a_row0 + 64 * rank, (uint16_t)0x3);
+                        else
+                            tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
                         const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
                         if (kb < p.b_split_kb)
                             tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kb * C::kBK, brow);
@@ -261,8 +290,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true, issued = false;
-            for (int g = blockIdx.x; g < total_tiles && ok; g += gridDim.x) {
-                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+            for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
+                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
                 if (ti.num_kb == 0) continue;
                 if (!tc::mbar_wait(acce_bar(acc), acc_ph ^ 1u, st, tmo, kSiteMmaAccEmpty)) { ok = false; break; }
                 tc::fence_after_sync();
@@ -298,7 +327,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         }
                     }
                     issued = true;
-                    tc::mma_commit(empty_bar(stage));
+                    if constexpr (CLN == 2) tc::mma_commit_multicast(empty_bar(stage), (uint16_t)0x3);
+                    else tc::mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -317,8 +347,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int row = q * 32 + lane;   // tile row owned by this thread
         int acc = 0;
         uint32_t acc_ph = 0;
-        for (int g = blockIdx.x; g < total_tiles; g += gridDim.x) {
-            TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, g);
+        for (int gi = gstart; gi < gtotal; gi += gstep) {
+            TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
             const bool has_acc = ti.num_kb > 0;
             if (has_acc) {
                 if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
@@ -486,6 +516,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    if constexpr (CLN == 2) tc::cluster_sync();   // no CTA leaves while its peer may still write to it
     if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 

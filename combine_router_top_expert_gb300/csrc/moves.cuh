@@ -37,6 +37,7 @@ struct GemmCommon {
     StatusBlock* status;
     unsigned long long timeout_ns;
     int num_sms;
+    int cluster;   // 2: grouped GEMMs run as CTA pairs sharing A tiles by multicast; 1: single CTAs
 };
 // Forward gate/up GEMM + SwiGLU. A: [rows, H] (bf16 or E4M3 + tile scales);
 // packed B: [E * 2I, H] (interleaved gate/up per il = BN/2 columns).

@@ -82,6 +82,10 @@ typedef struct {
 /* Run the forward as separate stage kernels (dispatch, grouped GEMMs,
  * combine) instead of the persistent megakernel. */
 #define MOK_FLAG_STAGED 1
+/* Run the staged grouped GEMMs as single CTAs instead of CTA pairs (two
+ * CTAs on neighbouring N-tiles that share the A tile through TMA multicast;
+ * same results either way). */
+#define MOK_FLAG_NO_CLUSTER 2
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use
