@@ -144,7 +144,8 @@ def main():
     ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--staged", action="store_true", help="time the stage kernels instead of the megakernel")
+    ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
+    ap.add_argument("--no-cluster", action="store_true", help="grouped GEMMs as single CTAs, not CTA pairs")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
     ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
     args = ap.parse_args()
@@ -173,9 +174,10 @@ def main():
     p = layer.problem(T)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    staged = args.staged or wl.backward
-    cfg = mok.make_config(flags=mok.FLAG_STAGED if staged else 0, ring_rows=wl.ring_rows,
-                          mover_ctas=args.movers, minibatch_tokens=args.minibatch)
+    staged = not args.megakernel or wl.backward
+    flags = (0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_NO_CLUSTER if args.no_cluster else 0)
+    cfg = mok.make_config(flags=flags, ring_rows=wl.ring_rows, mover_ctas=args.movers,
+                          minibatch_tokens=args.minibatch)
     b = layer.buffers(T, training=wl.backward, cfg=cfg)
     rt = b["routing"]
     mode = ("fwd+bwd (staged)" if wl.backward else
@@ -359,6 +361,7 @@ def main():
                    "mover_ctas": args.movers or 8, "path": mode,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
+        "gemm_cta_pairs": not args.no_cluster,
         "roofline": {"kernel": kern,
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

@@ -378,7 +378,7 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
         return MOK_ERR_INVALID;
     if (p->I_shared > 0 && !aligned(a->packed_shared, 256)) return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;
-    if (!training && !(cfg && (cfg->flags & MOK_FLAG_STAGED)) && mega_supported(p)) {
+    if (!training && cfg && (cfg->flags & MOK_FLAG_MEGAKERNEL) && mega_supported(p)) {
         if (mega_region_rows(p, cfg) < kTileM) return MOK_ERR_INVALID;
         return forward_mega(p, 1, a, cfg, stream);
     }

@@ -69,9 +69,9 @@ class MoELayer:
                                 stream=stream)
 
     def forward(self, x, training=False, cfg=None, stream=None, route=True):
-        """out [T, H] bf16 (a view of a reused buffer). Inference runs the
-        megakernel unless cfg has FLAG_STAGED (or the shape needs the staged
-        path); training runs the staged kernels and keeps activations."""
+        """out [T, H] bf16 (a view of a reused buffer). The stage kernels run
+        unless cfg has FLAG_MEGAKERNEL (inference only); training keeps the
+        activations the backward needs."""
         T = x.shape[0]
         b = self.buffers(T, training, cfg)
         if route:

@@ -27,7 +27,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches"]
 
-FLAG_STAGED = 1
+FLAG_MEGAKERNEL = 1
 FLAG_NO_CLUSTER = 2
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 

@@ -79,9 +79,10 @@ typedef struct {
     int32_t reserved[2];
 } mok_config;
 
-/* Run the forward as separate stage kernels (dispatch, grouped GEMMs,
- * combine) instead of the persistent megakernel. */
-#define MOK_FLAG_STAGED 1
+/* Run the inference forward as the persistent megakernel (mover/compute
+ * SM split, GPU-local counters, ring) instead of the stage kernels
+ * (dispatch, grouped GEMMs, combine). */
+#define MOK_FLAG_MEGAKERNEL 1
 /* Run the staged grouped GEMMs as single CTAs instead of CTA pairs (two
  * CTAs on neighbouring N-tiles that share the A tile through TMA multicast;
  * same results either way). */
@@ -176,17 +177,18 @@ size_t mok_saved_size(const mok_problem* p);
  * row to its (token, slot) partial, then out[t] = bf16(sum_{j=0..k-1}
  * w[t,j] * y[t,j] (+ shared[t])) in fp32 with j ascending. Bitwise
  * deterministic, and the same bits on either path.
- * Inference (saved == NULL) runs the persistent megakernel ([K-ja] 02): one
- * cooperative launch whose first cfg->mover_ctas CTAs gather minibatches into
- * a two-region ring while the other CTAs run the tensor-core tiles; the two
- * sides synchronise through GPU-local counters only. It needs every SM of the
- * device (the launch fails with MOK_ERR_CUDA if they cannot all be resident)
- * and tile widths that divide H and 2I (256 for BF16, 128 for MXFP8); other
- * shapes use the staged path. MOK_FLAG_STAGED, or `saved` != NULL (training:
- * keeps the activations the backward needs; BF16 only, MOK_ERR_UNSUPPORTED
- * for MXFP8), runs the stage kernels in sequence instead. The device status
- * reports MOK_ERR_CAPACITY if a ring region cannot hold the padded rows of
- * 16 tokens. */
+ * By default the stage kernels run in sequence on the stream. With
+ * MOK_FLAG_MEGAKERNEL, inference (saved == NULL) runs the persistent
+ * megakernel ([K-ja] 02) instead: one cooperative launch whose first
+ * cfg->mover_ctas CTAs gather minibatches into a two-region ring while the
+ * other CTAs run the tensor-core tiles; the two sides synchronise through
+ * GPU-local counters only. It needs every SM of the device (the launch fails
+ * with MOK_ERR_CUDA if they cannot all be resident) and tile widths that
+ * divide H and 2I (256 for BF16, 128 for MXFP8); other shapes use the stage
+ * kernels. The device status reports MOK_ERR_CAPACITY if a ring region
+ * cannot hold the padded rows of 16 tokens. `saved` != NULL (training) keeps
+ * the activations the backward needs (BF16 only; MOK_ERR_UNSUPPORTED for
+ * MXFP8). */
 mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a,
                            const mok_config* cfg, mok_stream_t stream);
 

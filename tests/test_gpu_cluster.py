@@ -10,7 +10,7 @@ from helpers import dtype_of, layer_for, to_dev_bf16
 
 def _staged(layer, x, T, extra=0):
     p = layer.problem(T)
-    cfg = mok.make_config(flags=mok.FLAG_STAGED | extra)
+    cfg = mok.make_config(flags=extra)
     ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
     out = torch.empty((T, layer.H), dtype=torch.bfloat16, device="cuda")
     mok.moe_forward(p, x, layer.packed, layer.buffers(T)["routing"], out, ws, packed_shared=layer.packed_shared,
