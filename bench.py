@@ -145,7 +145,7 @@ def main():
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
-    ap.add_argument("--no-cluster", action="store_true", help="grouped GEMMs as single CTAs, not CTA pairs")
+    ap.add_argument("--gemm-pairs", action="store_true", help="grouped GEMMs as CTA pairs sharing A by multicast")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
     ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
     args = ap.parse_args()
@@ -175,7 +175,7 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     staged = not args.megakernel or wl.backward
-    flags = (0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_NO_CLUSTER if args.no_cluster else 0)
+    flags = (0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_GEMM_PAIRS if args.gemm_pairs else 0)
     cfg = mok.make_config(flags=flags, ring_rows=wl.ring_rows, mover_ctas=args.movers,
                           minibatch_tokens=args.minibatch)
     b = layer.buffers(T, training=wl.backward, cfg=cfg)
@@ -238,7 +238,7 @@ def main():
             mok.dispatch(p, x, rt, A, A_sf, stream=stream)
             if ev is not None:
                 ev[0].record(stream)
-            mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, status_ws, stream=stream)
+            mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, status_ws, cfg=cfg, stream=stream)
             if ev is not None:
                 ev[1].record(stream)
             mok.combine(p, part, rt["topk_w"], out, stream=stream)
@@ -361,7 +361,7 @@ def main():
                    "mover_ctas": args.movers or 8, "path": mode,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
-        "gemm_cta_pairs": not args.no_cluster,
+        "gemm_cta_pairs": bool(args.gemm_pairs),
         "roofline": {"kernel": kern,
                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

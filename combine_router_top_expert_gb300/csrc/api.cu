@@ -150,7 +150,7 @@ GemmCommon make_common(void* ws, const mok_config* cfg) {
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (cfg && cfg->num_sms > 0) n = std::min(n, (int)cfg->num_sms);
     c.num_sms = n > 0 ? n : 1;
-    c.cluster = (cfg && (cfg->flags & MOK_FLAG_NO_CLUSTER)) ? 1 : 2;
+    c.cluster = (cfg && (cfg->flags & MOK_FLAG_GEMM_PAIRS)) ? 2 : 1;
     return c;
 }
 

@@ -342,42 +342,65 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
             if (local < cnt[e]) src = bt.x + (int64_t)(bt.row_src[src0[e] + local] / p.k) * H;
             const int64_t grow = (int64_t)mi.region * p.region_rows + row;
             if constexpr (!MX) {
+                // 8 independent 16-byte loads in flight per lane before the stores
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.ring) + grow * H);
                 const uint4* s4 = reinterpret_cast<const uint4*>(src);
-                for (int q = lane; q < H / 8; q += 32) dst[q] = src ? __ldg(s4 + q) : make_uint4(0, 0, 0, 0);
+                const int n16 = H / 8;
+                for (int q0 = 0; q0 < n16; q0 += 32 * 8) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int q = q0 + u * 32 + lane;
+                        v[u] = (src && q < n16) ? __ldg(s4 + q) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int q = q0 + u * 32 + lane;
+                        if (q < n16) dst[q] = v[u];
+                    }
+                }
             } else {
                 uint8_t* dst = static_cast<uint8_t*>(p.ring) + grow * H;
                 const int rt = (int)(grow / kTileM), r = (int)(grow % kTileM);
-                for (int bb = lane; bb < H / 32; bb += 32) {
-                    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                    uint32_t code = 0;
-                    if (src) {
+                const int nb = H / 32;
+                // two 32-element blocks per lane per pass: 8 loads in flight
+                for (int b0 = 0; b0 < nb; b0 += 64) {
+                    uint4 v[2][4];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int bb = b0 + u * 32 + lane;
                         const uint4* s4 = reinterpret_cast<const uint4*>(src + bb * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            v[u][i] = (src && bb < nb) ? __ldg(s4 + i) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int bb = b0 + u * 32 + lane;
+                        if (bb >= nb) continue;
                         float f[32];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const uint4 u = __ldg(s4 + i);
-                            f[8 * i + 0] = bf16_lo(u.x); f[8 * i + 1] = bf16_hi(u.x);
-                            f[8 * i + 2] = bf16_lo(u.y); f[8 * i + 3] = bf16_hi(u.y);
-                            f[8 * i + 4] = bf16_lo(u.z); f[8 * i + 5] = bf16_hi(u.z);
-                            f[8 * i + 6] = bf16_lo(u.w); f[8 * i + 7] = bf16_hi(u.w);
+                            f[8 * i + 0] = bf16_lo(v[u][i].x); f[8 * i + 1] = bf16_hi(v[u][i].x);
+                            f[8 * i + 2] = bf16_lo(v[u][i].y); f[8 * i + 3] = bf16_hi(v[u][i].y);
+                            f[8 * i + 4] = bf16_lo(v[u][i].z); f[8 * i + 5] = bf16_hi(v[u][i].z);
+                            f[8 * i + 6] = bf16_lo(v[u][i].w); f[8 * i + 7] = bf16_hi(v[u][i].w);
                         }
                         float amax = 0.f;
 #pragma unroll
                         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                        code = e8m0_code(amax);
+                        const uint32_t code = src ? e8m0_code(amax) : 0u;
                         const float inv = e8m0_inv_scale(code);
                         uint32_t w[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
                                    (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
-                        o0 = make_uint4(w[0], w[1], w[2], w[3]);
-                        o1 = make_uint4(w[4], w[5], w[6], w[7]);
+                        reinterpret_cast<uint4*>(dst + bb * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst + bb * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        p.ring_sf[((int64_t)rt * (H / 128) + bb / 4) * 512 + sf_chunk_offset(r, bb & 3)] =
+                            (uint8_t)code;
                     }
-                    reinterpret_cast<uint4*>(dst + bb * 32)[0] = o0;
-                    reinterpret_cast<uint4*>(dst + bb * 32)[1] = o1;
-                    p.ring_sf[((int64_t)rt * (H / 128) + bb / 4) * 512 + sf_chunk_offset(r, bb & 3)] = (uint8_t)code;
                 }
             }
         }

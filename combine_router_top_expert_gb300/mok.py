@@ -28,7 +28,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches"]
 
 FLAG_MEGAKERNEL = 1
-FLAG_NO_CLUSTER = 2
+FLAG_GEMM_PAIRS = 2
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 

@@ -83,10 +83,11 @@ typedef struct {
  * SM split, GPU-local counters, ring) instead of the stage kernels
  * (dispatch, grouped GEMMs, combine). */
 #define MOK_FLAG_MEGAKERNEL 1
-/* Run the staged grouped GEMMs as single CTAs instead of CTA pairs (two
- * CTAs on neighbouring N-tiles that share the A tile through TMA multicast;
- * same results either way). */
-#define MOK_FLAG_NO_CLUSTER 2
+/* Run the staged grouped GEMMs as CTA pairs (two CTAs on neighbouring
+ * N-tiles that share the A tile through TMA multicast) instead of single
+ * CTAs; same results either way (measured slower on GB300, kept as an
+ * option). */
+#define MOK_FLAG_GEMM_PAIRS 2
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use

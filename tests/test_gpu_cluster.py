@@ -30,8 +30,8 @@ def test_cluster_pairs_forward_bitwise(wl):
     layer = layer_for(inp, dtype_of(wl))
     x = to_dev_bf16(inp.x)
     layer.route(x)
-    pairs = _staged(layer, x, wl.T)
-    single = _staged(layer, x, wl.T, mok.FLAG_NO_CLUSTER)
+    pairs = _staged(layer, x, wl.T, mok.FLAG_GEMM_PAIRS)
+    single = _staged(layer, x, wl.T)
     assert torch.equal(pairs.view(torch.int16), single.view(torch.int16))
 
 
@@ -43,7 +43,7 @@ def test_cluster_pairs_backward_bitwise():
     x = to_dev_bf16(inp.x)
     dY = to_dev_bf16(inp.dY)
     res = []
-    for flags in (0, mok.FLAG_NO_CLUSTER):
+    for flags in (mok.FLAG_GEMM_PAIRS, 0):
         cfg = mok.make_config(flags=flags)
         layer.forward(x, training=True, cfg=cfg)
         g = layer.backward(x, dY, cfg=cfg)
