@@ -17,7 +17,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // Gate/up columns interleaved per this many columns in the packed weights
 // (half the N-tile of the gate/up GEMM).
 int gu_interleave(int I, int dtype) {
-    if (dtype == MOK_MXFP8) return 64;
+    (void)dtype;
     return 2 * I >= 256 ? 128 : 64;
 }
 
@@ -49,7 +49,11 @@ PackedLayout packed_layout(int E, int H, int I, int dtype) {
     L.gu = o; o += align_up((int64_t)E * 2 * I * H * eb, 1024);
     L.gu_sf = o; if (dtype == MOK_MXFP8) o += align_up((int64_t)E * 2 * I * H / 32, 1024);
     L.dn = o; o += align_up((int64_t)E * H * I * eb, 1024);
-    L.dn_sf = o; if (dtype == MOK_MXFP8) o += align_up((int64_t)E * H * I / 32, 1024);
+    L.dn_sf = o;
+    if (dtype == MOK_MXFP8) {
+        const int tn = down_tile_n(H, true);   // scales per tile of tn rows, whole 512-byte chunks
+        o += align_up((int64_t)E * (H / tn) * ((tn + 127) / 128) * (I / 128) * 512, 1024);
+    }
     L.total = o;
     return L;
 }
@@ -111,8 +115,7 @@ constexpr int kDefaultMovers = 8;
 
 // Megakernel tile width: both GEMMs use the same N-tile (BF16 256, MXFP8 128).
 bool mega_supported(const mok_problem* p) {
-    const int BN = p->dtype == MOK_MXFP8 ? 128 : 256;
-    return p->H % BN == 0 && (2 * p->I) % BN == 0;
+    return (2 * p->I) % 256 == 0 && p->H % down_tile_n(p->H, p->dtype == MOK_MXFP8) == 0;
 }
 
 int mega_region_rows(const mok_problem* p, const mok_config* cfg) {
@@ -221,10 +224,10 @@ mok_status mok_pack_weights(int32_t E, int32_t H, int32_t I, int32_t dtype, cons
     char* b = static_cast<char*>(packed);
     const bool mx = dtype == MOK_MXFP8;
     cudaError_t e = launch_pack(mx, W_gate, W_up, E, H, I, gu_interleave(I, dtype), b + L.gu,
-                                mx ? reinterpret_cast<uint8_t*>(b + L.gu_sf) : nullptr, s);
+                                mx ? reinterpret_cast<uint8_t*>(b + L.gu_sf) : nullptr, 128, s);
     if (e == cudaSuccess)
         e = launch_pack(mx, W_down, nullptr, E, I, H, 0, b + L.dn, mx ? reinterpret_cast<uint8_t*>(b + L.dn_sf) : nullptr,
-                        s);
+                        down_tile_n(H, mx), s);
     return cuda_status(e);
 }
 

@@ -131,16 +131,20 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.a_sf = A_sf;
     p.b_sf = Bgu_sf;
     p.sf_kchunks = H / 128;
-    p.n_tiles = 2 * I / (mx ? 128 : BN);
+    p.n_tiles = 2 * I / BN;
     const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, a_rows, H, eb, bk, cl ? 64 : 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, mx ? 128 : BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, BN)) return cudaErrorInvalidValue;
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
-        // MXFP8: 128-wide tiles (gate 64 | up 64), double-buffered accumulator
-        if (cl) return run<128, true, false, kEpiSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        // MXFP8: 256-wide tiles (gate 128 | up 128) with one accumulator (the
+        // block scales need the rest of tensor memory); 128-wide for I = 64
+        if (BN == 256) {
+            if (cl) return run<256, true, false, kEpiSwiGLU, 4, 1, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+            return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
+        }
         return run<128, true, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
@@ -169,7 +173,9 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     p.a_sf = h_sf;
     p.b_sf = Bdn_sf;
     p.sf_kchunks = I / 128;
-    const int BN = (H % 256 == 0 && !mx) ? 256 : 128;
+    // MXFP8: 224-wide tiles when H allows (double-buffered accumulator with
+    // the scales in the tensor-memory gaps), else 128; BF16: 256 or 128
+    const int BN = down_tile_n(H, mx);
     p.n_tiles = H / BN;
     const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
     CUtensorMap ta, tb;
@@ -178,6 +184,10 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
+        if (BN == 224) {
+            if (cl) return run<224, true, false, kEpiScatter, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+            return run<224, true, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        }
         if (cl) return run<128, true, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }

@@ -62,22 +62,32 @@ struct GemmCfg {
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
     static constexpr int kBytesB = BN * 128;
     static constexpr int kStageBytes = kBytesA + kBytesB;
+    static constexpr int kNChunks = (BN + 127) / 128;   // 128-row scale chunks of a B tile
     static constexpr int kSfaBytes = MX ? 512 : 0;
-    static constexpr int kSfbBytes = MX ? (BN / 128) * 512 : 0;
+    static constexpr int kSfbBytes = MX ? kNChunks * 512 : 0;
     static constexpr int kSfStage = kSfaBytes + kSfbBytes;
     static constexpr int kBK = MX ? 128 : 64;           // K elements per stage (128 bytes)
     static constexpr int kUmmaK = MX ? 32 : 16;
     static constexpr int kMmasPerStage = kBK / kUmmaK;  // 4
-    static constexpr int kAccCols = BN * ACC_STAGES;
-    static constexpr int kSfCols = MX ? 4 + 4 * (BN / 128) : 0;
-    static constexpr int kTmemNeed = kAccCols + STAGES * kSfCols;
+    // Accumulator buffers start on 256-column boundaries when BN = 224, so the
+    // block scales (MXFP8) fit in the two 32-column gaps behind them.
+    static constexpr int kAccStride = BN == 224 ? 256 : BN;
+    static constexpr int kAccCols = kAccStride * ACC_STAGES;
+    static constexpr int kSfCols = MX ? 4 + 4 * kNChunks : 0;
+    static constexpr bool kSfInGaps = MX && BN == 224 && ACC_STAGES == 2;
+    static constexpr int kTmemNeed = kSfInGaps ? 512 : kAccCols + STAGES * kSfCols;
+    // first tensor-memory column of stage s's scales (A: 4 columns, then B)
+    __host__ __device__ static constexpr int sf_col(int s) {
+        return kSfInGaps ? BN + (s / 2) * 256 + (s % 2) * kSfCols : kAccCols + s * kSfCols;
+    }
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kBarOffset = STAGES * (kStageBytes + kSfStage);
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kBarOffset + 256;
     static_assert(kTmemNeed <= 512, "tensor memory budget");
-    static_assert(BN % 64 == 0 && BN <= 256, "BN");
-    static_assert(!MX || (BN % 128 == 0), "MXFP8 tiles need whole 128-row scale chunks");
+    static_assert(BN % 32 == 0 && BN <= 256, "BN");
+    static_assert(EPI != kEpiSwiGLU || (BN / 2) % 32 == 0, "SwiGLU tiles hold whole 32-column gate/up chunks");
+    static_assert(!kSfInGaps || (STAGES <= 4 && 2 * kSfCols <= 256 - BN), "scale columns must fit the gaps");
     static_assert(!(MX && MN_MAJOR), "MXFP8 operands are K-major");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
@@ -264,11 +274,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             const int art = ti.a_row0 / kTileM;
                             tc::bulk_load(sf_tile(stage), p.a_sf + ((int64_t)art * p.sf_kchunks + kb) * 512, 512,
                                           full_bar(stage));
+                            if constexpr (BN == 224) {
+                                // B scales packed per 224-row tile: two chunks side by side
+                                tc::bulk_load(sf_tile(stage) + 512,
+                                              p.b_sf + ((int64_t)(brow / 224) * p.sf_kchunks + kb) * 1024, 1024,
+                                              full_bar(stage));
+                            } else {
 #pragma unroll
-                            for (int j = 0; j < BN / 128; ++j) {
-                                const int brt = brow / kTileM + j;
-                                tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
-                                              p.b_sf + ((int64_t)brt * p.sf_kchunks + kb) * 512, 512, full_bar(stage));
+                                for (int j = 0; j < C::kNChunks; ++j) {
+                                    const int brt = brow / kTileM + j;
+                                    tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
+                                                  p.b_sf + ((int64_t)brt * p.sf_kchunks + kb) * 512, 512,
+                                                  full_bar(stage));
+                                }
                             }
                         }
                     }
@@ -295,17 +313,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (ti.num_kb == 0) continue;
                 if (!tc::mbar_wait(acce_bar(acc), acc_ph ^ 1u, st, tmo, kSiteMmaAccEmpty)) { ok = false; break; }
                 tc::fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                const uint32_t d = tmem + (uint32_t)(acc * C::kAccStride);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (!tc::mbar_wait(full_bar(stage), ph, st, tmo, kSiteMmaFull)) { ok = false; break; }
                     tc::fence_after_sync();
                     uint32_t sfa_t = 0, sfb_t = 0;
                     if constexpr (MX) {
-                        sfa_t = tmem + (uint32_t)(C::kAccCols + stage * C::kSfCols);
+                        sfa_t = tmem + (uint32_t)C::sf_col(stage);
                         sfb_t = sfa_t + 4;
                         tc::tmem_cp_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
 #pragma unroll
-                        for (int j = 0; j < BN / 128; ++j)
+                        for (int j = 0; j < C::kNChunks; ++j)
                             tc::tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
                                                        tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
                     }
@@ -354,7 +372,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
                 tc::fence_after_sync();
             }
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
 
             if constexpr (EPI == kEpiSwiGLU) {
                 const int I = p.split_col;

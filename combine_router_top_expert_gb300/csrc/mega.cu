@@ -234,6 +234,7 @@ struct MegaParams {
     int* g1_mb;      // [kMaxMinibatches]
     int* g2_mb;      // [kMaxMinibatches]
     int* comb_next;  // [kMaxMinibatches]
+    int bn2;         // N-tile of the down GEMM (224, 256 or 128)
     int n_movers;
     int test_flags;
     StatusBlock* status;
@@ -490,9 +491,12 @@ template <bool MX>
 __global__ void __launch_bounds__(192, 1)
 mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmGU,
             const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmDN, const MegaParams p) {
-    constexpr int BN = MX ? 128 : 256;
-    constexpr int STAGES = MX ? 6 : 4;
-    constexpr int ACC = 2;
+    // gate/up tiles are 256 wide (gate 128 | up 128); MXFP8 keeps one
+    // accumulator because its block scales take the rest of tensor memory.
+    // Down tiles are bn2 wide and use the first bn2 accumulator columns.
+    constexpr int BN = 256;
+    constexpr int STAGES = 4;
+    constexpr int ACC = MX ? 1 : 2;
     using C = GemmCfg<BN, MX, false, kEpiSwiGLU, STAGES, ACC>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ uint32_t s_tmem_base;
@@ -501,7 +505,8 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* st = p.status;
     const uint64_t tmo = p.timeout_ns;
-    const int NT1 = 2 * p.I / BN, NT2 = p.H / BN;
+    const int BN2 = p.bn2;
+    const int NT1 = 2 * p.I / BN, NT2 = p.H / BN2;
     const int kb1 = p.H / C::kBK, kb2 = p.I / C::kBK;
     const PlanView& v = p.plan;
     int next_comb = 0;
@@ -602,22 +607,29 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                 const int nkb = t.kind == 0 ? kb1 : kb2;
                 const void* tmA = t.kind == 0 ? (const void*)&tmRing : (const void*)&tmH;
                 const void* tmB = t.kind == 0 ? (const void*)&tmGU : (const void*)&tmDN;
-                const int brow = t.e * (t.kind == 0 ? 2 * p.I : p.H) + t.n * BN;
+                const int bnt = t.kind == 0 ? BN : BN2;
+                const int nch = (bnt + 127) / 128;
+                const int brow = t.e * (t.kind == 0 ? 2 * p.I : p.H) + t.n * bnt;
                 const uint8_t* asf = t.kind == 0 ? p.ring_sf : p.h_sf;
                 const uint8_t* bsf = t.kind == 0 ? p.gu_sf : p.dn_sf;
                 const int kch = t.kind == 0 ? p.H / 128 : p.I / 128;
+                const uint32_t tx = C::kBytesA + bnt * 128 + (MX ? 512 * (1 + nch) : 0);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
-                    tc::mbar_expect_tx(full_bar(stage), C::kStageBytes + C::kSfStage);
+                    tc::mbar_expect_tx(full_bar(stage), tx);
                     tc::tma_load_2d(a_tile(stage), tmA, full_bar(stage), kb * C::kBK, t.a_row0);
                     tc::tma_load_2d(b_tile(stage), tmB, full_bar(stage), kb * C::kBK, brow);
                     if constexpr (MX) {
                         tc::bulk_load(sf_tile(stage), asf + ((int64_t)(t.a_row0 / kTileM) * kch + kb) * 512, 512,
                                       full_bar(stage));
-#pragma unroll
-                        for (int j = 0; j < BN / 128; ++j)
-                            tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
-                                          bsf + ((int64_t)(brow / kTileM + j) * kch + kb) * 512, 512, full_bar(stage));
+                        if (bnt == 224)   // down scales kept per 224-row tile: two chunks in one copy
+                            tc::bulk_load(sf_tile(stage) + 512, bsf + ((int64_t)(brow / 224) * kch + kb) * 1024, 1024,
+                                          full_bar(stage));
+                        else
+                            for (int j = 0; j < nch; ++j)
+                                tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
+                                              bsf + ((int64_t)(brow / kTileM + j) * kch + kb) * 512, 512,
+                                              full_bar(stage));
                     }
                     last_par[stage] = (int)ph;
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
@@ -638,19 +650,20 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
             for (int g = cidx; g < total && ok; g += ncomp) {
                 const MegaTile t = mega_decode(p, g, NT1, NT2);
                 const int nkb = t.kind == 0 ? kb1 : kb2;
+                const int bnt = t.kind == 0 ? BN : BN2;
+                const int nch = (bnt + 127) / 128;
                 if (!tc::mbar_wait(acce_bar(acc), acc_ph ^ 1u, st, tmo, kSiteMmaAccEmpty)) { ok = false; break; }
                 tc::fence_after_sync();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                const uint32_t d = tmem + (uint32_t)(acc * C::kAccStride);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!tc::mbar_wait(full_bar(stage), ph, st, tmo, kSiteMmaFull)) { ok = false; break; }
                     tc::fence_after_sync();
                     uint32_t sfa_t = 0, sfb_t = 0;
                     if constexpr (MX) {
-                        sfa_t = tmem + (uint32_t)(C::kAccCols + stage * C::kSfCols);
+                        sfa_t = tmem + (uint32_t)C::sf_col(stage);
                         sfb_t = sfa_t + 4;
                         tc::tmem_cp_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
-#pragma unroll
-                        for (int j = 0; j < BN / 128; ++j)
+                        for (int j = 0; j < nch; ++j)
                             tc::tmem_cp_32x128b_warpx4(
                                 sfb_t + 4 * j, tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
                     }
@@ -659,8 +672,8 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                         const uint64_t ad = tc::make_sdesc(a_tile(stage) + kk * 32, 16, 1024, tc::kLayoutSW128);
                         const uint64_t bd = tc::make_sdesc(b_tile(stage) + kk * 32, 16, 1024, tc::kLayoutSW128);
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (MX) tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
-                        else tc::mma_bf16(d, ad, bd, tc::idesc_bf16(128, BN, false, false), accum);
+                        if constexpr (MX) tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, bnt, kk, kk), sfa_t, sfb_t, accum);
+                        else tc::mma_bf16(d, ad, bd, tc::idesc_bf16(128, bnt, false, false), accum);
                     }
                     issued = true;
                     tc::mma_commit(empty_bar(stage));
@@ -695,7 +708,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
             const bool okw = tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull);
             if (!bar_and(1, 128, okw)) break;  // all 128 epilogue threads agree
             tc::fence_after_sync();
-            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
             if (t.kind == 0) {
                 const int I = p.I;
                 const int64_t prow = t.a_row0 + row;
@@ -741,7 +754,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                 int64_t dest = -1;
                 if (lrow < v.cnt[t.mb * p.E + t.e]) dest = bt.row_src[v.src0[t.mb * p.E + t.e] + lrow];
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = 0; c0 < BN2; c0 += 32) {
                     uint32_t r[32];
                     tc::tmem_ld_32x32b_x32(tbase + c0, r);
                     tc::tmem_ld_wait();
@@ -750,7 +763,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    uint4* dst = reinterpret_cast<uint4*>(bt.partials + dest * p.H + t.n * BN + c0);
+                    uint4* dst = reinterpret_cast<uint4*>(bt.partials + dest * p.H + t.n * BN2 + c0);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
@@ -861,8 +874,8 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     cudaError_t e = cudaMemsetAsync(counters, 0, counter_bytes, s);
     if (e != cudaSuccess) return e;
 
-    const int BN = mx ? 128 : 256;
-    const int NT1 = 2 * I / BN, NT2 = H / BN;
+    const int BN = 256, BN2 = down_tile_n(H, mx);
+    const int NT1 = 2 * I / BN, NT2 = H / BN2;
     const int nblk = ceil_div(T, kPlanTB);
     const size_t psm = (size_t)(nblk + 1) * E * 4;
     if (psm > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(plan_batch_kernel), (int)psm);
@@ -892,6 +905,7 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     p.g1_mb = counters + 2 * kMaxMinibatches * E;
     p.g2_mb = p.g1_mb + kMaxMinibatches;
     p.comb_next = p.g2_mb + kMaxMinibatches;
+    p.bn2 = BN2;
     p.n_movers = L.n_movers;
     p.test_flags = L.test_flags;
     p.status = L.status;
@@ -902,7 +916,7 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     if (!tmap2d(&tR, ring, rrows, H, (int)eb, 128)) return cudaErrorInvalidValue;
     if (!tmap2d(&tGU, L.gu, (int64_t)E * 2 * I, H, (int)eb, BN)) return cudaErrorInvalidValue;
     if (!tmap2d(&tH, hbuf, rrows, I, (int)eb, 128)) return cudaErrorInvalidValue;
-    if (!tmap2d(&tDN, L.dn, (int64_t)E * H, I, (int)eb, BN)) return cudaErrorInvalidValue;
+    if (!tmap2d(&tDN, L.dn, (int64_t)E * H, I, (int)eb, BN2)) return cudaErrorInvalidValue;
 
     // Cooperative launch: refused unless every CTA can be resident at once,
     // which the counter waits between CTAs rely on.
@@ -916,7 +930,7 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (mx) {
-        using C = GemmCfg<128, true, false, kEpiSwiGLU, 6, 2>;
+        using C = GemmCfg<256, true, false, kEpiSwiGLU, 4, 1>;
         ensure_smem_attr(reinterpret_cast<const void*>(mega_kernel<true>), C::kSmemBytes);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         e = cudaLaunchKernelEx(&cfg, mega_kernel<true>, tR, tGU, tH, tDN, p);

@@ -168,7 +168,7 @@ combine_kernel(const __nv_bfloat16* __restrict__ partials, const float* __restri
 template <bool MX>
 __global__ void __launch_bounds__(256)
 pack_kernel(const __nv_bfloat16* __restrict__ src0, const __nv_bfloat16* __restrict__ src1, int K, int Nsrc,
-            int il, void* __restrict__ dst, uint8_t* __restrict__ dst_sf) {
+            int il, void* __restrict__ dst, uint8_t* __restrict__ dst_sf, int sf_tile) {
     const int Ndst = src1 ? 2 * Nsrc : Nsrc;
     const int e = blockIdx.z;
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
@@ -209,8 +209,14 @@ pack_kernel(const __nv_bfloat16* __restrict__ src0, const __nv_bfloat16* __restr
         uint4* d = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst) + grow * K + kb * 32);
         d[0] = make_uint4(w[0], w[1], w[2], w[3]);
         d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        const int64_t rt = grow / kTileM;
-        dst_sf[(rt * (K / 128) + kb / 4) * 512 + sf_chunk_offset((int)(grow % kTileM), kb & 3)] = (uint8_t)code;
+        if (sf_tile == 224) {
+            const int64_t nt = grow / 224;
+            const int rr = (int)(grow % 224);
+            dst_sf[((nt * (K / 128) + kb / 4) * 2 + rr / 128) * 512 + sf_chunk_offset(rr % 128, kb & 3)] = (uint8_t)code;
+        } else {
+            const int64_t rt = grow / kTileM;
+            dst_sf[(rt * (K / 128) + kb / 4) * 512 + sf_chunk_offset((int)(grow % kTileM), kb & 3)] = (uint8_t)code;
+        }
     }
 }
 
@@ -370,15 +376,17 @@ cudaError_t launch_combine(const void* partials, const float* w, const float* sh
 }
 
 cudaError_t launch_pack(bool mx, const void* src0, const void* src1, int E, int K, int Nsrc, int il, void* dst,
-                        uint8_t* dst_sf, cudaStream_t s) {
+                        uint8_t* dst_sf, int sf_tile, cudaStream_t s) {
     const int Ndst = src1 ? 2 * Nsrc : Nsrc;
     dim3 grid(ceil_div(Ndst, 128), K / 32, E);
     if (mx)
         pack_kernel<true><<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src0),
-                                               static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf);
+                                               static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf,
+                                               sf_tile);
     else
         pack_kernel<false><<<grid, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src0),
-                                                static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf);
+                                                static_cast<const __nv_bfloat16*>(src1), K, Nsrc, il, dst, dst_sf,
+                                                sf_tile);
     return cudaGetLastError();
 }
 

@@ -20,14 +20,23 @@ cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, 
                             const void* scale_src, const float* wslot, cudaStream_t s);
 cudaError_t launch_combine(const void* partials, const float* w, const float* shared, void* out, int T, int H,
                            int k, cudaStream_t s);
+// MXFP8 scales go per tile of sf_tile rows (128, or 224 for the down
+// weights when H % 224 == 0: two 512-byte chunks per tile and K-chunk).
 cudaError_t launch_pack(bool mx, const void* src0, const void* src1, int E, int K, int Nsrc, int il, void* dst,
-                        uint8_t* dst_sf, cudaStream_t s);
+                        uint8_t* dst_sf, int sf_tile, cudaStream_t s);
 // stage 0: gw, dl; stage 1: dX, dW_r
 cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* w, const int32_t* idx,
                              const void* x, const float* WrT, const void* da, int T, int H, int E, int k, float* gw,
                              float* dl, float* dl_full, float* dwr_part, void* dX, float* dWr, int stage,
                              cudaStream_t s);
 int64_t dwr_partial_floats(int H, int E);
+
+// N-tile of the down GEMM; MXFP8 down weights keep their block scales per
+// tile of this many rows.
+inline int down_tile_n(int H, bool mx) {
+    if (mx) return H % 224 == 0 ? 224 : 128;
+    return H % 256 == 0 ? 256 : 128;
+}
 
 // gemm.cu
 // Raise a kernel's dynamic shared memory limit (per device) to at least `bytes`.

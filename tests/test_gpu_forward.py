@@ -17,6 +17,8 @@ FWD_CASES = [
     # MXFP8 operands, skewed routing
     synth.small("ragged_mx", T=600, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
     synth.small("mx_k8", T=200, H=1024, I=512, E=32, k=8, dtype="mxfp8"),
+    # MXFP8 down GEMM on 224-wide tiles (H = 4 x 224), scales per 224-row tile
+    synth.small("mx_h896", T=700, H=896, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
     # BF16 shared expert added to MXFP8 routed experts
     synth.small("mx_shared", T=300, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2, shared_I=256),
     # one token; one expert with k=1 (dense SwiGLU)

@@ -18,6 +18,7 @@ CASES = [
     synth.small("mega_bf16_skew", T=600, H=256, I=2048, E=8, k=4, zipf_s=1.2),
     synth.small("mega_mx", T=1000, H=512, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
     synth.small("mega_mx_k8", T=300, H=1024, I=512, E=32, k=8, dtype="mxfp8"),
+    synth.small("mega_mx_h896", T=700, H=896, I=256, E=8, k=2, dtype="mxfp8", zipf_s=1.2),
 ]
 
 
