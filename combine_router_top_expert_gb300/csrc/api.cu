@@ -113,7 +113,8 @@ mok_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_E
 
 constexpr int kDefaultMovers = 8;
 
-// Megakernel tile width: both GEMMs use the same N-tile (BF16 256, MXFP8 128).
+// Megakernel tiles: gate/up 256 wide (gate 128 | up 128), down as the staged
+// down GEMM (down_tile_n).
 bool mega_supported(const mok_problem* p) {
     return (2 * p->I) % 256 == 0 && p->H % down_tile_n(p->H, p->dtype == MOK_MXFP8) == 0;
 }
@@ -466,7 +467,7 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
     float* part = reinterpret_cast<float*>(ws + L.part);
     float* WrT = reinterpret_cast<float*>(ws + L.wrt);
     // reverse-combine (pull): dy rows in expert order, gate gradients
-    if (e == cudaSuccess) e = launch_transpose_wr(a->W_r, WrT, H, E, s);
+    if (e == cudaSuccess) e = launch_transpose_wr(a->W_r, WrT, H, E, 1, s);
     if (e == cudaSuccess)
         e = launch_dispatch(false, a->dY, T, H, E, k, r.counts, r.offsets, r.row_src, dy, nullptr, a->dY, r.topk_w, s);
     if (e == cudaSuccess)

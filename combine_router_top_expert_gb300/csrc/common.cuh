@@ -46,6 +46,7 @@ enum WaitSite : int32_t {
     kSiteEpiAccFull = 4,
     kSiteDrain = 5,
     kSiteCounter = 6,
+    kSiteRouterChunk = 7,
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

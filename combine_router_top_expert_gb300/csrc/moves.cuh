@@ -10,7 +10,8 @@ size_t route_workspace_bytes(int T, int H, int E, int k);
 cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,
                                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_src, int32_t* slot_row, void* ws, cudaStream_t s);
-cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, cudaStream_t s);
+// W_r [H, E] -> `copies` identical copies of WrT [E, H], back to back.
+cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, int copies, cudaStream_t s);
 
 // moves.cu
 // Gather rows into the padded expert-contiguous layout. BF16 with `wslot`:

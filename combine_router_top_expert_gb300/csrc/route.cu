@@ -13,16 +13,63 @@
 //                       permutation row_src / slot_row
 #include "common.cuh"
 #include "moves.cuh"
+#include "tc.cuh"
 
 namespace mok {
 
-constexpr int kRouteTT = 16;       // tokens per CTA
-constexpr int kRouteThreads = 256;
+constexpr int kRouteTTMax = 32;    // tokens per CTA, at most
+constexpr int kRouteTTMin = 4;     // tokens per CTA, at least (sizes the histogram)
+constexpr int kRouteThreads = 256; // layout kernel
+constexpr int kTopkThreads = 512;  // top-k kernel: 8 expert quads x 2 token groups
 constexpr int kRouteChunk = 256;   // h values per pipeline chunk (32 lanes x 8)
+constexpr uint64_t kRouteTimeoutNs = 4000000000ull;   // bound on every wait of the top-k kernel
 
-// W_r [H, E] -> WrT [E, H] so each expert's weights are contiguous.
-__global__ void transpose_wr_kernel(const float* __restrict__ W_r, float* __restrict__ WrT, int H, int E) {
+// Router weights in the order the top-k kernel streams them: per 256-wide h
+// chunk c and 32-expert group g one contiguous 32 KB block [32 experts][256],
+// zero-padded past H and E, and inside each 256-wide row h = 8L + 4j + i
+// stored at j*128 + 4L + i (so lane L reads its 8 values as two conflict-free
+// 16-byte words). One bulk copy then moves a whole chunk into shared memory.
+__host__ __device__ inline int64_t router_chunk_floats() { return 32 * (int64_t)kRouteChunk; }
+__host__ __device__ inline int64_t router_copy_floats(int E, int H) {
+    return (int64_t)ceil_div(H, kRouteChunk) * ceil_div(E, 32) * router_chunk_floats();
+}
+
+// Identical copies of that layout (at most 16, at most 4 MB in all): every
+// CTA streams the same chunks at about the same time, and reading one of
+// several copies spreads those reads over more L2 slices.
+int route_wr_copies(int E, int H) {
+    const int64_t one = router_copy_floats(E, H) * 4;
+    int64_t r = one > 0 ? ((int64_t)4 << 20) / one : 1;
+    return (int)(r < 1 ? 1 : r > 16 ? 16 : r);
+}
+
+__device__ __forceinline__ int router_h_pos(int hl) { return ((hl >> 2) & 1) * 128 + (hl >> 3) * 4 + (hl & 3); }
+
+// W_r [H, E] -> the chunk layout above, copy blockIdx.z. Grid: (8 * chunks,
+// expert groups, copies), block (32, 8).
+__global__ void router_weight_layout_kernel(const float* __restrict__ W_r, float* __restrict__ dst_copies, int H,
+                                            int E) {
     __shared__ float tile[32][33];
+    const int EG = ceil_div(E, 32);
+    float* __restrict__ dst = dst_copies + (int64_t)blockIdx.z * router_copy_floats(E, H);
+    const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int h = h0 + i, e = e0 + threadIdx.x;
+        tile[i][threadIdx.x] = (h < H && e < E) ? W_r[(int64_t)h * E + e] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int h = h0 + threadIdx.x;   // expert e0 + i: row i of group blockIdx.y
+        const int c = h / kRouteChunk, hl = h % kRouteChunk;
+        dst[(((int64_t)c * EG + blockIdx.y) * 32 + i) * kRouteChunk + router_h_pos(hl)] = tile[threadIdx.x][i];
+    }
+}
+
+// W_r [H, E] -> `copies` identical copies of WrT [E, H] (the backward's
+// layout), back to back.
+__global__ void transpose_wr_kernel(const float* __restrict__ W_r, float* __restrict__ WrT_copies, int H, int E) {
+    __shared__ float tile[32][33];
+    float* __restrict__ WrT = WrT_copies + (int64_t)blockIdx.z * E * H;   // copy blockIdx.z
     int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
         int h = h0 + i, e = e0 + threadIdx.x;
@@ -40,120 +87,172 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
     return va > vb || (va == vb && ea < eb);
 }
 
-// 16-byte global -> shared copy that bypasses L1; `bytes` = 0 fills zeros.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int bytes) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// One CTA = kRouteTT tokens x all experts. Warp w owns experts
-// eg + 4w .. eg + 4w + 3 of each 32-expert group eg; lane c owns summation
-// chain c (h = 256*i + 8*c + m). The x and router-weight chunks of 256 h
-// values stream through a double-buffered shared-memory pipeline (cp.async),
-// so chunk i+1 is in flight while chunk i is multiplied. Dynamic shared
-// memory:
-//   xs [2][kRouteTT][256] bf16 | ws [2][32][256] f32 | lg [kRouteTT][E] f32 |
-//   slog [kRouteTT][k] f32 | cnt [E] i32
-__global__ void __launch_bounds__(kRouteThreads)
-route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ WrT,
-                  const float* __restrict__ bias, int T, int H, int E, int k,
-                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ hist) {
-    extern __shared__ __align__(16) unsigned char route_smem[];
-    __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(route_smem);
-    float* ws = reinterpret_cast<float*>(route_smem + 2 * kRouteTT * kRouteChunk * 2);
-    float* lg = ws + 2 * 32 * kRouteChunk;
-    float* slog = lg + kRouteTT * E;
-    int32_t* cnt = reinterpret_cast<int32_t*>(slog + kRouteTT * k);
+// One CTA = TT = 2*TW tokens x all experts, 16 warps. Warp w owns experts
+// 4*(w%8) .. +3 of each 32-expert group and tokens TW*(w/8) .. +TW-1; lane
+// L owns summation chain L (h = 256*i + 8*L + m). The chunks (c, g) of the
+// router weights (one 32 KB bulk copy each, from the layout above) and the
+// matching raw x rows (one bulk copy per token) stream through a STAGES-deep
+// shared-memory ring, one mbarrier per slot; thread 0 issues the copies. x
+// is converted to fp32 once per CTA, one chunk ahead, into a double buffer,
+// so the inner loop is fused multiply-adds fed by conflict-free 16-byte
+// shared loads. Every wait is bounded: after a timeout the status block
+// records it, no thread waits again, and the CTA runs to its end (its
+// results are then garbage; the caller sees MOK_ERR_TIMEOUT).
+// Dynamic shared memory:
+//   bars [STAGES] u64 (128 B) | ws [STAGES][32][256] f32 | xr [STAGES][TT][256] bf16 |
+//   xf [2][TT][256] f32 | lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
+template <int TW, int STAGES>
+__global__ void __launch_bounds__(kTopkThreads)
+route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr_copies, int wr_copies,
+                  const float* __restrict__ bias, int T, int H, int E, int k, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_w, int32_t* __restrict__ hist, StatusBlock* st, uint64_t tmo) {
+    constexpr int TT = 2 * TW;
+    constexpr int NT = kTopkThreads;
+    static_assert(TT <= kRouteTTMax && TT >= kRouteTTMin && STAGES >= 3 && STAGES <= 16, "router tile");
+    extern __shared__ __align__(128) unsigned char route_smem[];
+    const uint32_t bar0 = tc::smem_u32(route_smem);
+    float* ws = reinterpret_cast<float*>(route_smem + 128);
+    __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(ws + STAGES * 32 * kRouteChunk);
+    float* xf = reinterpret_cast<float*>(xr + STAGES * TT * kRouteChunk);
+    float* lg = xf + 2 * TT * kRouteChunk;
+    float* slog = lg + TT * E;
+    int32_t* cnt = reinterpret_cast<int32_t*>(slog + TT * k);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * kRouteTT;
-    const int ntok = min(kRouteTT, T - t0);
+    const int quad = warp & 7, tg = warp >> 3;
+    const int t0 = blockIdx.x * TT;
+    const int ntok = min(TT, T - t0);
     const int nchunks = ceil_div(H, kRouteChunk);
+    const int EG = ceil_div(E, 32);
+    const int total = nchunks * EG;   // chunk sequence n = g * nchunks + c
+    const float* __restrict__ Wr = Wr_copies + (int64_t)(blockIdx.x % wr_copies) * total * router_chunk_floats();
 
-    for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+    for (int e = tid; e < E; e += NT) cnt[e] = 0;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) tc::mbar_init(bar0 + 8u * s, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
 
-    // issue the copies of chunk c (expert group eg) into buffer b
-    auto load_chunk = [&](int eg, int c, int b) {
-        const int h0 = c * kRouteChunk;
-        __nv_bfloat16* xb = xs + b * kRouteTT * kRouteChunk;
-        float* wb = ws + b * 32 * kRouteChunk;
-        for (int v = tid; v < kRouteTT * (kRouteChunk / 8); v += kRouteThreads) {
-            const int t = v / (kRouteChunk / 8), c8 = (v % (kRouteChunk / 8)) * 8;
-            const bool ok = t < ntok && h0 + c8 < H;
-            const __nv_bfloat16* src = ok ? x + (int64_t)(t0 + t) * H + h0 + c8 : x;
-            cp_async16(xb + t * kRouteChunk + c8, src, ok ? 16 : 0);
+    bool ok = true;
+    int issued = 0, seen = 0;   // thread 0: chunks issued / chunks it has seen land
+    // thread 0: the copies of chunk n into slot n % STAGES (nothing more
+    // once one of its waits gave up)
+    auto issue = [&](int n) {
+        if (!ok || n >= total) return;
+        issued = n + 1;
+        const int g = n / nchunks, c = n % nchunks, slot = n % STAGES;
+        const int h0 = c * kRouteChunk, hw = min(kRouteChunk, H - h0);
+        const uint32_t bar = bar0 + 8u * slot;
+        tc::mbar_expect_tx(bar, (uint32_t)(router_chunk_floats() * 4 + (int64_t)ntok * hw * 2));
+        tc::bulk_load(tc::smem_u32(ws + slot * 32 * kRouteChunk),
+                      Wr + ((int64_t)c * EG + g) * router_chunk_floats(), (uint32_t)(router_chunk_floats() * 4), bar);
+        const uint32_t xd = tc::smem_u32(xr + slot * TT * kRouteChunk);
+        for (int t = 0; t < ntok; ++t)
+            tc::bulk_load(xd + t * kRouteChunk * 2, x + (int64_t)(t0 + t) * H + h0, (uint32_t)hw * 2, bar);
+    };
+    auto wait = [&](int n) {
+        if (ok && n < total) {
+            ok = tc::mbar_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1), st, tmo, kSiteRouterChunk);
+            if (ok) seen = n + 1;
         }
-        for (int v = tid; v < 32 * (kRouteChunk / 4); v += kRouteThreads) {
-            const int e = v / (kRouteChunk / 4), c4 = (v % (kRouteChunk / 4)) * 4;
-            const bool ok = eg + e < E && h0 + c4 < H;
-            const float* src = ok ? WrT + (int64_t)(eg + e) * H + h0 + c4 : WrT;
-            cp_async16(wb + e * kRouteChunk + c4, src, ok ? 16 : 0);
+    };
+    // raw x of slot b -> fp32 buffer d (the h order above)
+    auto convert_x = [&](int b, int d) {
+        const __nv_bfloat16* xb = xr + b * TT * kRouteChunk;
+        for (int v = tid; v < TT * (kRouteChunk / 8); v += NT) {
+            const int t = v / (kRouteChunk / 8), L = v % (kRouteChunk / 8);
+            const uint4 r = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * L);
+            float* o = xf + (d * TT + t) * kRouteChunk + 4 * L;
+            *reinterpret_cast<float4*>(o) = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
+            *reinterpret_cast<float4*>(o + 128) = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
         }
-        cp_async_commit();
     };
 
-    for (int eg = 0; eg < E; eg += 32) {
-        float acc[kRouteTT][4];
+    if (tid == 0)
+        for (int n = 0; n < STAGES - 1; ++n) issue(n);
+    wait(0);
+    convert_x(0, 0);
+    float acc[TW][4];
+    for (int n = 0; n < total; ++n) {
+        wait(n + 1);       // its x is converted below
+        __syncthreads();   // x(n) converted by every thread; chunk n - 1 consumed
+        if (tid == 0) issue(n + STAGES - 1);   // into slot (n - 1) % STAGES
+        if (n + 1 < total) convert_x((n + 1) % STAGES, (n + 1) & 1);
+        const int g = n / nchunks, c = n % nchunks;
+        if (c == 0) {
 #pragma unroll
-        for (int t = 0; t < kRouteTT; ++t)
+            for (int t = 0; t < TW; ++t)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
-
-        __syncthreads();  // buffers free (previous expert group done)
-        load_chunk(eg, 0, 0);
-        for (int c = 0; c < nchunks; ++c) {
-            if (c + 1 < nchunks) {
-                load_chunk(eg, c + 1, (c + 1) & 1);
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
-            __syncthreads();
-            const int h0 = c * kRouteChunk;
-            const __nv_bfloat16* xb = xs + (c & 1) * kRouteTT * kRouteChunk;
-            const float* wb = ws + (c & 1) * 32 * kRouteChunk;
-            if (h0 + 8 * lane < H) {
-                float wv[4][8];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float4 a = *reinterpret_cast<const float4*>(wb + (4 * warp + q) * kRouteChunk + 8 * lane);
-                    float4 b = *reinterpret_cast<const float4*>(wb + (4 * warp + q) * kRouteChunk + 8 * lane + 4);
-                    wv[q][0] = a.x; wv[q][1] = a.y; wv[q][2] = a.z; wv[q][3] = a.w;
-                    wv[q][4] = b.x; wv[q][5] = b.y; wv[q][6] = b.z; wv[q][7] = b.w;
-                }
-#pragma unroll
-                for (int t = 0; t < kRouteTT; ++t) {
-                    uint4 xv = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * lane);
-                    float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
-                                   bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-#pragma unroll
-                        for (int m = 0; m < 8; ++m) acc[t][q] = fmaf(xf[m], wv[q][m], acc[t][q]);
-                }
-            }
-            __syncthreads();  // buffer (c & 1) may be refilled by the next iteration
+                for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
         }
-        // butterfly across the 32 chains, then the bias
-#pragma unroll
-        for (int t = 0; t < kRouteTT; ++t)
+        const float* wb = ws + (n % STAGES) * 32 * kRouteChunk;
+        const float* xb = xf + ((n & 1) * TT + tg * TW) * kRouteChunk;
+        if (c * kRouteChunk + 8 * lane < H) {
+            float wv[4][8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                float s = acc[t][q];
+                const float* wr = wb + (4 * quad + q) * kRouteChunk + 4 * lane;
+                const float4 a = *reinterpret_cast<const float4*>(wr);
+                const float4 b = *reinterpret_cast<const float4*>(wr + 128);
+                wv[q][0] = a.x; wv[q][1] = a.y; wv[q][2] = a.z; wv[q][3] = a.w;
+                wv[q][4] = b.x; wv[q][5] = b.y; wv[q][6] = b.z; wv[q][7] = b.w;
+            }
+            // two tokens at a time, h (m) outermost: each step issues 8
+            // independent FMAs, one per (token, expert) chain; every chain
+            // accumulates its h values in ascending order
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) s = s + __shfl_xor_sync(0xffffffffu, s, off);
-                int e = eg + 4 * warp + q;
-                if (lane == 0 && e < E && t < ntok) lg[t * E + e] = bias ? s + bias[e] : s;
+            for (int t2 = 0; t2 < TW; t2 += 2) {
+                float xv[2][8];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (t2 + u < TW) {
+                        const float* xr2 = xb + (t2 + u) * kRouteChunk + 4 * lane;
+                        const float4 a = *reinterpret_cast<const float4*>(xr2);
+                        const float4 b = *reinterpret_cast<const float4*>(xr2 + 128);
+                        xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+                        xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
+                    }
+                }
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (t2 + u < TW) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[t2 + u][q] = fmaf(xv[u][m], wv[q][m], acc[t2 + u][q]);
+                        }
+            }
+        }
+        if (c == nchunks - 1) {
+            // butterfly across the 32 chains, then the bias
+#pragma unroll
+            for (int t = 0; t < TW; ++t)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float s = acc[t][q];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) s = s + __shfl_xor_sync(0xffffffffu, s, off);
+                    const int e = 32 * g + 4 * quad + q, tt = tg * TW + t;
+                    if (lane == 0 && e < E && tt < ntok) lg[tt * E + e] = bias ? s + bias[e] : s;
+                }
+        }
+    }
+    if (tid == 0 && seen < issued) {
+        // a wait gave up: let the copies still in flight (at most one per
+        // slot) land before the CTA exits, within the same time bound
+        const uint64_t start = globaltimer_ns();
+        for (int n = seen; n < issued; ++n)
+            while (!tc::mbar_try_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1)) &&
+                   globaltimer_ns() - start < tmo) {
             }
     }
     __syncthreads();
 
     // top-k per token: warp w takes tokens w, w + 8, ...
     const int nq = (E + 31) / 32;
-    for (int t = warp; t < ntok; t += kRouteThreads / 32) {
+    for (int t = warp; t < ntok; t += NT / 32) {
         float v[kMaxE / 32];
 #pragma unroll
         for (int q = 0; q < kMaxE / 32; ++q) {
@@ -195,29 +294,29 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         for (int j = lane; j < k; j += 32) topk_w[(int64_t)(t0 + t) * k + j] = expf(slog[t * k + j] - l0) / den;
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kRouteThreads) hist[(int64_t)blockIdx.x * E + e] = cnt[e];
+    for (int e = tid; e < E; e += NT) hist[(int64_t)blockIdx.x * E + e] = cnt[e];
 }
 
-size_t route_topk_smem_bytes(int E, int k) {
-    return (size_t)2 * kRouteTT * kRouteChunk * 2 + 2 * 32 * kRouteChunk * 4 + (size_t)kRouteTT * E * 4 +
-           (size_t)kRouteTT * k * 4 + (size_t)E * 4;
+size_t route_topk_smem_bytes(int TT, int STAGES, int E, int k) {
+    return (size_t)128 + (size_t)STAGES * 32 * kRouteChunk * 4 + (size_t)STAGES * TT * kRouteChunk * 2 +
+           (size_t)2 * TT * kRouteChunk * 4 + (size_t)TT * E * 4 + (size_t)TT * k * 4 + (size_t)E * 4;
 }
 
 // Counts, offsets and the stable (expert, token) permutation. CTA b handles
-// the same kRouteTT tokens as route_topk_kernel's CTA b: its rows for expert e
+// the same tt tokens as route_topk_kernel's CTA b: its rows for expert e
 // start at offsets[e] + (rows of e in CTAs < b).
 __global__ void __launch_bounds__(kRouteThreads)
 route_layout_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ hist, int T, int E,
-                    int k, int nblocks, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                    int k, int tt, int nblocks, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                     int32_t* __restrict__ row_src, int32_t* __restrict__ slot_row) {
     __shared__ int32_t pre[kMaxE], tot[kMaxE], off[kMaxE + 1];
     __shared__ int32_t part[kRouteThreads];
     __shared__ int32_t part2[kRouteThreads];
-    __shared__ unsigned char sel[kRouteTT][kMaxE];
+    __shared__ unsigned char sel[kRouteTTMax][kMaxE];
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
-    const int t0 = b * kRouteTT;
-    const int ntok = min(kRouteTT, T - t0);
+    const int t0 = b * tt;
+    const int ntok = min(tt, T - t0);
 
     // per-expert sums over blocks (before b, and over all): `per` threads
     // share one expert, then combine their partial sums
@@ -250,7 +349,7 @@ route_layout_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
         for (int e = 0; e < E; ++e) { off[e] = s; s += tot[e]; }
         off[E] = s;
     }
-    for (int i = tid; i < kRouteTT * E; i += kRouteThreads) sel[i / E][i % E] = 0;
+    for (int i = tid; i < kRouteTTMax * E; i += kRouteThreads) sel[i / E][i % E] = 0;
     __syncthreads();
     if (b == 0) {
         for (int e = tid; e < E; e += kRouteThreads) counts[e] = tot[e];
@@ -275,39 +374,94 @@ route_layout_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     }
 }
 
-cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, cudaStream_t s) {
-    transpose_wr_kernel<<<dim3(ceil_div(H, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(W_r, WrT, H, E);
+cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, int copies, cudaStream_t s) {
+    transpose_wr_kernel<<<dim3(ceil_div(H, 32), ceil_div(E, 32), copies), dim3(32, 8), 0, s>>>(W_r, WrT, H, E);
     return cudaGetLastError();
 }
 
+// status | router weight copies | per-CTA expert histogram
 size_t route_workspace_bytes(int T, int H, int E, int k) {
     (void)k;
-    int nblocks = ceil_div(T, kRouteTT);
-    return (size_t)kStatusBytes + align_up((int64_t)E * H * 4, 256) + align_up((int64_t)nblocks * E * 4, 256);
+    int nblocks = ceil_div(T, kRouteTTMin);
+    return (size_t)kStatusBytes + align_up((int64_t)route_wr_copies(E, H) * router_copy_floats(E, H) * 4, 256) +
+           align_up((int64_t)nblocks * E * 4, 256);
+}
+
+cudaError_t launch_router_weight_layout(const float* W_r, float* dst, int H, int E, int copies, cudaStream_t s) {
+    router_weight_layout_kernel<<<dim3(8 * ceil_div(H, kRouteChunk), ceil_div(E, 32), copies), dim3(32, 8), 0, s>>>(
+        W_r, dst, H, E);
+    return cudaGetLastError();
+}
+
+// Launch the top-k kernel with 2*TW tokens per CTA and a STAGES-deep ring.
+template <int TW, int STAGES>
+cudaError_t launch_topk_variant(const __nv_bfloat16* x, const float* Wr, int wr_copies, const float* bias, int T,
+                                int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* hist,
+                                StatusBlock* st, uint64_t timeout_ns, cudaStream_t s) {
+    const size_t smem = route_topk_smem_bytes(2 * TW, STAGES, E, k);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    auto kern = route_topk_kernel<TW, STAGES>;
+    if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
+    kern<<<ceil_div(T, 2 * TW), kTopkThreads, smem, s>>>(x, Wr, wr_copies, bias, T, H, E, k, topk_idx, topk_w, hist,
+                                                         st, timeout_ns);
+    return cudaGetLastError();
+}
+
+// Tokens per CTA (2*TW, TW in {2, 4, 9, 14}). One CTA per SM; a CTA's time
+// is about (fixed cost of streaming every weight chunk, worth ~5 tokens per
+// warp) + TW, so the kernel takes about rounds x (TW + 5), rounds = CTAs
+// over SMs. Pick the cheapest that fits shared memory, larger tiles on ties.
+constexpr int kRouteStages(int tw) { return tw == 14 ? 3 : 4; }
+int route_tokens_per_cta(int T, int num_sms, int E, int k) {
+    const int tws[4] = {14, 9, 4, 2};
+    int best = 2;
+    int64_t best_cost = -1;
+    for (int tw : tws) {
+        if (route_topk_smem_bytes(2 * tw, kRouteStages(tw), E, k) > 227 * 1024) continue;
+        const int64_t rounds = ceil_div(ceil_div(T, 2 * tw), num_sms > 0 ? num_sms : 1);
+        const int64_t cost = rounds * (tw + 5);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tw; }
+    }
+    return 2 * best;
+}
+
+cudaError_t launch_route_topk(const __nv_bfloat16* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                              int tt, int32_t* topk_idx, float* topk_w, int32_t* hist, StatusBlock* st,
+                              uint64_t tmo, cudaStream_t s) {
+    const int r = route_wr_copies(E, H);
+    if (tt == 28) return launch_topk_variant<14, kRouteStages(14)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist,
+                                                                   st, tmo, s);
+    if (tt == 18) return launch_topk_variant<9, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
+    if (tt == 8) return launch_topk_variant<4, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
+    if (tt == 4) return launch_topk_variant<2, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,
                                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_src, int32_t* slot_row, void* ws, cudaStream_t s) {
     char* base = static_cast<char*>(ws) + kStatusBytes;
-    float* WrT = reinterpret_cast<float*>(base);
-    int32_t* hist = reinterpret_cast<int32_t*>(base + align_up((int64_t)E * H * 4, 256));
-    int nblocks = ceil_div(T, kRouteTT);
+    float* Wr = reinterpret_cast<float*>(base);
+    const int copies = route_wr_copies(E, H);
+    int32_t* hist = reinterpret_cast<int32_t*>(base + align_up((int64_t)copies * router_copy_floats(E, H) * 4, 256));
+    cudaError_t err = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+    if (err != cudaSuccess) return err;
     if (T == 0) {
         cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
         return cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
     }
-    transpose_wr_kernel<<<dim3(ceil_div(H, 32), ceil_div(E, 32)), dim3(32, 8), 0, s>>>(W_r, WrT, H, E);
-    cudaError_t err = cudaGetLastError();
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int tt = route_tokens_per_cta(T, sms, E, k);
+    const int nblocks = ceil_div(T, tt);
+    err = launch_router_weight_layout(W_r, Wr, H, E, copies, s);
     if (err != cudaSuccess) return err;
-    size_t smem = route_topk_smem_bytes(E, k);
-    if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(route_topk_kernel), (int)smem);
-    route_topk_kernel<<<nblocks, kRouteThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(x), WrT, bias, T, H, E,
-                                                        k, topk_idx, topk_w, hist);
+    err = launch_route_topk(static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, k, tt, topk_idx, topk_w, hist,
+                            static_cast<StatusBlock*>(ws), kRouteTimeoutNs, s);
     // the layout kernel must never run on top-k results that were not produced
-    err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    route_layout_kernel<<<nblocks, kRouteThreads, 0, s>>>(topk_idx, hist, T, E, k, nblocks, counts, offsets,
+    route_layout_kernel<<<nblocks, kRouteThreads, 0, s>>>(topk_idx, hist, T, E, k, tt, nblocks, counts, offsets,
                                                           row_src, slot_row);
     return cudaGetLastError();
 }

@@ -99,7 +99,11 @@ typedef struct {
 /* token, keep each expert's tokens adjacent for the grouped GEMM).           */
 /* ------------------------------------------------------------------------- */
 
-/* Workspace bytes mok_route_layout needs (device memory, any content). */
+/* Workspace bytes mok_route_layout needs (device memory, any content): a
+ * 256-byte status block first (read it with mok_device_status), then the
+ * router weights re-laid out in the order the kernel streams them (fp32,
+ * padded to 256-wide h chunks and 32-expert groups; up to 4 MB of identical
+ * copies), then per-block expert histograms. */
 size_t mok_route_workspace_size(int32_t T, int32_t H, int32_t E, int32_t k);
 
 /* logits[t,e] = sum_h x[t,h] * W_r[h,e] (+ bias[e]) in binary32, in this fixed
@@ -114,7 +118,11 @@ size_t mok_route_workspace_size(int32_t T, int32_t H, int32_t E, int32_t k);
  *   x [T,H] bf16, W_r [H,E] f32, bias [E] f32 or NULL;
  *   outputs topk_idx [T,k] i32, topk_w [T,k] f32, counts [E] i32,
  *   offsets [E+1] i32, row_src [T*k] i32, slot_row [T*k] i32.
- * Logits must be finite (non-finite inputs give unspecified routing). */
+ * Logits must be finite (non-finite inputs give unspecified routing).
+ * Requires H % 8 == 0, x 16-byte aligned, workspace 256-byte aligned.
+ * Device-side waits are bounded: one that gives up is recorded in the
+ * workspace's status block (mok_device_status: MOK_ERR_TIMEOUT) and the
+ * outputs are then unspecified. */
 mok_status mok_route_layout(const void* x, const float* W_r, const float* bias,
                             int32_t T, int32_t H, int32_t E, int32_t k,
                             int32_t* topk_idx, float* topk_w, int32_t* counts,
@@ -298,8 +306,9 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.
  *   - Problems whose scratch exceeds the array (mok_route_workspace_size(T, H,
- *     E, k) > MOK_ROUTE_STATIC_SCRATCH_BYTES; e.g. E*H*4 bytes of transposed
- *     router weights must fit) return MOK_ERR_INVALID; nothing is enqueued.
+ *     E, k) > MOK_ROUTE_STATIC_SCRATCH_BYTES; e.g. one copy of the re-laid
+ *     router weights, about E*H*4 bytes, must fit) return MOK_ERR_INVALID;
+ *     nothing is enqueued.
  *   - All calls on a device share that device's array, which keeps the last
  *     call's contents; the kernels overwrite every byte they read, so nothing
  *     needs clearing, but calls that overlap on the same GPU (e.g. issued on

@@ -15,6 +15,9 @@ CASES = [
     dict(T=257, H=384, E=256, k=16),
     dict(T=40, H=128, E=5, k=5),
     dict(T=33, H=1152, E=64, k=1),
+    # enough tokens for the 18- and 28-token CTA tiles on a 152-SM part
+    dict(T=2600, H=256, E=64, k=6),
+    dict(T=4096, H=384, E=32, k=8),
 ]
 
 
