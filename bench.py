@@ -44,9 +44,10 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """nvidia-smi clock/throttle samples while the steps run; the SM clock is
+    the median over samples taken under load (GPU utilisation >= 50%)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -59,10 +60,18 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def wait_first(self, timeout_s=3.0):
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < timeout_s:
+            self.f.flush()
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -76,17 +85,27 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
+            if len(parts) >= 10:
                 rows.append(parts)
         os.unlink(self.path)
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        loaded = [r for r in rows if (num(r[4]) or 0.0) >= 50.0]
+        use = loaded or rows
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in use if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower().startswith("active")})
+        reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_median": statistics.median(pw) if pw else None, "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len(loaded)}
 
 
 def dist_env():
@@ -96,18 +115,37 @@ def dist_env():
     return ws, rank, local
 
 
-def cpu_baseline(inp, wl, n_tokens=48):
-    """The oracle as it stands on a bounded sample of the workload's tokens."""
+def oracle_layer_seconds(inp, wl, t0, n):
+    """Wall time of the oracle as it stands running the layer on tokens
+    [t0, t0+n) of the workload's input, as a layer of n tokens: routing,
+    layout and the expert FFNs (fp64), plus for backward workloads the
+    oracle's backward of those tokens (dX rows and two weight columns)."""
     import oracle
     dt = oracle.MODE_MXFP8 if wl.dtype == "mxfp8" else oracle.MODE_BF16
-    t0 = time.perf_counter()
-    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
-    toks = np.arange(min(n_tokens, wl.T), dtype=np.int32)
-    oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=dt, tokens=toks, shared=inp.shared)
-    dt_s = time.perf_counter() - t0
-    return {"value": len(toks) / dt_s, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"routing of all {wl.T} tokens + layer output of the first {len(toks)} tokens "
-                      f"({len(toks) * wl.k} routed rows), fp64, {dt_s:.1f} s"}
+    x = np.ascontiguousarray(inp.x[t0:t0 + n])
+    t_start = time.perf_counter()
+    r = oracle.route(x, inp.W_r, wl.k, inp.bias)
+    oracle.moe_forward(x, inp.Wg, inp.Wu, inp.Wd, r, mode=dt, shared=inp.shared)
+    if wl.backward:
+        dY = np.ascontiguousarray(inp.dY[t0:t0 + n])
+        oracle.moe_backward_sampled(x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, dY, r, np.arange(n, dtype=np.int32),
+                                    [(0, 0), (wl.E - 1, wl.I - 1)], mode=dt)
+    return time.perf_counter() - t_start
+
+
+def oracle_sample_text(wl, n, steps):
+    what = "forward" + (" + backward (dX rows, 2 weight columns)" if wl.backward else "")
+    return (f"{steps} x {n} tokens of the workload's input, each run as a layer of {n} tokens "
+            f"(routing, layout, {what}; fp64 oracle)")
+
+
+def cpu_baseline(inp, wl, n_tokens=32):
+    """The oracle as it stands on a bounded sample of the workload's tokens."""
+    import oracle
+    n = min(n_tokens, wl.T)
+    dt_s = oracle_layer_seconds(inp, wl, 0, n)
+    return {"value": n / dt_s, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": oracle_sample_text(wl, n, 1) + f", {dt_s:.1f} s"}
 
 
 def run_reference(args, wl):
@@ -117,21 +155,21 @@ def run_reference(args, wl):
     inp = synth.make_inputs(wl)
     import oracle
     oracle.build()
-    n_tok = 16
-    for _ in range(args.warmup):
-        pass  # the oracle has nothing to warm
+    # size each step's sample so all K steps take about two minutes
+    per_token = oracle_layer_seconds(inp, wl, 0, 1)
+    n_tok = int(max(1, min(32, 120.0 / max(1, args.steps) / max(per_token, 1e-6))))
     times = []
-    for _ in range(args.steps):
-        cb = cpu_baseline(inp, wl, n_tokens=n_tok)
-        times.append(n_tok / cb["value"])
+    for i in range(args.steps):
+        t0 = (i * n_tok) % max(1, wl.T - n_tok + 1)
+        times.append(oracle_layer_seconds(inp, wl, t0, n_tok))
     v = n_tok * len(times) / sum(times)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                                             "k": wl.k, "operands": wl.dtype},
-            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "value": v, "unit": "tokens/s",
-                             "sample": f"per step: routing of all tokens + output of {n_tok} tokens"},
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": v, "unit": "tokens/s",
+                             "sample": oracle_sample_text(wl, n_tok, args.steps)},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -139,8 +177,8 @@ def run_reference(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -260,6 +298,11 @@ def main():
         flops = 6.0 * H * wl.I * T * wl.k
         kern = "forward megakernel (dispatch + grouped GEMMs + combine, one launch; plus 2 plan launches)"
 
+    # clocks are sampled from before the warm-up steps to the end of the timed
+    # steps (nvidia-smi needs a moment before its first sample)
+    clocks = ClockSampler(local)
+    clocks.start()
+    clocks.wait_first()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -267,13 +310,11 @@ def main():
     if st[0] != mok.OK:
         raise SystemExit(f"device status after warm-up: {st}")
 
-    clocks = ClockSampler(local)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
     for i in range(args.steps):
         flush.zero_()
         s0, s1, g0, g1 = evs[i]
@@ -292,46 +333,76 @@ def main():
         raise SystemExit(f"device status after timed steps: {st}")
     tokens_per_step = T * len(xs)
 
-    # end to end through the public API with host buffers: pinned inputs in,
-    # route + forward (+ backward), result back to pinned host memory
+    # end to end through the public API with host buffers: every step copies
+    # its inputs in from pinned host memory and its result back out; steps are
+    # pipelined the way a serving loop would run them (copy streams in and out
+    # beside the compute stream, two buffer slots), so the copies of steps i+1
+    # and i-1 overlap the kernels of step i
     x_host = [torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory() for xb in inp.xs]
+    dY_host = (torch.from_numpy(inp.dY.view(np.int16)).view(torch.bfloat16).pin_memory() if wl.backward else None)
+    out_host = [[torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in xs] for _ in range(2)]
+    x_slot = [[torch.empty_like(xb) for xb in xs] for _ in range(2)]
+    dY_slot = [torch.empty_like(dY) for _ in range(2)] if wl.backward else None
+    out_slot = [[torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs] for _ in range(2)]
+    grads_slot = None
     if wl.backward:
-        dY_host = torch.from_numpy(inp.dY.view(np.int16)).view(torch.bfloat16).pin_memory()
-        dY_dev2 = torch.empty_like(dY)
-    out_host = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in xs]
-    x_dev2 = [torch.empty_like(xb) for xb in xs]
+        grads_slot = [dict(dX=out_slot[i][0], dW_gate=torch.empty_like(layer.Wg), dW_up=torch.empty_like(layer.Wu),
+                           dW_down=torch.empty_like(layer.Wd),
+                           dW_r=torch.empty((H, wl.E), dtype=torch.float32, device=dev)) for i in range(2)]
+    route_e2e = [layer.buffers(T, wl.backward)["routing"]] if len(xs) == 1 else routings
+    c_in, c_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_done + ev_out:
+        e.record(stream)
 
-    def e2e_step():
-        for xh, xd in zip(x_host, x_dev2):
-            xd.copy_(xh, non_blocking=True)
-        if wl.backward:
-            dY_dev2.copy_(dY_host, non_blocking=True)
-            layer.forward(x_dev2[0], training=True, cfg=cfg, stream=stream)
-            g = layer.backward(x_dev2[0], dY_dev2, cfg=cfg, stream=stream)
-            out_host[0].copy_(g["dX"], non_blocking=True)
-        elif len(xs) > 1:
-            for xd, rb in zip(x_dev2, routings):
-                mok.route_layout(xd, layer.W_r, wl.k, layer.bias, out=rb, workspace=b["route_ws"], stream=stream)
-            mok.moe_forward_batches(p, x_dev2, layer.packed, routings, outs, ws_b,
+    def e2e_step(sl):
+        c_in.wait_event(ev_done[sl])            # step i-2 finished reading this slot
+        with torch.cuda.stream(c_in):
+            for xh, xd in zip(x_host, x_slot[sl]):
+                xd.copy_(xh, non_blocking=True)
+            if wl.backward:
+                dY_slot[sl].copy_(dY_host, non_blocking=True)
+        ev_in[sl].record(c_in)
+        stream.wait_event(ev_in[sl])
+        stream.wait_event(ev_out[sl])           # step i-2's result has left this slot
+        with torch.cuda.stream(stream):
+            xsl = x_slot[sl]
+            if wl.backward:
+                layer.forward(xsl[0], training=True, cfg=cfg, stream=stream)
+                layer.backward(xsl[0], dY_slot[sl], cfg=cfg, stream=stream, grads=grads_slot[sl])
+            else:
+                for xd, rb in zip(xsl, route_e2e):
+                    mok.route_layout(xd, layer.W_r, wl.k, layer.bias, out=rb, workspace=b["route_ws"],
+                                     stream=stream)
+                if len(xs) > 1:
+                    mok.moe_forward_batches(p, xsl, layer.packed, route_e2e, out_slot[sl], ws_b,
+                                            packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
+                else:
+                    mok.moe_forward(p, xsl[0], layer.packed, route_e2e[0], out_slot[sl][0], b["ws"],
                                     packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
-            for o, oh in zip(outs, out_host):
+        ev_done[sl].record(stream)
+        c_out.wait_event(ev_done[sl])
+        with torch.cuda.stream(c_out):
+            for o, oh in zip(out_slot[sl], out_host[sl]):
                 oh.copy_(o, non_blocking=True)
-        else:
-            y = layer.forward(x_dev2[0], cfg=cfg, stream=stream)
-            out_host[0].copy_(y, non_blocking=True)
+        ev_out[sl].record(c_out)
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(4):
+        e2e_step(i % 2)
     torch.cuda.synchronize(dev)
-    e2e_ms = []
-    for i in range(max(3, args.steps // 2)):
-        flush.zero_()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        e2e_step()
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms.append(a0.elapsed_time(a1))
+    n_e2e = max(4, args.steps)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(c_in)
+    for i in range(n_e2e):
+        e2e_step(i % 2)
+    c_out.wait_event(ev_done[(n_e2e - 1) % 2])
+    a1.record(c_out)
+    torch.cuda.synchronize(dev)
+    e2e_ms = [a0.elapsed_time(a1)]
+    if mok.device_status(status_ws)[0] != mok.OK:
+        raise SystemExit(f"device status after end-to-end steps: {mok.device_status(status_ws)}")
 
     # aggregate over ranks: total tokens / max time
     t_max = total_ms
@@ -343,7 +414,7 @@ def main():
     if rank != 0:
         return
     value = ws * tokens_per_step * args.steps / (t_max / 1000.0)
-    e2e_val = ws * tokens_per_step * len(e2e_ms) / (e2e_max / 1000.0)
+    e2e_val = ws * tokens_per_step * n_e2e / (e2e_max / 1000.0)
     peaks = load_peaks()
     fl = flops
     g_ms = statistics.mean(gemm_ms)
@@ -372,7 +443,10 @@ def main():
                 "h2d_bytes_per_step": tokens_per_step * H * 2 * (2 if wl.backward else 1),
                 "d2h_bytes_per_step": tokens_per_step * H * 2,
                 "api": "mok_route_layout + " + ("mok_moe_forward(training) + mok_moe_backward" if wl.backward else
-                                                "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward")},
+                                                "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward"),
+                "steps": n_e2e,
+                "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams overlap step i's kernels; "
+                              "no L2 flush (each step's working set, the expert weights, is larger than L2)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "stage_ms": {"step_median": statistics.median(step_ms), "timed_kernels_median": statistics.median(gemm_ms)},
