@@ -273,6 +273,8 @@ def main():
         def step(ev=None):
             # route/layout, dispatch, grouped GEMMs, combine (7 launches)
             layer.route(x, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
             mok.dispatch(p, x, rt, A, A_sf, stream=stream)
             if ev is not None:
                 ev[0].record(stream)
@@ -310,16 +312,15 @@ def main():
     if st[0] != mok.OK:
         raise SystemExit(f"device status after warm-up: {st}")
 
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
         flush.zero_()
-        s0, s1, g0, g1 = evs[i]
+        s0, s1, g0, g1, x0 = evs[i]
         s0.record(stream)
-        step((g0, g1))
+        step((g0, g1, x0))
         s1.record(stream)
     torch.cuda.synchronize(dev)
     if ws > 1:
@@ -327,6 +328,31 @@ def main():
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     gemm_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    stage_lines = None
+    if staged and not wl.backward and len(xs) == 1:
+        # the other stages of the staged step, each against its own bound
+        peaks0 = load_peaks()
+        R = T * wl.k
+        eb = 1 if dtype == mok.MXFP8 else 2
+        route_ms = statistics.median(e[0].elapsed_time(e[4]) for e in evs)
+        disp_ms = statistics.median(e[4].elapsed_time(e[2]) for e in evs)
+        comb_ms = statistics.median(e[3].elapsed_time(e[1]) for e in evs)
+        disp_b = T * H * 2 + R * H * eb + (R * H // 32 if dtype == mok.MXFP8 else 0)
+        comb_b = R * H * 2 + R * 4 + T * H * 2
+        fma_peak = 152 * 128 * 2 * 2.07e9 / 1e12   # fp32 FMA: SMs x lanes x 2 FLOP x max SM clock
+        stage_lines = {
+            "route_topk_layout": {"ms": route_ms, "bound": "alu", "unit": "TFLOP/s",
+                                  "achieved": 2.0 * T * wl.E * H / (route_ms / 1e3) / 1e12, "peak": fma_peak,
+                                  "frac": 2.0 * T * wl.E * H / (route_ms / 1e3) / 1e12 / fma_peak,
+                                  "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz",
+                                  "note": "3 launches (weight re-layout, logits + top-k, layout)"},
+            "dispatch": {"ms": disp_ms, "bound": "hbm", "unit": "GB/s", "bytes": disp_b,
+                         "achieved": disp_b / (disp_ms / 1e3) / 1e9, "peak": peaks0["hbm"],
+                         "frac": disp_b / (disp_ms / 1e3) / 1e9 / peaks0["hbm"]},
+            "combine": {"ms": comb_ms, "bound": "hbm", "unit": "GB/s", "bytes": comb_b,
+                        "achieved": comb_b / (comb_ms / 1e3) / 1e9, "peak": peaks0["hbm"],
+                        "frac": comb_b / (comb_ms / 1e3) / 1e9 / peaks0["hbm"]},
+        }
     total_ms = sum(step_ms)
     st = mok.device_status(status_ws)
     if st[0] != mok.OK:
@@ -447,6 +473,7 @@ def main():
                 "steps": n_e2e,
                 "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams overlap step i's kernels; "
                               "no L2 flush (each step's working set, the expert weights, is larger than L2)"},
+        "stage_rooflines": stage_lines,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "stage_ms": {"step_median": statistics.median(step_ms), "timed_kernels_median": statistics.median(gemm_ms)},

@@ -140,12 +140,10 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
         // MXFP8: 256-wide tiles (gate 128 | up 128) with one accumulator (the
-        // block scales need the rest of tensor memory); 128-wide for I = 64
-        if (BN == 256) {
-            if (cl) return run<256, true, false, kEpiSwiGLU, 4, 1, 2>(ta, tb, tb, p, tub, c.num_sms, s);
-            return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
-        }
-        return run<128, true, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        // block scales need the rest of tensor memory); I is a multiple of 128
+        if (BN != 256) return cudaErrorInvalidValue;
+        if (cl) return run<256, true, false, kEpiSwiGLU, 4, 1, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
         if (cl) return run<256, false, false, kEpiSwiGLU, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);

@@ -87,6 +87,7 @@ struct GemmCfg {
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(EPI != kEpiSwiGLU || (BN / 2) % 32 == 0, "SwiGLU tiles hold whole 32-column gate/up chunks");
+    static_assert(!(MX && EPI == kEpiSwiGLU) || (BN / 2) % 128 == 0, "MXFP8 h tiles hold whole 128-wide scale chunks");
     static_assert(!kSfInGaps || (STAGES <= 4 && 2 * kSfCols <= 256 - BN), "scale columns must fit the gaps");
     static_assert(!(MX && MN_MAJOR), "MXFP8 operands are K-major");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -378,6 +379,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int I = p.split_col;
                 const int64_t prow = ti.row_base + row;
                 const bool live = p.identity_rows > 0 ? (prow < p.identity_rows) : true;
+                uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
                     uint32_t gr[32], ur[32];
@@ -408,8 +410,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         uint8_t* dst = static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc;
                         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
                         reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc / 128;
-                        p.out_sf[chunk * 512 + sf_chunk_offset((int)(prow % kTileM), (hc / 32) & 3)] = (uint8_t)code;
+                        // the four codes of a 128-wide chunk leave as one word
+                        sfw |= code << (8 * ((hc / 32) & 3));
+                        if (((hc / 32) & 3) == 3) {
+                            const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc / 128;
+                            *reinterpret_cast<uint32_t*>(p.out_sf + chunk * 512 +
+                                                         sf_chunk_offset((int)(prow % kTileM), 0)) = sfw;
+                            sfw = 0;
+                        }
                     } else {
                         uint32_t w[16];
 #pragma unroll

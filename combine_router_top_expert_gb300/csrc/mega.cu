@@ -712,6 +712,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
             if (t.kind == 0) {
                 const int I = p.I;
                 const int64_t prow = t.a_row0 + row;
+                uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
                     uint32_t gr[32], ur[32];
@@ -736,8 +737,14 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                         uint8_t* dst = static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc;
                         reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
                         reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc / 128;
-                        p.h_sf[chunk * 512 + sf_chunk_offset((int)(prow % kTileM), (hc / 32) & 3)] = (uint8_t)code;
+                        // the four codes of a 128-wide chunk leave as one word
+                        sfw |= code << (8 * ((hc / 32) & 3));
+                        if (((hc / 32) & 3) == 3) {
+                            const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc / 128;
+                            *reinterpret_cast<uint32_t*>(p.h_sf + chunk * 512 +
+                                                         sf_chunk_offset((int)(prow % kTileM), 0)) = sfw;
+                            sfw = 0;
+                        }
                     } else {
                         uint32_t w[16];
 #pragma unroll

@@ -68,7 +68,17 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
             if (!src) {
                 for (int c = lane; c < n; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
             } else if (!wslot) {
-                for (int c = lane; c < n; c += 32) dst[c] = __ldg(s4 + c);
+                // four 16-byte loads in flight per lane before their stores
+                int c = lane;
+                for (; c + 96 < n; c += 128) {
+                    const uint4 v0 = __ldg(s4 + c), v1 = __ldg(s4 + c + 32), v2 = __ldg(s4 + c + 64),
+                                v3 = __ldg(s4 + c + 96);
+                    dst[c] = v0;
+                    dst[c + 32] = v1;
+                    dst[c + 64] = v2;
+                    dst[c + 96] = v3;
+                }
+                for (; c < n; c += 32) dst[c] = __ldg(s4 + c);
             } else {
                 // reverse-combine: dy = w[t,j] * dY[t], rounded to bf16
                 for (int c = lane; c < n; c += 32) {
@@ -85,10 +95,14 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
             uint8_t* dst = static_cast<uint8_t*>(A) + (int64_t)pr * H;
             const int nb = H / 32;
             const int rt = pr / kTileM, r = pr % kTileM;
-            for (int b = lane; b < nb; b += 32) {
+            // lane b%32 quantises block b; the four blocks of a 128-wide chunk
+            // (lanes 4c..4c+3) store their codes as one 32-bit word
+            for (int b0 = 0; b0 < nb; b0 += 32) {
+                const int b = b0 + lane;
+                const bool act = b < nb;   // nb is a multiple of 4: chunks are whole
                 uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
                 uint32_t code = 0;
-                if (src) {
+                if (src && act) {
                     const uint4* s4 = reinterpret_cast<const uint4*>(src + b * 32);
                     uint4 v[4];
 #pragma unroll
@@ -114,9 +128,17 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
                     o0 = make_uint4(w[0], w[1], w[2], w[3]);
                     o1 = make_uint4(w[4], w[5], w[6], w[7]);
                 }
-                reinterpret_cast<uint4*>(dst + b * 32)[0] = o0;
-                reinterpret_cast<uint4*>(dst + b * 32)[1] = o1;
-                A_sf[((int64_t)rt * (H / 128) + b / 4) * 512 + sf_chunk_offset(r, b & 3)] = (uint8_t)code;
+                uint32_t word = code;
+                word |= __shfl_down_sync(0xffffffffu, code, 1) << 8;
+                word |= __shfl_down_sync(0xffffffffu, code, 2) << 16;
+                word |= __shfl_down_sync(0xffffffffu, code, 3) << 24;
+                if (act) {
+                    reinterpret_cast<uint4*>(dst + b * 32)[0] = o0;
+                    reinterpret_cast<uint4*>(dst + b * 32)[1] = o1;
+                    if ((lane & 3) == 0)
+                        *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)rt * (H / 128) + b / 4) * 512 +
+                                                     sf_chunk_offset(r, 0)) = word;
+                }
             }
         }
     }
