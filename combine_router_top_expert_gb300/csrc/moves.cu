@@ -66,19 +66,19 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
             const uint4* s4 = reinterpret_cast<const uint4*>(src);
             const int n = H / 8;
             if (!src) {
-                for (int c = lane; c < n; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+                for (int c = lane; c < n; c += 32) __stcs(dst + c, make_uint4(0, 0, 0, 0));
             } else if (!wslot) {
-                // four 16-byte loads in flight per lane before their stores
+                // eight 16-byte loads in flight per lane before their stores;
+                // the rows stream out (evict-first: read back only by the GEMM)
                 int c = lane;
-                for (; c + 96 < n; c += 128) {
-                    const uint4 v0 = __ldg(s4 + c), v1 = __ldg(s4 + c + 32), v2 = __ldg(s4 + c + 64),
-                                v3 = __ldg(s4 + c + 96);
-                    dst[c] = v0;
-                    dst[c + 32] = v1;
-                    dst[c + 64] = v2;
-                    dst[c + 96] = v3;
+                for (; c + 224 < n; c += 256) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) __stcs(dst + c + 32 * u, v[u]);
                 }
-                for (; c < n; c += 32) dst[c] = __ldg(s4 + c);
+                for (; c < n; c += 32) __stcs(dst + c, __ldg(s4 + c));
             } else {
                 // reverse-combine: dy = w[t,j] * dY[t], rounded to bf16
                 for (int c = lane; c < n; c += 32) {
@@ -158,7 +158,7 @@ combine_kernel(const __nv_bfloat16* __restrict__ partials, const float* __restri
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
         for (int j = 0; j < k; ++j) {
             const float wj = __ldg(w + (int64_t)t * k + j);
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(partials + ((int64_t)t * k + j) * H) + c);
+            uint4 v = __ldcs(reinterpret_cast<const uint4*>(partials + ((int64_t)t * k + j) * H) + c);
             acc[0] = fmaf(wj, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wj, bf16_hi(v.x), acc[1]);
             acc[2] = fmaf(wj, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wj, bf16_hi(v.y), acc[3]);
             acc[4] = fmaf(wj, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wj, bf16_hi(v.z), acc[5]);
