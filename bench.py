@@ -183,7 +183,7 @@ def main():
     ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
-    ap.add_argument("--gemm-pairs", action="store_true", help="grouped GEMMs as CTA pairs sharing A by multicast")
+    ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
     ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
     args = ap.parse_args()

@@ -49,7 +49,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
 template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
                 int64_t tiles_ub, int num_sms, cudaStream_t s) {
-    using C = GemmCfg<BN, MX, MN, EPI, S, ACC>;
+    using C = GemmCfg<BN, MX, MN, EPI, S, ACC, CLN>;
     auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC, CLN>;
     ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     cudaLaunchConfig_t cfg = {};
@@ -132,21 +132,21 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.b_sf = Bgu_sf;
     p.sf_kchunks = H / 128;
     p.n_tiles = 2 * I / BN;
-    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
+    // 2-SM pairs (BF16, 256-wide, grouped rows): each CTA loads half of B
+    const bool cl = c.cluster == 2 && !mx && BN == 256 && identity_rows == 0;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, A, a_rows, H, eb, bk, cl ? 64 : 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, A, a_rows, H, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
         // MXFP8: 256-wide tiles (gate 128 | up 128) with one accumulator (the
         // block scales need the rest of tensor memory); I is a multiple of 128
         if (BN != 256) return cudaErrorInvalidValue;
-        if (cl) return run<256, true, false, kEpiSwiGLU, 4, 1, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
-        if (cl) return run<256, false, false, kEpiSwiGLU, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        if (cl) return run<256, false, false, kEpiSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<256, false, false, kEpiSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     return run<128, false, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -175,22 +175,18 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     // the scales in the tensor-memory gaps), else 128; BF16: 256 or 128
     const int BN = down_tile_n(H, mx);
     p.n_tiles = H / BN;
-    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0;
+    const bool cl = c.cluster == 2 && !mx && BN == 256 && identity_rows == 0;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, h, a_rows, I, eb, bk, cl ? 64 : 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, Bdn, (int64_t)p.E * H, I, eb, bk, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, h, a_rows, I, eb, bk, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Bdn, (int64_t)p.E * H, I, eb, bk, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
-        if (BN == 224) {
-            if (cl) return run<224, true, false, kEpiScatter, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
-            return run<224, true, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
-        }
-        if (cl) return run<128, true, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        if (BN == 224) return run<224, true, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
-        if (cl) return run<256, false, false, kEpiScatter, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        if (cl) return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -208,12 +204,12 @@ cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I
     p.split_col = I;
     const int BN = I % 256 == 0 ? 256 : (I % 128 == 0 ? 128 : 64);
     p.n_tiles = I / BN;
-    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0 && BN == 256;
+    const bool cl = c.cluster == 2 && BN == 256;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, dy, a_rows, H, 2, 64, cl ? 64 : 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, dy, a_rows, H, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
-    if (cl) return run<256, false, false, kEpiDSwiGLU, 4, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    if (cl) return run<256, false, false, kEpiDSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, false, kEpiDSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     if (BN == 128) return run<128, false, false, kEpiDSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     return run<64, false, false, kEpiDSwiGLU, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -234,13 +230,13 @@ cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, 
     p.ldo = H;
     const int BN = H % 256 == 0 ? 256 : 128;
     p.n_tiles = H / BN;
-    const bool cl = c.cluster == 2 && p.n_tiles % 2 == 0 && BN == 256;
+    const bool cl = c.cluster == 2 && BN == 256;
     CUtensorMap ta, tb, tb2;
-    if (!make_tmap(&ta, dgu, a_rows, 2 * I, 2, 64, cl ? 64 : 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, W_gate, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb2, W_up, (int64_t)E * H, I, 2, 64, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&ta, dgu, a_rows, 2 * I, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, W_gate, (int64_t)E * H, I, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb2, W_up, (int64_t)E * H, I, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
-    if (cl) return run<256, false, false, kEpiScatter, 4, 2, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+    if (cl) return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
 }

@@ -56,11 +56,14 @@ struct GemmParams {
     unsigned long long timeout_ns;
 };
 
-template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES>
+// CLN = 2: one CTA of a 2-SM pair, which holds its 128 A rows and half of
+// the BN B rows of the pair's 256 x BN tile.
+template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN = 1>
 struct GemmCfg {
+    static_assert(CLN == 1 || (CLN == 2 && !MX && !MN_MAJOR && BN % 32 == 0), "2-SM pairs: BF16, K-major");
     static constexpr int kThreads = 192;
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
-    static constexpr int kBytesB = BN * 128;
+    static constexpr int kBytesB = BN / CLN * 128;
     static constexpr int kStageBytes = kBytesA + kBytesB;
     static constexpr int kNChunks = (BN + 127) / 128;   // 128-row scale chunks of a B tile
     static constexpr int kSfaBytes = MX ? 512 : 0;
@@ -108,7 +111,8 @@ struct Sched {
     int toff[kMaxE + 1];   // first tile of each expert
 };
 
-template <int BN, bool MN_MAJOR>
+// Tiles per expert: (m-tiles, or m-tile pairs for 2-SM pairs) x n_tiles.
+template <int BN, bool MN_MAJOR, int CLN = 1>
 __device__ __forceinline__ void build_sched(const GemmParams& p, Sched& s) {
     if (threadIdx.x == 0) {
         int rows = 0, tiles = 0;
@@ -118,7 +122,7 @@ __device__ __forceinline__ void build_sched(const GemmParams& p, Sched& s) {
             s.poff[e] = rows;
             s.toff[e] = tiles;
             rows += p.identity_rows > 0 ? cnt : mt * kTileM;
-            tiles += p.m_fixed > 0 ? ceil_div(p.m_fixed, kTileM) * p.n_tiles : mt * p.n_tiles;
+            tiles += p.m_fixed > 0 ? ceil_div(p.m_fixed, kTileM) * p.n_tiles : ceil_div(mt, CLN) * p.n_tiles;
         }
         s.poff[p.E] = rows;
         s.toff[p.E] = tiles;
@@ -161,30 +165,49 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// Cluster pairs: pair index gp covers the two N-neighbour tiles (2n', 2n'+1)
-// of one (expert, m-tile); rank picks the CTA's own tile. n_tiles is even.
-__device__ __forceinline__ int pair_tile(const GemmParams& p, const Sched& s, int gp, int rank) {
-    int lo = 0, hi = p.E - 1;  // last e with toff[e] / 2 <= gp
+// 2-SM pairs: pair tile g covers m-tiles 2mp and 2mp+1 of one expert (n
+// fastest-varying after mp, as for single tiles); CTA `rank` takes m-tile
+// 2mp + rank. An expert with an odd number of m-tiles leaves the last pair's
+// second half outside its segment: that CTA's rows are not valid (valid = 0)
+// and its epilogue stores nothing.
+__device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const Sched& s, int g, int rank) {
+    TileInfo ti;
+    int lo = 0, hi = p.E - 1;  // last e with toff[e] <= g
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
-        if (s.toff[mid] / 2 <= gp) lo = mid; else hi = mid - 1;
+        if (s.toff[mid] <= g) lo = mid; else hi = mid - 1;
     }
-    const int mt = (s.toff[lo + 1] - s.toff[lo]) / p.n_tiles;
-    const int pl = gp - s.toff[lo] / 2;
-    const int np = pl / mt, m = pl % mt;
-    return s.toff[lo] + (2 * np + rank) * mt + m;
+    const int e = lo;
+    const int cnt = p.counts[e];
+    const int mt = ceil_div(cnt, kTileM);
+    const int mp = ceil_div(mt, 2);
+    const int local = g - s.toff[e];
+    ti.e = e;
+    ti.n = local / mp;
+    ti.m = 2 * (local % mp) + rank;
+    ti.a_row0 = s.poff[e] + ti.m * kTileM;
+    ti.num_kb = p.num_kb;
+    ti.row_base = ti.a_row0;
+    ti.local_row0 = ti.m * kTileM;
+    ti.valid = ti.m < mt ? 1 : 0;
+    return ti;
 }
 
-// CLN = 2: launched as clusters of two CTAs that compute N-neighbour tiles of
-// the same (expert, m-tile); each loads half of the shared A tile and
-// multicasts it to both, so per K-block each CTA fetches 40 KB instead of
-// 48 KB from L2 (BF16, BN=256) or 24 KB instead of 32 KB (MXFP8, BN=128).
+// CLN = 2: launched as clusters of two CTAs forming a 2-SM pair
+// (tcgen05 cta_group::2). Both CTAs load their own 128 A rows and half of
+// the B rows into their own shared memory, signalling the leader's (rank 0)
+// full barrier; the leader's MMA thread issues M=256 MMAs over both CTAs'
+// operands, each CTA's tensor memory receiving its own 128 accumulator rows,
+// and its commits release the stage and publish the accumulator in both
+// CTAs; both CTAs' epilogues drain their own rows and release the
+// accumulator on the leader's barrier. Per K-block each CTA stages 32 KB
+// instead of 48 KB (BN = 256), so 6 stages fit.
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
-    using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES>;
-    static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR), "cluster pairs share K-major A tiles");
+    using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>;
+    static_assert(CLN == 1 || (CLN == 2 && EPI != kEpiDense), "2-SM pairs: grouped-row GEMMs");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Sched sched;
     __shared__ uint32_t s_tmem_base;
@@ -205,15 +228,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     StatusBlock* st = p.status;
     const uint64_t tmo = p.timeout_ns;
 
-    build_sched<BN, MN_MAJOR>(p, sched);
+    build_sched<BN, MN_MAJOR, CLN>(p, sched);
     if (threadIdx.x == 32) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
-            tc::mbar_init(empty_bar(s), CLN);   // one MMA commit per CTA of the cluster
+            tc::mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < ACC_STAGES; ++a) {
             tc::mbar_init(accf_bar(a), 1);
-            tc::mbar_init(acce_bar(a), 128);
+            tc::mbar_init(acce_bar(a), 128 * CLN);   // pairs: both CTAs' epilogue threads (leader's barrier)
         }
         tc::mbar_init(drain_bar, 1);
         tc::fence_mbar_init();
@@ -224,20 +247,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tc::prefetch_tmap(&tmB2);
     }
     if (warp == 1) {
-        tc::tmem_alloc(tc::smem_u32(&s_tmem_base), C::kTmemCols);
-        tc::tmem_relinquish();
+        if constexpr (CLN == 2) {
+            tc::tmem_alloc_2sm(tc::smem_u32(&s_tmem_base), C::kTmemCols);
+            tc::tmem_relinquish_2sm();
+        } else {
+            tc::tmem_alloc(tc::smem_u32(&s_tmem_base), C::kTmemCols);
+            tc::tmem_relinquish();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if constexpr (CLN == 2) tc::cluster_sync();   // peers' barriers exist before any multicast
+    if constexpr (CLN == 2) tc::cluster_sync();   // the peer's barriers and tensor memory exist
     const uint32_t tmem = s_tmem_base;
-    const int total_tiles = sched.toff[p.E];
     const int rank = CLN == 2 ? (int)tc::cluster_ctarank() : 0;
-    const int gstart = CLN == 2 ? (int)blockIdx.x / 2 : (int)blockIdx.x;
-    const int gstep = CLN == 2 ? (int)gridDim.x / 2 : (int)gridDim.x;
-    const int gtotal = CLN == 2 ? total_tiles / 2 : total_tiles;
-    auto tile_of = [&](int gi) { return CLN == 2 ? pair_tile(p, sched, gi, rank) : gi; };
+    const int gstart = (int)blockIdx.x / CLN;
+    const int gstep = (int)gridDim.x / CLN;
+    const int gtotal = sched.toff[p.E];
+    auto decode = [&](int gi) {
+        if constexpr (CLN == 2) return decode_pair_tile(p, sched, gi, rank);
+        else return decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, gi);
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -248,9 +278,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             bool ok = true;
             for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
-                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
+                TileInfo ti = decode(gi);
                 for (int kb = 0; kb < ti.num_kb; ++kb) {
                     if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
+                    if constexpr (CLN == 2) {
+                        // both halves signal the leader's full barrier, which expects both
+                        const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2 * C::kStageBytes);
+                        tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, kb * C::kBK, ti.a_row0);
+                        const bool b1 = kb < p.b_split_kb;
+                        tc::tma_load_2d_2sm(b_tile(stage), b1 ? (const void*)&tmB : (const void*)&tmB2, lead_full,
+                                            (b1 ? kb : kb - p.b_split_kb) * C::kBK,
+                                            ti.e * p.b_rows_per_expert + ti.n * BN + rank * (BN / 2));
+                        last_par[stage] = (int)ph;
+                        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                        continue;
+                    }
                     tc::mbar_expect_tx(full_bar(stage), C::kStageBytes + C::kSfStage);
                     if constexpr (MN_MAJOR) {
                         const int krow = ti.a_row0 + kb * 64;
@@ -261,11 +304,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int j = 0; j < BN / 64; ++j)
                             tc::tma_load_2d(b_tile(stage) + 8192 * j, &tmB, full_bar(stage), ti.n * BN + 64 * j, krow);
                     } else {
-                        if constexpr (CLN == 2)
-                            tc::tma_load_2d_multicast(a_tile(stage) + rank * 8192, &tmA, full_bar(stage), kb * C::kBK,
-                                                      ti.a_row0 + 64 * rank, (uint16_t)0x3);
-                        else
-                            tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
+                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
                         const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
                         if (kb < p.b_split_kb)
                             tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kb * C::kBK, brow);
@@ -303,14 +342,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (pairs: the leader issues for both CTAs; the peer's warp 1 only
+        // allocated the tensor memory)
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t ph = 0;
             int acc = 0;
             uint32_t acc_ph = 0;
             bool ok = true, issued = false;
             for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
-                TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
+                TileInfo ti = decode(gi);
                 if (ti.num_kb == 0) continue;
                 if (!tc::mbar_wait(acce_bar(acc), acc_ph ^ 1u, st, tmo, kSiteMmaAccEmpty)) { ok = false; break; }
                 tc::fence_after_sync();
@@ -341,22 +382,26 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (MX) {
                             tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
+                        } else if constexpr (CLN == 2) {
+                            tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(256, BN, false, false), accum);
                         } else {
                             tc::mma_bf16(d, ad, bd, tc::idesc_bf16(128, BN, MN_MAJOR, MN_MAJOR), accum);
                         }
                     }
                     issued = true;
-                    if constexpr (CLN == 2) tc::mma_commit_multicast(empty_bar(stage), (uint16_t)0x3);
+                    if constexpr (CLN == 2) tc::mma_commit_2sm_multicast(empty_bar(stage), (uint16_t)0x3);
                     else tc::mma_commit(empty_bar(stage));
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                tc::mma_commit(accf_bar(acc));
+                if constexpr (CLN == 2) tc::mma_commit_2sm_multicast(accf_bar(acc), (uint16_t)0x3);
+                else tc::mma_commit(accf_bar(acc));
                 if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
             }
             if (!ok && issued) {
                 // every MMA issued so far must finish before tensor memory is freed
-                tc::mma_commit(drain_bar);
+                if constexpr (CLN == 2) tc::mma_commit_2sm(drain_bar);
+                else tc::mma_commit(drain_bar);
                 tc::mbar_wait(drain_bar, 0, st, tmo, kSiteDrain);
             }
         }
@@ -367,7 +412,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int gi = gstart; gi < gtotal; gi += gstep) {
-            TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, tile_of(gi));
+            TileInfo ti = decode(gi);
             const bool has_acc = ti.num_kb > 0;
             if (has_acc) {
                 if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
@@ -378,7 +423,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if constexpr (EPI == kEpiSwiGLU) {
                 const int I = p.split_col;
                 const int64_t prow = ti.row_base + row;
-                const bool live = p.identity_rows > 0 ? (prow < p.identity_rows) : true;
+                const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid;
                 uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -472,7 +517,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const float* gb = static_cast<const float*>(p.gu) + prow * (int64_t)(2 * I);
                 __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)(2 * I);
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = 0; c0 < BN && ti.valid; c0 += 32) {   // pairs: no rows outside the expert
                     uint32_t r[32];
                     tc::tmem_ld_32x32b_x32(tbase + c0, r);
                     tc::tmem_ld_wait();
@@ -534,7 +579,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             if (has_acc) {
                 tc::fence_before_sync();
-                tc::mbar_arrive(acce_bar(acc));
+                if constexpr (CLN == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acce_bar(acc), 0));
+                else tc::mbar_arrive(acce_bar(acc));
                 if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
             }
         }
@@ -542,8 +588,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if constexpr (CLN == 2) tc::cluster_sync();   // no CTA leaves while its peer may still write to it
-    if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+    if constexpr (CLN == 2) {
+        tc::cluster_sync();   // no CTA frees or leaves while its peer may still use the pair's resources
+        if (warp == 1) tc::tmem_dealloc_2sm(tmem, C::kTmemCols);
+    } else {
+        if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
+    }
 }
 
 }  // namespace mok

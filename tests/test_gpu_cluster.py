@@ -1,6 +1,10 @@
-"""Grouped GEMMs as CTA pairs (two N-neighbour tiles sharing the A tile by
-TMA multicast) move data differently but compute the same tiles in the same
-order, so every output must be bit-identical to the single-CTA kernels."""
+"""Grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2: one M=256 MMA over
+two CTAs' 128-row A halves and 128-row B halves) against the single-CTA
+kernels. Every output element is still one K-ordered tensor-core dot product
+with fp32 accumulation, so the results must be bit-identical; experts with
+an odd number of 128-row tiles exercise the pair whose second half lies
+outside the expert (its rows must not be written). MXFP8 runs single CTAs
+either way."""
 import pytest
 import torch
 
@@ -23,8 +27,9 @@ def _staged(layer, x, T, extra=0):
 @pytest.mark.gpu
 @pytest.mark.parametrize("wl", [
     synth.small("cl_bf16", T=700, H=512, I=256, E=8, k=2, zipf_s=1.2, shared_I=256),
+    synth.small("cl_bf16_odd", T=600, H=768, I=512, E=4, k=2),
     synth.small("cl_mx", T=700, H=1024, I=256, E=8, k=4, dtype="mxfp8", zipf_s=1.2),
-], ids=["bf16_shared", "mxfp8"])
+], ids=["bf16_shared", "bf16_odd_tiles", "mxfp8"])
 def test_cluster_pairs_forward_bitwise(wl):
     inp = synth.make_inputs(wl)
     layer = layer_for(inp, dtype_of(wl))
