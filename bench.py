@@ -447,6 +447,16 @@ def main():
     achieved = fl / (g_ms / 1000.0) / 1e12
     long_region = total_ms > 1000.0
     peak = (peaks["bf16_sus"] if long_region else peaks["bf16"]) * (2.0 if dtype == mok.MXFP8 else 1.0)
+    # the GEMM pair's algorithmic HBM bytes: expert weights (+ MXFP8 scales),
+    # the gathered rows read, h written and read back, the partials written
+    R_rows = T * wl.k * len(xs)
+    ebw = (1.0 + 1.0 / 32) if dtype == mok.MXFP8 else 2.0
+    gemm_bytes = (3.0 * wl.E * H * wl.I * ebw + R_rows * H * ebw + 2.0 * R_rows * wl.I * ebw + R_rows * H * 2.0)
+    if wl.backward:
+        gemm_bytes = None   # the fwd+bwd step is tensor-bound at every size measured here
+    hbm_achieved = gemm_bytes / (g_ms / 1000.0) / 1e9 if gemm_bytes else None
+    # the bound of the workload: whichever of FLOP / peak and bytes / HBM peak is longer
+    hbm_bound = bool(gemm_bytes) and gemm_bytes / (peaks["hbm"] * 1e9) > fl / (peak * 1e12)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -459,12 +469,21 @@ def main():
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
         "gemm_cta_pairs": bool(args.gemm_pairs),
-        "roofline": {"kernel": kern,
-                     "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak,
-                     "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
-                                    (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
-                     "flops_per_step": fl, "ms_per_step": g_ms, "traffic": None},
+        "roofline": ({"kernel": kern,
+                      "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                      "frac": hbm_achieved / peaks["hbm"], "peak_source": f"{peaks['source']} hbm copy",
+                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": None,
+                      "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}}
+                     if hbm_bound else
+                     {"kernel": kern,
+                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                      "frac": achieved / peak,
+                      "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
+                                     (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
+                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": None,
+                      "hbm": ({"achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                               "frac": hbm_achieved / peaks["hbm"], "bytes_per_step": gemm_bytes}
+                              if gemm_bytes else None)}),
         "e2e": {"value": e2e_val, "unit": "tokens/s",
                 "h2d_bytes_per_step": tokens_per_step * H * 2 * (2 if wl.backward else 1),
                 "d2h_bytes_per_step": tokens_per_step * H * 2,
