@@ -174,6 +174,45 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b):
+    """One megakernel step with per-CTA trace records; fractions of the kernel
+    window each role spends working on tiles / moves, waiting on GPU-local
+    counters, in the weighted sums, and idle."""
+    import torch
+    cfg2 = mok.make_config(num_sms=cfg.num_sms, timeout_ms=cfg.timeout_ms, flags=cfg.flags | mok.FLAG_TRACE,
+                           mover_ctas=cfg.mover_ctas, minibatch_tokens=cfg.minibatch_tokens, ring_rows=cfg.ring_rows)
+    if len(xs) > 1:
+        mok.moe_forward_batches(p, xs, layer.packed, routings, [torch.empty_like(xb) for xb in xs], ws_b,
+                                packed_shared=layer.packed_shared, cfg=cfg2, stream=stream)
+        ws = ws_b
+    else:
+        layer.route(x, stream=stream)
+        layer.forward(x, cfg=cfg2, stream=stream, route=False)
+        ws = b["ws"]
+    torch.cuda.synchronize()
+    dev = torch.cuda.current_device()
+    n = torch.cuda.get_device_properties(dev).multi_processor_count
+    if cfg.num_sms:
+        n = min(n, cfg.num_sms)
+    rec = mok.megakernel_trace(ws, n).astype(np.float64)
+    t0, t1 = rec[:, 1].min(), rec[:, 4].max()
+    dur = t1 - t0
+    out = {"kernel_us": dur / 1e3, "ctas": int(n)}
+    for role, name in ((0, "movers"), (1, "compute")):
+        r = rec[rec[:, 0] == role]
+        if len(r) == 0:
+            continue
+        work = (r[:, 3] - r[:, 2] - r[:, 5]) / dur
+        out[name] = {"ctas": int(len(r)),
+                     "first_work_us": float(np.mean(r[:, 2] - t0) / 1e3),
+                     "work_frac": float(np.mean(work)),
+                     "counter_wait_frac": float(np.mean(r[:, 5] / dur)),
+                     "combine_frac": float(np.mean(r[:, 7] / dur)),
+                     "idle_frac": float(np.mean(1.0 - work - r[:, 5] / dur - r[:, 7] / dur)),
+                     "units_mean": float(np.mean(r[:, 6]))}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -186,6 +225,8 @@ def main():
     ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
     ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
+    ap.add_argument("--trace", action="store_true",
+                    help="megakernel: after the timed steps, one traced step; report the SM partition's busy/idle time")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -359,6 +400,11 @@ def main():
         raise SystemExit(f"device status after timed steps: {st}")
     tokens_per_step = T * len(xs)
 
+    sm_partition = None
+    if args.trace and (not staged or len(xs) > 1):
+        sm_partition = trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings if len(xs) > 1 else None,
+                                  ws_b if len(xs) > 1 else None)
+
     # end to end through the public API with host buffers: every step copies
     # its inputs in from pinned host memory and its result back out; steps are
     # pipelined the way a serving loop would run them (copy streams in and out
@@ -493,6 +539,7 @@ def main():
                 "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams overlap step i's kernels; "
                               "no L2 flush (each step's working set, the expert weights, is larger than L2)"},
         "stage_rooflines": stage_lines,
+        "sm_partition": sm_partition,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "stage_ms": {"step_median": statistics.median(step_ms), "timed_kernels_median": statistics.median(gemm_ms)},

@@ -346,6 +346,8 @@ static mok_status forward_mega(const mok_problem* p, int32_t nbatch, const mok_f
     L.n_movers = movers;
     L.grid = c.num_sms;
     L.test_flags = cfg ? cfg->flags : 0;
+    L.trace = (cfg && (cfg->flags & MOK_FLAG_TRACE)) ? reinterpret_cast<unsigned long long*>(ws + ML.scratch)
+                                                     : nullptr;
     L.status = c.status;
     L.timeout_ns = c.timeout_ns;
     return cuda_status(launch_mega(L, s));

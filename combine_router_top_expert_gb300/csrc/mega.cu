@@ -211,6 +211,8 @@ plan_finalize_kernel(int nbatch, int E, int NT1, int NT2, const int* __restrict_
 // ---------------------------------------------------------------------------
 struct MegaBatch {
     const __nv_bfloat16* x;   // [T, H]
+    const uint8_t* xq;        // MXFP8: x quantised per token row [T, H] E4M3 (the movers copy these)
+    const uint32_t* xsf;      // MXFP8: its scale words [T, H/128]
     const int32_t* row_src;   // [T*k]
     const float* topk_w;      // [T, k]
     __nv_bfloat16* partials;  // [T*k, H]
@@ -237,6 +239,7 @@ struct MegaParams {
     int bn2;         // N-tile of the down GEMM (224, 256 or 128)
     int n_movers;
     int test_flags;
+    unsigned long long* trace;   // per-CTA records, or NULL
     StatusBlock* status;
     unsigned long long timeout_ns;
 };
@@ -318,6 +321,14 @@ __device__ __forceinline__ MegaTile mega_decode(const MegaParams& p, int g, int 
     return t;
 }
 
+constexpr int kMoverLoads = 28;    // BF16 mover: 16-byte loads in flight per lane per pass
+constexpr int kMoverBlocks = 7;    // MXFP8 mover: 32-element blocks per lane per pass
+
+// One minibatch's pull-gather by the mover CTAs: warps take 8-row chunks of
+// the padded minibatch rows; inside a warp, lanes 4r..4r+3 copy row r of the
+// chunk (lane part q of a row takes its 16-byte words, or 32-element blocks,
+// q, q+4, q+8, ...), so the 8 rows' source lookups and loads are all in
+// flight together. A chunk is published (release) once all its rows landed.
 template <bool MX>
 __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nwarps, int lane) {
     const PlanView& v = p.plan;
@@ -328,6 +339,7 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
     const int* src0 = v.src0 + mb * p.E;
     const int H = p.H;
     const int nchunks = mi.rows / 8;
+    const int rr = lane >> 2, part = lane & 3;
     for (int c = gwarp; c < nchunks; c += nwarps) {
         const int r0 = c * 8;
         int lo = 0, hi = p.E - 1;  // expert owning padded row r0 (skips empty experts)
@@ -335,72 +347,75 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
             const int mid = (lo + hi + 1) >> 1;
             if (roff[mid] <= r0) lo = mid; else hi = mid - 1;
         }
-        const int e = lo;
-        for (int rr = 0; rr < 8; ++rr) {
-            const int row = r0 + rr;
-            const int local = row - roff[e];
-            const __nv_bfloat16* src = nullptr;
-            if (local < cnt[e]) src = bt.x + (int64_t)(bt.row_src[src0[e] + local] / p.k) * H;
-            const int64_t grow = (int64_t)mi.region * p.region_rows + row;
-            if constexpr (!MX) {
-                // 8 independent 16-byte loads in flight per lane before the stores
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.ring) + grow * H);
-                const uint4* s4 = reinterpret_cast<const uint4*>(src);
-                const int n16 = H / 8;
-                for (int q0 = 0; q0 < n16; q0 += 32 * 8) {
-                    uint4 v[8];
+        const int e = lo;   // a chunk never straddles experts: segments are 128-row multiples
+        const int row = r0 + rr;
+        const int local = row - roff[e];
+        const __nv_bfloat16* src = nullptr;
+        if (local < cnt[e]) src = bt.x + (int64_t)(bt.row_src[src0[e] + local] / p.k) * H;
+        const int64_t grow = (int64_t)mi.region * p.region_rows + row;
+        if constexpr (!MX) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.ring) + grow * H);
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
+            const int n16 = H / 8;
+            for (int q0 = part; q0 < n16; q0 += 4 * kMoverLoads) {
+                uint4 vv[kMoverLoads];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int q = q0 + u * 32 + lane;
-                        v[u] = (src && q < n16) ? __ldg(s4 + q) : make_uint4(0, 0, 0, 0);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int q = q0 + u * 32 + lane;
-                        if (q < n16) dst[q] = v[u];
-                    }
+                for (int u = 0; u < kMoverLoads; ++u) {
+                    const int q = q0 + 4 * u;
+                    vv[u] = (src && q < n16) ? __ldg(s4 + q) : make_uint4(0, 0, 0, 0);
                 }
-            } else {
-                uint8_t* dst = static_cast<uint8_t*>(p.ring) + grow * H;
-                const int rt = (int)(grow / kTileM), r = (int)(grow % kTileM);
-                const int nb = H / 32;
-                // two 32-element blocks per lane per pass: 8 loads in flight
-                for (int b0 = 0; b0 < nb; b0 += 64) {
-                    uint4 v[2][4];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int bb = b0 + u * 32 + lane;
-                        const uint4* s4 = reinterpret_cast<const uint4*>(src + bb * 32);
+                for (int u = 0; u < kMoverLoads; ++u) {
+                    const int q = q0 + 4 * u;
+                    if (q < n16) __stcg(dst + q, vv[u]);
+                }
+            }
+        } else {
+            uint8_t* dst = static_cast<uint8_t*>(p.ring) + grow * H;
+            const int rt = (int)(grow / kTileM), r = (int)(grow % kTileM);
+            const int nb = H / 32;   // a multiple of 4: the 4 lanes of a row share each 128-wide chunk
+            for (int b0 = 0; b0 < nb; b0 += 4 * kMoverBlocks) {
+                uint4 vv[kMoverBlocks][4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            v[u][i] = (src && bb < nb) ? __ldg(s4 + i) : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < kMoverBlocks; ++u) {
+                    const int bb = b0 + 4 * u + part;
+                    const uint4* s4 = reinterpret_cast<const uint4*>(src + bb * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        vv[u][i] = (src && bb < nb) ? __ldg(s4 + i) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kMoverBlocks; ++u) {
+                    const int bb = b0 + 4 * u + part;
+                    float f[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        f[8 * i + 0] = bf16_lo(vv[u][i].x); f[8 * i + 1] = bf16_hi(vv[u][i].x);
+                        f[8 * i + 2] = bf16_lo(vv[u][i].y); f[8 * i + 3] = bf16_hi(vv[u][i].y);
+                        f[8 * i + 4] = bf16_lo(vv[u][i].z); f[8 * i + 5] = bf16_hi(vv[u][i].z);
+                        f[8 * i + 6] = bf16_lo(vv[u][i].w); f[8 * i + 7] = bf16_hi(vv[u][i].w);
                     }
+                    float amax = 0.f;
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int bb = b0 + u * 32 + lane;
-                        if (bb >= nb) continue;
-                        float f[32];
+                    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                    const uint32_t code = src ? e8m0_code(amax) : 0u;
+                    const float inv = e8m0_inv_scale(code);
+                    uint32_t w[8];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            f[8 * i + 0] = bf16_lo(v[u][i].x); f[8 * i + 1] = bf16_hi(v[u][i].x);
-                            f[8 * i + 2] = bf16_lo(v[u][i].y); f[8 * i + 3] = bf16_hi(v[u][i].y);
-                            f[8 * i + 4] = bf16_lo(v[u][i].z); f[8 * i + 5] = bf16_hi(v[u][i].z);
-                            f[8 * i + 6] = bf16_lo(v[u][i].w); f[8 * i + 7] = bf16_hi(v[u][i].w);
-                        }
-                        float amax = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                        const uint32_t code = src ? e8m0_code(amax) : 0u;
-                        const float inv = e8m0_inv_scale(code);
-                        uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
-                                   (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
-                        reinterpret_cast<uint4*>(dst + bb * 32)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst + bb * 32)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        p.ring_sf[((int64_t)rt * (H / 128) + bb / 4) * 512 + sf_chunk_offset(r, bb & 3)] =
-                            (uint8_t)code;
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+                               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+                    // the row's 4 lanes hold blocks 4c..4c+3 of chunk c: one word of codes
+                    uint32_t word = code;
+                    word |= __shfl_down_sync(0xffffffffu, code, 1) << 8;
+                    word |= __shfl_down_sync(0xffffffffu, code, 2) << 16;
+                    word |= __shfl_down_sync(0xffffffffu, code, 3) << 24;
+                    if (bb < nb) {
+                        __stcg(reinterpret_cast<uint4*>(dst + bb * 32), make_uint4(w[0], w[1], w[2], w[3]));
+                        __stcg(reinterpret_cast<uint4*>(dst + bb * 32) + 1, make_uint4(w[4], w[5], w[6], w[7]));
+                        if (part == 0)
+                            *reinterpret_cast<uint32_t*>(p.ring_sf + ((int64_t)rt * (H / 128) + bb / 4) * 512 +
+                                                         sf_chunk_offset(r, 0)) = word;
                     }
                 }
             }
@@ -412,6 +427,113 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
         const bool withhold = (p.test_flags & MOK_FLAG_TEST_WITHHOLD_PUBLISH) && mb == 0 && c == nchunks - 1;
         if (lane == 0 && !withhold) red_release_add(&p.ready[mb * p.E + e], 8);
     }
+}
+
+// Pull-gather through the copy engines: lane 0 of each mover warp pumps the
+// rows of its 8-row chunks global -> shared -> ring with bulk copies, two row
+// buffers per warp (the load of row r+1 overlaps the store of row r), pad
+// rows from a zeroed buffer; MXFP8 copies the E4M3 rows of x quantised once
+// per token (quantize_rows, before the launch) and the warp's lanes place
+// their scale words in the ring's tile-ordered scale chunks. The chunk is
+// published once its stores have completed. A warp keeps two rows in flight
+// with one issuing thread, where register copies need every lane for a
+// fraction of that. Returns false if a bounded wait gave up.
+struct MoverSmem {
+    uint32_t bufs;    // [warps][2] row buffers
+    uint32_t zero;    // one zeroed row
+    uint32_t bars;    // [warps][2] mbarriers (8 bytes each)
+};
+
+template <bool MX>
+__device__ bool mover_pump_mb(const MegaParams& p, int mb, int gwarp, int nwarps, int lane, int warp,
+                              const MoverSmem& ms, uint32_t& phases) {
+    const PlanView& v = p.plan;
+    const MbInfo mi = v.mb[mb];
+    const MegaBatch bt = p.batches[mi.batch];
+    const int* roff = v.roff + mb * p.E;
+    const int* cnt = v.cnt + mb * p.E;
+    const int* src0 = v.src0 + mb * p.E;
+    const uint32_t rowb = (uint32_t)p.H * (MX ? 1 : 2);
+    const int nchunks = mi.rows / 8;
+    const int kc_row = p.H / 128;   // MXFP8 scale words per row
+    bool ok = true;
+    for (int c = gwarp; c < nchunks; c += nwarps) {
+        const int r0 = c * 8;
+        int lo = 0, hi = p.E - 1;  // expert owning padded row r0 (skips empty experts)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (roff[mid] <= r0) lo = mid; else hi = mid - 1;
+        }
+        const int e = lo;
+        int my_tok = -1;   // lane r < 8: source token of row r (-1: pad row)
+        if (lane < 8) {
+            const int local = r0 + lane - roff[e];
+            if (local < cnt[e]) my_tok = bt.row_src[src0[e] + local] / p.k;
+        }
+        const int64_t grow0 = (int64_t)mi.region * p.region_rows + r0;
+        if constexpr (MX) {
+            // scale words: row r's word kc goes to byte (r%32)*16 + (r/32)*4 of chunk (tile, kc)
+            for (int r = 0; r < 8; ++r) {
+                const int tok = __shfl_sync(0xffffffffu, my_tok, r);
+                const int64_t grow = grow0 + r;
+                for (int kc = lane; kc < kc_row; kc += 32) {
+                    const uint32_t wd = tok >= 0 ? __ldg(bt.xsf + (int64_t)tok * kc_row + kc) : 0u;
+                    *reinterpret_cast<uint32_t*>(p.ring_sf + ((grow / kTileM) * kc_row + kc) * 512 +
+                                                 sf_chunk_offset((int)(grow % kTileM), 0)) = wd;
+                }
+            }
+        }
+        int toks[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) toks[r] = __shfl_sync(0xffffffffu, my_tok, r);
+        if (lane == 0 && ok) {
+            const char* src[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r)
+                src[r] = toks[r] < 0 ? nullptr
+                         : MX ? reinterpret_cast<const char*>(bt.xq + (int64_t)toks[r] * p.H)
+                              : reinterpret_cast<const char*>(bt.x + (int64_t)toks[r] * p.H);
+            const uint32_t buf[2] = {ms.bufs + (uint32_t)(2 * warp) * rowb, ms.bufs + (uint32_t)(2 * warp + 1) * rowb};
+            const uint32_t bar[2] = {ms.bars + 16u * warp, ms.bars + 16u * warp + 8u};
+            char* ring = static_cast<char*>(p.ring) + grow0 * rowb;
+            tc::bulk_wait_read<0>();   // the previous chunk's stores no longer read the buffers
+            if (src[0]) {
+                tc::mbar_expect_tx(bar[0], rowb);
+                tc::bulk_load(buf[0], src[0], rowb, bar[0]);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int sl = r & 1;
+                if (r + 1 < 8 && src[r + 1]) {
+                    tc::bulk_wait_read<0>();   // the store of row r - 1 is done with buffer (r + 1) & 1
+                    tc::mbar_expect_tx(bar[sl ^ 1], rowb);
+                    tc::bulk_load(buf[sl ^ 1], src[r + 1], rowb, bar[sl ^ 1]);
+                }
+                if (src[r]) {
+                    if (!tc::mbar_wait(bar[sl], (phases >> sl) & 1u, p.status, p.timeout_ns, kSiteCounter)) {
+                        ok = false;
+                        break;
+                    }
+                    phases ^= 1u << sl;
+                    tc::bulk_store(ring + (int64_t)r * rowb, buf[sl], rowb);
+                } else {
+                    tc::bulk_store(ring + (int64_t)r * rowb, ms.zero, rowb);
+                }
+                tc::bulk_commit();
+            }
+            tc::bulk_wait<0>();   // the chunk's rows are written
+        }
+        // every lane's writes (MXFP8 scale words; lane 0's bulk copies) are
+        // ordered before lane 0's release, for the readers' TMA as well
+        tc::fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) return false;
+        const bool withhold = (p.test_flags & MOK_FLAG_TEST_WITHHOLD_PUBLISH) && mb == 0 && c == nchunks - 1;
+        if (lane == 0 && !withhold) red_release_add(&p.ready[mb * p.E + e], 8);
+    }
+    return true;
 }
 
 // Fixed-order weighted sum of tokens [t0, t1) of one batch (j ascending).
@@ -487,6 +609,21 @@ __device__ bool combine_loop(const MegaParams& p, int NT2, int* s_word, int& nex
     return true;
 }
 
+// Trace record of this CTA (thread 0 keeps the values; MOK_FLAG_TRACE).
+struct MegaTrace {
+    unsigned long long t_begin = 0, t_first = 0, t_work_end = 0, wait_ns = 0, units = 0, comb_ns = 0;
+    __device__ void write(unsigned long long* rec, int role) const {
+        rec[0] = (unsigned long long)role;
+        rec[1] = t_begin;
+        rec[2] = t_first;
+        rec[3] = t_work_end;
+        rec[4] = globaltimer_ns();
+        rec[5] = wait_ns;
+        rec[6] = units;
+        rec[7] = comb_ns;
+    }
+};
+
 template <bool MX>
 __global__ void __launch_bounds__(192, 1)
 mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmGU,
@@ -510,6 +647,9 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
     const int kb1 = p.H / C::kBK, kb2 = p.I / C::kBK;
     const PlanView& v = p.plan;
     int next_comb = 0;
+    const bool tracing = p.trace != nullptr;
+    MegaTrace tr;
+    if (tracing && threadIdx.x == 0) tr.t_begin = globaltimer_ns();
 
     if (v.hdr->error) {
         if (blockIdx.x == 0 && threadIdx.x == 0) record_failure(st, MOK_ERR_CAPACITY, 0);
@@ -521,25 +661,68 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         const int nwarps = p.n_movers * (blockDim.x / 32);
         const int gwarp = blockIdx.x * (blockDim.x / 32) + warp;
         const int n_mb = v.hdr->n_mb;
+        // BF16: rows go through the copy engines when the row buffers fit
+        const int nw = blockDim.x / 32;
+        const size_t rowb = (size_t)p.H * (MX ? 1 : 2);
+        const bool pump = (size_t)(2 * nw + 1) * rowb + 16 * nw <= (size_t)C::kBarOffset &&
+                          (!MX || p.batches[0].xq != nullptr);
+        MoverSmem ms{};
+        uint32_t phases = 0;
+        unsigned char* sm =
+            reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+        if (pump) {
+            const uint32_t base = tc::smem_u32(sm);
+            ms.bufs = base;
+            ms.zero = base + (uint32_t)(2 * nw * rowb);
+            ms.bars = ms.zero + (uint32_t)rowb;
+            uint4* z = reinterpret_cast<uint4*>(sm + (size_t)(2 * nw) * rowb);
+            for (int i = threadIdx.x; i < (int)(rowb / 16); i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+            if (lane == 0) {
+                tc::mbar_init(ms.bars + 16u * warp, 1);
+                tc::mbar_init(ms.bars + 16u * warp + 8u, 1);
+            }
+            tc::fence_mbar_init();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the zero row, for the bulk stores
+            __syncthreads();
+        }
         for (int mb = 0; mb < n_mb; ++mb) {
             if (mb >= 2) {
                 // the region is reused: every gate/up tile of mb-2 must be done
-                if (threadIdx.x == 0)
+                if (threadIdx.x == 0) {
+                    const unsigned long long w0 = tracing ? globaltimer_ns() : 0ull;
                     s_word[0] = wait_counter(&p.g1_mb[mb - 2], v.mb[mb - 2].mtiles * NT1, st, tmo, kSiteCounter);
+                    if (tracing) tr.wait_ns += globaltimer_ns() - w0;
+                }
                 __syncthreads();
                 const int ok = s_word[0];
                 __syncthreads();
                 if (!ok) return;
                 // results of finished minibatches go back while the region drains
+                const unsigned long long c0 = (tracing && threadIdx.x == 0) ? globaltimer_ns() : 0ull;
                 if (!combine_loop(p, NT2, s_word, next_comb, false)) return;
+                if (tracing && threadIdx.x == 0) tr.comb_ns += globaltimer_ns() - c0;
             }
-            mover_dispatch_mb<MX>(p, mb, gwarp, nwarps, lane);
+            if (tracing && threadIdx.x == 0 && mb == 0) tr.t_first = globaltimer_ns();
+            if (pump) {
+                if (!mover_pump_mb<MX>(p, mb, gwarp, nwarps, lane, warp, ms, phases)) return;
+            } else {
+                mover_dispatch_mb<MX>(p, mb, gwarp, nwarps, lane);
+            }
             __syncthreads();
-            if (threadIdx.x == 0) s_word[3] = abort_requested(st) ? 1 : 0;
+            if (threadIdx.x == 0) {
+                s_word[3] = abort_requested(st) ? 1 : 0;
+                tr.units++;
+            }
             __syncthreads();
             if (s_word[3]) return;   // the same decision in every thread
         }
+        if (tracing && threadIdx.x == 0) tr.t_work_end = globaltimer_ns();
+        const unsigned long long c1 = (tracing && threadIdx.x == 0) ? globaltimer_ns() : 0ull;
         combine_loop(p, NT2, s_word, next_comb, true);
+        if (tracing && threadIdx.x == 0) {
+            tr.comb_ns += globaltimer_ns() - c1;
+            tr.write(p.trace + 8 * blockIdx.x, 0);
+        }
         return;
     }
 
@@ -598,11 +781,18 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
             for (int g = cidx; g < total && ok; g += ncomp) {
                 const MegaTile t = mega_decode(p, g, NT1, NT2);
                 // the tile's inputs must be published before its first load
+                const unsigned long long w0 = tracing ? globaltimer_ns() : 0ull;
                 if (t.kind == 0)
                     ok = wait_counter(&p.ready[t.mb * p.E + t.e], t.mt * kTileM, st, tmo, kSiteCounter);
                 else
                     ok = wait_counter(&p.g1_e[t.mb * p.E + t.e], t.mt * NT1, st, tmo, kSiteCounter);
                 if (!ok) break;
+                if (tracing) {
+                    const unsigned long long w1 = globaltimer_ns();
+                    tr.wait_ns += w1 - w0;
+                    if (tr.units == 0) tr.t_first = w1;
+                    tr.units++;
+                }
                 tc::fence_proxy_async_global();
                 const int nkb = t.kind == 0 ? kb1 : kb2;
                 const void* tmA = t.kind == 0 ? (const void*)&tmRing : (const void*)&tmH;
@@ -796,10 +986,17 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (threadIdx.x == 0) s_word[3] = abort_requested(st) ? 1 : 0;
+    if (threadIdx.x == 0) {
+        s_word[3] = abort_requested(st) ? 1 : 0;
+        if (tracing) tr.t_work_end = globaltimer_ns();
+    }
     __syncthreads();
     if (!s_word[3]) combine_loop(p, NT2, s_word, next_comb, true);
     __syncthreads();
+    if (tracing && threadIdx.x == 0) {
+        tr.comb_ns = globaltimer_ns() - tr.t_work_end;
+        tr.write(p.trace + 8 * blockIdx.x, 1);
+    }
     if (warp == 1) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
@@ -841,7 +1038,7 @@ size_t mega_scratch_bytes(int nbatch, int T, int H, int I, int E, int k, int reg
     (void)T;
     (void)k;
     const int64_t eb = mx ? 1 : 2;
-    size_t o = 0;
+    size_t o = kMegaTraceBytes;
     o += plan_bytes(E);
     o += align_up((int64_t)nbatch * plan_stage_ints(E) * 4, 1024);        // plan staging
     o += align_up((int64_t)kMaxMinibatches * (2 * E + 3) * 4, 1024);      // counters
@@ -849,6 +1046,7 @@ size_t mega_scratch_bytes(int nbatch, int T, int H, int I, int E, int k, int reg
     if (mx) o += align_up(2 * (int64_t)region_rows * H / 32, 1024);
     o += align_up(2 * (int64_t)region_rows * I * eb, 1024);               // h
     if (mx) o += align_up(2 * (int64_t)region_rows * I / 32, 1024);
+    if (mx) o += (size_t)nbatch * (align_up((int64_t)T * H, 1024) + align_up((int64_t)T * H / 32, 1024));  // x quantised
     return o;
 }
 
@@ -856,7 +1054,8 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     const bool mx = L.mx;
     const int E = L.E, H = L.H, I = L.I, k = L.k, T = L.T, nb = L.nbatch;
     const int64_t eb = mx ? 1 : 2;
-    char* w = static_cast<char*>(L.scratch);
+    char* w = static_cast<char*>(L.scratch) + kMegaTraceBytes;
+    if (L.grid > kMegaTraceCtas) return cudaErrorInvalidValue;
     PlanView v = plan_view(w, E);
     w += plan_bytes(E);
     int* stage = reinterpret_cast<int*>(w);
@@ -872,6 +1071,19 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     w += align_up(2 * (int64_t)L.region_rows * I * eb, 1024);
     uint8_t* h_sf = nullptr;
     if (mx) { h_sf = reinterpret_cast<uint8_t*>(w); w += align_up(2 * (int64_t)L.region_rows * I / 32, 1024); }
+    // MXFP8: every batch's rows quantised once per token; the movers copy them
+    uint8_t* xq[kMaxBatches] = {};
+    uint8_t* xsf[kMaxBatches] = {};
+    if (mx) {
+        for (int b = 0; b < nb; ++b) {
+            xq[b] = reinterpret_cast<uint8_t*>(w);
+            w += align_up((int64_t)T * H, 1024);
+            xsf[b] = reinterpret_cast<uint8_t*>(w);
+            w += align_up((int64_t)T * H / 32, 1024);
+            cudaError_t eq = launch_quantize_rows(L.x[b], T, H, xq[b], xsf[b], s);
+            if (eq != cudaSuccess) return eq;
+        }
+    }
 
     PlanBatches pbs;
     for (int b = 0; b < nb; ++b) {
@@ -897,6 +1109,8 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     p.E = E; p.H = H; p.I = I; p.k = k; p.T = T; p.nbatch = nb;
     for (int b = 0; b < nb; ++b) {
         p.batches[b].x = static_cast<const __nv_bfloat16*>(L.x[b]);
+        p.batches[b].xq = xq[b];
+        p.batches[b].xsf = reinterpret_cast<const uint32_t*>(xsf[b]);
         p.batches[b].row_src = L.row_src[b];
         p.batches[b].topk_w = L.topk_w[b];
         p.batches[b].partials = static_cast<__nv_bfloat16*>(L.partials[b]);
@@ -915,6 +1129,7 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     p.bn2 = BN2;
     p.n_movers = L.n_movers;
     p.test_flags = L.test_flags;
+    p.trace = L.trace;
     p.status = L.status;
     p.timeout_ns = L.timeout_ns;
 

@@ -42,6 +42,55 @@ __device__ __forceinline__ int find_expert(const int32_t* poff, int E, int pr) {
 // ---------------------------------------------------------------------------
 // Pull-dispatch: one warp per padded row.
 // ---------------------------------------------------------------------------
+// One 32-element MXFP8 block: E8M0 code of its amax, E4M3 bytes of x / scale.
+__device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* src, uint4& o0, uint4& o1) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(s4 + i);
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[8 * i + 0] = bf16_lo(v[i].x); f[8 * i + 1] = bf16_hi(v[i].x);
+        f[8 * i + 2] = bf16_lo(v[i].y); f[8 * i + 3] = bf16_hi(v[i].y);
+        f[8 * i + 4] = bf16_lo(v[i].z); f[8 * i + 5] = bf16_hi(v[i].z);
+        f[8 * i + 6] = bf16_lo(v[i].w); f[8 * i + 7] = bf16_hi(v[i].w);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const uint32_t code = e8m0_code(amax);
+    const float inv = e8m0_inv_scale(code);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+    o0 = make_uint4(w[0], w[1], w[2], w[3]);
+    o1 = make_uint4(w[4], w[5], w[6], w[7]);
+    return code;
+}
+
+// Row-wise MXFP8 quantisation of x (warp per row; the codes the dispatch
+// writes): x_q [T, H] E4M3, x_sf bytes [T, H/32] (= words [T, H/128], byte j
+// of word c = scale of 32-block 4c + j).
+__global__ void __launch_bounds__(256)
+quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, uint8_t* __restrict__ xq,
+                     uint8_t* __restrict__ xsf) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = H / 32;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < T; t += (int64_t)gridDim.x * 8) {
+        for (int b = lane; b < nb; b += 32) {
+            uint4 o0, o1;
+            const uint32_t code = quantize_block32(x + t * H + b * 32, o0, o1);
+            uint4* dst = reinterpret_cast<uint4*>(xq + t * H + b * 32);
+            dst[0] = o0;
+            dst[1] = o1;
+            xsf[t * nb + b] = (uint8_t)code;
+        }
+    }
+}
+
 template <bool MX>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
@@ -102,32 +151,7 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
                 const bool act = b < nb;   // nb is a multiple of 4: chunks are whole
                 uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
                 uint32_t code = 0;
-                if (src && act) {
-                    const uint4* s4 = reinterpret_cast<const uint4*>(src + b * 32);
-                    uint4 v[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) v[i] = __ldg(s4 + i);
-                    float f[32];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        f[8 * i + 0] = bf16_lo(v[i].x); f[8 * i + 1] = bf16_hi(v[i].x);
-                        f[8 * i + 2] = bf16_lo(v[i].y); f[8 * i + 3] = bf16_hi(v[i].y);
-                        f[8 * i + 4] = bf16_lo(v[i].z); f[8 * i + 5] = bf16_hi(v[i].z);
-                        f[8 * i + 6] = bf16_lo(v[i].w); f[8 * i + 7] = bf16_hi(v[i].w);
-                    }
-                    float amax = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                    code = e8m0_code(amax);
-                    const float inv = e8m0_inv_scale(code);
-                    uint32_t w[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
-                               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
-                    o0 = make_uint4(w[0], w[1], w[2], w[3]);
-                    o1 = make_uint4(w[4], w[5], w[6], w[7]);
-                }
+                if (src && act) code = quantize_block32(src + b * 32, o0, o1);
                 uint32_t word = code;
                 word |= __shfl_down_sync(0xffffffffu, code, 1) << 8;
                 word |= __shfl_down_sync(0xffffffffu, code, 2) << 16;
@@ -386,6 +410,14 @@ cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, 
         dispatch_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts,
                                                       offsets, row_src, A, nullptr,
                                                       static_cast<const __nv_bfloat16*>(scale_src), wslot);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>(ceil_div(T, 8), (int64_t)sm_count() * 8);
+    quantize_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H,
+                                                static_cast<uint8_t*>(x_q), static_cast<uint8_t*>(x_sf));
     return cudaGetLastError();
 }
 

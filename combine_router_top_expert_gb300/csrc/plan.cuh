@@ -99,10 +99,15 @@ struct MegaLaunch {
     int n_movers;            // mover CTAs
     int grid;                // CTAs (<= SMs)
     int test_flags;          // MOK_FLAG_TEST_* bits
+    unsigned long long* trace;   // MOK_FLAG_TRACE: one 8 x u64 record per CTA, else NULL
     StatusBlock* status;
     unsigned long long timeout_ns;
 };
 
+// The scratch starts with the trace records (kMegaTraceBytes), then the plan,
+// counters, ring and h regions.
+constexpr int kMegaTraceCtas = 1024;
+constexpr size_t kMegaTraceBytes = (size_t)kMegaTraceCtas * 64;
 size_t mega_scratch_bytes(int nbatch, int T, int H, int I, int E, int k, int region_rows, bool mx);
 cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s);
 

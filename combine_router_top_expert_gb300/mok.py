@@ -29,6 +29,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
+FLAG_TRACE = 4
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 
@@ -306,6 +307,12 @@ def expert_ffn(p: Problem, A, A_sf, packed, routing, h, h_sf, partials, workspac
 def combine(p: Problem, partials, topk_w, out, shared=None, stream=None):
     rc = lib().mok_combine(ctypes.byref(p), _ptr(partials), _ptr(topk_w), _ptr(shared), _ptr(out), _stream(stream))
     _check(rc, "mok_combine")
+
+
+def megakernel_trace(workspace, n_ctas):
+    """Per-CTA megakernel records written under FLAG_TRACE: int64 [n_ctas, 8]
+    (role, t_begin, t_first, t_work_end, t_exit, wait_ns, units, combine_ns)."""
+    return workspace[256:256 + 64 * n_ctas].view(torch.int64).view(n_ctas, 8).cpu().numpy()
 
 
 def device_status(workspace, reset=False, stream=None):

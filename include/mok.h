@@ -91,6 +91,15 @@ typedef struct {
  * MXFP8 and the shared expert run single CTAs. Off by default (measured no
  * faster at 2560 tokens x 8 of 32 experts). */
 #define MOK_FLAG_GEMM_PAIRS 2
+/* Megakernel trace: the launch writes one record of eight uint64 per CTA
+ * (CTA i at byte offset 256 + 64*i of the workspace): [0] role (0 mover,
+ * 1 compute), [1] globaltimer at entry (ns), [2] start of its first unit of
+ * work (mover: first minibatch; compute: first tile's loads, after its
+ * counter wait), [3] end of its tile/move work, [4] exit, [5] ns spent
+ * waiting on GPU-local counters (compute: tile inputs published; mover:
+ * ring region free), [6] units done (tiles; minibatches), [7] ns in the
+ * weighted sums. Costs a few timer reads per tile. */
+#define MOK_FLAG_TRACE 4
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use

@@ -154,3 +154,40 @@ def test_withheld_publish_times_out_cleanly():
     ref = _staged(layer, x, wl.T)
     out, st = _forward(layer, x, mok.make_config(), wl.T)
     assert st == (mok.OK, 0) and torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_trace_records_and_unchanged_output():
+    """MOK_FLAG_TRACE: one record per CTA (movers first), ordered timestamps,
+    every gate/up and down tile counted once, output bit-identical."""
+    wl = CASES[2]
+    inp = synth.make_inputs(wl, seed=3)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    ref = _staged(layer, x, wl.T)
+    movers = 8
+    cfg = mok.make_config(mover_ctas=movers, minibatch_tokens=256, flags=mok.FLAG_TRACE)
+    cfg.flags |= mok.FLAG_MEGAKERNEL
+    p = layer.problem(wl.T)
+    ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
+    out = torch.empty((wl.T, layer.H), dtype=torch.bfloat16, device="cuda")
+    mok.moe_forward(p, x, layer.packed, layer.buffers(wl.T)["routing"], out, ws, packed_shared=layer.packed_shared,
+                    cfg=cfg)
+    torch.cuda.synchronize()
+    assert mok.device_status(ws) == (mok.OK, 0)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    rec = mok.megakernel_trace(ws, n)
+    assert np.all(rec[:movers, 0] == 0) and np.all(rec[movers:, 0] == 1)
+    assert np.all(rec[:, 1] <= rec[:, 4]) and np.all(rec[:, 3] <= rec[:, 4])
+    work = rec[:, 6] > 0
+    assert np.all(rec[work, 1] <= rec[work, 2]) and np.all(rec[work, 2] <= rec[work, 3])
+    counts = layer.buffers(wl.T)["routing"]["counts"].cpu().numpy()
+    n_mb = int(np.max(rec[:movers, 6]))
+    assert n_mb >= 2   # 1000 tokens in minibatches of at most 256
+    # every tile of both GEMMs ran once (tiles per minibatch sum to at least the
+    # whole batch's, since each minibatch pads its experts' rows separately)
+    nt1, nt2 = 2 * wl.I // 256, wl.H // 128
+    tiles_min = int(np.sum((counts + 127) // 128)) * (nt1 + nt2)
+    assert int(rec[movers:, 6].sum()) >= tiles_min
