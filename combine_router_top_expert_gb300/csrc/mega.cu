@@ -575,11 +575,13 @@ constexpr int kCombineChunk = 4;
 // in minibatch order. blocking: wait for each minibatch in turn (a CTA with
 // no other work); otherwise stop at the first unfinished minibatch. Called
 // by every thread of the CTA; all decisions are broadcast through s_word.
-__device__ bool combine_loop(const MegaParams& p, int NT2, int* s_word, int& next_mb, bool blocking) {
+__device__ bool combine_loop(const MegaParams& p, int NT2, int* s_word, int& next_mb, bool blocking,
+                             int budget = 1 << 30, int* done = nullptr) {
     const PlanView& v = p.plan;
     const int n_mb = v.hdr->n_mb;
     StatusBlock* st = p.status;
-    while (next_mb < n_mb) {
+    int taken = 0;
+    while (next_mb < n_mb && taken < budget) {
         const MbInfo mi = v.mb[next_mb];
         const int tiles2 = mi.mtiles * NT2;
         if (threadIdx.x == 0) {
@@ -595,17 +597,20 @@ __device__ bool combine_loop(const MegaParams& p, int NT2, int* s_word, int& nex
         if (ok == 0) return true;
         const MegaBatch bt = p.batches[mi.batch];
         const int nch = ceil_div(mi.t1 - mi.t0, kCombineChunk);
-        for (;;) {
+        bool drained = false;
+        while (taken < budget) {
             if (threadIdx.x == 0) s_word[1] = atomicAdd(&p.comb_next[next_mb], 1);
             __syncthreads();
             const int ch = s_word[1];
             __syncthreads();
-            if (ch >= nch) break;
+            if (ch >= nch) { drained = true; break; }
             const int t0 = mi.t0 + ch * kCombineChunk;
             combine_tokens(p, bt, t0, min(mi.t1, t0 + kCombineChunk));
+            ++taken;
         }
-        ++next_mb;
+        if (drained) ++next_mb;
     }
+    if (done) *done = taken;
     return true;
 }
 
@@ -687,20 +692,34 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         }
         for (int mb = 0; mb < n_mb; ++mb) {
             if (mb >= 2) {
-                // the region is reused: every gate/up tile of mb-2 must be done
-                if (threadIdx.x == 0) {
-                    const unsigned long long w0 = tracing ? globaltimer_ns() : 0ull;
-                    s_word[0] = wait_counter(&p.g1_mb[mb - 2], v.mb[mb - 2].mtiles * NT1, st, tmo, kSiteCounter);
-                    if (tracing) tr.wait_ns += globaltimer_ns() - w0;
+                // the region is reused once every gate/up tile of mb-2 is done;
+                // until then the movers take weighted-sum chunks of finished
+                // minibatches, one at a time, so a free region is never kept
+                // waiting (bounded by the same time limit as every wait)
+                const int target = v.mb[mb - 2].mtiles * NT1;
+                const unsigned long long w0 = globaltimer_ns();
+                for (;;) {
+                    if (threadIdx.x == 0) {
+                        int ok = ld_acquire(&p.g1_mb[mb - 2]) >= target ? 1 : 0;
+                        if (!ok && abort_requested(st)) ok = -1;
+                        if (!ok && globaltimer_ns() - w0 > tmo) {
+                            record_failure(st, MOK_ERR_TIMEOUT, kSiteCounter);
+                            ok = -1;
+                        }
+                        s_word[0] = ok;
+                    }
+                    __syncthreads();
+                    const int ok = s_word[0];
+                    __syncthreads();
+                    if (ok < 0) return;
+                    if (ok > 0) break;
+                    int did = 0;
+                    const unsigned long long c0 = (tracing && threadIdx.x == 0) ? globaltimer_ns() : 0ull;
+                    if (!combine_loop(p, NT2, s_word, next_comb, false, 1, &did)) return;
+                    if (tracing && threadIdx.x == 0) tr.comb_ns += globaltimer_ns() - c0;
+                    if (!did && threadIdx.x == 0) __nanosleep(200);
                 }
-                __syncthreads();
-                const int ok = s_word[0];
-                __syncthreads();
-                if (!ok) return;
-                // results of finished minibatches go back while the region drains
-                const unsigned long long c0 = (tracing && threadIdx.x == 0) ? globaltimer_ns() : 0ull;
-                if (!combine_loop(p, NT2, s_word, next_comb, false)) return;
-                if (tracing && threadIdx.x == 0) tr.comb_ns += globaltimer_ns() - c0;
+                if (tracing && threadIdx.x == 0) tr.wait_ns += globaltimer_ns() - w0;
             }
             if (tracing && threadIdx.x == 0 && mb == 0) tr.t_first = globaltimer_ns();
             if (pump) {
