@@ -158,8 +158,10 @@ GemmCommon make_common(void* ws, const mok_config* cfg) {
     return c;
 }
 
-bool routing_ok(const mok_routing* r) {
-    return r && r->topk_idx && r->topk_w && r->counts && r->offsets && r->row_src && r->slot_row;
+// Routing arrays present (the per-token ones may be empty when T == 0).
+bool routing_ok(const mok_routing* r, int32_t T = 1) {
+    return r && r->counts && r->offsets &&
+           (T == 0 || (r->topk_idx && r->topk_w && r->row_src && r->slot_row));
 }
 
 // Requires an sm_103-class device for the tensor-core kernels.
@@ -254,7 +256,7 @@ size_t mok_workspace_size_batches(const mok_problem* p, int32_t nbatch, const mo
 
 mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
                         mok_stream_t stream) {
-    if (!problem_ok(p) || !routing_ok(r) || !A || (p->T > 0 && !x)) return MOK_ERR_INVALID;
+    if (!problem_ok(p) || !routing_ok(r, p->T) || !A || (p->T > 0 && !x)) return MOK_ERR_INVALID;
     if (p->dtype == MOK_MXFP8 && !A_sf) return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;
     return cuda_status(launch_dispatch(p->dtype == MOK_MXFP8, x, p->T, p->H, p->E, p->k, r->counts, r->offsets,
@@ -265,7 +267,7 @@ mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* 
 mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf, const void* packed,
                           const mok_routing* r, void* h, void* h_sf, void* partials, const mok_config* cfg,
                           void* workspace, mok_stream_t stream) {
-    if (!problem_ok(p) || !routing_ok(r) || !A || !packed || !h || !partials || !workspace) return MOK_ERR_INVALID;
+    if (!problem_ok(p) || !routing_ok(r, p->T) || !A || !packed || !h || !partials || !workspace) return MOK_ERR_INVALID;
     const bool mx = p->dtype == MOK_MXFP8;
     if (mx && (!A_sf || !h_sf)) return MOK_ERR_INVALID;
     if (!aligned(A, 1024) || !aligned(h, 1024) || !aligned(packed, 256) || !aligned(workspace, 256))
@@ -362,7 +364,7 @@ mok_status mok_moe_forward_batches(const mok_problem* p, int32_t nbatch, const m
         !aligned(a[0].packed, 256))
         return MOK_ERR_INVALID;
     for (int b = 0; b < nbatch; ++b) {
-        if (!routing_ok(&a[b].routing) || !a[b].out || a[b].saved) return MOK_ERR_INVALID;
+        if (!routing_ok(&a[b].routing, p->T) || !a[b].out || a[b].saved) return MOK_ERR_INVALID;
         if (p->T > 0 && (!a[b].x || !aligned(a[b].x, 16) || !aligned(a[b].out, 16))) return MOK_ERR_INVALID;
     }
     if (mega_region_rows(p, cfg) < kTileM) return MOK_ERR_INVALID;
@@ -372,7 +374,7 @@ mok_status mok_moe_forward_batches(const mok_problem* p, int32_t nbatch, const m
 
 mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mok_config* cfg,
                            mok_stream_t stream) {
-    if (!problem_ok(p) || !a || !routing_ok(&a->routing) || !a->packed || !a->out || !a->workspace)
+    if (!problem_ok(p) || !a || !routing_ok(&a->routing, p->T) || !a->packed || !a->out || !a->workspace)
         return MOK_ERR_INVALID;
     if (p->T > 0 && !a->x) return MOK_ERR_INVALID;
     if ((p->I_shared > 0) != (a->packed_shared != nullptr)) return MOK_ERR_INVALID;
@@ -433,12 +435,13 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
 
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const mok_config* cfg,
                             mok_stream_t stream) {
-    if (!problem_ok(p) || !a || !routing_ok(&a->routing)) return MOK_ERR_INVALID;
+    if (!problem_ok(p) || !a || !routing_ok(&a->routing, p->T)) return MOK_ERR_INVALID;
     if (p->dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
     if (p->I_shared > 0) return MOK_ERR_UNSUPPORTED;
-    if (!a->x || !a->W_r || !a->W_gate || !a->W_up || !a->W_down || !a->dY || !a->saved || !a->dX ||
-        !a->dW_gate || !a->dW_up || !a->dW_down || !a->dW_r || !a->workspace)
+    if (!a->W_r || !a->W_gate || !a->W_up || !a->W_down || !a->saved || !a->dW_gate || !a->dW_up || !a->dW_down ||
+        !a->dW_r || !a->workspace)
         return MOK_ERR_INVALID;
+    if (p->T > 0 && (!a->x || !a->dY || !a->dX)) return MOK_ERR_INVALID;   // token arrays may be empty
     if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->saved, 1024))
         return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;

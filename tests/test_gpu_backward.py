@@ -11,6 +11,10 @@ BWD_CASES = [
     synth.small("bwd_tiny", T=64, H=128, I=64, E=8, k=2, backward=True),
     synth.small("bwd_ragged", T=500, H=512, I=256, E=4, k=2, backward=True),
     synth.small("bwd_skew", T=300, H=256, I=512, E=8, k=4, zipf_s=1.2, backward=True),
+    # one expert, k = 1: a dense SwiGLU FFN (router gradient is zero)
+    synth.small("bwd_dense", T=130, H=256, I=128, E=1, k=1, backward=True),
+    # k = E: every token through every expert
+    synth.small("bwd_all_experts", T=96, H=256, I=128, E=4, k=4, backward=True),
 ]
 
 

@@ -26,6 +26,11 @@ FWD_CASES = [
     synth.small("dense", T=130, H=256, I=128, E=1, k=1),
     # more experts than tokens can fill: several experts get zero rows
     synth.small("sparse", T=8, H=256, I=128, E=64, k=1),
+    # every token to every expert (k = E: the weights are the full softmax)
+    synth.small("all_experts", T=100, H=256, I=128, E=4, k=4),
+    # the largest expert count the routing kernels take (256), BF16 and MXFP8
+    synth.small("e256", T=300, H=256, I=128, E=256, k=8, zipf_s=1.2),
+    synth.small("mx_e256", T=200, H=512, I=128, E=256, k=4, dtype="mxfp8"),
 ]
 
 
@@ -152,3 +157,27 @@ def test_invalid_arguments_rejected_on_host():
     with pytest.raises(mok.MokError) as ei:
         mok.moe_forward(p_mx, x, layer.packed, b["routing"], b["out"], b["ws"], saved=b["ws"])
     assert ei.value.code == mok.ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_empty_batch():
+    """T = 0: routing yields zero counts and offsets, forward and training
+    forward + backward run no tile and report MOK_OK."""
+    wl = synth.small("empty", T=8, H=256, I=128, E=4, k=2)
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x0 = torch.empty((0, wl.H), dtype=torch.bfloat16, device="cuda")
+    r = layer.route(x0)
+    torch.cuda.synchronize()
+    assert int(r["counts"].abs().sum()) == 0 and int(r["offsets"].abs().sum()) == 0
+    out = layer.forward(x0, route=False)
+    torch.cuda.synchronize()
+    assert out.shape[0] == 0 and layer.status(0) == (mok.OK, 0)
+    layer.forward(x0, training=True)
+    g = layer.backward(x0, torch.empty_like(x0))
+    torch.cuda.synchronize()
+    assert layer.status(0, training=True) == (mok.OK, 0)
+    assert g["dX"].shape[0] == 0
+    # nothing routed: every weight gradient is zero
+    for n in ("dW_gate", "dW_up", "dW_down", "dW_r"):
+        assert float(g[n].float().abs().max()) == 0.0, n
