@@ -46,9 +46,24 @@ bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int
     return r == CUDA_SUCCESS;
 }
 
+// Scale chunks as a 2-D byte tensor: a 512-byte chunk is two 256-byte rows
+// (no swizzle); the pair kernels load one chunk per TMA box of 256 x 2.
+bool make_tmap_chunks(CUtensorMap* m, const void* base, int64_t chunks) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {256, (cuuint64_t)(2 * chunks)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, 2};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
-cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
-                int64_t tiles_ub, int num_sms, cudaStream_t s) {
+cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& sa,
+                const CUtensorMap& sb, const GemmParams& p, int64_t tiles_ub, int num_sms, cudaStream_t s) {
     using C = GemmCfg<BN, MX, MN, EPI, S, ACC, CLN>;
     auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC, CLN>;
     ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
@@ -79,9 +94,15 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
     }
     if (grid < 1) return cudaSuccess;
     cfg.gridDim = dim3(grid);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, b2, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, b2, sa, sb, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
+cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
+                int64_t tiles_ub, int num_sms, cudaStream_t s) {
+    return run<BN, MX, MN, EPI, S, ACC, CLN>(a, b, b2, b, b, p, tiles_ub, num_sms, s);
 }
 
 GemmParams base_params(const GemmCommon& c) {
@@ -132,8 +153,8 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.b_sf = Bgu_sf;
     p.sf_kchunks = H / 128;
     p.n_tiles = 2 * I / BN;
-    // 2-SM pairs (BF16, 256-wide, grouped rows): each CTA loads half of B
-    const bool cl = c.cluster == 2 && !mx && BN == 256 && identity_rows == 0;
+    // 2-SM pairs (256-wide, grouped rows): each CTA loads half of B
+    const bool cl = c.cluster == 2 && BN == 256 && identity_rows == 0;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, a_rows, H, eb, bk, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
@@ -143,6 +164,13 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
         // MXFP8: 256-wide tiles (gate 128 | up 128) with one accumulator (the
         // block scales need the rest of tensor memory); I is a multiple of 128
         if (BN != 256) return cudaErrorInvalidValue;
+        if (cl) {
+            CUtensorMap tsa, tsb;
+            if (!make_tmap_chunks(&tsa, A_sf, (a_rows / kTileM) * (H / 128)) ||
+                !make_tmap_chunks(&tsb, Bgu_sf, (int64_t)p.E * 2 * I / kTileM * (H / 128)))
+                return cudaErrorInvalidValue;
+            return run<256, true, false, kEpiSwiGLU, 6, 1, 2>(ta, tb, tb, tsa, tsb, p, tub, c.num_sms, s);
+        }
         return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {

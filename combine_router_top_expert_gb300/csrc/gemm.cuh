@@ -60,7 +60,7 @@ struct GemmParams {
 // the BN B rows of the pair's 256 x BN tile.
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN = 1>
 struct GemmCfg {
-    static_assert(CLN == 1 || (CLN == 2 && !MX && !MN_MAJOR && BN % 32 == 0), "2-SM pairs: BF16, K-major");
+    static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR && BN % 32 == 0 && (!MX || BN == 256)), "2-SM pairs: K-major");
     static constexpr int kThreads = 192;
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
     static constexpr int kBytesB = BN / CLN * 128;
@@ -205,7 +205,8 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN>
 __global__ void __launch_bounds__(192, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
     using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>;
     static_assert(CLN == 1 || (CLN == 2 && EPI != kEpiDense), "2-SM pairs: grouped-row GEMMs");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -245,6 +246,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tc::prefetch_tmap(&tmA);
         tc::prefetch_tmap(&tmB);
         tc::prefetch_tmap(&tmB2);
+        if constexpr (MX && CLN == 2) {
+            tc::prefetch_tmap(&tmSA);
+            tc::prefetch_tmap(&tmSB);
+        }
     }
     if (warp == 1) {
         if constexpr (CLN == 2) {
@@ -284,12 +289,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if constexpr (CLN == 2) {
                         // both halves signal the leader's full barrier, which expects both
                         const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
-                        if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2 * C::kStageBytes);
+                        if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2 * (C::kStageBytes + C::kSfStage));
                         tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, kb * C::kBK, ti.a_row0);
                         const bool b1 = kb < p.b_split_kb;
+                        const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
                         tc::tma_load_2d_2sm(b_tile(stage), b1 ? (const void*)&tmB : (const void*)&tmB2, lead_full,
-                                            (b1 ? kb : kb - p.b_split_kb) * C::kBK,
-                                            ti.e * p.b_rows_per_expert + ti.n * BN + rank * (BN / 2));
+                                            (b1 ? kb : kb - p.b_split_kb) * C::kBK, brow + rank * (BN / 2));
+                        if constexpr (MX) {
+                            // scale chunks (512 B = two 256-byte rows of tmSA / tmSB): this CTA's A
+                            // rows, and all BN rows of B (the pair MMA reads B's scales in each CTA)
+                            tc::tma_load_2d_2sm(sf_tile(stage), &tmSA, lead_full, 0,
+                                                2 * ((ti.a_row0 / kTileM) * p.sf_kchunks + kb));
+#pragma unroll
+                            for (int j = 0; j < C::kNChunks; ++j)
+                                tc::tma_load_2d_2sm(sf_tile(stage) + 512 * (1 + j), &tmSB, lead_full, 0,
+                                                    2 * ((brow / kTileM + j) * p.sf_kchunks + kb));
+                        }
                         last_par[stage] = (int)ph;
                         if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                         continue;
@@ -363,11 +378,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if constexpr (MX) {
                         sfa_t = tmem + (uint32_t)C::sf_col(stage);
                         sfb_t = sfa_t + 4;
-                        tc::tmem_cp_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
+                        if constexpr (CLN == 2) {
+                            tc::tmem_cp_2sm_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
 #pragma unroll
-                        for (int j = 0; j < C::kNChunks; ++j)
-                            tc::tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                                       tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
+                            for (int j = 0; j < C::kNChunks; ++j)
+                                tc::tmem_cp_2sm_32x128b_warpx4(
+                                    sfb_t + 4 * j, tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
+                        } else {
+                            tc::tmem_cp_32x128b_warpx4(sfa_t, tc::make_sdesc(sf_tile(stage), 0, 128, tc::kLayoutNone));
+#pragma unroll
+                            for (int j = 0; j < C::kNChunks; ++j)
+                                tc::tmem_cp_32x128b_warpx4(
+                                    sfb_t + 4 * j, tc::make_sdesc(sf_tile(stage) + 512 * (1 + j), 0, 128, tc::kLayoutNone));
+                        }
                     }
 #pragma unroll
                     for (int kk = 0; kk < C::kMmasPerStage; ++kk) {
@@ -380,7 +403,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             bd = tc::make_sdesc(b_tile(stage) + kk * 32, 16, 1024, tc::kLayoutSW128);
                         }
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (MX) {
+                        if constexpr (MX && CLN == 2) {
+                            tc::mma_mxf8_2sm(d, ad, bd, tc::idesc_mxf8(256, BN, kk, kk), sfa_t, sfb_t, accum);
+                        } else if constexpr (MX) {
                             tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
                         } else if constexpr (CLN == 2) {
                             tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(256, BN, false, false), accum);

@@ -238,6 +238,23 @@ __device__ __forceinline__ void mma_bf16_2sm(uint32_t d, uint64_t adesc, uint64_
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// CTA pair, MXFP8 block-scaled: each CTA's tensor memory holds the scales
+// of its own A rows (sfa) and of all N rows of B (sfb).
+__device__ __forceinline__ void mma_mxf8_2sm(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+// CTA pair: copies the described shared-memory block of each CTA into that
+// CTA's tensor memory at taddr (32 rows x 16 bytes, into all four quadrants).
+__device__ __forceinline__ void tmem_cp_2sm_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive once on the mbarrier at `bar` in every CTA of `mask` when every
 // pair MMA this thread issued before has completed.
 __device__ __forceinline__ void mma_commit_2sm_multicast(uint32_t bar, uint16_t mask) {

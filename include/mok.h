@@ -83,13 +83,14 @@ typedef struct {
  * SM split, GPU-local counters, ring) instead of the stage kernels
  * (dispatch, grouped GEMMs, combine). */
 #define MOK_FLAG_MEGAKERNEL 1
-/* Run the staged BF16 grouped GEMMs (forward gate/up and down, backward
- * dgrad) as 2-SM CTA pairs: tcgen05 cta_group::2 MMAs of 256 rows over two
- * CTAs, each staging its own 128 A rows and half of the B rows. Results are
+/* Run the staged grouped GEMMs (BF16 forward gate/up and down, backward
+ * dgrad; MXFP8 gate/up) as 2-SM CTA pairs: tcgen05 cta_group::2 MMAs of 256
+ * rows over two CTAs, each staging its own 128 A rows and half of the B rows
+ * (MXFP8: its A rows' block scales and all B rows' scales). Results are
  * bit-identical to the default single-CTA kernels; experts whose row count
- * is an odd number of 128-row tiles leave half of their last pair idle.
- * MXFP8 and the shared expert run single CTAs. Off by default (measured no
- * faster at 2560 tokens x 8 of 32 experts). */
+ * is an odd number of 128-row tiles leave half of their last pair idle. The
+ * shared expert and the MXFP8 down GEMM run single CTAs. Off by default
+ * (measured no faster). */
 #define MOK_FLAG_GEMM_PAIRS 2
 /* Megakernel trace: the launch writes one record of eight uint64 per CTA
  * (CTA i at byte offset 256 + 64*i of the workspace): [0] role (0 mover,
