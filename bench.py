@@ -11,8 +11,9 @@ SwiGLU, grouped down GEMM with push-combine, fixed-order weighted sum.
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
 on the launching stream; L2 is flushed (a 256 MiB write) before every timed
 step. Multi-GPU (torchrun, N > 1): every rank runs an independent replica of
-the layer (the layer does not shard on one node without expert parallelism);
-rank 0 reports the aggregate over ranks with the max time.
+the layer on its own token shard with the same weights (data parallel; no
+collective on the data path, since expert parallelism needs peer GPUs in one
+NVLink domain); rank 0 reports all ranks' tokens over the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -113,6 +114,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks (identity on
+    one rank): the slowest rank's timings set the whole job's rate."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world_size, units_per_rank_step, steps, slowest_ms):
+    """Units processed by all ranks per second of the slowest rank's time."""
+    return world_size * units_per_rank_step * steps / (slowest_ms / 1000.0)
 
 
 def oracle_layer_seconds(inp, wl, t0, n):
@@ -244,7 +262,8 @@ def main():
     from combine_router_top_expert_gb300.layer import MoELayer, to_dev_bf16
 
     dtype = mok.MXFP8 if wl.dtype == "mxfp8" else mok.BF16
-    inp = synth.make_inputs(wl)
+    # data-parallel replicas: every rank holds the same weights and its own tokens
+    inp = synth.make_inputs(wl, shard=rank)
     layer = MoELayer(inp.W_r, inp.Wg, inp.Wu, inp.Wd, wl.k, dtype=dtype, bias=inp.bias, shared=inp.shared,
                      device=dev, keep_unpacked=wl.backward)
     T, H = wl.T, wl.H
@@ -477,16 +496,12 @@ def main():
         raise SystemExit(f"device status after end-to-end steps: {mok.device_status(status_ws)}")
 
     # aggregate over ranks: total tokens / max time
-    t_max = total_ms
-    e2e_max = sum(e2e_ms)
-    if ws > 1:
-        tt = torch.tensor([total_ms, e2e_max], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max, e2e_max = tt.tolist()
+    t_max, e2e_max = max_over_ranks([total_ms, sum(e2e_ms)], dev)
     if rank != 0:
+        torch.distributed.destroy_process_group()
         return
-    value = ws * tokens_per_step * args.steps / (t_max / 1000.0)
-    e2e_val = ws * tokens_per_step * n_e2e / (e2e_max / 1000.0)
+    value = whole_job_rate(ws, tokens_per_step, args.steps, t_max)
+    e2e_val = whole_job_rate(ws, tokens_per_step, n_e2e, e2e_max)
     peaks = load_peaks()
     fl = flops
     g_ms = statistics.mean(gemm_ms)

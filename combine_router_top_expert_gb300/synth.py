@@ -9,8 +9,12 @@ order):
   W_gate [E, H, I], W_up [E, H, I], W_down [E, I, H] ~ N(0, 0.02), drawn in
       fp32 expert by expert and rounded to BF16 (round to nearest even)
   shared expert (optional) W_sg [H, Is], W_su [H, Is], W_sd [Is, H] likewise
-  x [T, H] ~ N(0, 1) rounded to BF16, from a generator seeded ``seed + batch``
-  dY [T, H] ~ N(0, 1) rounded to BF16, from a generator seeded ``seed + 1000``
+  x [T, H] ~ N(0, 1) rounded to BF16, from a generator seeded
+      ``seed + batch + SHARD_STRIDE * shard``
+  dY [T, H] ~ N(0, 1) rounded to BF16, from a generator seeded
+      ``seed + 1000 + SHARD_STRIDE * shard``
+Data-parallel shards (one per rank) share every weight and draw their own
+tokens; shard 0 is the single-GPU input.
 Skewed routing uses a per-expert logit bias b_e = ln(p_e) with p a Zipf law
 of exponent s over the E experts: p_e = (e+1)^-s / sum_n n^-s.
 """
@@ -106,12 +110,15 @@ class LayerInputs:
         return self.xs[0]
 
 
-def make_x(wl: Workload, batch: int = 0, seed: int = 0) -> np.ndarray:
-    g = torch.Generator().manual_seed(seed + batch)
+SHARD_STRIDE = 100_003
+
+
+def make_x(wl: Workload, batch: int = 0, seed: int = 0, shard: int = 0) -> np.ndarray:
+    g = torch.Generator().manual_seed(seed + batch + SHARD_STRIDE * shard)
     return _normal_bf16(g, (wl.T, wl.H), 1.0)
 
 
-def make_inputs(wl: Workload, seed: int = 0, with_x: bool = True) -> LayerInputs:
+def make_inputs(wl: Workload, seed: int = 0, with_x: bool = True, shard: int = 0) -> LayerInputs:
     g = torch.Generator().manual_seed(seed)
     W_r = (torch.randn((wl.H, wl.E), generator=g, dtype=torch.float32) * 0.02).numpy()
     Wg = np.empty((wl.E, wl.H, wl.I), np.uint16)
@@ -128,9 +135,9 @@ def make_inputs(wl: Workload, seed: int = 0, with_x: bool = True) -> LayerInputs
     bias = zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None
     inp = LayerInputs(wl, W_r, bias, Wg, Wu, Wd, shared)
     if with_x:
-        inp.xs = [make_x(wl, b, seed) for b in range(wl.batches)]
+        inp.xs = [make_x(wl, b, seed, shard) for b in range(wl.batches)]
     if wl.backward:
-        gd = torch.Generator().manual_seed(seed + 1000)
+        gd = torch.Generator().manual_seed(seed + 1000 + SHARD_STRIDE * shard)
         inp.dY = _normal_bf16(gd, (wl.T, wl.H), 1.0)
     return inp
 
