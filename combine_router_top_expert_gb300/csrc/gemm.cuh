@@ -7,13 +7,16 @@
 // partial, the backward dgrad GEMMs, and the backward wgrad GEMMs that reduce
 // over each expert's rows.
 //
-// CTA layout (192 threads, one CTA per SM, persistent over tiles):
+// CTA layout (one CTA per SM, persistent over tiles):
 //   warp 0     TMA producer: streams A and B K-blocks into a ring of smem
 //              stages (and, for MXFP8, the 512-byte scale chunks)
 //   warp 1     allocates tensor memory; one lane issues tcgen05.mma into a
 //              double-buffered fp32 accumulator in TMEM
 //   warps 2-5  epilogue: tcgen05.ld the accumulator (one row per thread) and
 //              apply the fused epilogue, then release the accumulator
+//   (MXFP8 gate/up: warps 2-9, two per TMEM lane quadrant; its block scales
+//   leave room for one accumulator only, so these warps copy the tile to
+//   registers and release the accumulator before the SwiGLU arithmetic)
 // Every wait is bounded (StatusBlock); nothing traps.
 #pragma once
 
@@ -61,7 +64,11 @@ struct GemmParams {
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN = 1>
 struct GemmCfg {
     static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR && BN % 32 == 0 && (!MX || BN == 256)), "2-SM pairs: K-major");
-    static constexpr int kThreads = 192;
+    // MXFP8 gate/up keeps one accumulator (its scales take the rest of TMEM)
+    // and hides the epilogue behind the next tile with 8 epilogue warps.
+    static constexpr bool kWideEpi = MX && EPI == kEpiSwiGLU && ACC_STAGES == 1;
+    static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
     static constexpr int kBytesB = BN / CLN * 128;
     static constexpr int kStageBytes = kBytesA + kBytesB;
@@ -203,7 +210,7 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
 // accumulator on the leader's barrier. Per K-block each CTA stages 32 KB
 // instead of 48 KB (BN = 256), so 6 stages fit.
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSA,
                     const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
@@ -237,7 +244,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < ACC_STAGES; ++a) {
             tc::mbar_init(accf_bar(a), 1);
-            tc::mbar_init(acce_bar(a), 128 * CLN);   // pairs: both CTAs' epilogue threads (leader's barrier)
+            // pairs: both CTAs' epilogue threads arrive on the leader's barrier
+            tc::mbar_init(acce_bar(a), 32 * C::kEpiWarps * CLN);
         }
         tc::mbar_init(drain_bar, 1);
         tc::fence_mbar_init();
@@ -445,7 +453,59 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
 
-            if constexpr (EPI == kEpiSwiGLU) {
+            if constexpr (C::kWideEpi) {
+                // this warp's 64 h columns: gate and up pre-activations to
+                // registers, accumulator released, then SwiGLU and two
+                // 32-element MXFP8 blocks (scale codes 2*eg and 2*eg+1 of the
+                // tile's 128-wide scale chunk)
+                const int eg = (warp - 2) >> 2;
+                const int I = p.split_col;
+                const int64_t prow = ti.row_base + row;
+                const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid;
+                uint32_t gr0[32], gr1[32], ur0[32], ur1[32];
+                tc::tmem_ld_32x32b_x32(tbase + 64 * eg, gr0);
+                tc::tmem_ld_32x32b_x32(tbase + 64 * eg + 32, gr1);
+                tc::tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * eg, ur0);
+                tc::tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * eg + 32, ur1);
+                tc::tmem_ld_wait();
+                tc::fence_before_sync();
+                if constexpr (CLN == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acce_bar(acc), 0));
+                else tc::mbar_arrive(acce_bar(acc));
+                if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+                if (live) {
+                    const int hc0 = ti.n * (BN / 2) + 64 * eg;
+                    uint32_t codes = 0;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        float hv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float gv = __uint_as_float(b ? gr1[i] : gr0[i]);
+                            const float uv = __uint_as_float(b ? ur1[i] : ur0[i]);
+                            hv[i] = silu_f(gv) * uv;
+                        }
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+                        const uint32_t code = e8m0_code(amax);
+                        const float inv = e8m0_inv_scale(code);
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            uint32_t lo = f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv);
+                            uint32_t hi = f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
+                            w[i] = lo | (hi << 16);
+                        }
+                        uint8_t* dst = static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc0 + 32 * b;
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        codes |= code << (8 * b);
+                    }
+                    const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc0 / 128;
+                    *reinterpret_cast<uint16_t*>(p.out_sf + chunk * 512 +
+                                                 sf_chunk_offset((int)(prow % kTileM), 2 * eg)) = (uint16_t)codes;
+                }
+            } else if constexpr (EPI == kEpiSwiGLU) {
                 const int I = p.split_col;
                 const int64_t prow = ti.row_base + row;
                 const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid;
@@ -602,7 +662,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
             }
-            if (has_acc) {
+            if (has_acc && !C::kWideEpi) {
                 tc::fence_before_sync();
                 if constexpr (CLN == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acce_bar(acc), 0));
                 else tc::mbar_arrive(acce_bar(acc));

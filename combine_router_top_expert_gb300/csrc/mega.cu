@@ -630,16 +630,19 @@ struct MegaTrace {
 };
 
 template <bool MX>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<256, MX, false, kEpiSwiGLU, 4, MX ? 1 : 2>::kThreads, 1)
 mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmGU,
             const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmDN, const MegaParams p) {
     // gate/up tiles are 256 wide (gate 128 | up 128); MXFP8 keeps one
-    // accumulator because its block scales take the rest of tensor memory.
+    // accumulator because its block scales take the rest of tensor memory,
+    // and runs 8 epilogue warps (two per TMEM lane quadrant) that copy a
+    // tile to registers and release the accumulator before any arithmetic.
     // Down tiles are bn2 wide and use the first bn2 accumulator columns.
     constexpr int BN = 256;
     constexpr int STAGES = 4;
     constexpr int ACC = MX ? 1 : 2;
     using C = GemmCfg<BN, MX, false, kEpiSwiGLU, STAGES, ACC>;
+    constexpr int ET = 32 * C::kEpiWarps;   // epilogue threads
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_word[4];
@@ -768,7 +771,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         }
         for (int a = 0; a < ACC; ++a) {
             tc::mbar_init(accf_bar(a), 1);
-            tc::mbar_init(acce_bar(a), 128);
+            tc::mbar_init(acce_bar(a), ET);
         }
         tc::mbar_init(drain_bar, 1);
         tc::fence_mbar_init();
@@ -901,7 +904,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const int etid = threadIdx.x - 64;  // 0..127
+        const int etid = threadIdx.x - 64;  // 0..ET-1
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int g = cidx; g < total; g += ncomp) {
@@ -911,14 +914,94 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                 // h region reuse: the down tiles of mb-2 must have read it
                 if (etid == 0)
                     s_word[2] = wait_counter(&p.g2_mb[t.mb - 2], v.mb[t.mb - 2].mtiles * NT2, st, tmo, kSiteCounter);
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                asm volatile("bar.sync 1, %0;" ::"r"(ET) : "memory");
                 if (!s_word[2]) break;
             }
             const bool okw = tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull);
-            if (!bar_and(1, 128, okw)) break;  // all 128 epilogue threads agree
+            if (!bar_and(1, ET, okw)) break;  // all epilogue threads agree
             tc::fence_after_sync();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
-            if (t.kind == 0) {
+            if constexpr (C::kWideEpi) {
+                // MXFP8: this warp's columns to registers, accumulator released
+                const int eg = (warp - 2) >> 2;
+                if (t.kind == 0) {
+                    // 64 h columns: two 32-element blocks, scale codes 2*eg, 2*eg+1
+                    uint32_t gr0[32], gr1[32], ur0[32], ur1[32];
+                    tc::tmem_ld_32x32b_x32(tbase + 64 * eg, gr0);
+                    tc::tmem_ld_32x32b_x32(tbase + 64 * eg + 32, gr1);
+                    tc::tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * eg, ur0);
+                    tc::tmem_ld_32x32b_x32(tbase + BN / 2 + 64 * eg + 32, ur1);
+                    tc::tmem_ld_wait();
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(acce_bar(acc));
+                    const int I = p.I;
+                    const int64_t prow = t.a_row0 + row;
+                    const int hc0 = t.n * (BN / 2) + 64 * eg;
+                    uint32_t codes = 0;
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        float hv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            hv[i] = silu_f(__uint_as_float(b ? gr1[i] : gr0[i])) * __uint_as_float(b ? ur1[i] : ur0[i]);
+                        float amax = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+                        const uint32_t code = e8m0_code(amax);
+                        const float inv = e8m0_inv_scale(code);
+                        uint32_t w[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            w[i] = f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
+                                   (f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
+                        uint8_t* dst = static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc0 + 32 * b;
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        codes |= code << (8 * b);
+                    }
+                    const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc0 / 128;
+                    *reinterpret_cast<uint16_t*>(p.h_sf + chunk * 512 +
+                                                 sf_chunk_offset((int)(prow % kTileM), 2 * eg)) = (uint16_t)codes;
+                } else {
+                    // 32-column chunks eg, eg+2, eg+4, eg+6 of the bn2-wide tile
+                    const MegaBatch bt = p.batches[mi.batch];
+                    const int lrow = t.local_row0 + row;
+                    int64_t dest = -1;
+                    if (lrow < v.cnt[t.mb * p.E + t.e]) dest = bt.row_src[v.src0[t.mb * p.E + t.e] + lrow];
+                    const int nch = BN2 / 32;
+                    // packed to BF16 two chunks at a time (fewer live registers);
+                    // chunks past the tile read its last chunk again, unused
+                    uint32_t w0[16], w1[16], w2[16], w3[16];
+                    auto load_pair = [&](int c, uint32_t(&wa)[16], uint32_t(&wb)[16]) {
+                        uint32_t ra[32], rb[32];
+                        tc::tmem_ld_32x32b_x32(tbase + 32 * min(c, nch - 1), ra);
+                        tc::tmem_ld_32x32b_x32(tbase + 32 * min(c + 2, nch - 1), rb);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            wa[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                            wb[i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+                        }
+                    };
+                    load_pair(eg, w0, w1);
+                    load_pair(eg + 4, w2, w3);
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(acce_bar(acc));
+                    if (dest >= 0) {
+                        __nv_bfloat16* orow = bt.partials + dest * p.H + t.n * BN2;
+                        auto store_chunk = [&](int c, const uint32_t(&w)[16]) {
+                            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        };
+                        if (eg < nch) store_chunk(eg, w0);
+                        if (eg + 2 < nch) store_chunk(eg + 2, w1);
+                        if (eg + 4 < nch) store_chunk(eg + 4, w2);
+                        if (eg + 6 < nch) store_chunk(eg + 6, w3);
+                    }
+                }
+            } else if (t.kind == 0) {
                 const int I = p.I;
                 const int64_t prow = t.a_row0 + row;
                 uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
@@ -984,13 +1067,15 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 }
             }
-            tc::fence_before_sync();
-            tc::mbar_arrive(acce_bar(acc));
+            if constexpr (!C::kWideEpi) {
+                tc::fence_before_sync();
+                tc::mbar_arrive(acce_bar(acc));
+            }
             if (++acc == ACC) { acc = 0; acc_ph ^= 1u; }
-            // publish the tile: all 128 epilogue threads' stores, then one release
+            // publish the tile: all epilogue threads' stores, then one release
             __threadfence();
             tc::fence_proxy_async_global();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(ET) : "memory");
             if (etid == 0) {
                 if (t.kind == 0) {
                     red_release_add(&p.g1_e[t.mb * p.E + t.e], 1);
@@ -1166,18 +1251,19 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.gridDim = dim3(L.grid);
-    cfg.blockDim = dim3(192);
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (mx) {
         using C = GemmCfg<256, true, false, kEpiSwiGLU, 4, 1>;
         ensure_smem_attr(reinterpret_cast<const void*>(mega_kernel<true>), C::kSmemBytes);
+        cfg.blockDim = dim3(C::kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         e = cudaLaunchKernelEx(&cfg, mega_kernel<true>, tR, tGU, tH, tDN, p);
     } else {
         using C = GemmCfg<256, false, false, kEpiSwiGLU, 4, 2>;
         ensure_smem_attr(reinterpret_cast<const void*>(mega_kernel<false>), C::kSmemBytes);
+        cfg.blockDim = dim3(C::kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         e = cudaLaunchKernelEx(&cfg, mega_kernel<false>, tR, tGU, tH, tDN, p);
     }
