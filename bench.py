@@ -195,7 +195,9 @@ def run_reference(args, wl):
 def trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b):
     """One megakernel step with per-CTA trace records; fractions of the kernel
     window each role spends working on tiles / moves, waiting on GPU-local
-    counters, in the weighted sums, and idle."""
+    counters, in the weighted sums, and idle (before its first unit of work
+    and after it exits). A mover's weighted-sum chunks taken while it waits
+    for a ring region count as weighted sums, not as waiting."""
     import torch
     cfg2 = mok.make_config(num_sms=cfg.num_sms, timeout_ms=cfg.timeout_ms, flags=cfg.flags | mok.FLAG_TRACE,
                            mover_ctas=cfg.mover_ctas, minibatch_tokens=cfg.minibatch_tokens, ring_rows=cfg.ring_rows)
@@ -220,7 +222,9 @@ def trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b):
         r = rec[rec[:, 0] == role]
         if len(r) == 0:
             continue
-        work = (r[:, 3] - r[:, 2] - r[:, 5]) / dur
+        comb_final = r[:, 4] - r[:, 3]                      # the pass after the tile/move work
+        comb_in_window = np.maximum(r[:, 7] - comb_final, 0.0)
+        work = (r[:, 3] - r[:, 2] - r[:, 5] - comb_in_window) / dur
         out[name] = {"ctas": int(len(r)),
                      "first_work_us": float(np.mean(r[:, 2] - t0) / 1e3),
                      "work_frac": float(np.mean(work)),
@@ -243,6 +247,8 @@ def main():
     ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
     ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
+    ap.add_argument("--mb-token-ranges", action="store_true",
+                    help="megakernel minibatches as token ranges (default: runs of expert tiles)")
     ap.add_argument("--trace", action="store_true",
                     help="megakernel: after the timed steps, one traced step; report the SM partition's busy/idle time")
     args = ap.parse_args()
@@ -273,7 +279,8 @@ def main():
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     staged = not args.megakernel or wl.backward
-    flags = (0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_GEMM_PAIRS if args.gemm_pairs else 0)
+    flags = ((0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_GEMM_PAIRS if args.gemm_pairs else 0) |
+             (mok.FLAG_MB_TOKEN_RANGES if args.mb_token_ranges else 0))
     cfg = mok.make_config(flags=flags, ring_rows=wl.ring_rows, mover_ctas=args.movers,
                           minibatch_tokens=args.minibatch)
     b = layer.buffers(T, training=wl.backward, cfg=cfg)
@@ -527,6 +534,7 @@ def main():
                    "operands": wl.dtype, "routing": "zipf s=1.2 bias" if wl.zipf_s else "uniform",
                    "macro_batches": len(xs), "shared_expert_I": wl.shared_I, "ring_rows": wl.ring_rows or "default",
                    "mover_ctas": args.movers or 8, "path": mode,
+                   "minibatches": ("token ranges" if args.mb_token_ranges else "expert-tile runs") if (not staged or len(xs) > 1) else None,
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
         "gemm_cta_pairs": bool(args.gemm_pairs),

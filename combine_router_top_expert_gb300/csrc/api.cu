@@ -345,6 +345,7 @@ static mok_status forward_mega(const mok_problem* p, int32_t nbatch, const mok_f
     L.scratch = ws + ML.scratch;
     L.region_rows = mega_region_rows(p, cfg);
     L.max_tokens = (cfg && cfg->minibatch_tokens > 0) ? cfg->minibatch_tokens : p->T;
+    L.tile_cuts = !(cfg && (cfg->flags & MOK_FLAG_MB_TOKEN_RANGES));
     L.n_movers = movers;
     L.grid = c.num_sms;
     L.test_flags = cfg ? cfg->flags : 0;

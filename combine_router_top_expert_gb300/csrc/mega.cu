@@ -57,19 +57,77 @@ constexpr int kMaxMbPerBatch = 512;
 
 __host__ __device__ inline int64_t plan_stage_ints(int E) { return 2 + (int64_t)kMaxMbPerBatch * (2 + 2 * E); }
 
-// Per-batch plan: one CTA per macro-batch. Rows of expert e before token t
-// are the lower bound of t in the expert's row_src segment (sorted by token).
-// One warp then cuts minibatches greedily, block (16 tokens) by block. Output
-// in a per-batch staging area: [0] minibatches, [1] error, then per
-// minibatch: t0, t1, E segment starts, E segment ends.
+// Per-batch plan: one CTA per macro-batch. Output in a per-batch staging
+// area: [0] minibatches, [1] error, then per minibatch: t0, t1 (the tokens
+// whose weighted sums it releases), E segment starts, E segment ends
+// (indices into the batch's row_src).
+//
+// Tile cuts (default): the batch's expert-contiguous layout, padded per
+// expert to 128-row tiles as for the staged GEMMs, is cut into runs of
+// consecutive tiles, each run at most a ring region (and at most
+// max_tokens * k rows when max_tokens < T). Only each expert's last tile
+// over the whole batch is partial; every token's rows are final once the
+// batch's last minibatch is, so that minibatch releases all T tokens.
+//
+// Token cuts (MOK_FLAG_MB_TOKEN_RANGES): rows of expert e before token t are
+// the lower bound of t in the expert's row_src segment (sorted by token);
+// one warp cuts minibatches greedily, block (16 tokens) by block, while the
+// block range's per-expert padded rows fit a region. Each minibatch releases
+// its own tokens, but pads every expert's rows separately.
 __global__ void __launch_bounds__(256)
 plan_batch_kernel(const PlanBatches batches, int T, int E, int k, int region_rows, int max_tokens,
-                  int* __restrict__ stage) {
+                  int tile_cuts, int* __restrict__ stage) {
     extern __shared__ int ps[];
     const int b = blockIdx.x;
     const int nblk = ceil_div(T, kPlanTB);
     int* P = ps;  // [(nblk + 1) * E]
     const PlanBatch pb = batches.b[b];
+    if (tile_cuts) {
+        if (threadIdx.x >= 32) return;
+        int* out = stage + (int64_t)b * plan_stage_ints(E);
+        const int lane = threadIdx.x;
+        int run = 0;   // P[e] = tiles of the experts before e
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int mt = e < E ? ceil_div(pb.offsets[e + 1] - pb.offsets[e], kTileM) : 0;
+            int incl = mt;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            if (e < E) P[e] = run + incl - mt;
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        const int total = run;
+        int R = region_rows / kTileM;
+        if (max_tokens < T) R = min(R, max(1, ceil_div(max_tokens * k, kTileM)));
+        const int nmb = (total == 0 || R < 1) ? 0 : ceil_div(total, R);
+        if (R < 1 || nmb > kMaxMbPerBatch) {
+            if (lane == 0) { out[0] = 0; out[1] = 1; }
+            return;
+        }
+        for (int j = 0; j < nmb; ++j) {
+            int* m = out + 2 + j * (2 + 2 * E);
+            const int g0 = j * R, g1 = min(total, g0 + R);
+            if (lane == 0) { m[0] = j == nmb - 1 ? 0 : T; m[1] = T; }
+            for (int e = lane; e < E; e += 32) {
+                const int o0 = pb.offsets[e], c = pb.offsets[e + 1] - o0;
+                const int te = P[e], mt = ceil_div(c, kTileM);
+                const int lo = max(g0, te), hi = min(g1, te + mt);
+                int s0 = o0, s1 = o0;
+                if (lo < hi) {
+                    s0 = o0 + (lo - te) * kTileM;
+                    s1 = o0 + min((hi - te) * kTileM, c);
+                }
+                m[2 + e] = s0;
+                m[2 + E + e] = s1;
+            }
+        }
+        if (lane == 0) { out[0] = nmb; out[1] = 0; }
+        return;
+    }
     for (int i = threadIdx.x; i < (nblk + 1) * E; i += blockDim.x) {
         const int blk = i / E, e = i % E;
         const int tb = min(blk * kPlanTB, T);
@@ -701,6 +759,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                 // waiting (bounded by the same time limit as every wait)
                 const int target = v.mb[mb - 2].mtiles * NT1;
                 const unsigned long long w0 = globaltimer_ns();
+                const unsigned long long comb0 = tr.comb_ns;
                 for (;;) {
                     if (threadIdx.x == 0) {
                         int ok = ld_acquire(&p.g1_mb[mb - 2]) >= target ? 1 : 0;
@@ -722,7 +781,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                     if (tracing && threadIdx.x == 0) tr.comb_ns += globaltimer_ns() - c0;
                     if (!did && threadIdx.x == 0) __nanosleep(200);
                 }
-                if (tracing && threadIdx.x == 0) tr.wait_ns += globaltimer_ns() - w0;
+                if (tracing && threadIdx.x == 0) tr.wait_ns += (globaltimer_ns() - w0) - (tr.comb_ns - comb0);
             }
             if (tracing && threadIdx.x == 0 && mb == 0) tr.t_first = globaltimer_ns();
             if (pump) {
@@ -1202,7 +1261,7 @@ cudaError_t launch_mega(const MegaLaunch& L, cudaStream_t s) {
     const int nblk = ceil_div(T, kPlanTB);
     const size_t psm = (size_t)(nblk + 1) * E * 4;
     if (psm > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(plan_batch_kernel), (int)psm);
-    plan_batch_kernel<<<nb, 256, psm, s>>>(pbs, T, E, k, L.region_rows, L.max_tokens, stage);
+    plan_batch_kernel<<<nb, 256, psm, s>>>(pbs, T, E, k, L.region_rows, L.max_tokens, L.tile_cuts ? 1 : 0, stage);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     plan_finalize_kernel<<<1, 256, 0, s>>>(nb, E, NT1, NT2, stage, v);

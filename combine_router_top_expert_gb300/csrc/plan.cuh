@@ -95,7 +95,8 @@ struct MegaLaunch {
     const uint8_t* dn_sf;
     void* scratch;           // mega_scratch_bytes
     int region_rows;         // rows of each of the two ring regions (multiple of 128)
-    int max_tokens;          // tokens per minibatch at most
+    int max_tokens;          // tokens per minibatch at most (tile cuts: rows <= max_tokens * k)
+    bool tile_cuts;          // minibatches are runs of 128-row expert tiles (else token ranges)
     int n_movers;            // mover CTAs
     int grid;                // CTAs (<= SMs)
     int test_flags;          // MOK_FLAG_TEST_* bits

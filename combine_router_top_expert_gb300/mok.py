@@ -30,6 +30,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
 FLAG_TRACE = 4
+FLAG_MB_TOKEN_RANGES = 8
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 

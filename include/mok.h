@@ -73,7 +73,9 @@ typedef struct {
     int32_t timeout_ms;       /* limit of every device-side wait; 0 = 4000 */
     int32_t flags;            /* MOK_FLAG_* */
     int32_t mover_ctas;       /* megakernel: SMs that move tokens; 0 = 8 */
-    int32_t minibatch_tokens; /* megakernel: most tokens per minibatch; 0 = as many as a ring region holds */
+    int32_t minibatch_tokens; /* megakernel: most tokens per minibatch (default expert-tile cuts: at most
+                                 minibatch_tokens * k rows, rounded up to a 128-row tile); 0 = as many as
+                                 a ring region holds */
     int32_t ring_rows;        /* megakernel: ring token buffer rows, split in two regions;
                                  0 = two regions of mok_padded_rows_max rows each */
     int32_t reserved[2];
@@ -98,9 +100,18 @@ typedef struct {
  * work (mover: first minibatch; compute: first tile's loads, after its
  * counter wait), [3] end of its tile/move work, [4] exit, [5] ns spent
  * waiting on GPU-local counters (compute: tile inputs published; mover:
- * ring region free), [6] units done (tiles; minibatches), [7] ns in the
- * weighted sums. Costs a few timer reads per tile. */
+ * ring region free, less the weighted-sum chunks it took meanwhile), [6]
+ * units done (tiles; minibatches), [7] ns in the weighted sums (mover: the
+ * chunks taken while waiting plus the final pass after [3]). Costs a few
+ * timer reads per tile. */
 #define MOK_FLAG_TRACE 4
+/* Megakernel minibatches as token ranges: each minibatch holds the rows of
+ * a range of tokens, padded per expert to 128-row tiles, and its tokens'
+ * weighted sums run as soon as its down tiles are done. By default a
+ * minibatch is a run of consecutive 128-row tiles of the batch's
+ * expert-contiguous layout (padded once per expert over the whole batch),
+ * and a batch's weighted sums run once all of its minibatches are done. */
+#define MOK_FLAG_MB_TOKEN_RANGES 8
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use

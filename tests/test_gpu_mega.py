@@ -73,11 +73,15 @@ def test_megakernel_independent_of_minibatch_ring_and_movers(wl):
         mok.make_config(minibatch_tokens=160, ring_rows=2 * 1536),   # ring forces the cut
         mok.make_config(mover_ctas=1),
         mok.make_config(mover_ctas=24, minibatch_tokens=300),
+        # token-range minibatches: each pads its experts' rows separately
+        mok.make_config(minibatch_tokens=64, flags=mok.FLAG_MB_TOKEN_RANGES),
+        mok.make_config(minibatch_tokens=160, ring_rows=2 * 1536, flags=mok.FLAG_MB_TOKEN_RANGES),
     ]
     for cfg in configs:
         out, st = _forward(layer, x, cfg, wl.T)
-        assert st == (mok.OK, 0), (cfg.minibatch_tokens, cfg.ring_rows, cfg.mover_ctas, st)
-        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), (cfg.minibatch_tokens, cfg.mover_ctas)
+        what = (cfg.minibatch_tokens, cfg.ring_rows, cfg.mover_ctas, cfg.flags)
+        assert st == (mok.OK, 0), (what, st)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), what
 
 
 @pytest.mark.gpu
@@ -96,7 +100,8 @@ def test_megakernel_bitwise_reruns():
 
 
 @pytest.mark.gpu
-def test_macro_batches_through_one_ring_with_shared_expert():
+@pytest.mark.parametrize("cut_flags", [0, mok.FLAG_MB_TOKEN_RANGES], ids=["tile_cuts", "token_ranges"])
+def test_macro_batches_through_one_ring_with_shared_expert(cut_flags):
     """Several macro-batches (own tokens, same weights) stream through one
     launch and a small ring; each output equals that batch's staged forward,
     shared BF16 expert included."""
@@ -111,7 +116,7 @@ def test_macro_batches_through_one_ring_with_shared_expert():
         routings.append({n: v.clone() for n, v in r.items()})
         refs.append(_staged(layer, x, wl.T).clone())
     p = layer.problem(wl.T)
-    cfg = mok.make_config(ring_rows=2 * 1024, minibatch_tokens=128)
+    cfg = mok.make_config(ring_rows=2 * 1024, minibatch_tokens=128, flags=cut_flags)
     ws = mok.alloc_bytes(mok.workspace_size_batches(p, len(xs), cfg))
     outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda") for _ in xs]
     mok.moe_forward_batches(p, xs, layer.packed, routings, outs, ws, packed_shared=layer.packed_shared, cfg=cfg)
@@ -125,15 +130,35 @@ def test_macro_batches_through_one_ring_with_shared_expert():
 
 
 @pytest.mark.gpu
-def test_ring_smaller_than_one_token_block_reports_capacity():
+def test_ring_of_one_tile():
+    """A ring region of one 128-row tile: token-range minibatches cannot hold
+    a 16-token block's padded rows (capacity error, device still usable);
+    expert-tile runs still fit, one tile per minibatch."""
     wl = CASES[0]
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    out, st = _forward(layer, x, mok.make_config(ring_rows=2 * 128, flags=mok.FLAG_MB_TOKEN_RANGES), wl.T)
+    assert st[0] == mok.ERR_CAPACITY
+    ref = _staged(layer, x, wl.T)       # the device is still usable
+    for cfg in (mok.make_config(), mok.make_config(ring_rows=2 * 128)):
+        out, st = _forward(layer, x, cfg, wl.T)
+        assert st == (mok.OK, 0) and torch.equal(out.view(torch.int16), ref.view(torch.int16)), cfg.ring_rows
+
+
+@pytest.mark.gpu
+def test_too_many_minibatches_reports_capacity():
+    """Expert-tile runs of one tile each: 40000 tokens x 2 rows need more
+    than 512 minibatches per macro-batch, which the plan refuses."""
+    wl = synth.small("mega_many_mb", T=40000, H=128, I=128, E=8, k=2)
     inp = synth.make_inputs(wl)
     layer = layer_for(inp, mok.BF16)
     x = to_dev_bf16(inp.x)
     layer.route(x)
     out, st = _forward(layer, x, mok.make_config(ring_rows=2 * 128), wl.T)
     assert st[0] == mok.ERR_CAPACITY
-    ref = _staged(layer, x, wl.T)       # the device is still usable
+    ref = _staged(layer, x, wl.T)
     out, st = _forward(layer, x, mok.make_config(), wl.T)
     assert st == (mok.OK, 0) and torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
@@ -157,7 +182,8 @@ def test_withheld_publish_times_out_cleanly():
 
 
 @pytest.mark.gpu
-def test_trace_records_and_unchanged_output():
+@pytest.mark.parametrize("cut_flags", [0, mok.FLAG_MB_TOKEN_RANGES], ids=["tile_cuts", "token_ranges"])
+def test_trace_records_and_unchanged_output(cut_flags):
     """MOK_FLAG_TRACE: one record per CTA (movers first), ordered timestamps,
     every gate/up and down tile counted once, output bit-identical."""
     wl = CASES[2]
@@ -167,7 +193,7 @@ def test_trace_records_and_unchanged_output():
     layer.route(x)
     ref = _staged(layer, x, wl.T)
     movers = 8
-    cfg = mok.make_config(mover_ctas=movers, minibatch_tokens=256, flags=mok.FLAG_TRACE)
+    cfg = mok.make_config(mover_ctas=movers, minibatch_tokens=256, flags=mok.FLAG_TRACE | cut_flags)
     cfg.flags |= mok.FLAG_MEGAKERNEL
     p = layer.problem(wl.T)
     ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
@@ -181,13 +207,22 @@ def test_trace_records_and_unchanged_output():
     rec = mok.megakernel_trace(ws, n)
     assert np.all(rec[:movers, 0] == 0) and np.all(rec[movers:, 0] == 1)
     assert np.all(rec[:, 1] <= rec[:, 4]) and np.all(rec[:, 3] <= rec[:, 4])
+    # waiting and weighted sums are disjoint spans of the CTA's lifetime
+    assert np.all(rec[:, 5] + rec[:, 7] <= rec[:, 4] - rec[:, 1] + 2000)
     work = rec[:, 6] > 0
     assert np.all(rec[work, 1] <= rec[work, 2]) and np.all(rec[work, 2] <= rec[work, 3])
     counts = layer.buffers(wl.T)["routing"]["counts"].cpu().numpy()
     n_mb = int(np.max(rec[:movers, 6]))
     assert n_mb >= 2   # 1000 tokens in minibatches of at most 256
-    # every tile of both GEMMs ran once (tiles per minibatch sum to at least the
-    # whole batch's, since each minibatch pads its experts' rows separately)
     nt1, nt2 = 2 * wl.I // 256, wl.H // 128
-    tiles_min = int(np.sum((counts + 127) // 128)) * (nt1 + nt2)
-    assert int(rec[movers:, 6].sum()) >= tiles_min
+    mtiles = int(np.sum((counts + 127) // 128))
+    tiles_min = mtiles * (nt1 + nt2)
+    if cut_flags:
+        # token ranges: tiles per minibatch sum to at least the whole batch's,
+        # since each minibatch pads its experts' rows separately
+        assert int(rec[movers:, 6].sum()) >= tiles_min
+    else:
+        # tile cuts: exactly the staged GEMMs' tiles, in runs of at most
+        # 256 * k rows
+        assert int(rec[movers:, 6].sum()) == tiles_min
+        assert n_mb == -(-mtiles // -(-256 * wl.k // 128))
