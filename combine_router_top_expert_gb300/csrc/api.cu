@@ -410,8 +410,10 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     const char* pk = static_cast<const char*>(a->packed);
     const int64_t rows = padded_rows_max(p->T, p->E, p->k);
     if (e == cudaSuccess)
+        // pad rows stay unwritten for inference (their GEMM rows are never
+        // stored); training keeps them zero for the weight gradients
         e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
-                            nullptr, s);
+                            nullptr, s, training);
     if (e == cudaSuccess)
         e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H, p->I,
                         r.counts, 0, rows, h, h_sf, gu, c, s);

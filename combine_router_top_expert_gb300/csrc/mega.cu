@@ -489,8 +489,10 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
 
 // Pull-gather through the copy engines: lane 0 of each mover warp pumps the
 // rows of its 8-row chunks global -> shared -> ring with bulk copies, two row
-// buffers per warp (the load of row r+1 overlaps the store of row r), pad
-// rows from a zeroed buffer; MXFP8 copies the E4M3 rows of x quantised once
+// buffers per warp (the load of row r+1 overlaps the store of row r); pad
+// rows are not written (the GEMM rows they feed are never stored, and a
+// region's old rows are finite or never read back); MXFP8 copies the E4M3
+// rows of x quantised once
 // per token (quantize_rows, before the launch) and the warp's lanes place
 // their scale words in the ring's tile-ordered scale chunks. The chunk is
 // published once its stores have completed. A warp keeps two rows in flight
@@ -498,7 +500,6 @@ __device__ void mover_dispatch_mb(const MegaParams& p, int mb, int gwarp, int nw
 // fraction of that. Returns false if a bounded wait gave up.
 struct MoverSmem {
     uint32_t bufs;    // [warps][2] row buffers
-    uint32_t zero;    // one zeroed row
     uint32_t bars;    // [warps][2] mbarriers (8 bytes each)
 };
 
@@ -534,8 +535,9 @@ __device__ bool mover_pump_mb(const MegaParams& p, int mb, int gwarp, int nwarps
             for (int r = 0; r < 8; ++r) {
                 const int tok = __shfl_sync(0xffffffffu, my_tok, r);
                 const int64_t grow = grow0 + r;
+                if (tok < 0) continue;   // pad rows feed only GEMM rows that are never stored
                 for (int kc = lane; kc < kc_row; kc += 32) {
-                    const uint32_t wd = tok >= 0 ? __ldg(bt.xsf + (int64_t)tok * kc_row + kc) : 0u;
+                    const uint32_t wd = __ldg(bt.xsf + (int64_t)tok * kc_row + kc);
                     *reinterpret_cast<uint32_t*>(p.ring_sf + ((grow / kTileM) * kc_row + kc) * 512 +
                                                  sf_chunk_offset((int)(grow % kTileM), 0)) = wd;
                 }
@@ -574,10 +576,8 @@ __device__ bool mover_pump_mb(const MegaParams& p, int mb, int gwarp, int nwarps
                     }
                     phases ^= 1u << sl;
                     tc::bulk_store(ring + (int64_t)r * rowb, buf[sl], rowb);
-                } else {
-                    tc::bulk_store(ring + (int64_t)r * rowb, ms.zero, rowb);
-                }
-                tc::bulk_commit();
+                    tc::bulk_commit();
+                }   // pad rows stay unwritten: their GEMM rows are never stored
             }
             tc::bulk_wait<0>();   // the chunk's rows are written
         }
@@ -730,7 +730,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         // BF16: rows go through the copy engines when the row buffers fit
         const int nw = blockDim.x / 32;
         const size_t rowb = (size_t)p.H * (MX ? 1 : 2);
-        const bool pump = (size_t)(2 * nw + 1) * rowb + 16 * nw <= (size_t)C::kBarOffset &&
+        const bool pump = (size_t)(2 * nw) * rowb + 16 * nw <= (size_t)C::kBarOffset &&
                           (!MX || p.batches[0].xq != nullptr);
         MoverSmem ms{};
         uint32_t phases = 0;
@@ -739,16 +739,12 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
         if (pump) {
             const uint32_t base = tc::smem_u32(sm);
             ms.bufs = base;
-            ms.zero = base + (uint32_t)(2 * nw * rowb);
-            ms.bars = ms.zero + (uint32_t)rowb;
-            uint4* z = reinterpret_cast<uint4*>(sm + (size_t)(2 * nw) * rowb);
-            for (int i = threadIdx.x; i < (int)(rowb / 16); i += blockDim.x) z[i] = make_uint4(0, 0, 0, 0);
+            ms.bars = base + (uint32_t)(2 * nw * rowb);
             if (lane == 0) {
                 tc::mbar_init(ms.bars + 16u * warp, 1);
                 tc::mbar_init(ms.bars + 16u * warp + 8u, 1);
             }
             tc::fence_mbar_init();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the zero row, for the bulk stores
             __syncthreads();
         }
         for (int mb = 0; mb < n_mb; ++mb) {

@@ -95,7 +95,8 @@ template <bool MX>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
                 const int32_t* __restrict__ offsets, const int32_t* __restrict__ row_src, void* __restrict__ A,
-                uint8_t* __restrict__ A_sf, const __nv_bfloat16* __restrict__ scale_src, const float* __restrict__ wslot) {
+                uint8_t* __restrict__ A_sf, const __nv_bfloat16* __restrict__ scale_src, const float* __restrict__ wslot,
+                int zero_pads) {
     __shared__ int32_t poff[kMaxE + 1];
     padded_offsets(counts, E, poff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,6 +110,8 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
             const int slot = row_src[offsets[e] + local];
             src = (scale_src ? scale_src : x) + (int64_t)(slot / k) * H;
             if (wslot) wmul = wslot[slot];
+        } else if (!zero_pads) {
+            continue;   // inference: pad rows feed only GEMM rows that are never stored
         }
         if constexpr (!MX) {
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(A) + (int64_t)pr * H);
@@ -399,17 +402,18 @@ static int sm_count() {
 
 cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, const int32_t* counts,
                             const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
-                            const void* scale_src, const float* wslot, cudaStream_t s) {
+                            const void* scale_src, const float* wslot, cudaStream_t s, bool zero_pads) {
     int64_t rows = padded_rows_max(T, E, k);
     int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
     if (blocks < 1) blocks = 1;
     if (mx)
         dispatch_kernel<true><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts, offsets,
-                                                     row_src, A, A_sf, nullptr, nullptr);
+                                                     row_src, A, A_sf, nullptr, nullptr, zero_pads ? 1 : 0);
     else
         dispatch_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts,
                                                       offsets, row_src, A, nullptr,
-                                                      static_cast<const __nv_bfloat16*>(scale_src), wslot);
+                                                      static_cast<const __nv_bfloat16*>(scale_src), wslot,
+                                                      zero_pads ? 1 : 0);
     return cudaGetLastError();
 }
 

@@ -18,7 +18,7 @@ cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, int 
 // the rows are scale_src[t] * wslot[t*k+j] (reverse-combine of the backward).
 cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, const int32_t* counts,
                             const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
-                            const void* scale_src, const float* wslot, cudaStream_t s);
+                            const void* scale_src, const float* wslot, cudaStream_t s, bool zero_pads = true);
 cudaError_t launch_combine(const void* partials, const float* w, const float* shared, void* out, int T, int H,
                            int k, cudaStream_t s);
 // MXFP8 scales go per tile of sf_tile rows (128, or 224 for the down
