@@ -61,6 +61,21 @@ bool make_tmap_chunks(CUtensorMap* m, const void* base, int64_t chunks) {
     return r == CUDA_SUCCESS;
 }
 
+// Dense-epilogue output [E, rows, width] BF16 with row pitch ld elements,
+// stored in 32 x 32 x 1 boxes from unswizzled shared memory.
+bool make_tmap_out3d(CUtensorMap* m, void* base, int E, int64_t rows, int64_t width, int64_t ld) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, (cuuint64_t)E};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(rows * ld * 2)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& sa,
                 const CUtensorMap& sb, const GemmParams& p, int64_t tiles_ub, int num_sms, cudaStream_t s) {
@@ -284,10 +299,18 @@ cudaError_t gemm_wgrad(const void* Aact, int M, const void* B, int N, int E, con
     if (!make_tmap(&ta, Aact, a_rows, M, 2, 64, 64)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, B, a_rows, N, 2, 64, 64)) return cudaErrorInvalidValue;
     p.n_tiles = N / BN;
+    // outputs: out0 holds columns [0, min(split, N)), out1 (if any) [split, N)
+    CUtensorMap to0, to1;
+    if (!make_tmap_out3d(&to0, out0, E, M, p.ldo, p.ldo)) return cudaErrorInvalidValue;
+    if (split_col < N) {
+        if (!out1 || !make_tmap_out3d(&to1, out1, E, M, N - split_col, p.ldo)) return cudaErrorInvalidValue;
+    } else {
+        to1 = to0;
+    }
     const int64_t tub = (int64_t)E * ((M + kTileM - 1) / kTileM) * p.n_tiles;
-    if (BN == 256) return run<256, false, true, kEpiDense, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
-    if (BN == 128) return run<128, false, true, kEpiDense, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
-    return run<64, false, true, kEpiDense, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    if (BN == 256) return run<256, false, true, kEpiDense, 4, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
+    if (BN == 128) return run<128, false, true, kEpiDense, 6, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
+    return run<64, false, true, kEpiDense, 8, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
 }
 
 }  // namespace mok

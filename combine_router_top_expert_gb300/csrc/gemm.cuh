@@ -93,7 +93,11 @@ struct GemmCfg {
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kBarOffset = STAGES * (kStageBytes + kSfStage);
-    static constexpr int kSmemBytes = 1024 /*align slack*/ + kBarOffset + 256;
+    // dense epilogue: per epilogue warp two 32 x 32 BF16 staging blocks for
+    // its TMA stores, 1 KB past the barriers
+    static constexpr int kEpiStageOffset = kBarOffset + 1024;
+    static constexpr int kEpiStageBytes = EPI == kEpiDense ? 4 * 2 * 2048 : 0;
+    static constexpr int kSmemBytes = 1024 /*align slack*/ + kBarOffset + (EPI == kEpiDense ? 1024 : 256) + kEpiStageBytes;
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
     static_assert(EPI != kEpiSwiGLU || (BN / 2) % 32 == 0, "SwiGLU tiles hold whole 32-column gate/up chunks");
@@ -212,8 +216,11 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN>
 __global__ void __launch_bounds__(GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>::kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSA,
-                    const __grid_constant__ CUtensorMap tmSB, const GemmParams p) {
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmX0,
+                    const __grid_constant__ CUtensorMap tmX1, const GemmParams p) {
+    // tmX0 / tmX1: MXFP8 2-SM pairs - the A and B scale chunks as 256-byte
+    // rows; dense epilogue - the outputs out0 / out1 as [E, m_fixed, width]
+    // BF16 (boxes of 32 x 32 x 1); unused otherwise
     using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>;
     static_assert(CLN == 1 || (CLN == 2 && EPI != kEpiDense), "2-SM pairs: grouped-row GEMMs");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -254,9 +261,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         tc::prefetch_tmap(&tmA);
         tc::prefetch_tmap(&tmB);
         tc::prefetch_tmap(&tmB2);
-        if constexpr (MX && CLN == 2) {
-            tc::prefetch_tmap(&tmSA);
-            tc::prefetch_tmap(&tmSB);
+        if constexpr ((MX && CLN == 2) || EPI == kEpiDense) {
+            tc::prefetch_tmap(&tmX0);
+            tc::prefetch_tmap(&tmX1);
         }
     }
     if (warp == 1) {
@@ -306,11 +313,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         if constexpr (MX) {
                             // scale chunks (512 B = two 256-byte rows of tmSA / tmSB): this CTA's A
                             // rows, and all BN rows of B (the pair MMA reads B's scales in each CTA)
-                            tc::tma_load_2d_2sm(sf_tile(stage), &tmSA, lead_full, 0,
+                            tc::tma_load_2d_2sm(sf_tile(stage), &tmX0, lead_full, 0,
                                                 2 * ((ti.a_row0 / kTileM) * p.sf_kchunks + kb));
 #pragma unroll
                             for (int j = 0; j < C::kNChunks; ++j)
-                                tc::tma_load_2d_2sm(sf_tile(stage) + 512 * (1 + j), &tmSB, lead_full, 0,
+                                tc::tma_load_2d_2sm(sf_tile(stage) + 512 * (1 + j), &tmX1, lead_full, 0,
                                                     2 * ((brow / kTileM + j) * p.sf_kchunks + kb));
                         }
                         last_par[stage] = (int)ph;
@@ -637,8 +644,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             } else {  // kEpiDense
-                const bool live = ti.row_base + row < p.m_fixed;
-                const int64_t mrow = (int64_t)ti.e * p.m_fixed + ti.row_base + row;
+                // 32 x 32 BF16 blocks through shared memory, written by TMA
+                // stores (rows past m_fixed are clipped by the map's extent);
+                // a warp's two staging blocks alternate, and a block is
+                // rewritten only once the store issued from it two chunks
+                // earlier has read it
+                const int ew = warp - 2;
+                const int mrow0 = ti.row_base + q * 32;   // first row of this warp's 32, within the expert
+                const int rot = (lane >> 1) & 3;           // store order: 4-way bank conflicts at most
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN; c0 += 32) {
                     uint32_t r[32];
@@ -649,17 +662,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                         for (int i = 0; i < 32; ++i) r[i] = 0u;
                     }
-                    if (!live) continue;
-                    const int col = ti.n * BN + c0;
-                    __nv_bfloat16* ob;
-                    if (col < p.split_col) ob = static_cast<__nv_bfloat16*>(p.out0) + mrow * p.ldo + col;
-                    else ob = static_cast<__nv_bfloat16*>(p.out1) + mrow * p.ldo + (col - p.split_col);
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    uint4* dst = reinterpret_cast<uint4*>(ob);
+                    const uint32_t buf = smem_base + C::kEpiStageOffset + (uint32_t)(ew * 2 + ((c0 >> 5) & 1)) * 2048u;
+                    if (lane == 0) tc::bulk_wait_read<1>();
+                    __syncwarp();
+                    const uint32_t rowp = buf + (uint32_t)lane * 64u;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int t = 0; t < 4; ++t) {
+                        const int j = (t + rot) & 3;
+                        const uint32_t a0 = j == 0 ? w[0] : j == 1 ? w[4] : j == 2 ? w[8] : w[12];
+                        const uint32_t a1 = j == 0 ? w[1] : j == 1 ? w[5] : j == 2 ? w[9] : w[13];
+                        const uint32_t a2 = j == 0 ? w[2] : j == 1 ? w[6] : j == 2 ? w[10] : w[14];
+                        const uint32_t a3 = j == 0 ? w[3] : j == 1 ? w[7] : j == 2 ? w[11] : w[15];
+                        tc::st_shared_v4(rowp + (uint32_t)j * 16u, a0, a1, a2, a3);
+                    }
+                    tc::fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0 && mrow0 < p.m_fixed) {
+                        const int col = ti.n * BN + c0;
+                        if (col < p.split_col) tc::tma_store_3d(&tmX0, buf, col, mrow0, ti.e);
+                        else tc::tma_store_3d(&tmX1, buf, col - p.split_col, mrow0, ti.e);
+                        tc::bulk_commit();
+                    }
                 }
             }
             if (has_acc && !C::kWideEpi) {
@@ -668,6 +694,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 else tc::mbar_arrive(acce_bar(acc));
                 if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
             }
+        }
+        if constexpr (EPI == kEpiDense) {
+            if (lane == 0) tc::bulk_wait<0>();   // stores done with shared memory (and written) before exit
         }
     }
     tc::fence_before_sync();
