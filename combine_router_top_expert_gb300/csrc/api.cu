@@ -270,7 +270,8 @@ mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf,
     if (!problem_ok(p) || !routing_ok(r, p->T) || !A || !packed || !h || !partials || !workspace) return MOK_ERR_INVALID;
     const bool mx = p->dtype == MOK_MXFP8;
     if (mx && (!A_sf || !h_sf)) return MOK_ERR_INVALID;
-    if (!aligned(A, 1024) || !aligned(h, 1024) || !aligned(packed, 256) || !aligned(workspace, 256))
+    if (!aligned(A, 1024) || !aligned(h, 1024) || !aligned(packed, 256) || !aligned(workspace, 256) ||
+        !aligned(partials, 32))
         return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
@@ -445,7 +446,8 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
         !a->dW_r || !a->workspace)
         return MOK_ERR_INVALID;
     if (p->T > 0 && (!a->x || !a->dY || !a->dX)) return MOK_ERR_INVALID;   // token arrays may be empty
-    if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->saved, 1024))
+    if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->saved, 1024) ||
+        !aligned(a->dW_gate, 16) || !aligned(a->dW_up, 16) || !aligned(a->dW_down, 16))
         return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;

@@ -503,9 +503,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             uint32_t hi = f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
                             w[i] = lo | (hi << 16);
                         }
-                        uint8_t* dst = static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc0 + 32 * b;
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        tc::stg_v8(static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc0 + 32 * b, w);
                         codes |= code << (8 * b);
                     }
                     const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc0 / 128;
@@ -544,9 +542,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             uint32_t hi = f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv);
                             w[i] = lo | (hi << 16);
                         }
-                        uint8_t* dst = static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc;
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        tc::stg_v8(static_cast<uint8_t*>(p.out0) + prow * (int64_t)I + hc, w);
                         // the four codes of a 128-wide chunk leave as one word
                         sfw |= code << (8 * ((hc / 32) & 3));
                         if (((hc / 32) & 3) == 3) {
@@ -559,19 +555,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)I + hc);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)I + hc;
+                        tc::stg_v8(dst, w);
+                        tc::stg_v8(dst + 16, w + 8);
                     }
                     if (p.gu != nullptr) {
                         // pre-activations kept in fp32 for the backward's dSwiGLU
                         float* gb = static_cast<float*>(p.gu) + prow * (int64_t)(2 * I);
-                        uint4* dg = reinterpret_cast<uint4*>(gb + hc);
-                        uint4* du = reinterpret_cast<uint4*>(gb + I + hc);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            dg[i] = make_uint4(gr[4 * i], gr[4 * i + 1], gr[4 * i + 2], gr[4 * i + 3]);
-                            du[i] = make_uint4(ur[4 * i], ur[4 * i + 1], ur[4 * i + 2], ur[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) {
+                            tc::stg_v8(gb + hc + 8 * i, gr + 8 * i);
+                            tc::stg_v8(gb + I + hc + 8 * i, ur + 8 * i);
                         }
                     }
                 }
@@ -591,16 +585,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (dest < 0) continue;
                     const int col = ti.n * BN + c0;
                     if (p.out_f32) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.out0) + dest * p.ldo + col);
+                        float* dst = static_cast<float*>(p.out0) + dest * p.ldo + col;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) tc::stg_v8(dst + 8 * i, r + 8 * i);
                     } else {
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out0) + dest * p.ldo + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out0) + dest * p.ldo + col;
+                        tc::stg_v8(dst, w);
+                        tc::stg_v8(dst + 16, w + 8);
                     }
                 }
             } else if constexpr (EPI == kEpiDSwiGLU) {
@@ -615,12 +609,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc::tmem_ld_wait();
                     const int col = ti.n * BN + c0;
                     uint32_t dgw[16], duw[16];
+                    uint32_t gw32[32], uw32[32];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        tc::ldg_v8(gb + col + 8 * i, gw32 + 8 * i);
+                        tc::ldg_v8(gb + I + col + 8 * i, uw32 + 8 * i);
+                    }
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const float4 g4 = reinterpret_cast<const float4*>(gb + col)[i];
-                        const float4 u4 = reinterpret_cast<const float4*>(gb + I + col)[i];
-                        const float Gv[4] = {g4.x, g4.y, g4.z, g4.w};
-                        const float Uv[4] = {u4.x, u4.y, u4.z, u4.w};
+                        const float Gv[4] = {__uint_as_float(gw32[4 * i]), __uint_as_float(gw32[4 * i + 1]),
+                                             __uint_as_float(gw32[4 * i + 2]), __uint_as_float(gw32[4 * i + 3])};
+                        const float Uv[4] = {__uint_as_float(uw32[4 * i]), __uint_as_float(uw32[4 * i + 1]),
+                                             __uint_as_float(uw32[4 * i + 2]), __uint_as_float(uw32[4 * i + 3])};
                         float dg4[4], du4[4];
 #pragma unroll
                         for (int q2 = 0; q2 < 4; ++q2) {
@@ -635,13 +635,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         duw[2 * i] = pack_bf16x2(du4[0], du4[1]);
                         duw[2 * i + 1] = pack_bf16x2(du4[2], du4[3]);
                     }
-                    uint4* dg = reinterpret_cast<uint4*>(ob + col);
-                    uint4* du = reinterpret_cast<uint4*>(ob + I + col);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        dg[i] = make_uint4(dgw[4 * i], dgw[4 * i + 1], dgw[4 * i + 2], dgw[4 * i + 3]);
-                        du[i] = make_uint4(duw[4 * i], duw[4 * i + 1], duw[4 * i + 2], duw[4 * i + 3]);
-                    }
+                    tc::stg_v8(ob + col, dgw);
+                    tc::stg_v8(ob + col + 16, dgw + 8);
+                    tc::stg_v8(ob + I + col, duw);
+                    tc::stg_v8(ob + I + col + 16, duw + 8);
                 }
             } else {  // kEpiDense
                 // 32 x 32 BF16 blocks through shared memory, written by TMA

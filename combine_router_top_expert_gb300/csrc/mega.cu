@@ -1009,9 +1009,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                         for (int i = 0; i < 8; ++i)
                             w[i] = f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
                                    (f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
-                        uint8_t* dst = static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc0 + 32 * b;
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        tc::stg_v8(static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc0 + 32 * b, w);
                         codes |= code << (8 * b);
                     }
                     const int64_t chunk = (prow / kTileM) * (int64_t)(I / 128) + hc0 / 128;
@@ -1045,10 +1043,8 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                     if (dest >= 0) {
                         __nv_bfloat16* orow = bt.partials + dest * p.H + t.n * BN2;
                         auto store_chunk = [&](int c, const uint32_t(&w)[16]) {
-                            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                            tc::stg_v8(orow + 32 * c, w);
+                            tc::stg_v8(orow + 32 * c + 16, w + 8);
                         };
                         if (eg < nch) store_chunk(eg, w0);
                         if (eg + 2 < nch) store_chunk(eg + 2, w1);
@@ -1081,9 +1077,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                         for (int i = 0; i < 8; ++i)
                             w[i] = f32x2_to_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
                                    (f32x2_to_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
-                        uint8_t* dst = static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc;
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        tc::stg_v8(static_cast<uint8_t*>(p.hbuf) + prow * (int64_t)I + hc, w);
                         // the four codes of a 128-wide chunk leave as one word
                         sfw |= code << (8 * ((hc / 32) & 3));
                         if (((hc / 32) & 3) == 3) {
@@ -1096,10 +1090,9 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-                        uint4* dst =
-                            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.hbuf) + prow * (int64_t)I + hc);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.hbuf) + prow * (int64_t)I + hc;
+                        tc::stg_v8(dst, w);
+                        tc::stg_v8(dst + 16, w + 8);
                     }
                 }
             } else {
@@ -1117,9 +1110,9 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                    uint4* dst = reinterpret_cast<uint4*>(bt.partials + dest * p.H + t.n * BN2 + c0);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    __nv_bfloat16* dst = bt.partials + dest * p.H + t.n * BN2 + c0;
+                    tc::stg_v8(dst, w);
+                    tc::stg_v8(dst + 16, w + 8);
                 }
             }
             if constexpr (!C::kWideEpi) {

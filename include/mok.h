@@ -260,7 +260,8 @@ mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* 
  * (BF16 or MXFP8 as dtype), y = h W_down[e], y row pushed to partials[t*k+j]
  * ([T*k, H] bf16, unweighted). h/h_sf are caller scratch of
  * [rows_max, I] (bf16 or E4M3; h_sf uses the same tile order as A_sf with I
- * in place of H; MXFP8 only). A and h must be 1024-B aligned. `workspace`
+ * in place of H; MXFP8 only). A and h must be 1024-B aligned, partials
+ * 32-B aligned (rows leave in 32-byte stores). `workspace`
  * supplies the 256-byte device status block (its first 256 bytes). */
 mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf,
                           const void* packed, const mok_routing* r, void* h, void* h_sf,
@@ -304,7 +305,8 @@ typedef struct {
  * dW_gate = A^T dG, dW_up = A^T dU, dW_down = h^T dy; router: dl_j =
  * w_j (gw_j - sum_i w_i gw_i), dW_r = x^T dl, and dX[t] = sum_j da[t,j] +
  * sum_j dl_j W_r[:, e_j] in fixed order. The bias gets no gradient.
- * Bitwise deterministic. */
+ * Bitwise deterministic. dW_gate, dW_up and dW_down must be 16-B aligned
+ * (written by TMA stores), workspace and saved 1024-B aligned. */
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
                             const mok_config* cfg, mok_stream_t stream);
 
