@@ -214,8 +214,10 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     p.a_sf = h_sf;
     p.b_sf = Bdn_sf;
     p.sf_kchunks = I / 128;
-    // MXFP8: 224-wide tiles when H allows (double-buffered accumulator with
-    // the scales in the tensor-memory gaps), else 128; BF16: 256 or 128
+    // MXFP8: 256-wide tiles when H allows (one accumulator, 8 epilogue warps
+    // that release it before their stores), else 224 (double-buffered
+    // accumulator with the scales in the tensor-memory gaps), else 128;
+    // BF16: 256 or 128
     const int BN = down_tile_n(H, mx);
     p.n_tiles = H / BN;
     const bool cl = c.cluster == 2 && !mx && BN == 256 && identity_rows == 0;
@@ -225,6 +227,7 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     const int64_t mt = identity_rows > 0 ? (identity_rows + kTileM - 1) / kTileM : mtiles_ub(a_rows, E);
     const int64_t tub = mt * p.n_tiles;
     if (mx) {
+        if (BN == 256) return run<256, true, false, kEpiScatter, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
         if (BN == 224) return run<224, true, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
         return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }

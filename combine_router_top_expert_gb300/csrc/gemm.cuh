@@ -64,9 +64,10 @@ struct GemmParams {
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN = 1>
 struct GemmCfg {
     static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR && BN % 32 == 0 && (!MX || BN == 256)), "2-SM pairs: K-major");
-    // MXFP8 gate/up keeps one accumulator (its scales take the rest of TMEM)
-    // and hides the epilogue behind the next tile with 8 epilogue warps.
-    static constexpr bool kWideEpi = MX && EPI == kEpiSwiGLU && ACC_STAGES == 1;
+    // MXFP8 tiles 256 wide keep one accumulator (their scales take the rest
+    // of TMEM) and hide the epilogue behind the next tile with 8 epilogue
+    // warps.
+    static constexpr bool kWideEpi = MX && (EPI == kEpiSwiGLU || EPI == kEpiScatter) && ACC_STAGES == 1;
     static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
@@ -460,7 +461,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
 
-            if constexpr (C::kWideEpi) {
+            if constexpr (C::kWideEpi && EPI == kEpiScatter) {
+                // this warp's 32-column chunks eg, eg+2, eg+4, eg+6 to
+                // registers (packed to BF16 two at a time), accumulator
+                // released, then pushed to the row's slot
+                const int eg = (warp - 2) >> 2;
+                int64_t dest = -1;
+                const int lrow = ti.local_row0 + row;
+                if (p.identity_rows > 0) {
+                    if (lrow < p.identity_rows) dest = lrow;
+                } else if (ti.valid && lrow < p.counts[ti.e]) {
+                    dest = p.row_src[p.offsets[ti.e] + lrow];
+                }
+                constexpr int nch = BN / 32;
+                uint32_t w0[16], w1[16], w2[16], w3[16];
+                auto load_pair = [&](int c, uint32_t(&wa)[16], uint32_t(&wb)[16]) {
+                    uint32_t ra[32], rb[32];
+                    tc::tmem_ld_32x32b_x32(tbase + 32 * min(c, nch - 1), ra);
+                    tc::tmem_ld_32x32b_x32(tbase + 32 * min(c + 2, nch - 1), rb);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        wa[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                        wb[i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+                    }
+                };
+                load_pair(eg, w0, w1);
+                load_pair(eg + 4, w2, w3);
+                tc::fence_before_sync();
+                if constexpr (CLN == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acce_bar(acc), 0));
+                else tc::mbar_arrive(acce_bar(acc));
+                if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+                if (dest >= 0) {
+                    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out0) + dest * p.ldo + ti.n * BN;
+                    auto store_chunk = [&](int c, const uint32_t(&w)[16]) {
+                        tc::stg_v8(orow + 32 * c, w);
+                        tc::stg_v8(orow + 32 * c + 16, w + 8);
+                    };
+                    if (eg < nch) store_chunk(eg, w0);
+                    if (eg + 2 < nch) store_chunk(eg + 2, w1);
+                    if (eg + 4 < nch) store_chunk(eg + 4, w2);
+                    if (eg + 6 < nch) store_chunk(eg + 6, w3);
+                }
+            } else if constexpr (C::kWideEpi) {
                 // this warp's 64 h columns: gate and up pre-activations to
                 // registers, accumulator released, then SwiGLU and two
                 // 32-element MXFP8 blocks (scale codes 2*eg and 2*eg+1 of the

@@ -35,7 +35,7 @@ int64_t dwr_partial_floats(int H, int E);
 // N-tile of the down GEMM; MXFP8 down weights keep their block scales per
 // tile of this many rows.
 inline int down_tile_n(int H, bool mx) {
-    if (mx) return H % 224 == 0 ? 224 : 128;
+    if (mx) return H % 256 == 0 ? 256 : H % 224 == 0 ? 224 : 128;
     return H % 256 == 0 ? 256 : 128;
 }
 

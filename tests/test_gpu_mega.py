@@ -214,7 +214,9 @@ def test_trace_records_and_unchanged_output(cut_flags):
     counts = layer.buffers(wl.T)["routing"]["counts"].cpu().numpy()
     n_mb = int(np.max(rec[:movers, 6]))
     assert n_mb >= 2   # 1000 tokens in minibatches of at most 256
-    nt1, nt2 = 2 * wl.I // 256, wl.H // 128
+    # down tiles: 256 wide when H allows, else 224, else 128 (MXFP8)
+    bn2 = 256 if wl.H % 256 == 0 else 224 if wl.H % 224 == 0 else 128
+    nt1, nt2 = 2 * wl.I // 256, wl.H // bn2
     mtiles = int(np.sum((counts + 127) // 128))
     tiles_min = mtiles * (nt1 + nt2)
     if cut_flags:
