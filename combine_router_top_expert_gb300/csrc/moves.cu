@@ -348,7 +348,9 @@ __global__ void dl_scatter_kernel(const float* __restrict__ dl, const int32_t* _
 
 // dW_r partial sums over a token range: part[split][h][e] = sum_{t in split}
 // x[t,h] dl_full[t,e], t ascending. One thread per h, 32 experts per pass.
-constexpr int kDwrSplits = 8;
+// 32 token ranges keep about six CTAs per SM busy at T = 4096 (the work is
+// a few hundred dependent FMAs per loaded x value, so it needs warps).
+constexpr int kDwrSplits = 32;
 __global__ void __launch_bounds__(256)
 dwr_partial_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ dl_full, int T, int H, int E,
                    float* __restrict__ part) {
