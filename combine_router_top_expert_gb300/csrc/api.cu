@@ -61,7 +61,7 @@ PackedLayout packed_layout(int E, int H, int I, int dtype) {
 // Forward buffers. When `saved` is given (BF16 training), A, GU, h and the
 // partials live there so the backward can read them.
 struct FwdLayout {
-    size_t A, A_sf, h, h_sf, partials, shared, hs, total;   // workspace offsets
+    size_t A, A_sf, h, h_sf, partials, xq, xsf, shared, hs, total;   // workspace offsets
     size_t sA, sGU, sh, spart, saved_total;                  // saved offsets
 };
 
@@ -75,6 +75,10 @@ FwdLayout fwd_layout(const mok_problem* p, bool training) {
     if (!training) { L.h = o; o += align_up(rows * p->I * eb, 1024); }
     L.h_sf = o; if (p->dtype == MOK_MXFP8) o += align_up(rows * p->I / 32, 1024);
     if (!training) { L.partials = o; o += align_up((int64_t)p->T * p->k * p->H * 2, 1024); }
+    if (!training && p->dtype == MOK_MXFP8) {   // x quantised once per token before the gather
+        L.xq = o; o += align_up((int64_t)p->T * p->H, 1024);
+        L.xsf = o; o += align_up((int64_t)p->T * p->H / 32, 1024);
+    }
     if (p->I_shared > 0) {
         L.shared = o; o += align_up((int64_t)p->T * p->H * 4, 1024);
         L.hs = o; o += align_up((int64_t)p->T * p->I_shared * 2, 1024);
@@ -264,6 +268,25 @@ mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* 
                                        (cudaStream_t)stream));
 }
 
+mok_status mok_quantize_rows(const void* x, int32_t T, int32_t H, void* x_q, void* x_sf, mok_stream_t stream) {
+    if (T < 0 || H <= 0 || H % 128 != 0) return MOK_ERR_INVALID;
+    if (T > 0 && (!x || !x_q || !x_sf || !aligned(x, 16) || !aligned(x_q, 16) || !aligned(x_sf, 4)))
+        return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(launch_quantize_rows(x, T, H, x_q, x_sf, (cudaStream_t)stream));
+}
+
+mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const void* x_sf, const mok_routing* r,
+                                  void* A, void* A_sf, mok_stream_t stream) {
+    if (!problem_ok(p) || p->dtype != MOK_MXFP8 || !routing_ok(r, p->T) || !A || !A_sf || !aligned(A, 16))
+        return MOK_ERR_INVALID;
+    if (p->T > 0 && (!x_q || !x_sf || !aligned(x_q, 16) || !aligned(x_sf, 4))) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    if (p->T == 0) return MOK_OK;
+    return cuda_status(launch_dispatch_q(x_q, x_sf, p->T, p->H, p->E, p->k, r->counts, r->offsets, r->row_src, A,
+                                         static_cast<uint8_t*>(A_sf), (cudaStream_t)stream));
+}
+
 mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf, const void* packed,
                           const mok_routing* r, void* h, void* h_sf, void* partials, const mok_config* cfg,
                           void* workspace, mok_stream_t stream) {
@@ -413,8 +436,13 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     if (e == cudaSuccess)
         // pad rows stay unwritten for inference (their GEMM rows are never
         // stored); training keeps them zero for the weight gradients
-        e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
-                            nullptr, s, training);
+        e = (mx && !training)
+                ? launch_quantize_rows(a->x, p->T, p->H, ws + L.xq, ws + L.xsf, s)
+                : launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf,
+                                  nullptr, nullptr, s, training);
+    if (e == cudaSuccess && mx && !training)
+        e = launch_dispatch_q(ws + L.xq, ws + L.xsf, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A,
+                              A_sf, s);
     if (e == cudaSuccess)
         e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H, p->I,
                         r.counts, 0, rows, h, h_sf, gu, c, s);

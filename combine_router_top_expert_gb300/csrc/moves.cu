@@ -91,6 +91,45 @@ quantize_rows_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, uint8_t*
     }
 }
 
+// Pull-dispatch of rows already quantised once per token (quantize_rows):
+// each routed row copies its token's E4M3 bytes, and the row's scale words
+// (four codes per 128-wide chunk) go to the tile-ordered scale chunks. Pad
+// rows are not written (inference: their GEMM rows are never stored). The
+// bytes equal the fused quantising dispatch's, each token quantised once
+// instead of k times.
+__global__ void __launch_bounds__(256)
+dispatch_q_kernel(const uint8_t* __restrict__ xq, const uint32_t* __restrict__ xsf, int H, int E, int k,
+                  const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                  const int32_t* __restrict__ row_src, uint8_t* __restrict__ A, uint8_t* __restrict__ A_sf) {
+    __shared__ int32_t poff[kMaxE + 1];
+    padded_offsets(counts, E, poff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = poff[E];
+    const int kc_row = H / 128;
+    for (int pr = blockIdx.x * 8 + warp; pr < total; pr += gridDim.x * 8) {
+        const int e = find_expert(poff, E, pr);
+        const int local = pr - poff[e];
+        if (local >= counts[e]) continue;
+        const int64_t tok = row_src[offsets[e] + local] / k;
+        const uint4* s4 = reinterpret_cast<const uint4*>(xq + tok * H);
+        uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H);
+        const int n = H / 16;
+        int c = lane;
+        for (; c + 224 < n; c += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) __stcs(dst + c + 32 * u, v[u]);
+        }
+        for (; c < n; c += 32) __stcs(dst + c, __ldg(s4 + c));
+        const int rt = pr / kTileM, r = pr % kTileM;
+        for (int q = lane; q < kc_row; q += 32)
+            *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)rt * kc_row + q) * 512 + sf_chunk_offset(r, 0)) =
+                __ldg(xsf + tok * kc_row + q);
+    }
+}
+
 template <bool MX>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
@@ -416,6 +455,17 @@ cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, 
                                                       offsets, row_src, A, nullptr,
                                                       static_cast<const __nv_bfloat16*>(scale_src), wslot,
                                                       zero_pads ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, int E, int k, const int32_t* counts,
+                              const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
+                              cudaStream_t s) {
+    int64_t rows = padded_rows_max(T, E, k);
+    int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
+    if (blocks < 1) blocks = 1;
+    dispatch_q_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(x_q), static_cast<const uint32_t*>(x_sf), H, E,
+                                             k, counts, offsets, row_src, static_cast<uint8_t*>(A), A_sf);
     return cudaGetLastError();
 }
 

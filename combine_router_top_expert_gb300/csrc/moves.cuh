@@ -60,6 +60,11 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
 // MXFP8 quantisation of each row of x [T, H] (the codes the dispatch writes):
 // x_q [T, H] E4M3, x_sf [T, H/32] E8M0 bytes.
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s);
+// MXFP8 pull-dispatch of rows quantised by launch_quantize_rows (same bytes
+// as launch_dispatch; pad rows left unwritten).
+cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, int E, int k, const int32_t* counts,
+                              const int32_t* offsets, const int32_t* row_src, void* A, uint8_t* A_sf,
+                              cudaStream_t s);
 cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* Bdn, const uint8_t* Bdn_sf, int E,
                       int H, int I, const int32_t* counts, const int32_t* offsets, const int32_t* row_src,
                       int identity_rows, int64_t a_rows, void* out, const GemmCommon& c, cudaStream_t s);

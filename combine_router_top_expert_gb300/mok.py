@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "MOK_OK", 1: "MOK_ERR_INVALID", 2: "MOK_ERR_CUDA", 3: "MOK_ER
 EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_size", "mok_pack_weights",
            "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
-           "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches"]
+           "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches",
+           "mok_quantize_rows", "mok_dispatch_quantized"]
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
@@ -105,6 +106,8 @@ def lib():
             L.mok_padded_rows_max.argtypes = [I32, I32, I32]
             L.mok_padded_rows_max.restype = ctypes.c_int64
             L.mok_dispatch.argtypes = [PP, P, PR, P, P, P]
+            L.mok_quantize_rows.argtypes = [P, I32, I32, P, P, P]
+            L.mok_dispatch_quantized.argtypes = [PP, P, P, PR, P, P, P]
             L.mok_expert_ffn.argtypes = [PP, P, P, P, PR, P, P, P, PC, P, P]
             L.mok_combine.argtypes = [PP, P, P, P, P, P]
             L.mok_moe_backward.argtypes = [PP, ctypes.POINTER(BwdArgs), PC, P]
@@ -113,7 +116,7 @@ def lib():
             L.mok_status_string.restype = ctypes.c_char_p
             L.mok_version.restype = ctypes.c_char_p
             for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
-                         "mok_moe_forward_batches", "mok_dispatch",
+                         "mok_moe_forward_batches", "mok_dispatch", "mok_quantize_rows", "mok_dispatch_quantized",
                          "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
@@ -294,6 +297,19 @@ def dispatch(p: Problem, x, routing, A, A_sf=None, stream=None):
     rs = routing_struct(routing)
     rc = lib().mok_dispatch(ctypes.byref(p), _ptr(x), ctypes.byref(rs), _ptr(A), _ptr(A_sf), _stream(stream))
     _check(rc, "mok_dispatch")
+
+
+def quantize_rows(x, x_q, x_sf, stream=None):
+    T, H = x.shape
+    rc = lib().mok_quantize_rows(_ptr(x), T, H, _ptr(x_q), _ptr(x_sf), _stream(stream))
+    _check(rc, "mok_quantize_rows")
+
+
+def dispatch_quantized(p: Problem, x_q, x_sf, routing, A, A_sf, stream=None):
+    rs = routing_struct(routing)
+    rc = lib().mok_dispatch_quantized(ctypes.byref(p), _ptr(x_q), _ptr(x_sf), ctypes.byref(rs), _ptr(A), _ptr(A_sf),
+                                      _stream(stream))
+    _check(rc, "mok_dispatch_quantized")
 
 
 def expert_ffn(p: Problem, A, A_sf, packed, routing, h, h_sf, partials, workspace, cfg: Config | None = None,

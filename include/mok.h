@@ -256,6 +256,21 @@ int64_t mok_padded_rows_max(int32_t T, int32_t E, int32_t k);
 mok_status mok_dispatch(const mok_problem* p, const void* x, const mok_routing* r,
                         void* A, void* A_sf, mok_stream_t stream);
 
+/* MXFP8 quantisation of every row of x [T, H] bf16 (H % 128 == 0), once per
+ * token (the same rule as mok_dispatch): x_q [T, H] E4M3 bytes and x_sf
+ * [T, H/32] E8M0 bytes, block b of row t at byte t*(H/32) + b. x_q 16-B and
+ * x_sf 4-B aligned. The quantising half of the MXFP8 dispatch that
+ * mok_moe_forward runs: each token is quantised once instead of k times. */
+mok_status mok_quantize_rows(const void* x, int32_t T, int32_t H, void* x_q, void* x_sf,
+                             mok_stream_t stream);
+
+/* MXFP8 pull-dispatch of rows quantised by mok_quantize_rows: A and A_sf as
+ * mok_dispatch writes them for routed rows (the same bytes); pad rows are
+ * left unwritten (the forward never stores the GEMM rows they feed).
+ * p->dtype must be MOK_MXFP8; A 16-B aligned. */
+mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const void* x_sf,
+                                  const mok_routing* r, void* A, void* A_sf, mok_stream_t stream);
+
 /* Grouped expert FFN on the dispatched rows: h = SwiGLU(A W_gate[e], A W_up[e])
  * (BF16 or MXFP8 as dtype), y = h W_down[e], y row pushed to partials[t*k+j]
  * ([T*k, H] bf16, unweighted). h/h_sf are caller scratch of

@@ -113,6 +113,44 @@ def test_dispatch_bytes(dt):
 
 
 @pytest.mark.gpu
+def test_quantize_once_then_gather():
+    """mok_quantize_rows gives the oracle's MXFP8 codes and scales per token;
+    mok_dispatch_quantized then writes the same routed rows and scales as the
+    quantising mok_dispatch."""
+    wl = synth.small("disp_q", T=333, H=1024, I=128, E=8, k=3, zipf_s=1.2)
+    inp = synth.make_inputs(wl, seed=2)
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    rt = layer.route(x)
+    p = layer.problem(wl.T)
+    xq = mok.alloc_bytes(wl.T * wl.H).view(wl.T, wl.H)
+    xsf = mok.alloc_bytes(wl.T * wl.H // 32).view(wl.T, wl.H // 32)
+    mok.quantize_rows(x, xq, xsf)
+    torch.cuda.synchronize()
+    codes, scales = oracle.mx_quantize_bf16_rows(inp.x)
+    assert np.array_equal(xq.cpu().numpy(), codes)
+    assert np.array_equal(xsf.cpu().numpy(), scales)
+    rows = mok.padded_rows_max(wl.T, wl.E, wl.k)
+    A1, A2 = mok.alloc_bytes(rows * wl.H).view(rows, wl.H), mok.alloc_bytes(rows * wl.H).view(rows, wl.H)
+    S1, S2 = mok.alloc_bytes(rows * wl.H // 32), mok.alloc_bytes(rows * wl.H // 32)
+    mok.dispatch(p, x, rt, A1, S1)
+    mok.dispatch_quantized(p, xq, xsf, rt, A2, S2)
+    torch.cuda.synchronize()
+    counts = r["counts"]
+    poff = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    live = np.zeros(poff[-1], bool)
+    for e in range(wl.E):
+        live[poff[e]:poff[e] + counts[e]] = True
+    assert np.array_equal(A2[:poff[-1]].cpu().numpy()[live], A1[:poff[-1]].cpu().numpy()[live])
+    sf1 = untile_sf(S1.cpu().numpy(), poff[-1], wl.H)
+    sf2 = untile_sf(S2.cpu().numpy(), poff[-1], wl.H)
+    assert np.array_equal(sf2[live], sf1[live])
+    with pytest.raises(mok.MokError):
+        mok.quantize_rows(x[:, :1000], xq, xsf)     # H % 128 != 0
+
+
+@pytest.mark.gpu
 def test_stages_compose_to_forward():
     """dispatch -> expert_ffn -> combine gives the same bits as moe_forward."""
     wl = synth.small("stages", T=256, H=512, I=256, E=8, k=2, dtype="mxfp8")
