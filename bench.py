@@ -116,6 +116,14 @@ def dist_env():
     return ws, rank, local
 
 
+# DRAM bytes per step of the grouped GEMM pair (dram__bytes_read.sum +
+# dram__bytes_write.sum of both launches) from one ncu capture of the current
+# kernels; the 32-expert figure is the 8-expert profiling case's traffic x 4
+# (experts and routed rows both 4x; summary in profiles/). None: not captured
+# since the kernels last changed.
+GEMM_PAIR_TRAFFIC = {"bf16_fwd_T2560": 3.716e9}
+
+
 def max_over_ranks(values, device):
     """Element-wise maximum of a list of floats over all ranks (identity on
     one rank): the slowest rank's timings set the whole job's rate."""
@@ -548,7 +556,7 @@ def main():
         "roofline": ({"kernel": kern,
                       "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
                       "frac": hbm_achieved / peaks["hbm"], "peak_source": f"{peaks['source']} hbm copy",
-                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": None,
+                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": GEMM_PAIR_TRAFFIC.get(wl.name),
                       "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}}
                      if hbm_bound else
                      {"kernel": kern,
@@ -556,7 +564,7 @@ def main():
                       "frac": achieved / peak,
                       "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
                                      (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
-                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": None,
+                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": GEMM_PAIR_TRAFFIC.get(wl.name),
                       "hbm": ({"achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
                                "frac": hbm_achieved / peaks["hbm"], "bytes_per_step": gemm_bytes}
                               if gemm_bytes else None)}),
