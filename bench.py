@@ -525,6 +525,8 @@ def main():
     value = whole_job_rate(ws, tokens_per_step, args.steps, t_max)
     e2e_val = whole_job_rate(ws, tokens_per_step, n_e2e, e2e_max)
     peaks = load_peaks()
+    # captured traffic belongs to the single-CTA stage kernels only
+    traffic = GEMM_PAIR_TRAFFIC.get(wl.name) if staged and len(xs) == 1 and not args.gemm_pairs else None
     fl = flops
     g_ms = statistics.mean(gemm_ms)
     achieved = fl / (g_ms / 1000.0) / 1e12
@@ -556,7 +558,7 @@ def main():
         "roofline": ({"kernel": kern,
                       "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
                       "frac": hbm_achieved / peaks["hbm"], "peak_source": f"{peaks['source']} hbm copy",
-                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": GEMM_PAIR_TRAFFIC.get(wl.name),
+                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": traffic,
                       "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}}
                      if hbm_bound else
                      {"kernel": kern,
@@ -564,7 +566,7 @@ def main():
                       "frac": achieved / peak,
                       "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
                                      (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
-                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": GEMM_PAIR_TRAFFIC.get(wl.name),
+                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": traffic,
                       "hbm": ({"achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
                                "frac": hbm_achieved / peaks["hbm"], "bytes_per_step": gemm_bytes}
                               if gemm_bytes else None)}),
