@@ -603,13 +603,26 @@ __device__ void combine_tokens(const MegaParams& p, const MegaBatch& bt, int t0,
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            for (int j = 0; j < k; ++j) {
-                const float wj = bt.topk_w[(int64_t)t * k + j];
-                const uint4 u = reinterpret_cast<const uint4*>(bt.partials + ((int64_t)t * k + j) * H)[c];
-                acc[0] = fmaf(wj, bf16_lo(u.x), acc[0]); acc[1] = fmaf(wj, bf16_hi(u.x), acc[1]);
-                acc[2] = fmaf(wj, bf16_lo(u.y), acc[2]); acc[3] = fmaf(wj, bf16_hi(u.y), acc[3]);
-                acc[4] = fmaf(wj, bf16_lo(u.z), acc[4]); acc[5] = fmaf(wj, bf16_hi(u.z), acc[5]);
-                acc[6] = fmaf(wj, bf16_lo(u.w), acc[6]); acc[7] = fmaf(wj, bf16_hi(u.w), acc[7]);
+            // up to 4 slots' loads in flight, then their products in j order
+            for (int j0 = 0; j0 < k; j0 += 4) {
+                uint4 u[4];
+                float wj[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (j0 + q < k) {
+                        wj[q] = bt.topk_w[(int64_t)t * k + j0 + q];
+                        u[q] = __ldcs(reinterpret_cast<const uint4*>(bt.partials + ((int64_t)t * k + j0 + q) * H) + c);
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (j0 + q < k) {
+                        acc[0] = fmaf(wj[q], bf16_lo(u[q].x), acc[0]); acc[1] = fmaf(wj[q], bf16_hi(u[q].x), acc[1]);
+                        acc[2] = fmaf(wj[q], bf16_lo(u[q].y), acc[2]); acc[3] = fmaf(wj[q], bf16_hi(u[q].y), acc[3]);
+                        acc[4] = fmaf(wj[q], bf16_lo(u[q].z), acc[4]); acc[5] = fmaf(wj[q], bf16_hi(u[q].z), acc[5]);
+                        acc[6] = fmaf(wj[q], bf16_lo(u[q].w), acc[6]); acc[7] = fmaf(wj[q], bf16_hi(u[q].w), acc[7]);
+                    }
+                }
             }
             if (bt.shared) {
                 const float4* s = reinterpret_cast<const float4*>(bt.shared + (int64_t)t * H) + 2 * c;

@@ -222,13 +222,26 @@ combine_kernel(const __nv_bfloat16* __restrict__ partials, const float* __restri
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const float wj = __ldg(w + (int64_t)t * k + j);
-            uint4 v = __ldcs(reinterpret_cast<const uint4*>(partials + ((int64_t)t * k + j) * H) + c);
-            acc[0] = fmaf(wj, bf16_lo(v.x), acc[0]); acc[1] = fmaf(wj, bf16_hi(v.x), acc[1]);
-            acc[2] = fmaf(wj, bf16_lo(v.y), acc[2]); acc[3] = fmaf(wj, bf16_hi(v.y), acc[3]);
-            acc[4] = fmaf(wj, bf16_lo(v.z), acc[4]); acc[5] = fmaf(wj, bf16_hi(v.z), acc[5]);
-            acc[6] = fmaf(wj, bf16_lo(v.w), acc[6]); acc[7] = fmaf(wj, bf16_hi(v.w), acc[7]);
+        // up to 8 slots' loads in flight, then their products in j order
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            uint4 v[8];
+            float wj[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (j0 + q < k) {
+                    wj[q] = __ldg(w + (int64_t)t * k + j0 + q);
+                    v[q] = __ldcs(reinterpret_cast<const uint4*>(partials + ((int64_t)t * k + j0 + q) * H) + c);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (j0 + q < k) {
+                    acc[0] = fmaf(wj[q], bf16_lo(v[q].x), acc[0]); acc[1] = fmaf(wj[q], bf16_hi(v[q].x), acc[1]);
+                    acc[2] = fmaf(wj[q], bf16_lo(v[q].y), acc[2]); acc[3] = fmaf(wj[q], bf16_hi(v[q].y), acc[3]);
+                    acc[4] = fmaf(wj[q], bf16_lo(v[q].z), acc[4]); acc[5] = fmaf(wj[q], bf16_hi(v[q].z), acc[5]);
+                    acc[6] = fmaf(wj[q], bf16_lo(v[q].w), acc[6]); acc[7] = fmaf(wj[q], bf16_hi(v[q].w), acc[7]);
+                }
+            }
         }
         if (shared) {
             const float4* s = reinterpret_cast<const float4*>(shared + (int64_t)t * H) + 2 * c;
