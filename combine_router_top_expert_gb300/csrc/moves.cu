@@ -172,15 +172,24 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
                 for (; c < n; c += 32) __stcs(dst + c, __ldg(s4 + c));
             } else {
                 // reverse-combine: dy = w[t,j] * dY[t], rounded to bf16
-                for (int c = lane; c < n; c += 32) {
-                    uint4 v = __ldg(s4 + c);
+                // (eight 16-byte loads in flight per lane, as above)
+                auto scale = [&](const uint4& v) {
                     uint4 o;
                     o.x = pack_bf16x2(wmul * bf16_lo(v.x), wmul * bf16_hi(v.x));
                     o.y = pack_bf16x2(wmul * bf16_lo(v.y), wmul * bf16_hi(v.y));
                     o.z = pack_bf16x2(wmul * bf16_lo(v.z), wmul * bf16_hi(v.z));
                     o.w = pack_bf16x2(wmul * bf16_lo(v.w), wmul * bf16_hi(v.w));
-                    dst[c] = o;
+                    return o;
+                };
+                int c = lane;
+                for (; c + 224 < n; c += 256) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) dst[c + 32 * u] = scale(v[u]);
                 }
+                for (; c < n; c += 32) dst[c] = scale(__ldg(s4 + c));
             }
         } else {
             uint8_t* dst = static_cast<uint8_t*>(A) + (int64_t)pr * H;
@@ -368,10 +377,20 @@ dx_kernel(const __nv_bfloat16* __restrict__ da, const float* __restrict__ dl, co
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int j = 0; j < k; ++j) {
-            uint4 v = __ldg(reinterpret_cast<const uint4*>(da + ((int64_t)t * k + j) * H) + c);
-            acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-            acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+        // up to 8 slots' loads in flight, then their sums in j order
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (j0 + q < k) v[q] = __ldcs(reinterpret_cast<const uint4*>(da + ((int64_t)t * k + j0 + q) * H) + c);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (j0 + q < k) {
+                    acc[0] += bf16_lo(v[q].x); acc[1] += bf16_hi(v[q].x); acc[2] += bf16_lo(v[q].y);
+                    acc[3] += bf16_hi(v[q].y); acc[4] += bf16_lo(v[q].z); acc[5] += bf16_hi(v[q].z);
+                    acc[6] += bf16_lo(v[q].w); acc[7] += bf16_hi(v[q].w);
+                }
+            }
         }
         for (int j = 0; j < k; ++j) {
             const float d = dl[(int64_t)t * k + j];
