@@ -312,7 +312,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         tc::tma_load_2d_2sm(b_tile(stage), b1 ? (const void*)&tmB : (const void*)&tmB2, lead_full,
                                             (b1 ? kb : kb - p.b_split_kb) * C::kBK, brow + rank * (BN / 2));
                         if constexpr (MX) {
-                            // scale chunks (512 B = two 256-byte rows of tmSA / tmSB): this CTA's A
+                            // scale chunks (512 B = two 256-byte rows of tmX0 / tmX1): this CTA's A
                             // rows, and all BN rows of B (the pair MMA reads B's scales in each CTA)
                             tc::tma_load_2d_2sm(sf_tile(stage), &tmX0, lead_full, 0,
                                                 2 * ((ti.a_row0 / kTileM) * p.sf_kchunks + kb));
