@@ -70,6 +70,9 @@ struct GemmCfg {
     static constexpr bool kWideEpi = MX && (EPI == kEpiSwiGLU || EPI == kEpiScatter) && ACC_STAGES == 1;
     static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    // BF16 grouped-row forward tiles: an expert's last tile with at most 64
+    // rows runs M=64 MMAs (rows 16q..16q+15 land in TMEM lanes 32q..32q+15)
+    static constexpr bool kHalfTiles = !MX && !MN_MAJOR && CLN == 1 && (EPI == kEpiSwiGLU || EPI == kEpiScatter);
     static constexpr int kBytesA = 128 * 128;          // 128 rows (or K rows) x 128 bytes
     static constexpr int kBytesB = BN / CLN * 128;
     static constexpr int kStageBytes = kBytesA + kBytesB;
@@ -115,6 +118,7 @@ struct TileInfo {
     int row_base;    // first padded row of the tile (output row space of A rows)
     int local_row0;  // first expert-local row of the tile
     int valid;       // 0: skip
+    int half;        // 1: the expert's last tile holds at most 64 rows; one M=64 MMA per K step
 };
 
 // Per-CTA copy of the group schedule.
@@ -172,6 +176,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched
         ti.local_row0 = ti.m * kTileM;
     }
     ti.valid = 1;
+    ti.half = 0;
     return ti;
 }
 
@@ -202,6 +207,7 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
     ti.row_base = ti.a_row0;
     ti.local_row0 = ti.m * kTileM;
     ti.valid = ti.m < mt ? 1 : 0;
+    ti.half = 0;
     return ti;
 }
 
@@ -285,9 +291,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int gstart = (int)blockIdx.x / CLN;
     const int gstep = (int)gridDim.x / CLN;
     const int gtotal = sched.toff[p.E];
+    // M=64 last tiles: grouped rows only, and not when the forward keeps
+    // G|U for the backward (the weight gradients read every padded row)
+    const bool half_ok = C::kHalfTiles && p.identity_rows == 0 && p.m_fixed == 0 &&
+                         (EPI != kEpiSwiGLU || p.gu == nullptr);
     auto decode = [&](int gi) {
-        if constexpr (CLN == 2) return decode_pair_tile(p, sched, gi, rank);
-        else return decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, gi);
+        if constexpr (CLN == 2) {
+            return decode_pair_tile(p, sched, gi, rank);
+        } else {
+            TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, gi);
+            ti.half = half_ok && p.counts[ti.e] - ti.local_row0 <= 64 ? 1 : 0;
+            return ti;
+        }
     };
 
     if (warp == 0) {
@@ -426,7 +441,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         } else if constexpr (CLN == 2) {
                             tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(256, BN, false, false), accum);
                         } else {
-                            tc::mma_bf16(d, ad, bd, tc::idesc_bf16(128, BN, MN_MAJOR, MN_MAJOR), accum);
+                            tc::mma_bf16(d, ad, bd, tc::idesc_bf16(ti.half ? 64 : 128, BN, MN_MAJOR, MN_MAJOR), accum);
                         }
                     }
                     issued = true;
@@ -449,11 +464,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;          // TMEM lane quadrant of this warp
-        const int row = q * 32 + lane;   // tile row owned by this thread
         int acc = 0;
         uint32_t acc_ph = 0;
         for (int gi = gstart; gi < gtotal; gi += gstep) {
             TileInfo ti = decode(gi);
+            // tile row owned by this thread (-1: none, in the empty lanes of an M=64 tile)
+            const int row = ti.half ? (lane < 16 ? q * 16 + lane : -1) : q * 32 + lane;
             const bool has_acc = ti.num_kb > 0;
             if (has_acc) {
                 if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
@@ -556,7 +572,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else if constexpr (EPI == kEpiSwiGLU) {
                 const int I = p.split_col;
                 const int64_t prow = ti.row_base + row;
-                const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid;
+                const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid && row >= 0;
                 uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -615,7 +631,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else if constexpr (EPI == kEpiScatter) {
                 int64_t dest = -1;
                 const int lrow = ti.local_row0 + row;
-                if (p.identity_rows > 0) {
+                if (row < 0) {
+                    // an empty lane of an M=64 tile
+                } else if (p.identity_rows > 0) {
                     if (lrow < p.identity_rows) dest = lrow;
                 } else if (lrow < p.counts[ti.e]) {
                     dest = p.row_src[p.offsets[ti.e] + lrow];
