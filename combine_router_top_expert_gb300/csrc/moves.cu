@@ -114,15 +114,16 @@ dispatch_q_kernel(const uint8_t* __restrict__ xq, const uint32_t* __restrict__ x
         const uint4* s4 = reinterpret_cast<const uint4*>(xq + tok * H);
         uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H);
         const int n = H / 16;
-        int c = lane;
-        for (; c + 224 < n; c += 256) {
+        // batches of eight 16-byte loads in flight per lane (the last one masked)
+        for (int c = lane; c < n; c += 256) {
             uint4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+            for (int u = 0; u < 8; ++u)
+                if (c + 32 * u < n) v[u] = __ldg(s4 + c + 32 * u);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) __stcs(dst + c + 32 * u, v[u]);
+            for (int u = 0; u < 8; ++u)
+                if (c + 32 * u < n) __stcs(dst + c + 32 * u, v[u]);
         }
-        for (; c < n; c += 32) __stcs(dst + c, __ldg(s4 + c));
         const int rt = pr / kTileM, r = pr % kTileM;
         for (int q = lane; q < kc_row; q += 32)
             *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)rt * kc_row + q) * 512 + sf_chunk_offset(r, 0)) =
@@ -159,17 +160,18 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
             if (!src) {
                 for (int c = lane; c < n; c += 32) __stcs(dst + c, make_uint4(0, 0, 0, 0));
             } else if (!wslot) {
-                // eight 16-byte loads in flight per lane before their stores;
-                // the rows stream out (evict-first: read back only by the GEMM)
-                int c = lane;
-                for (; c + 224 < n; c += 256) {
+                // batches of eight 16-byte loads in flight per lane before
+                // their stores (the last batch masked); the rows stream out
+                // (evict-first: read back only by the GEMM)
+                for (int c = lane; c < n; c += 256) {
                     uint4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+                    for (int u = 0; u < 8; ++u)
+                        if (c + 32 * u < n) v[u] = __ldg(s4 + c + 32 * u);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) __stcs(dst + c + 32 * u, v[u]);
+                    for (int u = 0; u < 8; ++u)
+                        if (c + 32 * u < n) __stcs(dst + c + 32 * u, v[u]);
                 }
-                for (; c < n; c += 32) __stcs(dst + c, __ldg(s4 + c));
             } else {
                 // reverse-combine: dy = w[t,j] * dY[t], rounded to bf16
                 // (eight 16-byte loads in flight per lane, as above)
@@ -181,15 +183,15 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
                     o.w = pack_bf16x2(wmul * bf16_lo(v.w), wmul * bf16_hi(v.w));
                     return o;
                 };
-                int c = lane;
-                for (; c + 224 < n; c += 256) {
+                for (int c = lane; c < n; c += 256) {
                     uint4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) v[u] = __ldg(s4 + c + 32 * u);
+                    for (int u = 0; u < 8; ++u)
+                        if (c + 32 * u < n) v[u] = __ldg(s4 + c + 32 * u);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) dst[c + 32 * u] = scale(v[u]);
+                    for (int u = 0; u < 8; ++u)
+                        if (c + 32 * u < n) dst[c + 32 * u] = scale(v[u]);
                 }
-                for (; c < n; c += 32) dst[c] = scale(__ldg(s4 + c));
             }
         } else {
             uint8_t* dst = static_cast<uint8_t*>(A) + (int64_t)pr * H;
