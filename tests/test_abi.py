@@ -49,6 +49,15 @@ def test_sizes_and_host_validation():
     assert rc == mok.ERR_INVALID
     rc = L.mok_pack_weights(8, 100, 64, 0, None, None, None, None, 0, None)
     assert rc == mok.ERR_INVALID
+    rc = L.mok_quantize_rows(None, 64, 100, None, None, None)       # H % 128
+    assert rc == mok.ERR_INVALID
+    rc = L.mok_quantize_rows(None, 64, 128, None, None, None)       # null buffers
+    assert rc == mok.ERR_INVALID
+    pm = mok.make_problem(64, 128, 128, 8, 2, mok.MXFP8)
+    rc = L.mok_dispatch_quantized(ctypes.byref(p), None, None, None, None, None, None)   # BF16 problem
+    assert rc == mok.ERR_INVALID
+    rc = L.mok_dispatch_quantized(ctypes.byref(pm), None, None, None, None, None, None)  # no routing
+    assert rc == mok.ERR_INVALID
     assert L.mok_status_string(3) == b"device wait timed out"
 
 
