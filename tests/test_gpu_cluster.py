@@ -56,3 +56,41 @@ def test_cluster_pairs_backward_bitwise():
         res.append({n: t.clone() for n, t in g.items()})
     for n in res[0]:
         assert torch.equal(res[0][n].view(torch.uint8), res[1][n].view(torch.uint8)), n
+
+
+@pytest.mark.gpu
+def test_last_tiles_of_at_most_64_rows():
+    """Experts whose last 128-row tile holds 64, 65, 1, 127, 64 and 1 rows
+    (hand-made routing, k = 1): the single-CTA kernels run an M=64 MMA for
+    last tiles of at most 64 rows; the output equals the oracle and is
+    bit-identical to the 2-SM pair kernels, which run M=256 MMAs only."""
+    import numpy as np
+    import oracle
+    from helpers import TOL, assert_close, host_bf16_f64
+
+    counts = [64, 65, 1, 127, 192, 129]
+    E, T = len(counts), sum(counts)
+    wl = synth.small("m64_tiles", T=T, H=512, I=256, E=E, k=1)
+    inp = synth.make_inputs(wl, seed=5)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    idx = np.repeat(np.arange(E), counts).astype(np.int32)[:, None]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    order = np.arange(T, dtype=np.int32)            # tokens are already in expert order
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    rt = {"topk_idx": dev(idx), "topk_w": dev(np.ones((T, 1), np.float32)), "counts": dev(np.array(counts, np.int32)),
+          "offsets": dev(offsets), "row_src": dev(order), "slot_row": dev(order)}
+    p = layer.problem(T)
+    outs = []
+    for flags in (0, mok.FLAG_GEMM_PAIRS):
+        cfg = mok.make_config(flags=flags)
+        ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
+        out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")
+        mok.moe_forward(p, x, layer.packed, rt, out, ws, cfg=cfg)
+        torch.cuda.synchronize()
+        assert mok.device_status(ws) == (mok.OK, 0)
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    r = {"idx": idx, "w": np.ones((T, 1)), "offsets": offsets, "row_src": order}
+    ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_BF16)
+    assert_close(host_bf16_f64(outs[0]), ref, TOL[mok.BF16], "M=64 last tiles")
