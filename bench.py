@@ -117,11 +117,33 @@ def dist_env():
 
 
 # DRAM bytes per step of the grouped GEMM pair (dram__bytes_read.sum +
-# dram__bytes_write.sum of both launches) from one ncu capture of the current
-# kernels; the 32-expert figure is the 8-expert profiling case's traffic x 4
-# (experts and routed rows both 4x; summary in profiles/). None: not captured
-# since the kernels last changed.
-GEMM_PAIR_TRAFFIC = {"bf16_fwd_T2560": 3.722e9}
+# dram__bytes_write.sum of both launches) from one ncu capture, with the
+# hash of the GEMM kernel sources it was captured on; the 32-expert figure is
+# the 8-expert profiling case's traffic x 4 (experts and routed rows both
+# 4x). A capture whose sources no longer match the built kernels is stale and
+# reported as null.
+GEMM_SOURCES = ["gemm.cuh", "tc.cuh", "gemm.cu"]
+GEMM_PAIR_TRAFFIC = {"bf16_fwd_T2560": {"bytes": 3.722e9, "gemm_sources_sha1": "7bba3cc84fb159dd"}}
+
+
+def gemm_sources_sha1():
+    import hashlib
+    h = hashlib.sha1()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "combine_router_top_expert_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(name):
+    """(bytes, note) of the GEMM pair's captured DRAM traffic for workload
+    `name`, or (None, why) when there is none for the kernels as built."""
+    c = GEMM_PAIR_TRAFFIC.get(name)
+    if c is None:
+        return None, "not captured for this workload"
+    if c["gemm_sources_sha1"] != gemm_sources_sha1():
+        return None, "stale: captured on GEMM sources " + c["gemm_sources_sha1"]
+    return c["bytes"], "ncu capture on GEMM sources " + c["gemm_sources_sha1"]
 
 
 def max_over_ranks(values, device):
@@ -243,43 +265,39 @@ def trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b):
     return out
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
-    ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
-    ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
-    ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
-    ap.add_argument("--mb-token-ranges", action="store_true",
-                    help="megakernel minibatches as token ranges (default: runs of expert tiles)")
-    ap.add_argument("--trace", action="store_true",
-                    help="megakernel: after the timed steps, one traced step; report the SM partition's busy/idle time")
-    args = ap.parse_args()
-    wl = synth.WORKLOADS[args.workload]
-    if args.impl == "reference":
-        return run_reference(args, wl)
-
-    import torch
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-
+def build_layer(wl, dev, rank, inp=None):
+    """Host inputs and the layer (packed weights on `dev`). Workloads of one
+    expert shape draw the same weights (seed 0), so `inp` of one can be
+    reused for another: only its tokens (and the logit bias) are redrawn."""
     from combine_router_top_expert_gb300 import mok
-    from combine_router_top_expert_gb300.layer import MoELayer, to_dev_bf16
-
+    from combine_router_top_expert_gb300.layer import MoELayer
     dtype = mok.MXFP8 if wl.dtype == "mxfp8" else mok.BF16
-    # data-parallel replicas: every rank holds the same weights and its own tokens
-    inp = synth.make_inputs(wl, shard=rank)
+    if inp is None:
+        # data-parallel replicas: every rank holds the same weights and its own tokens
+        inp = synth.make_inputs(wl, shard=rank)
+    else:
+        inp = synth.LayerInputs(wl, inp.W_r, synth.zipf_bias(wl.E, wl.zipf_s) if wl.zipf_s else None,
+                                inp.Wg, inp.Wu, inp.Wd, inp.shared)
+        inp.xs = [synth.make_x(wl, b, 0, rank) for b in range(wl.batches)]
+        if wl.backward:
+            inp.dY = synth.make_dY(wl, 0, rank)
     layer = MoELayer(inp.W_r, inp.Wg, inp.Wu, inp.Wd, wl.k, dtype=dtype, bias=inp.bias, shared=inp.shared,
                      device=dev, keep_unpacked=wl.backward)
+    return inp, layer
+
+
+def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True):
+    """Time `steps` layer steps of workload `wl` after `warmup` untimed ones
+    (CUDA events per step, L2 flushed before each), then, with `with_e2e`,
+    the same steps end to end through the public API with host buffers.
+    Every rank calls this; returns the per-step record (timings already the
+    maximum over ranks) that line() turns into JSON."""
+    import torch
+    from combine_router_top_expert_gb300 import mok
+    from combine_router_top_expert_gb300.layer import to_dev_bf16
+    ws, rank, local = dist_env()
+
+    dtype = mok.MXFP8 if wl.dtype == "mxfp8" else mok.BF16
     T, H = wl.T, wl.H
     xs = [to_dev_bf16(xb, dev) for xb in inp.xs]
     x = xs[0]
@@ -293,6 +311,7 @@ def main():
                           minibatch_tokens=args.minibatch)
     b = layer.buffers(T, training=wl.backward, cfg=cfg)
     rt = b["routing"]
+    routings = ws_b = None
     mode = ("fwd+bwd (staged)" if wl.backward else
             f"{len(xs)} macro-batches, megakernel" if len(xs) > 1 else
             "staged kernels" if staged else "megakernel")
@@ -387,18 +406,18 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     clocks.wait_first()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
     st = mok.device_status(status_ws)
     if st[0] != mok.OK:
-        raise SystemExit(f"device status after warm-up: {st}")
+        raise SystemExit(f"{wl.name}: device status after warm-up: {st}")
 
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(5)) for _ in range(steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    for i in range(args.steps):
+    for i in range(steps):
         flush.zero_()
         s0, s1, g0, g1, x0 = evs[i]
         s0.record(stream)
@@ -438,24 +457,38 @@ def main():
     total_ms = sum(step_ms)
     st = mok.device_status(status_ws)
     if st[0] != mok.OK:
-        raise SystemExit(f"device status after timed steps: {st}")
-    tokens_per_step = T * len(xs)
+        raise SystemExit(f"{wl.name}: device status after timed steps: {st}")
 
     sm_partition = None
-    if args.trace and (not staged or len(xs) > 1):
-        sm_partition = trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings if len(xs) > 1 else None,
-                                  ws_b if len(xs) > 1 else None)
+    if trace and (not staged or len(xs) > 1):
+        sm_partition = trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b)
 
-    # end to end through the public API with host buffers: every step copies
-    # its inputs in from pinned host memory and its result back out; steps are
-    # pipelined the way a serving loop would run them (copy streams in and out
-    # beside the compute stream, two buffer slots), so the copies of steps i+1
-    # and i-1 overlap the kernels of step i
+    e2e = None
+    if with_e2e:
+        e2e = measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps)
+
+    # aggregate over ranks: the slowest rank's times
+    t_max, e2e_max = max_over_ranks([total_ms, e2e["ms"] if e2e else 0.0], dev)
+    return dict(wl=wl, dtype=dtype, steps=steps, warmup=warmup, total_ms=t_max, rank_total_ms=total_ms,
+                step_ms=step_ms, gemm_ms=gemm_ms, stage_lines=stage_lines, sm_partition=sm_partition, clocks=clk,
+                e2e=e2e, e2e_ms=e2e_max, launches_per_step=launches_per_step, flops=flops, kern=kern, mode=mode,
+                staged=staged, tokens_per_step=T * len(xs), batches=len(xs))
+
+
+def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps):
+    """End to end through the public API with host buffers: every step copies
+    its inputs in from pinned host memory and its result back out; steps are
+    pipelined the way a serving loop would run them (copy streams in and out
+    beside the compute stream, two buffer slots), so the copies of steps i+1
+    and i-1 overlap the kernels of step i."""
+    import torch
+    from combine_router_top_expert_gb300 import mok
+    T, H = wl.T, wl.H
     x_host = [torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory() for xb in inp.xs]
     dY_host = (torch.from_numpy(inp.dY.view(np.int16)).view(torch.bfloat16).pin_memory() if wl.backward else None)
     out_host = [[torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in xs] for _ in range(2)]
     x_slot = [[torch.empty_like(xb) for xb in xs] for _ in range(2)]
-    dY_slot = [torch.empty_like(dY) for _ in range(2)] if wl.backward else None
+    dY_slot = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in range(2)] if wl.backward else None
     out_slot = [[torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs] for _ in range(2)]
     grads_slot = None
     if wl.backward:
@@ -505,7 +538,7 @@ def main():
     for i in range(4):
         e2e_step(i % 2)
     torch.cuda.synchronize(dev)
-    n_e2e = max(8, args.steps)   # pipelined: amortise the first copy-in and last copy-out
+    n_e2e = max(8, steps)   # pipelined: amortise the first copy-in and last copy-out
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(c_in)
     for i in range(n_e2e):
@@ -513,28 +546,31 @@ def main():
     c_out.wait_event(ev_done[(n_e2e - 1) % 2])
     a1.record(c_out)
     torch.cuda.synchronize(dev)
-    e2e_ms = [a0.elapsed_time(a1)]
     if mok.device_status(status_ws)[0] != mok.OK:
-        raise SystemExit(f"device status after end-to-end steps: {mok.device_status(status_ws)}")
+        raise SystemExit(f"{wl.name}: device status after end-to-end steps: {mok.device_status(status_ws)}")
+    return dict(ms=a0.elapsed_time(a1), steps=n_e2e,
+                h2d=len(xs) * T * H * 2 * (2 if wl.backward else 1), d2h=len(xs) * T * H * 2,
+                api="mok_route_layout + " + ("mok_moe_forward(training) + mok_moe_backward" if wl.backward else
+                                             "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward"))
 
-    # aggregate over ranks: total tokens / max time
-    t_max, e2e_max = max_over_ranks([total_ms, sum(e2e_ms)], dev)
-    if rank != 0:
-        torch.distributed.destroy_process_group()
-        return
-    value = whole_job_rate(ws, tokens_per_step, args.steps, t_max)
-    e2e_val = whole_job_rate(ws, tokens_per_step, n_e2e, e2e_max)
+
+def roofline(m, args):
+    """The dominant kernels' roofline object of measurement `m`."""
+    from combine_router_top_expert_gb300 import mok
+    wl, dtype = m["wl"], m["dtype"]
     peaks = load_peaks()
+    H = wl.H
     # captured traffic belongs to the single-CTA stage kernels only
-    traffic = GEMM_PAIR_TRAFFIC.get(wl.name) if staged and len(xs) == 1 and not args.gemm_pairs else None
-    fl = flops
-    g_ms = statistics.mean(gemm_ms)
+    traffic, traffic_note = (captured_traffic(wl.name) if m["staged"] and m["batches"] == 1 and not args.gemm_pairs
+                             else (None, "not captured for this path"))
+    fl = m["flops"]
+    g_ms = statistics.mean(m["gemm_ms"])
     achieved = fl / (g_ms / 1000.0) / 1e12
-    long_region = total_ms > 1000.0
+    long_region = m["rank_total_ms"] > 1000.0
     peak = (peaks["bf16_sus"] if long_region else peaks["bf16"]) * (2.0 if dtype == mok.MXFP8 else 1.0)
     # the GEMM pair's algorithmic HBM bytes: expert weights (+ MXFP8 scales),
     # the gathered rows read, h written and read back, the partials written
-    R_rows = T * wl.k * len(xs)
+    R_rows = wl.T * wl.k * m["batches"]
     ebw = (1.0 + 1.0 / 32) if dtype == mok.MXFP8 else 2.0
     gemm_bytes = (3.0 * wl.E * H * wl.I * ebw + R_rows * H * ebw + 2.0 * R_rows * wl.I * ebw + R_rows * H * 2.0)
     if wl.backward:
@@ -542,48 +578,123 @@ def main():
     hbm_achieved = gemm_bytes / (g_ms / 1000.0) / 1e9 if gemm_bytes else None
     # the bound of the workload: whichever of FLOP / peak and bytes / HBM peak is longer
     hbm_bound = bool(gemm_bytes) and gemm_bytes / (peaks["hbm"] * 1e9) > fl / (peak * 1e12)
+    kern = m["kern"]
+    if hbm_bound:
+        return {"kernel": kern, "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": hbm_achieved / peaks["hbm"], "peak_source": f"{peaks['source']} hbm copy",
+                "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": traffic, "traffic_note": traffic_note,
+                "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}}
+    return {"kernel": kern, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
+                           (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
+            "flops_per_step": fl, "ms_per_step": g_ms, "traffic": traffic, "traffic_note": traffic_note,
+            "hbm": ({"achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": hbm_achieved / peaks["hbm"], "bytes_per_step": gemm_bytes} if gemm_bytes else None)}
+
+
+def config_of(m, args, ws):
+    wl = m["wl"]
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+            "operands": wl.dtype, "routing": "zipf s=1.2 bias" if wl.zipf_s else "uniform",
+            "macro_batches": m["batches"], "shared_expert_I": wl.shared_I, "ring_rows": wl.ring_rows or "default",
+            "mover_ctas": args.movers or 8, "path": m["mode"],
+            "minibatches": (("token ranges" if args.mb_token_ranges else "expert-tile runs")
+                            if (not m["staged"] or m["batches"] > 1) else None),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"}
+
+
+def e2e_of(m, ws):
+    e = m["e2e"]
+    return {"value": whole_job_rate(ws, m["tokens_per_step"], e["steps"], m["e2e_ms"]), "unit": "tokens/s",
+            "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"], "api": e["api"], "steps": e["steps"],
+            "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams overlap step i's kernels; "
+                          "no L2 flush (each step's working set, the expert weights, is larger than L2)"}
+
+
+# Sub-measurements of the default line: the metric's other halves ("fwd+bwd"
+# and MXFP8), on the same GPU in the same run.
+EXTRA_WORKLOADS = ("bf16_bwd_T4096", "mxfp8_zipf_T2560")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="bf16_fwd_T2560", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="mok", choices=["mok", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the fwd+bwd and MXFP8 sub-measurements of the default workload")
+    ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
+    ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
+    ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
+    ap.add_argument("--minibatch", type=int, default=0, help="megakernel minibatch tokens (0 = ring-limited)")
+    ap.add_argument("--mb-token-ranges", action="store_true",
+                    help="megakernel minibatches as token ranges (default: runs of expert tiles)")
+    ap.add_argument("--trace", action="store_true",
+                    help="megakernel: after the timed steps, one traced step; report the SM partition's busy/idle time")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from combine_router_top_expert_gb300 import mok
+
+    inp, layer = build_layer(wl, dev, rank)
+    m = measure(args, wl, inp, layer, dev, args.steps, args.warmup, trace=args.trace)
+    extras = []
+    if (args.workload == "bf16_fwd_T2560" and not args.no_extra and not args.megakernel and not args.gemm_pairs
+            and ws == 1):
+        # the same experts (same weight draw): BF16 fwd+bwd at T=4096 and the
+        # MXFP8 forward with Zipf-skewed routing at T=2560
+        del layer
+        torch.cuda.empty_cache()
+        for name in EXTRA_WORKLOADS:
+            wx = synth.WORKLOADS[name]
+            ix, lx = build_layer(wx, dev, rank, inp=inp)
+            mx = measure(args, wx, ix, lx, dev, max(20, args.steps // 4), max(3, args.warmup), with_e2e=True)
+            extras.append(mx)
+            del lx
+            torch.cuda.empty_cache()
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    value = whole_job_rate(ws, m["tokens_per_step"], m["steps"], m["total_ms"])
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if dtype == mok.BF16 else "mxfp8",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": m["steps"],
+        "warmup": m["warmup"], "ms_per_step": m["total_ms"] / m["steps"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if m["dtype"] == mok.BF16 else "mxfp8",
         "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "H": H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "operands": wl.dtype, "routing": "zipf s=1.2 bias" if wl.zipf_s else "uniform",
-                   "macro_batches": len(xs), "shared_expert_I": wl.shared_I, "ring_rows": wl.ring_rows or "default",
-                   "mover_ctas": args.movers or 8, "path": mode,
-                   "minibatches": ("token ranges" if args.mb_token_ranges else "expert-tile runs") if (not staged or len(xs) > 1) else None,
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": "flushed before every timed step (256 MiB write); per-step CUDA events"},
+        "config": config_of(m, args, ws),
         "gemm_cta_pairs": bool(args.gemm_pairs),
-        "roofline": ({"kernel": kern,
-                      "bound": "hbm", "achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                      "frac": hbm_achieved / peaks["hbm"], "peak_source": f"{peaks['source']} hbm copy",
-                      "bytes_per_step": gemm_bytes, "ms_per_step": g_ms, "traffic": traffic,
-                      "tensor": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak}}
-                     if hbm_bound else
-                     {"kernel": kern,
-                      "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                      "frac": achieved / peak,
-                      "peak_source": f"{peaks['source']} bf16 {'sustained' if long_region else 'burst'}" +
-                                     (" x2 (fp8 nominal ratio)" if dtype == mok.MXFP8 else ""),
-                      "flops_per_step": fl, "ms_per_step": g_ms, "traffic": traffic,
-                      "hbm": ({"achieved": hbm_achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                               "frac": hbm_achieved / peaks["hbm"], "bytes_per_step": gemm_bytes}
-                              if gemm_bytes else None)}),
-        "e2e": {"value": e2e_val, "unit": "tokens/s",
-                "h2d_bytes_per_step": tokens_per_step * H * 2 * (2 if wl.backward else 1),
-                "d2h_bytes_per_step": tokens_per_step * H * 2,
-                "api": "mok_route_layout + " + ("mok_moe_forward(training) + mok_moe_backward" if wl.backward else
-                                                "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward"),
-                "steps": n_e2e,
-                "pipelining": "H2D of step i+1 and D2H of step i-1 on two copy streams overlap step i's kernels; "
-                              "no L2 flush (each step's working set, the expert weights, is larger than L2)"},
-        "stage_rooflines": stage_lines,
-        "sm_partition": sm_partition,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
-        "stage_ms": {"step_median": statistics.median(step_ms), "timed_kernels_median": statistics.median(gemm_ms)},
+        "roofline": roofline(m, args),
+        "e2e": e2e_of(m, ws),
+        "stage_rooflines": m["stage_lines"],
+        "sm_partition": m["sm_partition"],
+        "gpu_launches": m["launches_per_step"] * m["steps"] + sum(x["launches_per_step"] * x["steps"]
+                                                                  for x in extras),
+        "clocks": m["clocks"],
+        "stage_ms": {"step_median": statistics.median(m["step_ms"]),
+                     "timed_kernels_median": statistics.median(m["gemm_ms"])},
     }
+    if extras:
+        line["also"] = [{"workload": x["wl"].name, "what": ("forward + backward" if x["wl"].backward else "forward"),
+                         "value": whole_job_rate(ws, x["tokens_per_step"], x["steps"], x["total_ms"]),
+                         "unit": "tokens/s", "ms_per_step": x["total_ms"] / x["steps"], "steps": x["steps"],
+                         "warmup": x["warmup"], "dtype": "bf16" if x["dtype"] == mok.BF16 else "mxfp8",
+                         "config": config_of(x, args, ws), "roofline": roofline(x, args), "e2e": e2e_of(x, ws),
+                         "stage_rooflines": x["stage_lines"], "clocks": x["clocks"],
+                         "gpu_launches": x["launches_per_step"] * x["steps"]} for x in extras]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, wl)
     print(json.dumps(line), flush=True)

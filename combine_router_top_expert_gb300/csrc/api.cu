@@ -525,8 +525,19 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
     return cuda_status(e);
 }
 
+mok_status mok_route_test_hook(int32_t withhold_copy, int32_t timeout_ms) {
+    if (timeout_ms < 0) return MOK_ERR_INVALID;
+    set_route_test_hook(withhold_copy != 0, (uint64_t)timeout_ms * 1000000ull);
+    return MOK_OK;
+}
+
 mok_status mok_device_status(const void* workspace, mok_stream_t stream, int32_t* detail, int32_t reset) {
-    if (!workspace) return MOK_ERR_INVALID;
+    if (!workspace) {
+        // the status block of mok_route_layout_static's array on this device
+        void* p = nullptr;
+        if (route_static_scratch(&p) != cudaSuccess || !p) return MOK_ERR_CUDA;
+        workspace = p;
+    }
     StatusBlock hb{};
     cudaStream_t s = (cudaStream_t)stream;
     if (cudaMemcpyAsync(&hb, workspace, sizeof(hb), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOK_ERR_CUDA;

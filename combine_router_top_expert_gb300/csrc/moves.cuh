@@ -10,6 +10,19 @@ size_t route_workspace_bytes(int T, int H, int E, int k);
 cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,
                                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
                                 int32_t* row_src, int32_t* slot_row, void* ws, cudaStream_t s);
+// Test hook of the routing kernels' bounded waits (process-wide): withhold
+// makes CTA 0 of the top-k kernel skip one copy so its wait runs out after
+// timeout_ns (0: the default limit).
+struct RouteTestHook {
+    int withhold;
+    uint64_t timeout_ns;
+};
+RouteTestHook route_test_hook();
+void set_route_test_hook(int withhold, uint64_t timeout_ns);
+// noalloc.cu: device address of the library's routing scratch array on the
+// current device (its first 256 bytes are the status block of
+// mok_route_layout_static)
+cudaError_t route_static_scratch(void** out);
 // W_r [H, E] -> `copies` identical copies of WrT [E, H], back to back.
 cudaError_t launch_transpose_wr(const float* W_r, float* WrT, int H, int E, int copies, cudaStream_t s);
 
@@ -47,7 +60,8 @@ struct GemmCommon {
     StatusBlock* status;
     unsigned long long timeout_ns;
     int num_sms;
-    int cluster;   // 2: grouped GEMMs run as CTA pairs sharing A tiles by multicast; 1: single CTAs
+    int cluster;   // 2: grouped GEMMs run as 2-SM CTA pairs (tcgen05 cta_group::2, B rows split
+                   // between the two CTAs, no multicast loads); 1: single CTAs
 };
 // Forward gate/up GEMM + SwiGLU. A: [rows, H] (bf16 or E4M3 + tile scales);
 // packed B: [E * 2I, H] (interleaved gate/up per il = BN/2 columns).

@@ -46,6 +46,10 @@ cudaError_t scratch_address(void** out) {
 
 }  // namespace
 
+namespace mok {
+cudaError_t route_static_scratch(void** out) { return scratch_address(out); }
+}  // namespace mok
+
 extern "C" mok_status mok_route_layout_static(const void* x, const float* W_r, const float* bias, int32_t T,
                                               int32_t H, int32_t E, int32_t k, int32_t* topk_idx, float* topk_w,
                                               int32_t* counts, int32_t* offsets, int32_t* row_src,
@@ -66,7 +70,10 @@ extern "C" mok_status mok_route_layout_static(const void* x, const float* W_r, c
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (major != 10 || minor != 3) return MOK_ERR_CUDA;
     // Every kernel writes its scratch (transposed router weights, block
-    // histograms) in full before reading it, so nothing is cleared here.
+    // histograms) in full before reading it; the 256-byte status block at the
+    // start of the array is cleared by the launch sequence itself, so a
+    // router wait that gives up in this call is what mok_device_status(NULL,
+    // ...) reports afterwards.
     cudaError_t e = launch_route_layout(x, W_r, bias, T, H, E, k, topk_idx, topk_w, counts, offsets, row_src,
                                         slot_row, scratch, (cudaStream_t)stream);
     return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;

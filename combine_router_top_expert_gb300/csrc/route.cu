@@ -106,7 +106,8 @@ template <int TW, int STAGES>
 __global__ void __launch_bounds__(kTopkThreads)
 route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr_copies, int wr_copies,
                   const float* __restrict__ bias, int T, int H, int E, int k, int32_t* __restrict__ topk_idx,
-                  float* __restrict__ topk_w, int32_t* __restrict__ hist, StatusBlock* st, uint64_t tmo) {
+                  float* __restrict__ topk_w, int32_t* __restrict__ hist, StatusBlock* st, uint64_t tmo,
+                  int withhold) {
     constexpr int TT = 2 * TW;
     constexpr int NT = kTopkThreads;
     static_assert(TT <= kRouteTTMax && TT >= kRouteTTMin && STAGES >= 3 && STAGES <= 16, "router tile");
@@ -139,9 +140,12 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
     int issued = 0, seen = 0;   // thread 0: chunks issued / chunks it has seen land
     // thread 0: the copies of chunk n into slot n % STAGES (nothing more
     // once one of its waits gave up)
+    // withhold (test hook): CTA 0 never issues chunk 1, so its wait runs out
+    const bool hold = withhold != 0 && blockIdx.x == 0;
     auto issue = [&](int n) {
         if (!ok || n >= total) return;
         issued = n + 1;
+        if (hold && n == 1) return;
         const int g = n / nchunks, c = n % nchunks, slot = n % STAGES;
         const int h0 = c * kRouteChunk, hw = min(kRouteChunk, H - h0);
         const uint32_t bar = bar0 + 8u * slot;
@@ -244,11 +248,18 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         // slot) land before the CTA exits, within the same time bound
         const uint64_t start = globaltimer_ns();
         for (int n = seen; n < issued; ++n)
-            while (!tc::mbar_try_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1)) &&
+            while (!(hold && n == 1) && !tc::mbar_try_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1)) &&
                    globaltimer_ns() - start < tmo) {
             }
     }
-    __syncthreads();
+    // after a give-up the logits of this CTA's tokens are incomplete: rank
+    // zeros instead, so the outputs stay valid routing (the lowest-index
+    // experts, distinct, equal weights) for whatever reads them before the
+    // caller sees the status
+    if (__syncthreads_or(!ok)) {
+        for (int i = tid; i < TT * E; i += NT) lg[i] = 0.f;
+        __syncthreads();
+    }
 
     // top-k per token: warp w takes tokens w, w + 8, ...
     const int nq = (E + 31) / 32;
@@ -397,13 +408,13 @@ cudaError_t launch_router_weight_layout(const float* W_r, float* dst, int H, int
 template <int TW, int STAGES>
 cudaError_t launch_topk_variant(const __nv_bfloat16* x, const float* Wr, int wr_copies, const float* bias, int T,
                                 int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* hist,
-                                StatusBlock* st, uint64_t timeout_ns, cudaStream_t s) {
+                                StatusBlock* st, uint64_t timeout_ns, int withhold, cudaStream_t s) {
     const size_t smem = route_topk_smem_bytes(2 * TW, STAGES, E, k);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     auto kern = route_topk_kernel<TW, STAGES>;
     if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
     kern<<<ceil_div(T, 2 * TW), kTopkThreads, smem, s>>>(x, Wr, wr_copies, bias, T, H, E, k, topk_idx, topk_w, hist,
-                                                         st, timeout_ns);
+                                                         st, timeout_ns, withhold);
     return cudaGetLastError();
 }
 
@@ -427,15 +438,22 @@ int route_tokens_per_cta(int T, int num_sms, int E, int k) {
 
 cudaError_t launch_route_topk(const __nv_bfloat16* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                               int tt, int32_t* topk_idx, float* topk_w, int32_t* hist, StatusBlock* st,
-                              uint64_t tmo, cudaStream_t s) {
+                              uint64_t tmo, int hold, cudaStream_t s) {
     const int r = route_wr_copies(E, H);
     if (tt == 28) return launch_topk_variant<14, kRouteStages(14)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist,
-                                                                   st, tmo, s);
-    if (tt == 18) return launch_topk_variant<9, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
-    if (tt == 8) return launch_topk_variant<4, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
-    if (tt == 4) return launch_topk_variant<2, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, s);
+                                                                   st, tmo, hold, s);
+    if (tt == 18) return launch_topk_variant<9, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
+    if (tt == 8) return launch_topk_variant<4, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
+    if (tt == 4) return launch_topk_variant<2, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
     return cudaErrorInvalidValue;
 }
+
+namespace {
+RouteTestHook g_route_hook{};
+}  // namespace
+
+RouteTestHook route_test_hook() { return g_route_hook; }
+void set_route_test_hook(int withhold, uint64_t timeout_ns) { g_route_hook = RouteTestHook{withhold, timeout_ns}; }
 
 cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,
                                 int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
@@ -457,8 +475,10 @@ cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bi
     const int nblocks = ceil_div(T, tt);
     err = launch_router_weight_layout(W_r, Wr, H, E, copies, s);
     if (err != cudaSuccess) return err;
+    const RouteTestHook hook = route_test_hook();
     err = launch_route_topk(static_cast<const __nv_bfloat16*>(x), Wr, bias, T, H, E, k, tt, topk_idx, topk_w, hist,
-                            static_cast<StatusBlock*>(ws), kRouteTimeoutNs, s);
+                            static_cast<StatusBlock*>(ws), hook.timeout_ns ? hook.timeout_ns : kRouteTimeoutNs,
+                            hook.withhold, s);
     // the layout kernel must never run on top-k results that were not produced
     if (err != cudaSuccess) return err;
     route_layout_kernel<<<nblocks, kRouteThreads, 0, s>>>(topk_idx, hist, T, E, k, tt, nblocks, counts, offsets,

@@ -26,7 +26,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches",
-           "mok_quantize_rows", "mok_dispatch_quantized"]
+           "mok_quantize_rows", "mok_dispatch_quantized", "mok_route_test_hook"]
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
@@ -112,12 +112,13 @@ def lib():
             L.mok_combine.argtypes = [PP, P, P, P, P, P]
             L.mok_moe_backward.argtypes = [PP, ctypes.POINTER(BwdArgs), PC, P]
             L.mok_device_status.argtypes = [P, P, ctypes.POINTER(I32), I32]
+            L.mok_route_test_hook.argtypes = [I32, I32]
             L.mok_status_string.argtypes = [I32]
             L.mok_status_string.restype = ctypes.c_char_p
             L.mok_version.restype = ctypes.c_char_p
             for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
                          "mok_moe_forward_batches", "mok_dispatch", "mok_quantize_rows", "mok_dispatch_quantized",
-                         "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status"):
+                         "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_route_test_hook"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -332,8 +333,14 @@ def megakernel_trace(workspace, n_ctas):
     return workspace[256:256 + 64 * n_ctas].view(torch.int64).view(n_ctas, 8).cpu().numpy()
 
 
+def route_test_hook(withhold_copy, timeout_ms=0):
+    """Test hook of the routing kernels' bounded waits (see mok.h)."""
+    _check(lib().mok_route_test_hook(int(withhold_copy), int(timeout_ms)), "mok_route_test_hook")
+
+
 def device_status(workspace, reset=False, stream=None):
-    """(status code, detail) recorded on the device by the last call."""
+    """(status code, detail) recorded on the device by the last call; with
+    workspace None, the last mok_route_layout_static call on this device."""
     d = ctypes.c_int32(0)
     rc = lib().mok_device_status(_ptr(workspace), _stream(stream), ctypes.byref(d), int(reset))
     return int(rc), int(d.value)

@@ -139,9 +139,14 @@ def make_inputs(wl: Workload, seed: int = 0, with_x: bool = True, shard: int = 0
     if with_x:
         inp.xs = [make_x(wl, b, seed, shard) for b in range(wl.batches)]
     if wl.backward:
-        gd = torch.Generator().manual_seed(seed + 1000 + SHARD_STRIDE * shard)
-        inp.dY = _normal_bf16(gd, (wl.T, wl.H), 1.0)
+        inp.dY = make_dY(wl, seed, shard)
     return inp
+
+
+def make_dY(wl: Workload, seed: int = 0, shard: int = 0) -> np.ndarray:
+    """Upstream gradient dY [T, H] ~ N(0, 1) rounded to BF16."""
+    gd = torch.Generator().manual_seed(seed + 1000 + SHARD_STRIDE * shard)
+    return _normal_bf16(gd, (wl.T, wl.H), 1.0)
 
 
 def bf16_to_f32(a: np.ndarray) -> np.ndarray:

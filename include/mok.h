@@ -354,7 +354,14 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
  *     call's contents; the kernels overwrite every byte they read, so nothing
  *     needs clearing, but calls that overlap on the same GPU (e.g. issued on
  *     different streams without ordering) race on the array: order them on
- *     one stream or with events. */
+ *     one stream or with events.
+ *   - Device-side waits are bounded as in mok_route_layout. A wait that gives
+ *     up is recorded in a 256-byte status block at the start of the array;
+ *     read it with mok_device_status(NULL, stream, &detail, reset) after the
+ *     call (MOK_ERR_TIMEOUT, detail 7: the routing outputs are then not the
+ *     routing of x). Each call clears that block when it starts, and all
+ *     calls on a device share it, so calls that overlap on the GPU also race
+ *     on their error reports: read the status before the next call. */
 mok_status mok_route_layout_static(const void* x, const float* W_r, const float* bias,
                                    int32_t T, int32_t H, int32_t E, int32_t k,
                                    int32_t* topk_idx, float* topk_w, int32_t* counts,
@@ -365,12 +372,24 @@ mok_status mok_route_layout_static(const void* x, const float* W_r, const float*
 /* Device status                                                               */
 /* ------------------------------------------------------------------------- */
 
-/* Synchronises `stream`, then returns the status the last forward/backward
- * using `workspace` recorded on the device (MOK_OK, MOK_ERR_TIMEOUT or
+/* Synchronises `stream`, then returns the status the last call using
+ * `workspace` recorded on the device (MOK_OK, MOK_ERR_TIMEOUT or
  * MOK_ERR_CAPACITY); *detail (if not NULL) receives a code naming the wait
- * that gave up. reset != 0 clears the word afterwards. */
+ * that gave up. reset != 0 clears the word afterwards. workspace == NULL
+ * reads the status of the last mok_route_layout_static call on the current
+ * device (the status block of the library's routing scratch array). */
 mok_status mok_device_status(const void* workspace, mok_stream_t stream, int32_t* detail,
                              int32_t reset);
+
+/* Test hook of the routing kernels' bounded waits, for both routing entry
+ * points: withhold_copy != 0 makes the first CTA of the top-k kernel skip one
+ * of its bulk copies in every following routing call, so its wait runs out
+ * after timeout_ms (0 = the default 4 s) and the call records
+ * MOK_ERR_TIMEOUT with detail 7 in its status block; the tokens of that CTA
+ * then get the lowest-index experts. withhold_copy = 0, timeout_ms = 0
+ * restores normal routing. Process-wide and not thread-safe: tests only.
+ * Returns MOK_ERR_INVALID for timeout_ms < 0. */
+mok_status mok_route_test_hook(int32_t withhold_copy, int32_t timeout_ms);
 
 /* Human-readable name of a status code (static string). */
 const char* mok_status_string(mok_status s);

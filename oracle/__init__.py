@@ -58,6 +58,7 @@ def lib():
                                            P, P, P, P, P]
             L.orc_moe_backward_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, I, P, I, P, P, I,
                                                    P, P, P, P]
+            L.orc_router_grad_columns.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P, P, I, P, I, P]
             L.orc_mx_quantize_rows.argtypes = [P, I64, I64, P, P]
             L.orc_mx_quantize_bf16_rows.argtypes = [P, I64, I64, P, P]
             L.orc_e4m3_value.argtypes = [ctypes.c_uint8]
@@ -281,3 +282,23 @@ def moe_backward_sampled(x, W_r, Wg, Wu, Wd, dY, routing, tokens, cols, mode=MOD
         _p(tok), len(tok), _p(ce), _p(ci), len(cols), _p(dX), _p(dWg), _p(dWu), _p(dWd))
     _check(rc, "moe_backward_sampled")
     return dX, dWg, dWu, dWd
+
+
+def router_grad_columns(x, Wg, Wu, Wd, dY, routing, experts, mode=MODE_BF16):
+    """dW_r[:, e] for each expert e in `experts` ([n, H] fp64), for inputs too
+    large for the full backward (runs every routed row of the tokens that
+    chose a listed expert)."""
+    x, Wg, Wu, Wd, dY = _inputs([x, Wg, Wu, Wd, dY], False)
+    T, H = x.shape
+    E, _, I = Wg.shape
+    k = routing["idx"].shape[1]
+    ce = np.ascontiguousarray(experts, dtype=np.int32)
+    out = np.empty((len(ce), H), np.float64)
+    rc = lib().orc_router_grad_columns(
+        _p(x), _p(Wg), _p(Wu), _p(Wd), _p(dY), T, H, I, E, k,
+        _p(np.ascontiguousarray(routing["idx"], dtype=np.int32)),
+        _p(np.ascontiguousarray(routing["w"], dtype=np.float64)),
+        _p(np.ascontiguousarray(routing["offsets"], dtype=np.int32)),
+        _p(np.ascontiguousarray(routing["row_src"], dtype=np.int32)), mode, _p(ce), len(ce), _p(out))
+    _check(rc, "router_grad_columns")
+    return out

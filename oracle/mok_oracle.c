@@ -853,6 +853,82 @@ int orc_moe_backward_sampled(const uint16_t* x, const float* W_r, const uint16_t
     return ORC_OK;
 }
 
+/* Columns dW_r[:, e] of the router gradient for the experts listed in
+ * `col_e` (n_col of them), computed for inputs too large for the full
+ * backward. The column of expert e sums x[t] * dl[t, j] over the tokens t
+ * whose slot j chose e, and dl[t, j] = w_j (gw_j - sum_i w_i gw_i) needs
+ * gw[t, i] = <dY[t], y[t, i]> for all k slots of such a token: so every
+ * routed row of every token that chose a listed expert is run through its
+ * expert (the forward's own row step, with the BF16 rounding of h in mode 0),
+ * expert by expert in layout order. Sums over tokens run in ascending token
+ * order. Inputs as in orc_moe_backward_sampled; out: dWr_cols [n_col, H]. */
+int orc_router_grad_columns(const uint16_t* x, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                            const uint16_t* dY, int T, int H, int I, int E, int k, const int32_t* idx,
+                            const double* w, const int32_t* offsets, const int32_t* row_src, int mode,
+                            const int32_t* col_e, int n_col, double* dWr_cols) {
+    if (mode != ORC_BF16 && mode != ORC_EXACT) return ORC_ERR;
+    for (int q = 0; q < n_col; ++q)
+        if (col_e[q] < 0 || col_e[q] >= E) return ORC_ERR;
+    unsigned char* need = (unsigned char*)calloc((size_t)(T > 0 ? T : 1), 1);
+    double* gw = (double*)calloc((size_t)T * k + 1, sizeof(double));
+    if (!need || !gw) { free(need); free(gw); return ORC_ERR; }
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j)
+            for (int q = 0; q < n_col; ++q)
+                if (idx[(long)t * k + j] == col_e[q]) need[t] = 1;
+    long HI = (long)H * I;
+    expert_w W;
+    if (alloc_expert(&W, HI)) { free(need); free(gw); return ORC_ERR; }
+    for (int e = 0; e < E; ++e) {
+        int r0 = offsets[e], r1 = offsets[e + 1];
+        int any = 0;
+        for (int r = r0; r < r1 && !any; ++r) any = need[row_src[r] / k];
+        if (!any) continue;
+        load_expert(Wg, Wu, Wd, 0, e, H, I, mode, &W);
+#pragma omp parallel
+        {
+            double* a = (double*)malloc(sizeof(double) * H);
+            double* G = (double*)malloc(sizeof(double) * I);
+            double* U = (double*)malloc(sizeof(double) * I);
+            double* hb = (double*)malloc(sizeof(double) * I);
+            double* y = (double*)malloc(sizeof(double) * H);
+#pragma omp for schedule(dynamic, 1)
+            for (int r = r0; r < r1; ++r) {
+                int slot = row_src[r];
+                int t = slot / k;
+                if (!need[t]) continue;
+                act_row(x, 0, t, H, ORC_BF16, a);
+                ffn_row(a, &W, H, I, mode, G, U, hb, y);
+                double g = 0.0;
+                for (int c = 0; c < H; ++c) g += bf16_to_f64(dY[(long)t * H + c]) * y[c];
+                gw[slot] = g;
+            }
+            free(a); free(G); free(U); free(hb); free(y);
+        }
+    }
+    free_expert(&W);
+    for (int q = 0; q < n_col; ++q) {
+        double* o = dWr_cols + (long)q * H;
+        for (int c = 0; c < H; ++c) o[c] = 0.0;
+    }
+    for (int t = 0; t < T; ++t) {
+        if (!need[t]) continue;
+        double m = 0.0;
+        for (int j = 0; j < k; ++j) m += w[(long)t * k + j] * gw[(long)t * k + j];
+        for (int j = 0; j < k; ++j) {
+            double dl = w[(long)t * k + j] * (gw[(long)t * k + j] - m);
+            for (int q = 0; q < n_col; ++q) {
+                if (idx[(long)t * k + j] != col_e[q]) continue;
+                double* o = dWr_cols + (long)q * H;
+                for (int c = 0; c < H; ++c) o[c] += bf16_to_f64(x[(long)t * H + c]) * dl;
+            }
+        }
+    }
+    free(need);
+    free(gw);
+    return ORC_OK;
+}
+
 /* Number of threads the OpenMP runtime will use. */
 int orc_num_threads(void) {
 #ifdef _OPENMP

@@ -30,7 +30,8 @@ def _check_routing(layer, ref, T, k):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["bf16_fwd_T2560", "mxfp8_zipf_T512", "mxfp8_zipf_T8192"])
+@pytest.mark.parametrize("name", ["bf16_fwd_T2560", "mxfp8_zipf_T512", "mxfp8_zipf_T2560", "mxfp8_zipf_T4096",
+                                  "mxfp8_zipf_T8192"])
 def test_fullsize_forward(name):
     wl = synth.WORKLOADS[name]
     inp = synth.make_inputs(wl)
@@ -75,12 +76,62 @@ def test_fullsize_backward_T4096():
     assert_close(gG, sG, c, "dW_gate columns")
     assert_close(gU, sU, c, "dW_up columns")
     assert_close(gD, sD, c, "dW_down rows")
-    # router gradient: each row of dW_r sums to zero (sum_j dl_j = 0 per token)
+    # router gradient: each row of dW_r sums to zero (sum_j dl_j = 0 per token),
+    # and the column of the least-loaded expert against the oracle's column
     dWr = g["dW_r"].double().cpu().numpy()
     assert np.max(np.abs(dWr.sum(1))) <= 1e-4 * np.abs(dWr).max() * wl.E
-    # bitwise determinism of every gradient
+    e_min = int(np.argmin(r["counts"]))
+    col = oracle.router_grad_columns(inp.x, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, [e_min])
+    assert_close(dWr[:, e_min][None], col, c, f"dW_r[:, {e_min}]", bf16_out=False)
+    # bitwise determinism of every gradient over ten runs
     first = {n: t.clone() for n, t in g.items()}
-    layer.forward(x, training=True)
-    again = layer.backward(x, dY)
-    for n in first:
-        assert torch.equal(again[n].view(torch.uint8), first[n].view(torch.uint8)), n
+    for _ in range(9):
+        layer.forward(x, training=True)
+        again = layer.backward(x, dY)
+        for n in first:
+            assert torch.equal(again[n].view(torch.uint8), first[n].view(torch.uint8)), n
+
+
+@pytest.mark.gpu
+def test_fullsize_ring_stream_16x4096():
+    """The 16-batch stream (T=4096 each, MXFP8 routed experts with Zipf-skewed
+    routing, one BF16 shared expert, a ring of 16384 rows = half the
+    worst-case routed rows) through one megakernel launch, as bench.py times
+    it: routing of the first and last batch bit for bit, sampled tokens of
+    both against the oracle (shared expert included), and a rerun bit for
+    bit."""
+    wl = synth.WORKLOADS["ring_stream_16x4096"]
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.MXFP8)
+    xs = [to_dev_bf16(xb) for xb in inp.xs]
+    routings = []
+    for xb in xs:
+        routings.append({n: v.clone() for n, v in layer.route(xb).items()})
+    p = layer.problem(wl.T)
+    cfg = mok.make_config(ring_rows=wl.ring_rows)
+    ws = mok.alloc_bytes(mok.workspace_size_batches(p, len(xs), cfg))
+    outs = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda") for _ in xs]
+    mok.moe_forward_batches(p, xs, layer.packed, routings, outs, ws, packed_shared=layer.packed_shared, cfg=cfg)
+    torch.cuda.synchronize()
+    assert mok.device_status(ws) == (mok.OK, 0)
+    first = [o.clone() for o in outs]
+    mok.moe_forward_batches(p, xs, layer.packed, routings, outs, ws, packed_shared=layer.packed_shared, cfg=cfg)
+    torch.cuda.synchronize()
+    for b in range(len(xs)):
+        assert torch.equal(outs[b].view(torch.int16), first[b].view(torch.int16)), b
+    xsel, got = [], []
+    for b in (0, len(xs) - 1):
+        ref_r = oracle.route(inp.xs[b], inp.W_r, wl.k, inp.bias)
+        g = {n: v.cpu().numpy() for n, v in routings[b].items()}
+        assert np.array_equal(g["topk_idx"], ref_r["idx"])
+        assert np.array_equal(g["counts"], ref_r["counts"])
+        assert np.array_equal(g["row_src"][:wl.R], ref_r["row_src"])
+        toks = _sample_tokens(wl.T, n=8, seed=b)
+        xsel.append(inp.xs[b][toks])
+        got.append(host_bf16_f64(first[b][toks]))
+    # each token's output depends on that token alone: route and run the
+    # sampled tokens of both batches as one small batch through the oracle
+    xcat = np.ascontiguousarray(np.concatenate(xsel))
+    r = oracle.route(xcat, inp.W_r, wl.k, inp.bias)
+    ref = oracle.moe_forward(xcat, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_MXFP8, shared=inp.shared)
+    assert_close(np.concatenate(got), ref, TOL[mok.MXFP8], "ring stream, batches 0 and 15")

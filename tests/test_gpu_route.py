@@ -76,3 +76,57 @@ def test_route_all_tokens_one_expert():
     ref = oracle.route(x, W_r, k, bias)
     assert ref["counts"][6] == T
     _compare(_run(x, W_r, k, bias), ref, T, k)
+
+
+@pytest.mark.gpu
+def test_route_follows_the_fixed_summation_order():
+    """The hand-built input of tests/golden/router_order.json, whose fp32
+    logits are (1, 2) only in the fixed chain/butterfly order (exact
+    arithmetic and chains over h mod 32 tie at (2, 2), which would rank
+    expert 0 first): the kernel must rank expert 1 first, with and without
+    the bias, and weight the two experts softmax(2, 1)."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "router_order.json")))
+    x = np.zeros((1, g["H"]), np.float32)
+    for h, v in g["x_nonzero"]:
+        x[0, h] = v
+    W = np.zeros((g["H"], g["E"]), np.float32)
+    for h, e, v in g["W_r_nonzero"]:
+        W[h, e] = v
+    xb = torch.tensor(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for bias in (None, np.array(g["bias"], np.float32)):
+        got = _run(xb, W, 2, bias)
+        assert got["topk_idx"][0].tolist() == g["k2"]["idx"]
+        if bias is None:
+            assert np.max(np.abs(got["topk_w"][0] - np.array(g["k2"]["w"]))) <= 1e-6
+        ref = oracle.route(xb, W, 2, bias)
+        _compare(got, ref, 1, 2)
+
+
+@pytest.mark.gpu
+def test_route_wait_that_gives_up_is_reported():
+    """A router copy withheld by the test hook: the chunk wait runs out after
+    the short limit, the workspace status reports MOK_ERR_TIMEOUT (detail 7)
+    and the outputs are still a valid layout; without the hook the same call
+    routes bit-exactly again."""
+    T, H, E, k = 700, 2048, 32, 8
+    g = torch.Generator().manual_seed(9)
+    x = synth._normal_bf16(g, (T, H), 1.0)
+    W_r = (torch.randn((H, E), generator=g) * 0.02).numpy()
+    xd, wd = to_dev_bf16(x), dev_f32(W_r)
+    ws = mok.alloc_bytes(mok.route_workspace_size(T, H, E, k))
+    mok.route_test_hook(1, timeout_ms=50)
+    try:
+        r = mok.route_layout(xd, wd, k, workspace=ws)
+        torch.cuda.synchronize()
+        assert mok.device_status(ws) == (mok.ERR_TIMEOUT, 7)
+        idx = r["topk_idx"].cpu().numpy()
+        assert idx.min() >= 0 and idx.max() < E and all(len(set(row)) == k for row in idx.tolist())
+        assert int(r["counts"].sum()) == T * k
+    finally:
+        mok.route_test_hook(0, 0)
+    r = mok.route_layout(xd, wd, k, workspace=ws)
+    torch.cuda.synchronize()
+    assert mok.device_status(ws) == (mok.OK, 0)
+    _compare({n: v.cpu().numpy() for n, v in r.items()}, oracle.route(x, W_r, k), T, k)

@@ -174,6 +174,36 @@ def test_router_logits_handle_ragged_H():
     assert np.array_equal(lg.astype(np.float64), bf16_val(x) @ W.astype(np.float64))
 
 
+def _router_order_inputs(g):
+    x = np.zeros((1, g["H"]), np.float32)
+    for h, v in g["x_nonzero"]:
+        x[0, h] = v
+    W = np.zeros((g["H"], g["E"]), np.float32)
+    for h, e, v in g["W_r_nonzero"]:
+        W[h, e] = v
+    return bf16_bits(x), W
+
+
+def test_router_logits_follow_the_fixed_order_hand_worked():
+    """Hand-worked fp32 logits (tests/golden/router_order.json) that only the
+    fixed chain/butterfly order gives: sequential sums, chains over h mod 32,
+    chains added in sequence, a reversed butterfly, the bias added first and
+    exact arithmetic each give another value."""
+    g = json.load(open(os.path.join(GOLDEN, "router_order.json")))
+    x, W = _router_order_inputs(g)
+    lg = oracle.router_logits(x, W)
+    assert lg[0].tolist() == g["logits"]
+    lgb = oracle.router_logits(x, W, np.array(g["bias"], np.float32))
+    assert lgb[0].tolist() == g["logits_with_bias"]
+    for name, v in g["other_readings"].items():   # the fixture tells the readings apart
+        assert v != (g["logits_with_bias"] if name == "bias_added_first" else g["logits"]), name
+    # the exact product sum differs from the fp32 result only by the absorbed +1
+    assert (bf16_val(x).astype(np.float64) @ W.astype(np.float64))[0].tolist() == g["other_readings"]["exact"]
+    r = oracle.route(x, W, 2)
+    assert r["idx"][0].tolist() == g["k2"]["idx"]
+    assert np.allclose(r["w"][0], g["k2"]["w"], rtol=1e-15)
+
+
 # ----------------------------------------------------------------------------- top-k, weights
 
 def _brute_topk(lg, k):
@@ -459,3 +489,44 @@ def test_sampled_backward_equals_full_backward():
         assert np.allclose(sG[q], dWg[e][:, i], rtol=1e-12, atol=1e-15)
         assert np.allclose(sU[q], dWu[e][:, i], rtol=1e-12, atol=1e-15)
         assert np.allclose(sD[q], dWd[e][i, :], rtol=1e-12, atol=1e-15)
+    # router-gradient columns one by one equal the full backward's
+    cw = oracle.router_grad_columns(inp.x, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, [2, 0])
+    assert np.allclose(cw[0], dWr[:, 2], rtol=1e-12, atol=1e-15 * np.abs(dWr).max())
+    assert np.allclose(cw[1], dWr[:, 0], rtol=1e-12, atol=1e-15 * np.abs(dWr).max())
+
+
+def _golden_backward_case(g):
+    x = bf16_bits(g["x"])
+    Wg, Wu, Wd = (bf16_bits(g[n]) for n in ("W_gate", "W_up", "W_down"))
+    dY = bf16_bits(g["dY"])
+    W_r = np.array(g["W_r"], np.float32)
+    idx = np.array(g["idx"], np.int32)
+    counts, offsets, row_src, slot_row = oracle.layout(idx, W_r.shape[1])
+    routing = dict(idx=idx, w=np.array(g["w"], np.float64), offsets=offsets, row_src=row_src)
+    return x, W_r, Wg, Wu, Wd, dY, routing
+
+
+@pytest.mark.parametrize("mode,key", [(oracle.MODE_BF16, "bf16"), (oracle.MODE_EXACT, "exact")])
+def test_backward_operand_rounding_hand_worked(mode, key):
+    """Hand-worked backward (tests/golden/backward_bf16_rounding.json) whose
+    values move when any one of the BF16 roundings of dy, dG or dU is dropped
+    or applied to another intermediate (dh instead of dG, say); every value is
+    a dyadic rational, so the comparison is exact."""
+    g = json.load(open(os.path.join(GOLDEN, "backward_bf16_rounding.json")))
+    x, W_r, Wg, Wu, Wd, dY, r = _golden_backward_case(g)
+    dX, dWg, dWu, dWd, dWr = oracle.moe_backward(x, W_r, Wg, Wu, Wd, dY, r, mode=mode)
+    exp = g[key]
+    assert dX.tolist() == exp["dX"]
+    assert dWg.tolist() == exp["dW_gate"]
+    assert dWu.tolist() == exp["dW_up"]
+    assert dWd.tolist() == exp["dW_down"]
+    assert dWr.tolist() == exp["dW_r"]
+    if key == "bf16":
+        # the sampled form of the backward follows the same roundings
+        sX, sG, sU, sD = oracle.moe_backward_sampled(x, W_r, Wg, Wu, Wd, dY, r, [0], [(0, 0), (1, 0)])
+        assert sX.tolist() == exp["dX"]
+        assert sG.tolist() == [[v[0] for v in exp["dW_gate"][e]] for e in (0, 1)]
+        assert sU.tolist() == [[v[0] for v in exp["dW_up"][e]] for e in (0, 1)]
+        assert sD.tolist() == [exp["dW_down"][e][0] for e in (0, 1)]
+        cw = oracle.router_grad_columns(x, Wg, Wu, Wd, dY, r, [0, 1])
+        assert cw.tolist() == [[row[0] for row in exp["dW_r"]], [row[1] for row in exp["dW_r"]]]

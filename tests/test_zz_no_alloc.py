@@ -42,6 +42,55 @@ def test_static_scratch_routing_matches_workspace_routing_twice():
         assert torch.equal(got["topk_w"].view(torch.int32), ref["topk_w"].view(torch.int32))
         o = oracle.route(x, W_r, c["k"], bias)
         assert np.array_equal(got["topk_idx"].cpu().numpy(), o["idx"])
+        assert mok.device_status(None) == (mok.OK, 0)
+
+
+@pytest.mark.gpu
+def test_static_scratch_calls_leave_device_memory_unchanged():
+    """After the first call (which looks up the array's address), further
+    calls allocate nothing: the device's free memory does not move."""
+    T, H, E, k = 2560, 7168, 32, 8
+    x, W_r, _ = _inputs(T, H, E, 3)
+    xd, wd = to_dev_bf16(x), dev_f32(W_r)
+    out = mok.route_layout_static(xd, wd, k)           # first call: outputs allocated here
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(5):
+        mok.route_layout_static(xd, wd, k, out=out)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert mok.device_status(None) == (mok.OK, 0)
+
+
+@pytest.mark.gpu
+def test_static_scratch_reports_a_router_wait_that_gave_up():
+    """The status block of the library's array is readable through
+    mok_device_status(NULL): a router copy withheld by the test hook makes a
+    wait run out, the call reports MOK_ERR_TIMEOUT (detail 7, the router's
+    chunk wait) and still returns valid routing arrays; the next call without
+    the hook clears the report and routes correctly again."""
+    T, H, E, k = 1000, 7168, 32, 8
+    x, W_r, _ = _inputs(T, H, E, 4)
+    xd, wd = to_dev_bf16(x), dev_f32(W_r)
+    mok.route_test_hook(1, timeout_ms=50)
+    try:
+        got = mok.route_layout_static(xd, wd, k)
+        torch.cuda.synchronize()
+        assert mok.device_status(None) == (mok.ERR_TIMEOUT, 7)
+        # the withheld CTA's tokens fall back to the lowest-index experts, so
+        # the arrays stay a valid layout
+        idx = got["topk_idx"].cpu().numpy()
+        assert idx.min() >= 0 and idx.max() < E
+        assert all(len(set(row)) == k for row in idx.tolist())
+        assert int(got["counts"].sum()) == T * k
+    finally:
+        mok.route_test_hook(0, 0)
+    ref = mok.route_layout(xd, wd, k)
+    got = mok.route_layout_static(xd, wd, k)
+    torch.cuda.synchronize()
+    assert mok.device_status(None) == (mok.OK, 0)
+    assert torch.equal(got["topk_idx"], ref["topk_idx"])
+    assert torch.equal(got["row_src"][:T * k], ref["row_src"][:T * k])
 
 
 @pytest.mark.gpu
