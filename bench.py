@@ -613,6 +613,74 @@ def e2e_of(m, ws):
                           "no L2 flush (each step's working set, the expert weights, is larger than L2)"}
 
 
+def torch_composed_forward(x, W_r, bias, Wg, Wu, Wd, k):
+    """The same layer written with stock PyTorch ops on the GPU, the way an
+    MoE layer is commonly composed in PyTorch: router matmul (fp32), top-k,
+    softmax over the selected logits, a stable sort of the routed rows by
+    expert, index_select gather, one cuBLAS matmul per expert and projection
+    (SwiGLU between), then the weighted index_add_ back into token order.
+    Context arm only (a stand-in for the "PyTorch" baseline class the pages
+    compare against); the routing of exact ties may differ from the fixed
+    order of the library's router."""
+    import torch
+    import torch.nn.functional as F
+    T, H = x.shape
+    E = W_r.shape[1]
+    logits = x.float() @ W_r
+    if bias is not None:
+        logits = logits + bias
+    val, idx = torch.topk(logits, k, dim=1)
+    w = torch.softmax(val, dim=1)
+    flat = idx.reshape(-1)
+    order = torch.argsort(flat, stable=True)
+    tok = order // k
+    counts = torch.bincount(flat, minlength=E).tolist()      # host sync, as in the usual loop form
+    xs = x.index_select(0, tok)
+    ys = torch.empty_like(xs)
+    s0 = 0
+    for e in range(E):
+        s1 = s0 + counts[e]
+        if s1 > s0:
+            a = xs[s0:s1]
+            h = F.silu(a @ Wg[e]) * (a @ Wu[e])
+            ys[s0:s1] = h @ Wd[e]
+        s0 = s1
+    out = torch.zeros((T, H), dtype=torch.float32, device=x.device)
+    out.index_add_(0, tok, ys.float() * w.reshape(-1)[order, None])
+    return out.to(torch.bfloat16)
+
+
+def measure_torch_composed(wl, inp, dev, steps, warmup):
+    """tokens/s of torch_composed_forward on the workload (BF16, CUDA events
+    per step, L2 flushed before each)."""
+    import torch
+    from combine_router_top_expert_gb300.layer import to_dev_bf16
+    x = to_dev_bf16(inp.x, dev)
+    W_r = torch.from_numpy(np.ascontiguousarray(inp.W_r)).to(dev)
+    bias = None if inp.bias is None else torch.from_numpy(inp.bias).to(dev)
+    Wg, Wu, Wd = (to_dev_bf16(a, dev) for a in (inp.Wg, inp.Wu, inp.Wd))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        torch_composed_forward(x, W_r, bias, Wg, Wu, Wd, wl.k)
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        torch_composed_forward(x, W_r, bias, Wg, Wu, Wd, wl.k)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms.append(e0.elapsed_time(e1))
+    del Wg, Wu, Wd
+    torch.cuda.empty_cache()
+    med = statistics.median(ms)
+    return {"what": "the same layer composed of stock PyTorch ops (index_select gather, one cuBLAS matmul per "
+                    "expert and projection, index_add_ combine), BF16, same inputs; context only",
+            "value": wl.T / (med / 1e3), "unit": "tokens/s", "ms_per_step": med, "steps": steps,
+            "torch": torch.__version__}
+
+
 # Sub-measurements of the default line: the metric's other halves ("fwd+bwd"
 # and MXFP8), on the same GPU in the same run.
 EXTRA_WORKLOADS = ("bf16_bwd_T4096", "mxfp8_zipf_T2560")
@@ -666,6 +734,9 @@ def main():
             extras.append(mx)
             del lx
             torch.cuda.empty_cache()
+    torch_arm = None
+    if args.workload == "bf16_fwd_T2560" and not args.no_extra and ws == 1:
+        torch_arm = measure_torch_composed(wl, inp, dev, 20, 3)
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
@@ -695,6 +766,8 @@ def main():
                          "config": config_of(x, args, ws), "roofline": roofline(x, args), "e2e": e2e_of(x, ws),
                          "stage_rooflines": x["stage_lines"], "clocks": x["clocks"],
                          "gpu_launches": x["launches_per_step"] * x["steps"]} for x in extras]
+    if torch_arm is not None:
+        line["context_torch_composed"] = torch_arm
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, wl)
     print(json.dumps(line), flush=True)

@@ -14,10 +14,12 @@ constexpr int kDefaultTimeoutMs = 4000;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Gate/up columns interleaved per this many columns in the packed weights
-// (half the N-tile of the gate/up GEMM).
+// Gate/up rows interleaved per this many rows in the packed weights. BF16:
+// 16, so any 32 consecutive packed rows hold the gate and up rows of the same
+// 16 features (one TMEM lane quadrant of a tile whose rows are weight rows
+// sees both). MXFP8: half the 256-wide N-tile of the gate/up GEMM.
 int gu_interleave(int I, int dtype) {
-    (void)dtype;
+    if (dtype == MOK_BF16) return 16;
     return 2 * I >= 256 ? 128 : 64;
 }
 
@@ -162,6 +164,16 @@ GemmCommon make_common(void* ws, const mok_config* cfg) {
     return c;
 }
 
+// BF16 inference GEMMs run on swapped-operand pair tiles (weight rows as M,
+// token tiles of any multiple of 16 rows as N) unless the caller asks for the
+// 128-row token tiles (MOK_FLAG_ROW_TILES) or their 2-SM pairs.
+bool use_swap(const mok_problem* p, const mok_config* cfg, bool training) {
+    if (p->dtype != MOK_BF16 || training) return false;
+    if (cfg && (cfg->flags & (MOK_FLAG_ROW_TILES | MOK_FLAG_GEMM_PAIRS))) return false;
+    return swap_supported(p->H, p->I);
+}
+int swap_policy(const mok_config* cfg) { return (cfg && (cfg->flags & MOK_FLAG_TOKEN_TILES_256)) ? 1 : 0; }
+
 // Routing arrays present (the per-token ones may be empty when T == 0).
 bool routing_ok(const mok_routing* r, int32_t T = 1) {
     return r && r->counts && r->offsets &&
@@ -304,9 +316,17 @@ mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf,
     PackedLayout L = packed_layout(p->E, p->H, p->I, p->dtype);
     const char* pk = static_cast<const char*>(packed);
     const int64_t rows = padded_rows_max(p->T, p->E, p->k);
-    cudaError_t e = gemm_gateup(mx, A, static_cast<const uint8_t*>(A_sf), pk + L.gu,
-                                reinterpret_cast<const uint8_t*>(pk + L.gu_sf), p->E, p->H, p->I, r->counts, 0, rows,
-                                h, static_cast<uint8_t*>(h_sf), nullptr, c, s);
+    cudaError_t e;
+    if (use_swap(p, cfg, false)) {
+        e = gemm_gateup_swap(A, pk + L.gu, p->E, p->H, p->I, r->counts, rows, h, swap_policy(cfg), c, s);
+        if (e == cudaSuccess)
+            e = gemm_down_swap(h, pk + L.dn, p->E, p->H, p->I, r->counts, r->offsets, r->row_src, rows, partials,
+                               swap_policy(cfg), c, s);
+        return cuda_status(e);
+    }
+    e = gemm_gateup(mx, A, static_cast<const uint8_t*>(A_sf), pk + L.gu,
+                    reinterpret_cast<const uint8_t*>(pk + L.gu_sf), p->E, p->H, p->I, r->counts, 0, rows,
+                    h, static_cast<uint8_t*>(h_sf), nullptr, c, s);
     if (e == cudaSuccess)
         e = gemm_down(mx, h, static_cast<const uint8_t*>(h_sf), pk + L.dn, reinterpret_cast<const uint8_t*>(pk + L.dn_sf),
                       p->E, p->H, p->I, r->counts, r->offsets, r->row_src, 0, rows, partials, c, s);
@@ -443,12 +463,19 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     if (e == cudaSuccess && mx && !training)
         e = launch_dispatch_q(ws + L.xq, ws + L.xsf, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A,
                               A_sf, s);
-    if (e == cudaSuccess)
-        e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H, p->I,
-                        r.counts, 0, rows, h, h_sf, gu, c, s);
-    if (e == cudaSuccess)
-        e = gemm_down(mx, h, h_sf, pk + PL.dn, reinterpret_cast<const uint8_t*>(pk + PL.dn_sf), p->E, p->H, p->I,
-                      r.counts, r.offsets, r.row_src, 0, rows, partials, c, s);
+    if (e == cudaSuccess && use_swap(p, cfg, training)) {
+        e = gemm_gateup_swap(A, pk + PL.gu, p->E, p->H, p->I, r.counts, rows, h, swap_policy(cfg), c, s);
+        if (e == cudaSuccess)
+            e = gemm_down_swap(h, pk + PL.dn, p->E, p->H, p->I, r.counts, r.offsets, r.row_src, rows, partials,
+                               swap_policy(cfg), c, s);
+    } else {
+        if (e == cudaSuccess)
+            e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H,
+                            p->I, r.counts, 0, rows, h, h_sf, gu, c, s);
+        if (e == cudaSuccess)
+            e = gemm_down(mx, h, h_sf, pk + PL.dn, reinterpret_cast<const uint8_t*>(pk + PL.dn_sf), p->E, p->H, p->I,
+                          r.counts, r.offsets, r.row_src, 0, rows, partials, c, s);
+    }
     float* shared = nullptr;
     if (e == cudaSuccess && p->I_shared > 0) {
         PackedLayout SL = packed_layout(1, p->H, p->I_shared, MOK_BF16);

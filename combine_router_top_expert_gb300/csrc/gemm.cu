@@ -9,6 +9,7 @@
 #include <utility>
 
 #include "gemm.cuh"
+#include "gemm_swap.cuh"
 #include "moves.cuh"
 
 namespace mok {
@@ -118,6 +119,45 @@ template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const GemmParams& p,
                 int64_t tiles_ub, int num_sms, cudaStream_t s) {
     return run<BN, MX, MN, EPI, S, ACC, CLN>(a, b, b2, b, b, p, tiles_ub, num_sms, s);
+}
+
+// Swapped-operand pair kernel: persistent clusters of two CTAs.
+template <int EPI, int S>
+cudaError_t run_swap(const CUtensorMap& w, const CUtensorMap& x, const SwapParams& p, int num_sms, cudaStream_t s) {
+    using C = SwapCfg<S>;
+    auto kern = grouped_gemm_swap_kernel<EPI, S>;
+    ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = s;
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        clusters = num_sms / 2;
+    }
+    clusters = std::min(clusters, num_sms / 2);
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(2 * clusters);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, w, x, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+SwapParams swap_params(const GemmCommon& c, int policy) {
+    SwapParams p{};
+    p.status = c.status;
+    p.timeout_ns = c.timeout_ns;
+    p.tile_policy = policy;
+    return p;
 }
 
 GemmParams base_params(const GemmCommon& c) {
@@ -236,6 +276,45 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
         return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+}
+
+bool swap_supported(int H, int I) { return I % 128 == 0 && H % 256 == 0 && H % 64 == 0; }
+
+cudaError_t gemm_gateup_swap(const void* A, const void* Bgu, int E, int H, int I, const int32_t* counts,
+                             int64_t a_rows, void* h, int policy, const GemmCommon& c, cudaStream_t s) {
+    if (!swap_supported(H, I)) return cudaErrorInvalidValue;
+    SwapParams p = swap_params(c, policy);
+    p.E = E;
+    p.num_kb = H / 64;
+    p.m_tiles = 2 * I / 256;
+    p.w_rows_per_expert = 2 * I;
+    p.counts = counts;
+    p.out = h;
+    p.ldo = I;
+    CUtensorMap tw, tx;
+    if (!make_tmap(&tw, Bgu, (int64_t)E * 2 * I, H, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tx, A, a_rows, H, 2, 64, 64)) return cudaErrorInvalidValue;
+    return run_swap<kSwapSwiGLU, 6>(tw, tx, p, c.num_sms, s);
+}
+
+cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, const int32_t* counts,
+                           const int32_t* offsets, const int32_t* row_src, int64_t a_rows, void* out, int policy,
+                           const GemmCommon& c, cudaStream_t s) {
+    if (!swap_supported(H, I)) return cudaErrorInvalidValue;
+    SwapParams p = swap_params(c, policy);
+    p.E = E;
+    p.num_kb = I / 64;
+    p.m_tiles = H / 256;
+    p.w_rows_per_expert = H;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.row_src = row_src;
+    p.out = out;
+    p.ldo = H;
+    CUtensorMap tw, tx;
+    if (!make_tmap(&tw, Bdn, (int64_t)E * H, I, 2, 64, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tx, h, a_rows, I, 2, 64, 64)) return cudaErrorInvalidValue;
+    return run_swap<kSwapScatter, 6>(tw, tx, p, c.num_sms, s);
 }
 
 cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I, const int32_t* counts,

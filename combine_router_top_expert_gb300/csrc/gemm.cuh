@@ -182,6 +182,33 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
+// Gate and up pre-activations of 32 consecutive h columns of a gate/up tile
+// (tile-local h columns c0 .. c0+31) from the accumulator at tbase. The
+// packed weights interleave gate and up rows per `il` rows: BF16 packs 16
+// (tile columns 32g .. 32g+15 are gate, 32g+16 .. 32g+31 up, of the same
+// 16 features), MXFP8 packs half the 256-wide tile (gate columns 0..127,
+// up 128..255).
+template <int BN, bool IL16>
+__device__ __forceinline__ void load_gate_up(uint32_t tbase, int c0, uint32_t (&gr)[32], uint32_t (&ur)[32]) {
+    if constexpr (IL16) {
+        uint32_t a[32], b[32];
+        tc::tmem_ld_32x32b_x32(tbase + 2 * c0, a);
+        tc::tmem_ld_32x32b_x32(tbase + 2 * c0 + 32, b);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            gr[i] = a[i];
+            ur[i] = a[16 + i];
+            gr[16 + i] = b[i];
+            ur[16 + i] = b[16 + i];
+        }
+    } else {
+        tc::tmem_ld_32x32b_x32(tbase + c0, gr);
+        tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c0, ur);
+        tc::tmem_ld_wait();
+    }
+}
+
 // 2-SM pairs: pair tile g covers m-tiles 2mp and 2mp+1 of one expert (n
 // fastest-varying after mp, as for single tiles); CTA `rank` takes m-tile
 // 2mp + rank. An expert with an odd number of m-tiles leaves the last pair's
@@ -577,9 +604,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
                     uint32_t gr[32], ur[32];
-                    tc::tmem_ld_32x32b_x32(tbase + c0, gr);
-                    tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c0, ur);
-                    tc::tmem_ld_wait();
+                    load_gate_up<BN, !MX>(tbase, c0, gr, ur);
                     const int hc = ti.n * (BN / 2) + c0;
                     float hv[32];
 #pragma unroll

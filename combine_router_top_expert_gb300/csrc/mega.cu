@@ -1072,9 +1072,7 @@ mega_kernel(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ 
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
                     uint32_t gr[32], ur[32];
-                    tc::tmem_ld_32x32b_x32(tbase + c0, gr);
-                    tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c0, ur);
-                    tc::tmem_ld_wait();
+                    load_gate_up<BN, !MX>(tbase, c0, gr, ur);
                     const int hc = t.n * (BN / 2) + c0;
                     float hv[32];
 #pragma unroll

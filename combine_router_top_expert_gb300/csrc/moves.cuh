@@ -69,6 +69,17 @@ struct GemmCommon {
 cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
                         int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows,
                         void* h, uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s);
+// BF16 inference forward with the operands swapped (gemm_swap.cuh): weight
+// rows as the M side of 2-SM pair tiles, token tiles of any multiple of 32
+// rows as N. h [a_rows, I] (rows of the padded layout; only routed rows are
+// written); down pushes each routed row to out[row_src[...]] (bf16).
+// policy: SwapTilePolicy. Needs I % 128 == 0 and H % 256 == 0.
+bool swap_supported(int H, int I);
+cudaError_t gemm_gateup_swap(const void* A, const void* Bgu, int E, int H, int I, const int32_t* counts,
+                             int64_t a_rows, void* h, int policy, const GemmCommon& c, cudaStream_t s);
+cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, const int32_t* counts,
+                           const int32_t* offsets, const int32_t* row_src, int64_t a_rows, void* out, int policy,
+                           const GemmCommon& c, cudaStream_t s);
 // Forward down GEMM; rows pushed to out[row_src[...]] (bf16) or, for
 // identity_rows > 0, out[row] as f32.
 // MXFP8 quantisation of each row of x [T, H] (the codes the dispatch writes):

@@ -32,6 +32,8 @@ FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
 FLAG_TRACE = 4
 FLAG_MB_TOKEN_RANGES = 8
+FLAG_ROW_TILES = 16
+FLAG_TOKEN_TILES_256 = 32
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 

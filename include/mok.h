@@ -112,6 +112,18 @@ typedef struct {
  * expert-contiguous layout (padded once per expert over the whole batch),
  * and a batch's weighted sums run once all of its minibatches are done. */
 #define MOK_FLAG_MB_TOKEN_RANGES 8
+/* BF16 inference forward on 128-row token tiles (the tokens as the M side of
+ * the tensor-core tiles, each expert's rows padded to whole tiles). By
+ * default the BF16 inference GEMMs swap the operands: the weight rows are the
+ * M side of 2-SM pair tiles (256 rows over two CTAs) and an expert's tokens
+ * are cut into tiles of any multiple of 32 rows up to 256 as the N side, so
+ * no tensor work is spent on padded rows and no CTA of a pair idles
+ * (needs I % 128 == 0 and H % 256 == 0; other shapes use the token tiles).
+ * The training forward (saved != NULL) and MXFP8 use the token tiles. */
+#define MOK_FLAG_ROW_TILES 16
+/* Swapped-operand tiles: cut each expert's tokens into tiles of 256 rows
+ * plus one remainder tile, instead of ceil(n/256) tiles of about equal size. */
+#define MOK_FLAG_TOKEN_TILES_256 32
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use

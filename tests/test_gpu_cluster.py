@@ -36,7 +36,7 @@ def test_cluster_pairs_forward_bitwise(wl):
     x = to_dev_bf16(inp.x)
     layer.route(x)
     pairs = _staged(layer, x, wl.T, mok.FLAG_GEMM_PAIRS)
-    single = _staged(layer, x, wl.T)
+    single = _staged(layer, x, wl.T, mok.FLAG_ROW_TILES)
     assert torch.equal(pairs.view(torch.int16), single.view(torch.int16))
 
 
@@ -82,7 +82,7 @@ def test_last_tiles_of_at_most_64_rows():
           "offsets": dev(offsets), "row_src": dev(order), "slot_row": dev(order)}
     p = layer.problem(T)
     outs = []
-    for flags in (0, mok.FLAG_GEMM_PAIRS):
+    for flags in (mok.FLAG_ROW_TILES, mok.FLAG_GEMM_PAIRS):
         cfg = mok.make_config(flags=flags)
         ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
         out = torch.empty((T, wl.H), dtype=torch.bfloat16, device="cuda")

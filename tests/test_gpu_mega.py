@@ -34,10 +34,14 @@ def _forward(layer, x, cfg, T):
 
 
 def _staged(layer, x, T):
+    """The stage kernels on 128-row token tiles, the tile shapes the
+    megakernel runs."""
     p = layer.problem(T)
-    ws = mok.alloc_bytes(mok.workspace_size(p))
+    cfg = mok.make_config(flags=mok.FLAG_ROW_TILES)
+    ws = mok.alloc_bytes(mok.workspace_size(p, cfg))
     out = torch.empty((T, layer.H), dtype=torch.bfloat16, device="cuda")
-    mok.moe_forward(p, x, layer.packed, layer.buffers(T)["routing"], out, ws, packed_shared=layer.packed_shared)
+    mok.moe_forward(p, x, layer.packed, layer.buffers(T)["routing"], out, ws, packed_shared=layer.packed_shared,
+                    cfg=cfg)
     torch.cuda.synchronize()
     return out
 
