@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmok.so")
-SOURCES = ["api.cu", "route.cu", "moves.cu", "gemm.cu", "noalloc.cu", "mega.cu"]
+SOURCES = ["api.cu", "route.cu", "moves.cu", "gemm.cu", "noalloc.cu", "mega.cu", "ep.cu"]
 HEADERS = ["common.cuh", "tc.cuh", "gemm.cuh", "gemm_swap.cuh", "moves.cuh", "plan.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v" if os.environ.get("MOK_PTXAS_V") else "-O3",

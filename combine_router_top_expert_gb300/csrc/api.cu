@@ -172,7 +172,7 @@ bool use_swap(const mok_problem* p, const mok_config* cfg, bool training) {
     if (cfg && (cfg->flags & (MOK_FLAG_ROW_TILES | MOK_FLAG_GEMM_PAIRS))) return false;
     return swap_supported(p->H, p->I);
 }
-int swap_policy(const mok_config* cfg) { return (cfg && (cfg->flags & MOK_FLAG_TOKEN_TILES_256)) ? 1 : 0; }
+int swap_policy(const mok_config* cfg) { return (cfg && (cfg->flags & MOK_FLAG_TOKEN_TILES_BALANCED)) ? 1 : 0; }
 
 // Routing arrays present (the per-token ones may be empty when T == 0).
 bool routing_ok(const mok_routing* r, int32_t T = 1) {

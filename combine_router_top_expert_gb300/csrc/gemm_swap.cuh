@@ -8,9 +8,9 @@
 // (tcgen05 cta_group::2) holds 256 weight rows (128 per CTA) as the A operand
 // and N tokens (N/2 per CTA) as the B operand, with N any multiple of 32 up
 // to 256 (the M=256 pair shape is used with N in steps of 32 only). An
-// expert's tokens are cut into tiles of about equal size, so at most 31 rows
-// of tensor work per expert are spent on padding (not a whole 128-row tile)
-// and no CTA of a pair is idle; the accumulator holds one weight row per TMEM lane and one token
+// expert's tokens are cut into tiles of 256 and one remainder tile, so at most
+// 31 rows of tensor work per expert are spent on padding (not a whole 128-row
+// tile) and no CTA of a pair is idle; the accumulator holds one weight row per TMEM lane and one token
 // per column.
 //
 // CTA layout (clusters of two CTAs, persistent over pair tiles):
@@ -39,9 +39,12 @@ namespace mok {
 
 enum SwapEpi : int { kSwapSwiGLU = 0, kSwapScatter = 1 };
 
-// Token tiles of an expert: balanced (rows split into ceil(n/256) tiles of
-// about equal size, each a multiple of 32) or 256 rows plus a remainder.
-enum SwapTilePolicy : int { kTilesBalanced = 0, kTiles256 = 1 };
+// Token tiles of an expert: 256 rows plus a remainder (default), or ceil(n/256)
+// tiles of about equal size, each a multiple of 32. Measured: a pair tile's
+// time follows the bytes its stages load (128 weight rows and up to 128 token
+// rows per CTA and K block), not its N, so tiles narrower than 256 tokens
+// cost nearly a full tile; the remainder cut loads fewer token rows.
+enum SwapTilePolicy : int { kTiles256 = 0, kTilesBalanced = 1 };
 
 struct SwapParams {
     int E;

@@ -26,14 +26,15 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_workspace_size", "mok_saved_size", "mok_moe_forward", "mok_padded_rows_max", "mok_dispatch",
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches",
-           "mok_quantize_rows", "mok_dispatch_quantized", "mok_route_test_hook"]
+           "mok_quantize_rows", "mok_dispatch_quantized", "mok_route_test_hook", "mok_ep_workspace_size",
+           "mok_ep_dispatch", "mok_ep_push"]
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
 FLAG_TRACE = 4
 FLAG_MB_TOKEN_RANGES = 8
 FLAG_ROW_TILES = 16
-FLAG_TOKEN_TILES_256 = 32
+FLAG_TOKEN_TILES_BALANCED = 32
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 
@@ -74,6 +75,12 @@ class BwdArgs(ctypes.Structure):
                 ("ws_bytes", ctypes.c_size_t)]
 
 
+class EpPeer(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("row_src", ctypes.c_void_p),
+                ("partials", ctypes.c_void_p), ("T", ctypes.c_int32)]
+
+
+EP_MAX_RANKS = 8
 _lock = threading.Lock()
 _lib = None
 
@@ -115,12 +122,18 @@ def lib():
             L.mok_moe_backward.argtypes = [PP, ctypes.POINTER(BwdArgs), PC, P]
             L.mok_device_status.argtypes = [P, P, ctypes.POINTER(I32), I32]
             L.mok_route_test_hook.argtypes = [I32, I32]
+            L.mok_ep_workspace_size.argtypes = [I32, I32]
+            L.mok_ep_workspace_size.restype = SZ
+            L.mok_ep_dispatch.argtypes = [I32, I32, I32, I32, I32, ctypes.POINTER(EpPeer), P, P, ctypes.c_int64, P, P,
+                                          P, P, P, P, SZ, P]
+            L.mok_ep_push.argtypes = [I32, I32, I32, I32, ctypes.POINTER(EpPeer), P, ctypes.c_int64, P, P, P, P]
             L.mok_status_string.argtypes = [I32]
             L.mok_status_string.restype = ctypes.c_char_p
             L.mok_version.restype = ctypes.c_char_p
             for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
                          "mok_moe_forward_batches", "mok_dispatch", "mok_quantize_rows", "mok_dispatch_quantized",
-                         "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_route_test_hook"):
+                         "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_route_test_hook",
+                         "mok_ep_dispatch", "mok_ep_push"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -352,3 +365,33 @@ def check_device_status(workspace, what="device", stream=None):
     rc, d = device_status(workspace, stream=stream)
     if rc != OK:
         raise MokError(rc, f"{what} (detail {d})")
+
+
+# --------------------------------------------------------------------------- expert parallelism
+
+def ep_workspace_size(G, E) -> int:
+    return int(lib().mok_ep_workspace_size(G, E))
+
+
+def _peers(peers):
+    arr = (EpPeer * len(peers))()
+    for i, q in enumerate(peers):
+        arr[i] = EpPeer(q["x"].data_ptr() if q.get("x") is not None else None, q["offsets"].data_ptr(),
+                        q["row_src"].data_ptr() if q.get("row_src") is not None else None,
+                        q["partials"].data_ptr() if q.get("partials") is not None else None, int(q["T"]))
+    return arr
+
+
+def ep_dispatch(G, rank, H, E, k, peers, counts_all, A, rows_cap, counts_local, offsets_local, src_rank, src_slot,
+                ident, workspace, stream=None):
+    """peers: list of G dicts {x, offsets, row_src, partials, T} (device tensors)."""
+    rc = lib().mok_ep_dispatch(G, rank, H, E, k, _peers(peers), _ptr(counts_all), _ptr(A), int(rows_cap),
+                               _ptr(counts_local), _ptr(offsets_local), _ptr(src_rank), _ptr(src_slot), _ptr(ident),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "mok_ep_dispatch")
+
+
+def ep_push(G, H, E, k, peers, ys, rows_cap, offsets_local, src_rank, src_slot, stream=None):
+    rc = lib().mok_ep_push(G, H, E, k, _peers(peers), _ptr(ys), int(rows_cap), _ptr(offsets_local), _ptr(src_rank),
+                           _ptr(src_slot), _stream(stream))
+    _check(rc, "mok_ep_push")

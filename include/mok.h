@@ -116,14 +116,16 @@ typedef struct {
  * the tensor-core tiles, each expert's rows padded to whole tiles). By
  * default the BF16 inference GEMMs swap the operands: the weight rows are the
  * M side of 2-SM pair tiles (256 rows over two CTAs) and an expert's tokens
- * are cut into tiles of any multiple of 32 rows up to 256 as the N side, so
- * no tensor work is spent on padded rows and no CTA of a pair idles
+ * are cut into tiles of 256 rows and one remainder tile (a multiple of 32
+ * rows) as the N side, so little tensor work is spent on padded rows and no
+ * CTA of a pair idles
  * (needs I % 128 == 0 and H % 256 == 0; other shapes use the token tiles).
  * The training forward (saved != NULL) and MXFP8 use the token tiles. */
 #define MOK_FLAG_ROW_TILES 16
-/* Swapped-operand tiles: cut each expert's tokens into tiles of 256 rows
- * plus one remainder tile, instead of ceil(n/256) tiles of about equal size. */
-#define MOK_FLAG_TOKEN_TILES_256 32
+/* Swapped-operand tiles: cut each expert's tokens into ceil(n/256) tiles of
+ * about equal size (multiples of 32) instead of tiles of 256 rows plus one
+ * remainder tile (the default; measured faster). */
+#define MOK_FLAG_TOKEN_TILES_BALANCED 32
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use
@@ -336,6 +338,67 @@ typedef struct {
  * (written by TMA stores), workspace and saved 1024-B aligned. */
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
                             const mok_config* cfg, mok_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Expert parallelism across ranks ([K-ja] 02: experts spread over GPUs, the  */
+/* expert side pulls the token rows it needs, results are pushed back to the  */
+/* tokens' slots; [RW] "Rebuilding the MoE layer around communication").      */
+/* ------------------------------------------------------------------------- */
+
+#define MOK_EP_MAX_RANKS 8
+
+/* One rank's buffers as this process reaches them (device pointers usable in
+ * this process: on one GPU ordinary allocations; across the GPUs of a node,
+ * pointers that map the peer's allocation, e.g. opened CUDA IPC handles). */
+typedef struct {
+    const void* x;            /* [T, H] bf16: the rank's tokens */
+    const int32_t* offsets;   /* [E+1]: the rank's routing layout over all E experts */
+    const int32_t* row_src;   /* [T*k]: the rank's expert-ordered row -> slot t*k+j */
+    void* partials;           /* [T*k, H] bf16: the rank's slot buffer (mok_ep_push writes it) */
+    int32_t T;                /* the rank's tokens */
+} mok_ep_peer;
+
+/* Workspace bytes of mok_ep_dispatch (0 for invalid G, E). */
+size_t mok_ep_workspace_size(int32_t G, int32_t E);
+
+/* Rank `rank` of G owns experts [rank*E/G, (rank+1)*E/G) (E % G == 0). After
+ * every rank routed its own tokens over all E experts (mok_route_layout) and
+ * the per-rank counts were all-gathered into counts_all [G, E] int32 (device,
+ * rank-major; the caller's collective also orders this call after every
+ * rank's routing), this call
+ *   - lays out the local experts' rows: local expert l gets counts_local[l] =
+ *     sum_s counts_all[s][rank*E/G + l] rows, ordered by source rank s, then
+ *     by the source's own layout order; offsets_local [E/G+1] (unpadded);
+ *   - pulls each row from its source: A[padded row] = x_s[t] with t*k+j =
+ *     row_src_s[offsets_s[e] + r], in the padded expert-contiguous layout of
+ *     mok_dispatch (each local expert's segment starts on a 128-row
+ *     boundary; pad rows are not written);
+ *   - records src_rank[row] = s, src_slot[row] = t*k+j, ident[row] = row for
+ *     the push and for the down GEMM's scatter.
+ * Then run mok_expert_ffn with the local problem {T = rows_cap, k = 1,
+ * E = E/G, H, I} and routing {counts_local, offsets_local, row_src = ident}
+ * (the other routing pointers only need to be non-NULL), writing y rows in
+ * local row order into `ys` (its partials), then mok_ep_push. peers: host
+ * array of G entries (entry `rank` is this rank's own buffers). rows_cap >=
+ * sum_s T_s*k + 128*E/G rows of A; src_rank, src_slot and ident hold
+ * rows_cap entries. Rows whose source layout disagrees with counts_all are
+ * skipped (src_rank -1). Plain loads only: no TMA or multicast touches peer
+ * memory. */
+mok_status mok_ep_dispatch(int32_t G, int32_t rank, int32_t H, int32_t E, int32_t k,
+                           const mok_ep_peer* peers, const int32_t* counts_all, void* A,
+                           int64_t rows_cap, int32_t* counts_local, int32_t* offsets_local,
+                           int32_t* src_rank, int32_t* src_slot, int32_t* ident, void* workspace,
+                           size_t ws_bytes, mok_stream_t stream);
+
+/* Push-combine: every local row's result ys[row] ([rows_cap, H] bf16, local
+ * row order; rows < offsets_local[E/G]) is stored into
+ * peers[src_rank[row]].partials at slot src_slot[row] (plain 16-byte
+ * stores; rows marked -1 by the dispatch are skipped). Once every rank's
+ * push is done (the caller's barrier), each rank sums its own slots with
+ * mok_combine. */
+mok_status mok_ep_push(int32_t G, int32_t H, int32_t E, int32_t k, const mok_ep_peer* peers,
+                       const void* ys, int64_t rows_cap, const int32_t* offsets_local,
+                       const int32_t* src_rank, const int32_t* src_slot, mok_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Routing without a caller workspace. The pages have no counterpart: this    */

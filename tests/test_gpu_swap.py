@@ -44,9 +44,9 @@ def test_swapped_tiles_match_oracle_and_both_cuts(wl):
     x = to_dev_bf16(inp.x)
     layer.route(x)
     bal = _forward(layer, x, wl.T, 0)
-    t256 = _forward(layer, x, wl.T, mok.FLAG_TOKEN_TILES_256)
+    bal2 = _forward(layer, x, wl.T, mok.FLAG_TOKEN_TILES_BALANCED)
     rows = _forward(layer, x, wl.T, mok.FLAG_ROW_TILES)
-    assert torch.equal(bal.view(torch.int16), t256.view(torch.int16))
+    assert torch.equal(bal.view(torch.int16), bal2.view(torch.int16))
     r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
     ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_BF16, shared=inp.shared)
     assert_close(host_bf16_f64(bal), ref, TOL[mok.BF16], wl.name)
@@ -73,8 +73,8 @@ def test_swapped_tiles_edge_counts():
     rt = {"topk_idx": dev(idx), "topk_w": dev(np.ones((T, 1), np.float32)), "counts": dev(np.array(counts, np.int32)),
           "offsets": dev(offsets), "row_src": dev(order), "slot_row": dev(order)}
     bal = _forward(layer, x, T, 0, rt)
-    t256 = _forward(layer, x, T, mok.FLAG_TOKEN_TILES_256, rt)
-    assert torch.equal(bal.view(torch.int16), t256.view(torch.int16))
+    bal2 = _forward(layer, x, T, mok.FLAG_TOKEN_TILES_BALANCED, rt)
+    assert torch.equal(bal.view(torch.int16), bal2.view(torch.int16))
     r = {"idx": idx, "w": np.ones((T, 1)), "offsets": offsets, "row_src": order}
     ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_BF16)
     assert_close(host_bf16_f64(bal), ref, TOL[mok.BF16], "edge counts")

@@ -1,7 +1,9 @@
 """The PyTorch-composed layer that bench.py times beside the library as a
 context arm computes the same layer: on tokens whose top-k experts agree
-with the oracle's fixed-order routing, its output is within the BF16
-tolerance of the oracle."""
+with the oracle's fixed-order routing, its output is close to the oracle.
+Stock BF16 ops round more intermediates than the library does (G, U,
+silu(G), h and every expert output y each to BF16, against h alone), so the
+bar is 5e-2 * rms rather than the library's 2e-2."""
 import numpy as np
 import pytest
 import torch
@@ -28,4 +30,4 @@ def test_torch_composed_layer_matches_oracle():
     same = np.array([set(a) == set(b) for a, b in zip(torch.topk(lg, wl.k, dim=1).indices.cpu().numpy().tolist(),
                                                       r["idx"].tolist())])
     assert same.mean() > 0.99
-    assert_close(host_bf16_f64(out)[same], ref[same], 2e-2, "torch-composed layer")
+    assert_close(host_bf16_f64(out)[same], ref[same], 5e-2, "torch-composed layer")
