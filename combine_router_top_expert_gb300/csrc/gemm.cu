@@ -77,6 +77,36 @@ bool make_tmap_out3d(CUtensorMap* m, void* base, int E, int64_t rows, int64_t wi
     return r == CUDA_SUCCESS;
 }
 
+// Clusters of two CTAs that can be resident at once for kernel `kern` with
+// launch configuration `cfg` (dynamic shared memory and block size fixed per
+// kernel), queried once per device and kernel: the occupancy query is a
+// driver call that measured slow when another process polled the GPU.
+int max_pair_clusters(const void* kern, cudaLaunchConfig_t cfg, int num_sms) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(dev, kern);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return std::min(it->second, num_sms / 2);
+    }
+    int dev_sms = 0;
+    cudaDeviceGetAttribute(&dev_sms, cudaDevAttrMultiProcessorCount, dev);
+    cfg.gridDim = dim3(2 * (dev_sms / 2));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        clusters = dev_sms / 2;
+    }
+    {
+        std::lock_guard<std::mutex> g(mu);
+        cache[key] = clusters;
+    }
+    return std::min(clusters, num_sms / 2);
+}
+
 template <int BN, bool MX, bool MN, int EPI, int S, int ACC, int CLN = 1>
 cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& sa,
                 const CUtensorMap& sb, const GemmParams& p, int64_t tiles_ub, int num_sms, cudaStream_t s) {
@@ -97,13 +127,7 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         // persistent: as many CTA pairs as can be resident at once
-        cfg.gridDim = dim3(2 * ((num_sms + 1) / 2));
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-            cudaGetLastError();
-            clusters = num_sms / 2;
-        }
-        clusters = std::min(clusters, num_sms / 2);
+        const int clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), cfg, num_sms);
         grid = 2 * (int)std::min<int64_t>((tiles_ub + 1) / 2, clusters);
     } else {
         grid = (int)std::min<int64_t>(tiles_ub, num_sms);
@@ -138,13 +162,7 @@ cudaError_t run_swap(const CUtensorMap& w, const CUtensorMap& x, const SwapParam
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = s;
-    cfg.gridDim = dim3(2 * (num_sms / 2));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess || clusters < 1) {
-        cudaGetLastError();
-        clusters = num_sms / 2;
-    }
-    clusters = std::min(clusters, num_sms / 2);
+    const int clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), cfg, num_sms);
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(2 * clusters);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, w, x, p);
