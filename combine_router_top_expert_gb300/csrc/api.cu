@@ -118,6 +118,9 @@ BwdLayout bwd_layout(const mok_problem* p) {
 mok_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
 
 constexpr int kDefaultMovers = 8;
+// The grouped GEMMs' producers prefetch the weight box this many K blocks
+// ahead of its load into L2 (beyond the shared-memory ring).
+constexpr int kL2PrefetchBlocks = 8;
 
 // Megakernel tiles: gate/up 256 wide (gate 128 | up 128), down as the staged
 // down GEMM (down_tile_n).
@@ -161,6 +164,7 @@ GemmCommon make_common(void* ws, const mok_config* cfg) {
     if (cfg && cfg->num_sms > 0) n = std::min(n, (int)cfg->num_sms);
     c.num_sms = n > 0 ? n : 1;
     c.cluster = (cfg && (cfg->flags & MOK_FLAG_GEMM_PAIRS)) ? 2 : 1;
+    c.l2_prefetch = (cfg && (cfg->flags & MOK_FLAG_NO_L2_PREFETCH)) ? 0 : kL2PrefetchBlocks;
     return c;
 }
 

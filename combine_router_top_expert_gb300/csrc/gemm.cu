@@ -175,12 +175,14 @@ SwapParams swap_params(const GemmCommon& c, int policy) {
     p.status = c.status;
     p.timeout_ns = c.timeout_ns;
     p.tile_policy = policy;
+    p.l2_prefetch = c.l2_prefetch;
     return p;
 }
 
 GemmParams base_params(const GemmCommon& c) {
     GemmParams p{};
     p.b_split_kb = 1 << 30;
+    p.l2_prefetch = c.l2_prefetch;
     p.status = c.status;
     p.timeout_ns = c.timeout_ns;
     return p;

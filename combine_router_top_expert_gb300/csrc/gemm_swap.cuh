@@ -57,6 +57,7 @@ struct SwapParams {
     void* out;              // SwiGLU: h [rows, ldo] bf16; scatter: partials [T*k, ldo] bf16
     int ldo;
     int tile_policy;
+    int l2_prefetch;        // K blocks ahead of the load at which the weight box is prefetched into L2 (0: off)
     StatusBlock* status;
     unsigned long long timeout_ns;
 };
@@ -201,13 +202,28 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
             int last_par[STAGES];
             for (int s = 0; s < STAGES; ++s) last_par[s] = -1;
             bool ok = true;
+            const int pf = p.l2_prefetch;
             for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
                 const SwapTile t = swap_decode(p, sched, gi);
                 const int half = t.N / 2;                 // token rows of this CTA (multiple of 16)
                 const int nb = half > 64 ? 2 : 1;         // 64-row boxes
                 const int wrow = t.e * p.w_rows_per_expert + t.m * 256 + rank * 128;
                 const int xrow = t.row0 + rank * half;
+                // weight rows of this CTA's next tile, for the prefetches that run past this one
+                int wnext = -1;
+                if (pf > 0 && gi + gstep < gtotal) {
+                    const SwapTile tn = swap_decode(p, sched, gi + gstep);
+                    wnext = tn.e * p.w_rows_per_expert + tn.m * 256 + rank * 128;
+                }
+                if (pf > 0 && gi == gstart)
+                    for (int kb = 0; kb < pf && kb < p.num_kb; ++kb) tc::tma_prefetch_2d(&tmW, kb * 64, wrow);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (pf > 0) {
+                        // the weight box pf K blocks ahead: this tile's, or the next tile's first ones
+                        if (kb + pf < p.num_kb) tc::tma_prefetch_2d(&tmW, (kb + pf) * 64, wrow);
+                        else if (wnext >= 0 && wnext != wrow && kb + pf - p.num_kb < p.num_kb)
+                            tc::tma_prefetch_2d(&tmW, (kb + pf - p.num_kb) * 64, wnext);
+                    }
                     if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
                     const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
                     if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2u * (C::kBytesA + nb * 8192u));

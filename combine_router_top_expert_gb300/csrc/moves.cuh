@@ -60,6 +60,7 @@ struct GemmCommon {
     StatusBlock* status;
     unsigned long long timeout_ns;
     int num_sms;
+    int l2_prefetch;   // K blocks ahead at which the GEMM producers prefetch weight boxes into L2 (0: off)
     int cluster;   // 2: grouped GEMMs run as 2-SM CTA pairs (tcgen05 cta_group::2, B rows split
                    // between the two CTAs, no multicast loads); 1: single CTAs
 };

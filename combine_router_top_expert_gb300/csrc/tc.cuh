@@ -74,6 +74,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// Prefetch of one tile box into L2 (no shared memory, no completion): a
+// later tma_load_2d of the same box then reads from L2 instead of DRAM.
+__device__ __forceinline__ void tma_prefetch_2d(const void* tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // CTA-pair (cta_group::2) tile load: data lands in this CTA's shared memory
 // at dst, completion is signalled on the mbarrier at `bar`, a shared::cluster
 // address that may be the peer CTA's (the pair's leader collects both halves).

@@ -126,6 +126,10 @@ typedef struct {
  * about equal size (multiples of 32) instead of tiles of 256 rows plus one
  * remainder tile (the default; measured faster). */
 #define MOK_FLAG_TOKEN_TILES_BALANCED 32
+/* The grouped GEMMs' TMA producers prefetch each weight box into L2 several
+ * K blocks ahead of its load (beyond the shared-memory ring, into the next
+ * tile at a tile's end); this flag turns the prefetches off. */
+#define MOK_FLAG_NO_L2_PREFETCH 64
 /* Test hook: a mover withholds the publish of the last 8-row chunk of the
  * first minibatch, so the tiles waiting for it give up after timeout_ms and
  * the call reports MOK_ERR_TIMEOUT (exercises the bounded waits; never use
