@@ -147,7 +147,8 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
 
 // Swapped-operand pair kernel: persistent clusters of two CTAs.
 template <int EPI, int S>
-cudaError_t run_swap(const CUtensorMap& w, const CUtensorMap& x, const SwapParams& p, int num_sms, cudaStream_t s) {
+cudaError_t run_swap(const CUtensorMap& w, const CUtensorMap& x64, const CUtensorMap& x32, const CUtensorMap& x16,
+                     const SwapParams& p, int num_sms, cudaStream_t s) {
     using C = SwapCfg<S>;
     auto kern = grouped_gemm_swap_kernel<EPI, S>;
     ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
@@ -165,7 +166,7 @@ cudaError_t run_swap(const CUtensorMap& w, const CUtensorMap& x, const SwapParam
     const int clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), cfg, num_sms);
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(2 * clusters);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, w, x, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, w, x64, x32, x16, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -182,7 +183,6 @@ SwapParams swap_params(const GemmCommon& c, int policy) {
 GemmParams base_params(const GemmCommon& c) {
     GemmParams p{};
     p.b_split_kb = 1 << 30;
-    p.l2_prefetch = c.l2_prefetch;
     p.status = c.status;
     p.timeout_ns = c.timeout_ns;
     return p;
@@ -311,10 +311,12 @@ cudaError_t gemm_gateup_swap(const void* A, const void* Bgu, int E, int H, int I
     p.counts = counts;
     p.out = h;
     p.ldo = I;
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx64, tx32, tx16;
     if (!make_tmap(&tw, Bgu, (int64_t)E * 2 * I, H, 2, 64, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tx, A, a_rows, H, 2, 64, 64)) return cudaErrorInvalidValue;
-    return run_swap<kSwapSwiGLU, 6>(tw, tx, p, c.num_sms, s);
+    if (!make_tmap(&tx64, A, a_rows, H, 2, 64, 64) || !make_tmap(&tx32, A, a_rows, H, 2, 64, 32) ||
+        !make_tmap(&tx16, A, a_rows, H, 2, 64, 16))
+        return cudaErrorInvalidValue;
+    return run_swap<kSwapSwiGLU, 6>(tw, tx64, tx32, tx16, p, c.num_sms, s);
 }
 
 cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, const int32_t* counts,
@@ -331,10 +333,12 @@ cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, 
     p.row_src = row_src;
     p.out = out;
     p.ldo = H;
-    CUtensorMap tw, tx;
+    CUtensorMap tw, tx64, tx32, tx16;
     if (!make_tmap(&tw, Bdn, (int64_t)E * H, I, 2, 64, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tx, h, a_rows, I, 2, 64, 64)) return cudaErrorInvalidValue;
-    return run_swap<kSwapScatter, 6>(tw, tx, p, c.num_sms, s);
+    if (!make_tmap(&tx64, h, a_rows, I, 2, 64, 64) || !make_tmap(&tx32, h, a_rows, I, 2, 64, 32) ||
+        !make_tmap(&tx16, h, a_rows, I, 2, 64, 16))
+        return cudaErrorInvalidValue;
+    return run_swap<kSwapScatter, 6>(tw, tx64, tx32, tx16, p, c.num_sms, s);
 }
 
 cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I, const int32_t* counts,

@@ -55,7 +55,6 @@ struct GemmParams {
     const uint8_t* a_sf;
     const uint8_t* b_sf;
     int sf_kchunks;         // 128-wide K chunks per row tile (= K / 128)
-    int l2_prefetch;        // K blocks ahead of the load at which the B (weight) box is prefetched into L2 (0: off)
     StatusBlock* status;
     unsigned long long timeout_ns;
 };
@@ -380,8 +379,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     } else {
                         tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
                         const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
-                        if (p.l2_prefetch > 0 && kb + p.l2_prefetch < p.b_split_kb && kb + p.l2_prefetch < ti.num_kb)
-                            tc::tma_prefetch_2d(&tmB, (kb + p.l2_prefetch) * C::kBK, brow);
                         if (kb < p.b_split_kb)
                             tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kb * C::kBK, brow);
                         else

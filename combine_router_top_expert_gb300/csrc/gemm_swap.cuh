@@ -16,7 +16,9 @@
 // CTA layout (clusters of two CTAs, persistent over pair tiles):
 //   warp 0     TMA producer (both CTAs): this CTA's 128 weight rows and its
 //              N/2 token rows of each 64-element K block, signalling the
-//              leader's full barrier
+//              leader's full barrier; it also prefetches the weight box
+//              l2_prefetch K blocks ahead into L2 (beyond the shared-memory
+//              ring, into the next tile at a tile's end)
 //   warp 1     allocates tensor memory; in the leader, one lane issues the
 //              M=256 MMAs into a double-buffered fp32 accumulator
 //   warps 2-5  epilogue (both CTAs): tcgen05.ld of this CTA's 128 lanes,
@@ -139,10 +141,13 @@ __device__ __forceinline__ SwapTile swap_decode(const SwapParams& p, const SwapS
 
 template <int EPI, int STAGES>
 __global__ void __launch_bounds__(SwapCfg<STAGES>::kThreads, 1)
-grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX64,
+                         const __grid_constant__ CUtensorMap tmX32, const __grid_constant__ CUtensorMap tmX16,
                          const SwapParams p) {
     // tmW: packed weights [E * w_rows_per_expert, K], boxes of 64 x 128 rows;
-    // tmX: token rows [rows, K], boxes of 64 x 64 rows; both 128-byte swizzled
+    // tmX64/32/16: token rows [rows, K] in boxes of 64 x 64, 32 and 16 rows, so
+    // a CTA loads exactly its N/2 token rows (a multiple of 16) in at most
+    // four copies; all 128-byte swizzled
     using C = SwapCfg<STAGES>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ SwapSched sched;
@@ -178,7 +183,9 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tmap(&tmW);
-        tc::prefetch_tmap(&tmX);
+        tc::prefetch_tmap(&tmX64);
+        tc::prefetch_tmap(&tmX32);
+        tc::prefetch_tmap(&tmX16);
     }
     if (warp == 1) {
         tc::tmem_alloc_2sm(tc::smem_u32(&s_tmem_base), C::kTmemCols);
@@ -206,7 +213,6 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
             for (int gi = gstart; gi < gtotal && ok; gi += gstep) {
                 const SwapTile t = swap_decode(p, sched, gi);
                 const int half = t.N / 2;                 // token rows of this CTA (multiple of 16)
-                const int nb = half > 64 ? 2 : 1;         // 64-row boxes
                 const int wrow = t.e * p.w_rows_per_expert + t.m * 256 + rank * 128;
                 const int xrow = t.row0 + rank * half;
                 // weight rows of this CTA's next tile, for the prefetches that run past this one
@@ -226,10 +232,17 @@ grouped_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_c
                     }
                     if (!tc::mbar_wait(empty_bar(stage), ph ^ 1u, st, tmo, kSiteProducerEmpty)) { ok = false; break; }
                     const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
-                    if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2u * (C::kBytesA + nb * 8192u));
+                    if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2u * (C::kBytesA + (uint32_t)half * 128u));
                     tc::tma_load_2d_2sm(a_tile(stage), &tmW, lead_full, kb * 64, wrow);
-                    for (int j = 0; j < nb; ++j)
-                        tc::tma_load_2d_2sm(b_tile(stage) + j * 8192, &tmX, lead_full, kb * 64, xrow + 64 * j);
+                    // this CTA's half token rows as 64-, 32- and 16-row boxes
+                    int r0 = 0;
+                    for (; r0 + 64 <= half; r0 += 64)
+                        tc::tma_load_2d_2sm(b_tile(stage) + r0 * 128, &tmX64, lead_full, kb * 64, xrow + r0);
+                    if (r0 + 32 <= half) {
+                        tc::tma_load_2d_2sm(b_tile(stage) + r0 * 128, &tmX32, lead_full, kb * 64, xrow + r0);
+                        r0 += 32;
+                    }
+                    if (r0 < half) tc::tma_load_2d_2sm(b_tile(stage) + r0 * 128, &tmX16, lead_full, kb * 64, xrow + r0);
                     last_par[stage] = (int)ph;
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }

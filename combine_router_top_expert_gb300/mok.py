@@ -36,6 +36,7 @@ FLAG_MB_TOKEN_RANGES = 8
 FLAG_ROW_TILES = 16
 FLAG_TOKEN_TILES_BALANCED = 32
 FLAG_NO_L2_PREFETCH = 64
+FLAG_SWAPPED_TILES = 128
 FLAG_TEST_WITHHOLD_PUBLISH = 256
 
 

@@ -52,7 +52,9 @@ def candidates(p: mok.Problem, batches: int = 1, ring_rows: int = 0, num_sms: in
     them through one ring of `ring_rows` rows (0: the library's default)."""
     out = [Candidate("staged")]
     if p.dtype == mok.BF16:
-        out += [Candidate("staged, balanced token tiles", mok.FLAG_TOKEN_TILES_BALANCED),
+        out += [Candidate("staged, swapped-operand pair tiles", mok.FLAG_SWAPPED_TILES),
+                Candidate("staged, swapped-operand pair tiles, balanced token tiles",
+                          mok.FLAG_SWAPPED_TILES | mok.FLAG_TOKEN_TILES_BALANCED),
                 Candidate("staged, 128-row token tiles", mok.FLAG_ROW_TILES),
                 Candidate("staged, 128-row token tiles as 2-SM pairs", mok.FLAG_GEMM_PAIRS)]
     elif p.dtype == mok.MXFP8:

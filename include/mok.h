@@ -112,16 +112,20 @@ typedef struct {
  * expert-contiguous layout (padded once per expert over the whole batch),
  * and a batch's weighted sums run once all of its minibatches are done. */
 #define MOK_FLAG_MB_TOKEN_RANGES 8
-/* BF16 inference forward on 128-row token tiles (the tokens as the M side of
- * the tensor-core tiles, each expert's rows padded to whole tiles). By
- * default the BF16 inference GEMMs swap the operands: the weight rows are the
- * M side of 2-SM pair tiles (256 rows over two CTAs) and an expert's tokens
- * are cut into tiles of 256 rows and one remainder tile (a multiple of 32
- * rows) as the N side, so little tensor work is spent on padded rows and no
- * CTA of a pair idles
- * (needs I % 128 == 0 and H % 256 == 0; other shapes use the token tiles).
- * The training forward (saved != NULL) and MXFP8 use the token tiles. */
+/* The BF16 inference GEMMs run either on 128-row token tiles (the tokens as
+ * the M side of the tensor-core tiles, each expert's rows padded to whole
+ * tiles) or with the operands swapped: the weight rows as the M side of 2-SM
+ * pair tiles (256 rows over two CTAs) and an expert's tokens cut into tiles
+ * of 256 rows and one remainder tile (a multiple of 32 rows) as the N side,
+ * so little tensor work is spent on padded rows and no CTA of a pair idles
+ * (needs I % 128 == 0 and H % 256 == 0). By default the swapped tiles run
+ * when the average rows per expert, T*k/E, is at least 256 and leaves no
+ * remainder modulo 256 or one of at least 192 rows (measured faster there;
+ * a narrow remainder tile costs most of a full one). MOK_FLAG_ROW_TILES forces
+ * the token tiles, MOK_FLAG_SWAPPED_TILES the swapped ones. The training
+ * forward (saved != NULL) and MXFP8 use the token tiles. */
 #define MOK_FLAG_ROW_TILES 16
+#define MOK_FLAG_SWAPPED_TILES 128
 /* Swapped-operand tiles: cut each expert's tokens into ceil(n/256) tiles of
  * about equal size (multiples of 32) instead of tiles of 256 rows plus one
  * remainder tile (the default; measured faster). */

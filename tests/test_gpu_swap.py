@@ -6,7 +6,9 @@ Each output element is still one K-ordered tensor-core dot product with
 fp32 accumulation; how an expert's tokens are cut into tiles cannot change
 it, so both cuts (balanced tiles; 256 rows plus a remainder) must give the
 same bits. Against the oracle the layer stays within the BF16 tolerance, and
-against the 128-row token tiles (the other operand order) too."""
+against the 128-row token tiles (the other operand order) too. The tests
+force the swapped tiles (MOK_FLAG_SWAPPED_TILES); by default the library
+picks them only for shapes where they measured faster."""
 import numpy as np
 import pytest
 import torch
@@ -43,8 +45,8 @@ def test_swapped_tiles_match_oracle_and_both_cuts(wl):
     layer = layer_for(inp, mok.BF16)
     x = to_dev_bf16(inp.x)
     layer.route(x)
-    bal = _forward(layer, x, wl.T, 0)
-    bal2 = _forward(layer, x, wl.T, mok.FLAG_TOKEN_TILES_BALANCED)
+    bal = _forward(layer, x, wl.T, mok.FLAG_SWAPPED_TILES)
+    bal2 = _forward(layer, x, wl.T, mok.FLAG_SWAPPED_TILES | mok.FLAG_TOKEN_TILES_BALANCED)
     rows = _forward(layer, x, wl.T, mok.FLAG_ROW_TILES)
     assert torch.equal(bal.view(torch.int16), bal2.view(torch.int16))
     r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
@@ -72,8 +74,8 @@ def test_swapped_tiles_edge_counts():
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     rt = {"topk_idx": dev(idx), "topk_w": dev(np.ones((T, 1), np.float32)), "counts": dev(np.array(counts, np.int32)),
           "offsets": dev(offsets), "row_src": dev(order), "slot_row": dev(order)}
-    bal = _forward(layer, x, T, 0, rt)
-    bal2 = _forward(layer, x, T, mok.FLAG_TOKEN_TILES_BALANCED, rt)
+    bal = _forward(layer, x, T, mok.FLAG_SWAPPED_TILES, rt)
+    bal2 = _forward(layer, x, T, mok.FLAG_SWAPPED_TILES | mok.FLAG_TOKEN_TILES_BALANCED, rt)
     assert torch.equal(bal.view(torch.int16), bal2.view(torch.int16))
     r = {"idx": idx, "w": np.ones((T, 1)), "offsets": offsets, "row_src": order}
     ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_BF16)
@@ -86,6 +88,7 @@ def test_swapped_tiles_bitwise_reruns():
     inp = synth.make_inputs(wl, seed=2)
     layer = layer_for(inp, mok.BF16)
     x = to_dev_bf16(inp.x)
-    first = layer.forward(x).clone()
+    cfg = mok.make_config(flags=mok.FLAG_SWAPPED_TILES)
+    first = layer.forward(x, cfg=cfg).clone()
     for _ in range(9):
-        assert torch.equal(layer.forward(x).view(torch.int16), first.view(torch.int16))
+        assert torch.equal(layer.forward(x, cfg=cfg).view(torch.int16), first.view(torch.int16))

@@ -15,13 +15,14 @@ def test_candidates_cover_paths_and_megakernel_knobs():
     names = [x.name for x in c]
     assert names[0] == "staged"
     assert any(x.flags == mok.FLAG_ROW_TILES for x in c)
-    assert any(x.flags == mok.FLAG_TOKEN_TILES_BALANCED for x in c)
+    assert any(x.flags == mok.FLAG_SWAPPED_TILES for x in c)
+    assert any(x.flags & mok.FLAG_TOKEN_TILES_BALANCED for x in c)
     mk = [x for x in c if x.megakernel]
     assert {x.mover_ctas for x in mk} == {4, 8, 16}
     assert {x.minibatch_tokens for x in mk} == {0, 1280}
     # MXFP8: no BF16-only tilings; shapes the megakernel cannot tile get none
     cm = tune.candidates(_p(dtype=mok.MXFP8), num_sms=152)
-    assert not any(x.flags & (mok.FLAG_ROW_TILES | mok.FLAG_TOKEN_TILES_BALANCED) for x in cm)
+    assert not any(x.flags & (mok.FLAG_ROW_TILES | mok.FLAG_SWAPPED_TILES) for x in cm)
     assert not any(x.megakernel for x in tune.candidates(_p(H=384, I=64), num_sms=152))
     # few SMs: mover counts that leave no compute half are dropped
     assert all(x.mover_ctas < 8 for x in tune.candidates(_p(), num_sms=16) if x.megakernel)
