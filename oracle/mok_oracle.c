@@ -560,7 +560,12 @@ int orc_moe_forward(const void* x, const void* Wg, const void* Wu, const void* W
  *   reverse-dispatch: dX[t] = sum_j da_j + sum_j dl_j W_r[:, e_j].
  * silu'(z) = s (1 + z (1 - s)), s = 1/(1+exp(-z)).
  * mode 0 (BF16): the GEMM operands the GPU stores in BF16 are rounded the same
- * way: h, dy, dG, dU. mode 2: no rounding. MXFP8 backward is not defined.
+ * way: h, dy, dG, dU. mode 2: no rounding. mode 1 (MXFP8): the forward as in
+ * orc_moe_forward mode 1, the same BF16 roundings of dy, dG, dU and h, and
+ * every backward GEMM operand quantised to MXFP8 along that GEMM's reduction
+ * dimension: dy and W_down along H (dh), dG, dU, W_gate, W_up along I (da),
+ * and x, h, dy, dG, dU along the expert's rows, 32 at a time (the weight
+ * gradients).
  * Logits must be those the routing used (fp32 logits widened, or fp64).
  * Inputs are BF16 bits (W_r binary32) when f64 == 0, doubles when f64 == 1.
  * Outputs are fp64: dX [T,H], dWg/dWu [E,H,I], dWd [E,I,H], dWr [H,E].
@@ -570,11 +575,39 @@ static double wr_at(const void* W_r, long i, int f64) {
     return f64 ? ((const double*)W_r)[i] : (double)((const float*)W_r)[i];
 }
 
+/* MXFP8 round trip of the rows of an [R, K] matrix along K (blocks of 32). */
+static void mx_roundtrip_rows(double* v, long R, int K) {
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < R; ++r) mx_roundtrip_vec(v + r * K, K);
+}
+
+/* MXFP8 round trip of the columns of an [R, C] matrix along R, in blocks of
+ * 32 consecutive rows starting at row 0 (the last block may be shorter: its
+ * scale comes from its own rows). */
+static void mx_roundtrip_cols(double* v, long R, int C) {
+#pragma omp parallel for schedule(static)
+    for (int c = 0; c < C; ++c) {
+        double blk[32];
+        uint8_t codes[32];
+        for (long r0 = 0; r0 < R; r0 += 32) {
+            int n = (int)(R - r0 < 32 ? R - r0 : 32);
+            for (int q = 0; q < 32; ++q) blk[q] = q < n ? v[(r0 + q) * C + c] : 0.0;
+            int sc = mx_quantize_block(blk, 32, 1, codes, 1);
+            for (int q = 0; q < n; ++q) v[(r0 + q) * C + c] = mx_value(codes[q], (uint8_t)sc);
+        }
+    }
+}
+
 int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void* Wu,
                      const void* Wd, const void* dY, int f64, int T, int H, int I, int E, int k,
                      const int32_t* idx, const double* w, const int32_t* offsets, const int32_t* row_src,
                      int mode, double* dX, double* dWg, double* dWu, double* dWd, double* dWr) {
-    if (mode != ORC_BF16 && mode != ORC_EXACT) return ORC_ERR;
+    if (mode != ORC_BF16 && mode != ORC_EXACT && mode != ORC_MXFP8) return ORC_ERR;
+    if (mode == ORC_MXFP8 && (H % 32 || I % 32)) return ORC_ERR;
+    const int mx = mode == ORC_MXFP8;
+    /* the BF16 roundings of the stored backward operands (dy, dG, dU, and h
+     * as the weight gradient reads it) apply in both quantised modes */
+    const int round_bf = mode != ORC_EXACT;
     long HI = (long)H * I;
     double* gw = (double*)calloc((size_t)T * k, sizeof(double));
     double* da = (double*)calloc((size_t)T * k * H, sizeof(double));
@@ -582,12 +615,26 @@ int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void*
     memset(dWg, 0, sizeof(double) * (size_t)E * HI);
     memset(dWu, 0, sizeof(double) * (size_t)E * HI);
     memset(dWd, 0, sizeof(double) * (size_t)E * HI);
-    expert_w W;
+    expert_w W, WB;   /* forward operands; MXFP8: the backward's dgrad operands */
     if (alloc_expert(&W, HI)) { free(gw); free(da); return ORC_ERR; }
+    if (mx && alloc_expert(&WB, HI)) { free_expert(&W); free(gw); free(da); return ORC_ERR; }
     for (int e = 0; e < E; ++e) {
         int r0 = offsets[e], r1 = offsets[e + 1];
         if (r1 == r0) continue;
         load_expert(Wg, Wu, Wd, f64, e, H, I, mode, &W);
+        if (mx) {
+            /* MXFP8 backward (reading of the pages' "MXFP8 backward", KuCoin
+             * ja/fil article, section 03, and RuntimeWire "Cursor's benchmark
+             * claims"): every backward GEMM takes MXFP8 operands blocked along
+             * its own reduction dimension. dh = dy W_down^T reduces over H, so
+             * W_down's rows are blocked along H; da = dG W_gate^T + dU W_up^T
+             * reduces over I, so W_gate's and W_up's rows are blocked along I. */
+            load_expert(Wg, Wu, Wd, f64, e, H, I, ORC_BF16, &WB);
+            mx_roundtrip_rows(WB.g, H, I);
+            mx_roundtrip_rows(WB.u, H, I);
+            mx_roundtrip_rows(WB.d, I, H);
+        }
+        const expert_w* Wb = mx ? &WB : &W;
         int nr = r1 - r0;
         /* per-row forward intermediates and gradients of this expert */
         double* A = (double*)malloc(sizeof(double) * (size_t)nr * H);
@@ -600,15 +647,28 @@ int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void*
         {
             double* G = (double*)malloc(sizeof(double) * I);
             double* U = (double*)malloc(sizeof(double) * I);
+            double* hq = (double*)malloc(sizeof(double) * I);
             double* y = (double*)malloc(sizeof(double) * H);
             double* dh = (double*)malloc(sizeof(double) * I);
+            double* af = (double*)malloc(sizeof(double) * H);
+            double* dyq = (double*)malloc(sizeof(double) * H);
+            double* dgq = (double*)malloc(sizeof(double) * I);
+            double* duq = (double*)malloc(sizeof(double) * I);
 #pragma omp for schedule(dynamic, 1)
             for (int q = 0; q < nr; ++q) {
                 int slot = row_src[r0 + q];
                 int t = slot / k;
                 double* a = A + (long)q * H;
-                act_row(x, f64, t, H, ORC_BF16, a);
-                ffn_row(a, &W, H, I, mode, G, U, HB + (long)q * I, y);
+                act_row(x, f64, t, H, ORC_BF16, a);            /* x as stored (BF16) */
+                act_row(x, f64, t, H, mode, af);               /* x as the forward GEMM reads it */
+                ffn_row(af, &W, H, I, mode, G, U, hq, y);
+                /* h as the weight gradient reads it: BF16 (mode 1 stores h in
+                 * BF16 for the backward besides the MXFP8 copy the down GEMM
+                 * reads), exact in mode 2 */
+                for (int i = 0; i < I; ++i) {
+                    double hv = silu(G[i]) * U[i];
+                    HB[(long)q * I + i] = mode == ORC_BF16 ? hq[i] : (mx ? orc_round_bf16(hv) : hv);
+                }
                 /* reverse-combine */
                 double wj = w[slot], g = 0.0;
                 double* dyr = DY + (long)q * H;
@@ -616,35 +676,50 @@ int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void*
                     double dYv = ld(dY, (long)t * H + c, f64);
                     g += dYv * y[c];
                     dyr[c] = wj * dYv;
-                    if (mode == ORC_BF16) dyr[c] = orc_round_bf16(dyr[c]);
+                    if (round_bf) dyr[c] = orc_round_bf16(dyr[c]);
+                    dyq[c] = dyr[c];
                 }
+                if (mx) mx_roundtrip_vec(dyq, H);
                 gw[slot] = g;
                 /* dgrad of the down projection and of SwiGLU */
                 for (int i = 0; i < I; ++i) {
                     double s = 0.0;
-                    const double* dr = W.d + (long)i * H;
-                    for (int c = 0; c < H; ++c) s += dyr[c] * dr[c];
+                    const double* dr = Wb->d + (long)i * H;
+                    for (int c = 0; c < H; ++c) s += dyq[c] * dr[c];
                     dh[i] = s;
                 }
                 for (int i = 0; i < I; ++i) {
                     double sg = 1.0 / (1.0 + exp(-G[i]));
                     double dgv = dh[i] * U[i] * sg * (1.0 + G[i] * (1.0 - sg));
                     double duv = dh[i] * G[i] * sg;
-                    if (mode == ORC_BF16) { dgv = orc_round_bf16(dgv); duv = orc_round_bf16(duv); }
+                    if (round_bf) { dgv = orc_round_bf16(dgv); duv = orc_round_bf16(duv); }
                     DG[(long)q * I + i] = dgv;
                     DU[(long)q * I + i] = duv;
+                    dgq[i] = dgv;
+                    duq[i] = duv;
                 }
+                if (mx) { mx_roundtrip_vec(dgq, I); mx_roundtrip_vec(duq, I); }
                 /* da = dG W_gate^T + dU W_up^T, pushed to slot (t, j) */
                 double* dar = da + (long)slot * H;
                 for (int c = 0; c < H; ++c) {
-                    const double* gr = W.g + (long)c * I;
-                    const double* ur = W.u + (long)c * I;
+                    const double* gr = Wb->g + (long)c * I;
+                    const double* ur = Wb->u + (long)c * I;
                     double s = 0.0;
-                    for (int i = 0; i < I; ++i) s += DG[(long)q * I + i] * gr[i] + DU[(long)q * I + i] * ur[i];
+                    for (int i = 0; i < I; ++i) s += dgq[i] * gr[i] + duq[i] * ur[i];
                     dar[c] = s;
                 }
             }
-            free(G); free(U); free(y); free(dh);
+            free(G); free(U); free(hq); free(y); free(dh); free(af); free(dyq); free(dgq); free(duq);
+        }
+        if (mx) {
+            /* the weight gradients reduce over the expert's rows (layout
+             * order): their operands are blocked along those rows, 32 at a
+             * time from the expert's first row */
+            mx_roundtrip_cols(A, nr, H);
+            mx_roundtrip_cols(HB, nr, I);
+            mx_roundtrip_cols(DY, nr, H);
+            mx_roundtrip_cols(DG, nr, I);
+            mx_roundtrip_cols(DU, nr, I);
         }
         /* wgrad: sums over the expert's rows in row order */
         double* dg = dWg + (long)e * HI;
@@ -668,6 +743,7 @@ int orc_moe_backward(const void* x, const void* W_r, const void* Wg, const void*
         free(A); free(HB); free(DY); free(DG); free(DU);
     }
     free_expert(&W);
+    if (mx) free_expert(&WB);
     /* router backward and reverse-dispatch */
     memset(dWr, 0, sizeof(double) * (size_t)H * E);
     double* dl = (double*)calloc((size_t)T * k, sizeof(double));

@@ -530,3 +530,111 @@ def test_backward_operand_rounding_hand_worked(mode, key):
         assert sD.tolist() == [exp["dW_down"][e][0] for e in (0, 1)]
         cw = oracle.router_grad_columns(x, Wg, Wu, Wd, dY, r, [0, 1])
         assert cw.tolist() == [[row[0] for row in exp["dW_r"]], [row[1] for row in exp["dW_r"]]]
+
+
+# ----------------------------------------------------------------------------- MXFP8 backward
+
+def _mx_q(v, axis):
+    """MXFP8 round trip along `axis` in blocks of 32 (the last block may be
+    short), with torch's float8_e4m3fn conversion as the element encoder and
+    the E8M0 rule X = floor(log2 amax) - 8 (clamped) as the block scale."""
+    v = np.moveaxis(np.asarray(v, np.float64), axis, 0)
+    out = np.empty_like(v)
+    for r0 in range(0, v.shape[0], 32):
+        blk = v[r0:r0 + 32]
+        amax = np.abs(blk).max(axis=0)
+        e = np.frexp(np.where(amax > 0, amax, 1.0))[1] - 1          # floor(log2 amax)
+        X = np.clip(np.where(amax > 0, e - 8, -127), -127, 127).astype(np.float64)
+        q = np.clip(blk / 2.0 ** X, -448.0, 448.0)
+        f8 = torch.from_numpy(np.ascontiguousarray(q)).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+        out[r0:r0 + 32] = f8 * 2.0 ** X
+    return np.moveaxis(out, 0, axis)
+
+
+def _mx_backward_numpy(xv, W_r, Wg, Wu, Wd, dYv, r):
+    """The MXFP8 backward written with numpy matmuls over explicitly
+    quantised operands (fp64); BF16 roundings by the oracle's pinned rounding."""
+    rb = np.vectorize(oracle.round_bf16)
+    T, H = xv.shape
+    E, _, I = Wg.shape
+    k = r["idx"].shape[1]
+    sig = lambda z: 1.0 / (1.0 + np.exp(-z))
+    dWg, dWu, dWd = np.zeros((E, H, I)), np.zeros((E, H, I)), np.zeros((E, I, H))
+    da = np.zeros((T * k, H))
+    gw = np.zeros(T * k)
+    for e in range(E):
+        rows = r["row_src"][r["offsets"][e]:r["offsets"][e + 1]]
+        if len(rows) == 0:
+            continue
+        t = rows // k
+        A = xv[t]
+        G = _mx_q(A, 1) @ _mx_q(Wg[e], 0)
+        U = _mx_q(A, 1) @ _mx_q(Wu[e], 0)
+        h = G * sig(G) * U
+        y = _mx_q(h, 1) @ _mx_q(Wd[e], 0)
+        gw[rows] = (dYv[t] * y).sum(1)
+        dy = rb(r["w"].reshape(-1)[rows][:, None] * dYv[t])
+        dh = _mx_q(dy, 1) @ _mx_q(Wd[e], 1).T
+        s = sig(G)
+        dG = rb(dh * U * s * (1.0 + G * (1.0 - s)))
+        dU = rb(dh * G * s)
+        da[rows] = _mx_q(dG, 1) @ _mx_q(Wg[e], 1).T + _mx_q(dU, 1) @ _mx_q(Wu[e], 1).T
+        hb = rb(h)
+        dWg[e] = _mx_q(A, 0).T @ _mx_q(dG, 0)
+        dWu[e] = _mx_q(A, 0).T @ _mx_q(dU, 0)
+        dWd[e] = _mx_q(hb, 0).T @ _mx_q(dy, 0)
+    w = r["w"]
+    gwr = gw.reshape(T, k)
+    dl = w * (gwr - (w * gwr).sum(1, keepdims=True))
+    dX = da.reshape(T, k, H).sum(1) + np.einsum("tj,htj->th", dl, W_r.astype(np.float64)[:, r["idx"]])
+    dWr = np.zeros((H, E))
+    for j in range(k):
+        np.add.at(dWr.T, r["idx"][:, j], dl[:, j:j + 1] * xv)
+    return dX, dWg, dWu, dWd, dWr
+
+
+def test_mxfp8_backward_equals_numpy_on_explicitly_quantised_operands():
+    """Random BF16 inputs: the oracle's MXFP8 backward equals the same
+    formulas evaluated with numpy matmuls on operands quantised along the
+    stated axes by torch's float8 conversion (dy and W_down along H for dh;
+    dG, dU, W_gate, W_up along I for da; x, h, dy, dG, dU along the expert's
+    rows for the weight gradients)."""
+    wl = synth.small("mxb", T=70, H=64, I=96, E=4, k=2, backward=True)
+    inp = synth.make_inputs(wl, seed=41)
+    r = oracle.route(inp.x, inp.W_r, wl.k)
+    got = oracle.moe_backward(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, mode=oracle.MODE_MXFP8)
+    ref = _mx_backward_numpy(bf16_val(inp.x), inp.W_r, bf16_val(inp.Wg), bf16_val(inp.Wu), bf16_val(inp.Wd),
+                             bf16_val(inp.dY), r)
+    for n, a, b in zip(("dX", "dW_gate", "dW_up", "dW_down", "dW_r"), got, ref):
+        assert np.allclose(a, b, rtol=1e-9, atol=1e-12 * np.abs(b).max()), n
+    # and the quantisation matters: the BF16-mode backward differs
+    b16 = oracle.moe_backward(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, mode=oracle.MODE_BF16)
+    assert not np.allclose(b16[1], got[1], rtol=1e-3)
+
+
+def test_mxfp8_backward_exact_operands_equal_bf16_backward():
+    """Inputs on which every MXFP8 quantisation of the backward is exact
+    (powers of two; G = 64 or 0, where silu and silu' are exact; one nonzero
+    per weight column or row): the MXFP8 backward equals the BF16 one bit for
+    bit, so the quantised mode adds nothing but the quantisations."""
+    T, H, I, E, k = 40, 64, 32, 4, 2
+    rng = np.random.default_rng(3)
+    x = rng.choice([0.0, 1.0, -1.0, 0.5, -0.5], (T, H))
+    x[:, 0] = 1.0
+    Wg = np.zeros((E, H, I)); Wu = np.zeros((E, H, I)); Wd = np.zeros((E, I, H))
+    for e in range(E):
+        Wg[e, 0] = rng.choice([0.0, 64.0], I)
+        Wu[e, 0] = rng.choice([1.0, -1.0, 0.5, -0.5], I)
+        for i in range(I):
+            Wd[e, i, rng.integers(H)] = rng.choice([1.0, -1.0, 0.5])
+    dY = rng.choice([1.0, -1.0, 2.0, -2.0], (T, H))
+    W_r = (rng.standard_normal((H, E)) * 0.1).astype(np.float32)
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, row_src, slot_row = oracle.layout(idx, E)
+    r = dict(idx=idx, w=np.full((T, k), 0.5), offsets=offsets, row_src=row_src)
+    args = [bf16_bits(a) for a in (x, Wg, Wu, Wd, dY)]
+    mx = oracle.moe_backward(args[0], W_r, args[1], args[2], args[3], args[4], r, mode=oracle.MODE_MXFP8)
+    bf = oracle.moe_backward(args[0], W_r, args[1], args[2], args[3], args[4], r, mode=oracle.MODE_BF16)
+    for a, b in zip(mx, bf):
+        assert np.array_equal(a, b)
+    assert np.abs(mx[1]).max() > 0 and np.abs(mx[3]).max() > 0
