@@ -67,14 +67,21 @@ struct FwdLayout {
     size_t sA, sGU, sh, spart, saved_total;                  // saved offsets
 };
 
+// Rows of the padded layout rounded up to whole 128-row tiles: buffers the
+// MXFP8 tile-order and column quantisers read or write cover whole tiles.
+int64_t rows_tiles(const mok_problem* p) { return align_up(padded_rows_max(p->T, p->E, p->k), kTileM); }
+
 FwdLayout fwd_layout(const mok_problem* p, bool training) {
     FwdLayout L{};
-    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
-    const int64_t eb = p->dtype == MOK_MXFP8 ? 1 : 2;
+    const int64_t rows = rows_tiles(p);
+    const bool mx = p->dtype == MOK_MXFP8;
+    const int64_t eb = mx ? 1 : 2;
     size_t o = kStatusBytes;
-    if (!training) { L.A = o; o += align_up(rows * p->H * eb, 1024); }
+    // MXFP8 training keeps the BF16 rows and h in `saved` and the GEMMs' MXFP8
+    // copies here
+    if (!training || mx) { L.A = o; o += align_up(rows * p->H * eb, 1024); }
     L.A_sf = o; if (p->dtype == MOK_MXFP8) o += align_up(rows * p->H / 32, 1024);
-    if (!training) { L.h = o; o += align_up(rows * p->I * eb, 1024); }
+    if (!training || mx) { L.h = o; o += align_up(rows * p->I * eb, 1024); }
     L.h_sf = o; if (p->dtype == MOK_MXFP8) o += align_up(rows * p->I / 32, 1024);
     if (!training) { L.partials = o; o += align_up((int64_t)p->T * p->k * p->H * 2, 1024); }
     if (!training && p->dtype == MOK_MXFP8) {   // x quantised once per token before the gather
@@ -97,11 +104,14 @@ FwdLayout fwd_layout(const mok_problem* p, bool training) {
 
 struct BwdLayout {
     size_t dy, dgu, da, gw, dl, dl_full, part, wrt, total;
+    // MXFP8: the dgrad operands (rows blocked along their K), the backward's
+    // weight copies, and the weight-gradient operands transposed (tokens as K)
+    size_t dyq, dysf, dguq, dgusf, wdq, wdsf, wgq, wgsf, wuq, wusf, atq, atsf, gutq, gutsf, htq, htsf, dytq, dytsf;
 };
 
 BwdLayout bwd_layout(const mok_problem* p) {
     BwdLayout L{};
-    const int64_t rows = padded_rows_max(p->T, p->E, p->k);
+    const int64_t rows = rows_tiles(p);
     size_t o = kStatusBytes;
     L.dy = o; o += align_up(rows * p->H * 2, 1024);
     L.dgu = o; o += align_up(rows * 2 * p->I * 2, 1024);
@@ -111,6 +121,22 @@ BwdLayout bwd_layout(const mok_problem* p) {
     L.dl_full = o; o += align_up((int64_t)p->T * p->E * 4, 1024);
     L.part = o; o += align_up(dwr_partial_floats(p->H, p->E) * 4, 1024);
     L.wrt = o; o += align_up((int64_t)p->E * p->H * 4, 1024);
+    if (p->dtype == MOK_MXFP8) {
+        const int64_t H = p->H, I = p->I, E = p->E;
+        auto q = [&](size_t& codes, size_t& sf, int64_t R, int64_t K) {
+            codes = o; o += align_up(R * K, 1024);
+            sf = o; o += align_up(R * K / 32, 1024);
+        };
+        q(L.dyq, L.dysf, rows, H);
+        q(L.dguq, L.dgusf, rows, 2 * I);
+        q(L.wdq, L.wdsf, E * I, H);
+        q(L.wgq, L.wgsf, E * H, I);
+        q(L.wuq, L.wusf, E * H, I);
+        q(L.atq, L.atsf, H, rows);
+        q(L.gutq, L.gutsf, 2 * I, rows);
+        q(L.htq, L.htsf, I, rows);
+        q(L.dytq, L.dytsf, H, rows);
+    }
     L.total = o;
     return L;
 }
@@ -275,7 +301,7 @@ size_t mok_saved_size(const mok_problem* p) {
 size_t mok_workspace_size(const mok_problem* p, const mok_config* cfg) {
     if (!problem_ok(p)) return 0;
     size_t f = fwd_layout(p, false).total;
-    size_t b = p->dtype == MOK_BF16 ? bwd_layout(p).total : 0;
+    size_t b = bwd_layout(p).total;
     size_t m = mega_supported(p) ? mega_layout(p, 1, cfg).total : 0;
     return std::max(std::max(f, b), m);
 }
@@ -440,7 +466,6 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     if ((p->I_shared > 0) != (a->packed_shared != nullptr)) return MOK_ERR_INVALID;
     const bool training = a->saved != nullptr;
     const bool mx = p->dtype == MOK_MXFP8;
-    if (training && mx) return MOK_ERR_UNSUPPORTED;
     if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->packed, 256) ||
         !aligned(a->x, 16) || !aligned(a->out, 16) || (training && !aligned(a->saved, 1024)))
         return MOK_ERR_INVALID;
@@ -454,8 +479,8 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     char* ws = static_cast<char*>(a->workspace);
     char* sv = static_cast<char*>(a->saved);
     FwdLayout L = fwd_layout(p, training);
-    void* A = training ? sv + L.sA : ws + L.A;
-    void* h = training ? sv + L.sh : ws + L.h;
+    void* A = (training && !mx) ? sv + L.sA : ws + L.A;
+    void* h = (training && !mx) ? sv + L.sh : ws + L.h;
     void* partials = training ? sv + L.spart : ws + L.partials;
     void* gu = training ? sv + L.sGU : nullptr;
     uint8_t* A_sf = mx ? reinterpret_cast<uint8_t*>(ws + L.A_sf) : nullptr;
@@ -468,16 +493,22 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     PackedLayout PL = packed_layout(p->E, p->H, p->I, p->dtype);
     const char* pk = static_cast<const char*>(a->packed);
     const int64_t rows = padded_rows_max(p->T, p->E, p->k);
-    if (e == cudaSuccess)
+    if (e == cudaSuccess) {
         // pad rows stay unwritten for inference (their GEMM rows are never
         // stored); training keeps them zero for the weight gradients
-        e = (mx && !training)
-                ? launch_quantize_rows(a->x, p->T, p->H, ws + L.xq, ws + L.xsf, s)
-                : launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf,
-                                  nullptr, nullptr, s, training);
+        if (mx && !training)
+            e = launch_quantize_rows(a->x, p->T, p->H, ws + L.xq, ws + L.xsf, s);
+        else if (mx)   // MXFP8 training: BF16 rows saved for the weight gradients, quantised for the GEMM
+            e = launch_dispatch(false, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, sv + L.sA,
+                                nullptr, nullptr, nullptr, s, true);
+        else
+            e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
+                                nullptr, s, training);
+    }
     if (e == cudaSuccess && mx && !training)
         e = launch_dispatch_q(ws + L.xq, ws + L.xsf, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A,
                               A_sf, s);
+    if (e == cudaSuccess && mx && training) e = launch_quantize_rows_tiled(sv + L.sA, rows_tiles(p), p->H, A, A_sf, s);
     if (e == cudaSuccess && use_swap(p, cfg, training)) {
         e = gemm_gateup_swap(A, pk + PL.gu, p->E, p->H, p->I, r.counts, rows, h, swap_policy(cfg), c, s);
         if (e == cudaSuccess)
@@ -486,7 +517,7 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
     } else {
         if (e == cudaSuccess)
             e = gemm_gateup(mx, A, A_sf, pk + PL.gu, reinterpret_cast<const uint8_t*>(pk + PL.gu_sf), p->E, p->H,
-                            p->I, r.counts, 0, rows, h, h_sf, gu, c, s);
+                            p->I, r.counts, 0, rows, h, h_sf, gu, c, s, (training && mx) ? sv + L.sh : nullptr);
         if (e == cudaSuccess)
             e = gemm_down(mx, h, h_sf, pk + PL.dn, reinterpret_cast<const uint8_t*>(pk + PL.dn_sf), p->E, p->H, p->I,
                           r.counts, r.offsets, r.row_src, 0, rows, partials, c, s);
@@ -510,8 +541,8 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const mok_config* cfg,
                             mok_stream_t stream) {
     if (!problem_ok(p) || !a || !routing_ok(&a->routing, p->T)) return MOK_ERR_INVALID;
-    if (p->dtype != MOK_BF16) return MOK_ERR_UNSUPPORTED;
     if (p->I_shared > 0) return MOK_ERR_UNSUPPORTED;
+    const bool mx = p->dtype == MOK_MXFP8;
     if (!a->W_r || !a->W_gate || !a->W_up || !a->W_down || !a->saved || !a->dW_gate || !a->dW_up || !a->dW_down ||
         !a->dW_r || !a->workspace)
         return MOK_ERR_INVALID;
@@ -553,13 +584,47 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
     if (e == cudaSuccess)
         e = launch_bwd_small(a->dY, sv + FL.spart, r.topk_w, r.topk_idx, a->x, WrT, da, T, H, E, k, gw, dl, dl_full,
                              part, a->dX, a->dW_r, 0, s);
-    // expert dgrad
-    if (e == cudaSuccess) e = gemm_dgrad_h(dy, a->W_down, E, H, I, r.counts, rows, sv + FL.sGU, dgu, c, s);
-    if (e == cudaSuccess)
-        e = gemm_dgrad_a(dgu, a->W_gate, a->W_up, E, H, I, r.counts, r.offsets, r.row_src, rows, da, c, s);
-    // expert wgrad (each expert's rows, in row order)
-    if (e == cudaSuccess) e = gemm_wgrad(sv + FL.sA, H, dgu, 2 * I, E, r.counts, rows, a->dW_gate, a->dW_up, I, c, s);
-    if (e == cudaSuccess) e = gemm_wgrad(sv + FL.sh, I, dy, H, E, r.counts, rows, a->dW_down, nullptr, H, c, s);
+    if (mx) {
+        // MXFP8: every GEMM operand quantised along that GEMM's reduction
+        // dimension; the weights' backward copies are made per call (the
+        // weights change with every optimizer step)
+        auto Q = [&](size_t off) { return ws + off; };
+        auto QS = [&](size_t off) { return reinterpret_cast<uint8_t*>(ws + off); };
+        const int64_t rp = rows_tiles(p);
+        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_down, (int64_t)E * I, H, Q(L.wdq), QS(L.wdsf), s);
+        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_gate, (int64_t)E * H, I, Q(L.wgq), QS(L.wgsf), s);
+        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_up, (int64_t)E * H, I, Q(L.wuq), QS(L.wusf), s);
+        // dh = dy W_down^T (K = H), dSwiGLU -> dG|dU (BF16)
+        if (e == cudaSuccess) e = launch_quantize_rows_tiled(dy, rp, H, Q(L.dyq), QS(L.dysf), s);
+        if (e == cudaSuccess)
+            e = gemm_dgrad_h_mx(Q(L.dyq), QS(L.dysf), Q(L.wdq), QS(L.wdsf), E, H, I, r.counts, rows, sv + FL.sGU, dgu,
+                                c, s);
+        // da = dG W_gate^T + dU W_up^T (K = I), pushed to the slots
+        if (e == cudaSuccess) e = launch_quantize_rows_tiled(dgu, rp, 2 * I, Q(L.dguq), QS(L.dgusf), s);
+        if (e == cudaSuccess)
+            e = gemm_dgrad_a_mx(Q(L.dguq), QS(L.dgusf), Q(L.wgq), QS(L.wgsf), Q(L.wuq), QS(L.wusf), E, H, I, r.counts,
+                                r.offsets, r.row_src, rows, da, c, s);
+        // weight gradients over each expert's tokens: operands blocked along the tokens
+        if (e == cudaSuccess) e = launch_quantize_cols_tiled(sv + FL.sA, rp, H, Q(L.atq), QS(L.atsf), s);
+        if (e == cudaSuccess) e = launch_quantize_cols_tiled(dgu, rp, 2 * I, Q(L.gutq), QS(L.gutsf), s);
+        if (e == cudaSuccess) e = launch_quantize_cols_tiled(sv + FL.sh, rp, I, Q(L.htq), QS(L.htsf), s);
+        if (e == cudaSuccess) e = launch_quantize_cols_tiled(dy, rp, H, Q(L.dytq), QS(L.dytsf), s);
+        if (e == cudaSuccess)
+            e = gemm_wgrad_mx(Q(L.atq), QS(L.atsf), H, Q(L.gutq), QS(L.gutsf), 2 * I, E, r.counts, rp, a->dW_gate,
+                              a->dW_up, I, c, s);
+        if (e == cudaSuccess)
+            e = gemm_wgrad_mx(Q(L.htq), QS(L.htsf), I, Q(L.dytq), QS(L.dytsf), H, E, r.counts, rp, a->dW_down,
+                              nullptr, H, c, s);
+    } else {
+        // expert dgrad
+        if (e == cudaSuccess) e = gemm_dgrad_h(dy, a->W_down, E, H, I, r.counts, rows, sv + FL.sGU, dgu, c, s);
+        if (e == cudaSuccess)
+            e = gemm_dgrad_a(dgu, a->W_gate, a->W_up, E, H, I, r.counts, r.offsets, r.row_src, rows, da, c, s);
+        // expert wgrad (each expert's rows, in row order)
+        if (e == cudaSuccess)
+            e = gemm_wgrad(sv + FL.sA, H, dgu, 2 * I, E, r.counts, rows, a->dW_gate, a->dW_up, I, c, s);
+        if (e == cudaSuccess) e = gemm_wgrad(sv + FL.sh, I, dy, H, E, r.counts, rows, a->dW_down, nullptr, H, c, s);
+    }
     // reverse-dispatch (push) + reduce, router gradient
     if (e == cudaSuccess)
         e = launch_bwd_small(a->dY, sv + FL.spart, r.topk_w, r.topk_idx, a->x, WrT, da, T, H, E, k, gw, dl, dl_full,

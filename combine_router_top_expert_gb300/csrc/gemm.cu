@@ -210,7 +210,7 @@ void ensure_smem_attr(const void* func, int bytes) {
 
 cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
                         int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows, void* h,
-                        uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s) {
+                        uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s, void* h_bf16) {
     const int BN = (2 * I) >= 256 ? 256 : 128;
     const int eb = mx ? 1 : 2;
     const int bk = 128 / eb;
@@ -223,6 +223,7 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.out0 = h;
     p.out_sf = h_sf;
     p.gu = gu_save;
+    p.out1_bf16 = h_bf16;
     p.split_col = I;
     p.a_sf = A_sf;
     p.b_sf = Bgu_sf;
@@ -388,6 +389,92 @@ cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, 
     if (cl) return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+}
+
+cudaError_t gemm_dgrad_h_mx(const void* dy_q, const uint8_t* dy_sf, const void* Wd_q, const uint8_t* Wd_sf, int E,
+                            int H, int I, const int32_t* counts, int64_t a_rows, const void* gu, void* dgu,
+                            const GemmCommon& c, cudaStream_t s) {
+    if (H % 128 || I % 128) return cudaErrorInvalidValue;
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.num_kb = H / 128;
+    p.b_rows_per_expert = I;
+    p.out0 = dgu;
+    p.gu = const_cast<void*>(gu);
+    p.split_col = I;
+    p.a_sf = dy_sf;
+    p.b_sf = Wd_sf;
+    p.sf_kchunks = H / 128;
+    p.n_tiles = I / 128;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, dy_q, a_rows, H, 1, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Wd_q, (int64_t)E * I, H, 1, 128, 128)) return cudaErrorInvalidValue;
+    const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    return run<128, true, false, kEpiDSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+}
+
+cudaError_t gemm_dgrad_a_mx(const void* dgu_q, const uint8_t* dgu_sf, const void* Wg_q, const uint8_t* Wg_sf,
+                            const void* Wu_q, const uint8_t* Wu_sf, int E, int H, int I, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* row_src, int64_t a_rows, void* da,
+                            const GemmCommon& c, cudaStream_t s) {
+    if (H % 128 || I % 128) return cudaErrorInvalidValue;
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.offsets = offsets;
+    p.row_src = row_src;
+    p.num_kb = 2 * I / 128;
+    p.b_split_kb = I / 128;
+    p.b_rows_per_expert = H;
+    p.out0 = da;
+    p.ldo = H;
+    p.a_sf = dgu_sf;
+    p.b_sf = Wg_sf;
+    p.b_sf2 = Wu_sf;
+    p.sf_kchunks = 2 * I / 128;
+    p.sf_kchunks_b = I / 128;
+    const int BN = H % 256 == 0 ? 256 : 128;
+    p.n_tiles = H / BN;
+    CUtensorMap ta, tb, tb2;
+    if (!make_tmap(&ta, dgu_q, a_rows, 2 * I, 1, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, Wg_q, (int64_t)E * H, I, 1, 128, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb2, Wu_q, (int64_t)E * H, I, 1, 128, BN)) return cudaErrorInvalidValue;
+    const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
+    if (BN == 256) return run<256, true, false, kEpiScatter, 4, 1>(ta, tb, tb2, p, tub, c.num_sms, s);
+    return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+}
+
+cudaError_t gemm_wgrad_mx(const void* AT_q, const uint8_t* AT_sf, int M, const void* BT_q, const uint8_t* BT_sf,
+                          int N, int E, const int32_t* counts, int64_t rows_pad, void* out0, void* out1,
+                          int split_col, const GemmCommon& c, cudaStream_t s) {
+    if (M % 128 || N % 128 || rows_pad % 128) return cudaErrorInvalidValue;
+    GemmParams p = base_params(c);
+    p.E = E;
+    p.counts = counts;
+    p.m_fixed = M;
+    p.kmajor_wgrad = 1;
+    p.out0 = out0;
+    p.out1 = out1;
+    p.split_col = split_col;
+    p.ldo = split_col < N ? split_col : N;
+    p.a_sf = AT_sf;
+    p.b_sf = BT_sf;
+    p.sf_kchunks = (int)(rows_pad / 128);
+    p.sf_kchunks_b = (int)(rows_pad / 128);
+    p.n_tiles = N / 128;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, AT_q, M, rows_pad, 1, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, BT_q, N, rows_pad, 1, 128, 128)) return cudaErrorInvalidValue;
+    CUtensorMap to0, to1;
+    if (!make_tmap_out3d(&to0, out0, E, M, p.ldo, p.ldo)) return cudaErrorInvalidValue;
+    if (split_col < N) {
+        if (!out1 || !make_tmap_out3d(&to1, out1, E, M, N - split_col, p.ldo)) return cudaErrorInvalidValue;
+    } else {
+        to1 = to0;
+    }
+    const int64_t tub = (int64_t)E * (M / kTileM) * p.n_tiles;
+    return run<128, true, false, kEpiDense, 6, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
 }
 
 cudaError_t gemm_wgrad(const void* Aact, int M, const void* B, int N, int E, const int32_t* counts, int64_t a_rows,

@@ -54,7 +54,14 @@ struct GemmParams {
     // MXFP8 scales of A and B (tile-ordered chunks)
     const uint8_t* a_sf;
     const uint8_t* b_sf;
-    int sf_kchunks;         // 128-wide K chunks per row tile (= K / 128)
+    const uint8_t* b_sf2;   // scales of the second B operand (K blocks >= b_split_kb)
+    int sf_kchunks;         // 128-wide K chunks per row tile of A (= K / 128)
+    int sf_kchunks_b;       // the same for B when it differs (0: as A)
+    // weight gradients on K-major MXFP8 operands: A is [m_fixed, K] and B is
+    // [N, K] with the tokens as K, each expert reducing over its own token
+    // range (the segment of its rows in the padded layout)
+    int kmajor_wgrad;
+    void* out1_bf16;        // MXFP8 SwiGLU: h also in BF16 [rows, I] (training forward), or NULL
     StatusBlock* status;
     unsigned long long timeout_ns;
 };
@@ -377,28 +384,36 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         for (int j = 0; j < BN / 64; ++j)
                             tc::tma_load_2d(b_tile(stage) + 8192 * j, &tmB, full_bar(stage), ti.n * BN + 64 * j, krow);
                     } else {
-                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), kb * C::kBK, ti.a_row0);
-                        const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
-                        if (kb < p.b_split_kb)
-                            tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kb * C::kBK, brow);
+                        // K-major: A box at (K offset, row), B box at (K offset, row); the
+                        // K-major weight gradients take the expert's token range as K
+                        const bool kw = p.kmajor_wgrad != 0;
+                        const int ax = kw ? ti.a_row0 + kb * C::kBK : kb * C::kBK;
+                        const int ay = kw ? ti.m * kTileM : ti.a_row0;
+                        tc::tma_load_2d(a_tile(stage), &tmA, full_bar(stage), ax, ay);
+                        const int brow = kw ? ti.n * BN : ti.e * p.b_rows_per_expert + ti.n * BN;
+                        const bool b1 = kb < p.b_split_kb;
+                        if (b1)
+                            tc::tma_load_2d(b_tile(stage), &tmB, full_bar(stage), kw ? ax : kb * C::kBK, brow);
                         else
                             tc::tma_load_2d(b_tile(stage), &tmB2, full_bar(stage), (kb - p.b_split_kb) * C::kBK, brow);
                         if constexpr (MX) {
-                            const int art = ti.a_row0 / kTileM;
-                            tc::bulk_load(sf_tile(stage), p.a_sf + ((int64_t)art * p.sf_kchunks + kb) * 512, 512,
+                            const int art = kw ? ti.m : ti.a_row0 / kTileM;
+                            const int akc = kw ? ax / 128 : kb;
+                            tc::bulk_load(sf_tile(stage), p.a_sf + ((int64_t)art * p.sf_kchunks + akc) * 512, 512,
                                           full_bar(stage));
+                            const uint8_t* bsf = b1 ? p.b_sf : p.b_sf2;
+                            const int bkc = kw ? ax / 128 : (b1 ? kb : kb - p.b_split_kb);
+                            const int bkn = p.sf_kchunks_b > 0 ? p.sf_kchunks_b : p.sf_kchunks;
                             if constexpr (BN == 224) {
                                 // B scales packed per 224-row tile: two chunks side by side
-                                tc::bulk_load(sf_tile(stage) + 512,
-                                              p.b_sf + ((int64_t)(brow / 224) * p.sf_kchunks + kb) * 1024, 1024,
-                                              full_bar(stage));
+                                tc::bulk_load(sf_tile(stage) + 512, bsf + ((int64_t)(brow / 224) * bkn + bkc) * 1024,
+                                              1024, full_bar(stage));
                             } else {
 #pragma unroll
                                 for (int j = 0; j < C::kNChunks; ++j) {
                                     const int brt = brow / kTileM + j;
-                                    tc::bulk_load(sf_tile(stage) + 512 * (1 + j),
-                                                  p.b_sf + ((int64_t)brt * p.sf_kchunks + kb) * 512, 512,
-                                                  full_bar(stage));
+                                    tc::bulk_load(sf_tile(stage) + 512 * (1 + j), bsf + ((int64_t)brt * bkn + bkc) * 512,
+                                                  512, full_bar(stage));
                                 }
                             }
                         }
@@ -567,6 +582,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
                 if (live) {
                     const int hc0 = ti.n * (BN / 2) + 64 * eg;
+                    if (p.gu != nullptr) {
+                        // training forward: the fp32 pre-activations for the backward's dSwiGLU
+                        float* gb = static_cast<float*>(p.gu) + prow * (int64_t)(2 * I);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            tc::stg_v8(gb + hc0 + 8 * i, gr0 + 8 * i);
+                            tc::stg_v8(gb + hc0 + 32 + 8 * i, gr1 + 8 * i);
+                            tc::stg_v8(gb + I + hc0 + 8 * i, ur0 + 8 * i);
+                            tc::stg_v8(gb + I + hc0 + 32 + 8 * i, ur1 + 8 * i);
+                        }
+                    }
                     uint32_t codes = 0;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
@@ -576,6 +602,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             const float gv = __uint_as_float(b ? gr1[i] : gr0[i]);
                             const float uv = __uint_as_float(b ? ur1[i] : ur0[i]);
                             hv[i] = silu_f(gv) * uv;
+                        }
+                        if (p.out1_bf16 != nullptr) {
+                            // training forward: h in BF16 for the weight gradient of W_down
+                            uint32_t hw[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) hw[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+                            __nv_bfloat16* hd = static_cast<__nv_bfloat16*>(p.out1_bf16) + prow * (int64_t)I + hc0 + 32 * b;
+                            tc::stg_v8(hd, hw);
+                            tc::stg_v8(hd + 16, hw + 8);
                         }
                         float amax = 0.f;
 #pragma unroll

@@ -503,6 +503,86 @@ cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, i
     return cudaGetLastError();
 }
 
+// MXFP8 quantisation of the rows of a row-major [R, K] BF16 matrix along K
+// (K % 128 == 0): codes [R, K] E4M3, scales in the tensor-core chunk order
+// (chunk (r / 128, c / 128) of 512 bytes at ((r / 128) * (K / 128) + c / 128)
+// * 512, byte sf_chunk_offset(r % 128, (c / 32) % 4)). One warp per row.
+__global__ void __launch_bounds__(256)
+quantize_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int K, uint8_t* __restrict__ q,
+                           uint8_t* __restrict__ sf) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nb = K / 32, nkc = K / 128;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + warp; r < R; r += (int64_t)gridDim.x * 8) {
+        for (int b = lane; b < nb; b += 32) {
+            uint4 o0, o1;
+            const uint32_t code = quantize_block32(src + r * K + b * 32, o0, o1);
+            uint4* dst = reinterpret_cast<uint4*>(q + r * K + b * 32);
+            dst[0] = o0;
+            dst[1] = o1;
+            sf[((r / kTileM) * nkc + b / 4) * 512 + sf_chunk_offset((int)(r % kTileM), b % 4)] = (uint8_t)code;
+        }
+    }
+}
+
+// MXFP8 quantisation of the columns of a row-major [R, F] BF16 matrix along
+// R in blocks of 32 rows, written transposed: codes [F, R] E4M3 (row f holds
+// column f, so a GEMM reducing over R reads it K-major) and scales in the
+// tensor-core chunk order of that [F, R] operand (chunk (f / 128, r / 128),
+// byte sf_chunk_offset(f % 128, (r / 32) % 4)). R % 128 == 0, F % 128 == 0.
+// A CTA takes 32 rows x 128 columns: the tile goes through shared memory and
+// each thread quantises one column block and stores its 32 codes at once.
+__global__ void __launch_bounds__(128)
+quantize_cols_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int F, uint8_t* __restrict__ qT,
+                           uint8_t* __restrict__ sfT) {
+    __shared__ float tile[32][129];
+    const int tid = threadIdx.x;
+    const int64_t nrb = R / 32;
+    const int nfc = F / 128;
+    const int64_t nkc = R / 128;
+    for (int64_t blk = blockIdx.x; blk < nrb * nfc; blk += gridDim.x) {
+        const int64_t r0 = (blk / nfc) * 32;
+        const int f0 = (int)(blk % nfc) * 128;
+        __syncthreads();
+        for (int i = 0; i < 32; ++i) tile[i][tid] = __bfloat162float(src[(r0 + i) * F + f0 + tid]);
+        __syncthreads();
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(tile[i][tid]));
+        const uint32_t code = e8m0_code(amax);
+        const float inv = e8m0_inv_scale(code);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = f32x2_to_e4m3x2(tile[4 * i][tid] * inv, tile[4 * i + 1][tid] * inv) |
+                   (f32x2_to_e4m3x2(tile[4 * i + 2][tid] * inv, tile[4 * i + 3][tid] * inv) << 16);
+        const int f = f0 + tid;
+        uint4* dst = reinterpret_cast<uint4*>(qT + (int64_t)f * R + r0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        sfT[((int64_t)(f / kTileM) * nkc + r0 / 128) * 512 + sf_chunk_offset(f % kTileM, (int)((r0 / 32) % 4))] =
+            (uint8_t)code;
+    }
+}
+
+cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    if (K % 128) return cudaErrorInvalidValue;
+    const int blocks = (int)std::min<int64_t>(ceil_div(R, 8), (int64_t)sm_count() * 8);
+    quantize_rows_tiled_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), R, K,
+                                                      static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_cols_tiled(const void* src, int64_t R, int F, void* qT, void* sfT, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    if (R % 128 || F % 128) return cudaErrorInvalidValue;
+    const int64_t n = (R / 32) * (F / 128);
+    const int blocks = (int)std::min<int64_t>(n, (int64_t)sm_count() * 16);
+    quantize_cols_tiled_kernel<<<blocks, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src), R, F,
+                                                      static_cast<uint8_t*>(qT), static_cast<uint8_t*>(sfT));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const int blocks = (int)std::min<int64_t>(ceil_div(T, 8), (int64_t)sm_count() * 8);

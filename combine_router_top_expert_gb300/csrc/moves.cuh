@@ -69,7 +69,26 @@ struct GemmCommon {
 // identity_rows > 0: A is a plain [identity_rows, H] matrix (shared expert).
 cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
                         int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows,
-                        void* h, uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s);
+                        void* h, uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s,
+                        void* h_bf16 = nullptr);
+// MXFP8 backward GEMMs (operands quantised along each GEMM's reduction
+// dimension, scales in the tensor-core chunk order):
+//   dgrad of the down projection: dh = dy W_down^T with dy [a_rows, H] and
+//     W_down as [E*I, H], dSwiGLU epilogue (saved fp32 G|U) -> dG|dU bf16;
+//   dgrad of gate/up: da = dG W_gate^T + dU W_up^T with dG|dU [a_rows, 2I] and
+//     W_gate, W_up as [E*H, I], each row pushed to its slot;
+//   weight gradients: out[e] = A^T B over expert e's token range, A given
+//     transposed as [M, rows_pad] and B as [N, rows_pad] (tokens as K).
+cudaError_t gemm_dgrad_h_mx(const void* dy_q, const uint8_t* dy_sf, const void* Wd_q, const uint8_t* Wd_sf, int E,
+                            int H, int I, const int32_t* counts, int64_t a_rows, const void* gu, void* dgu,
+                            const GemmCommon& c, cudaStream_t s);
+cudaError_t gemm_dgrad_a_mx(const void* dgu_q, const uint8_t* dgu_sf, const void* Wg_q, const uint8_t* Wg_sf,
+                            const void* Wu_q, const uint8_t* Wu_sf, int E, int H, int I, const int32_t* counts,
+                            const int32_t* offsets, const int32_t* row_src, int64_t a_rows, void* da,
+                            const GemmCommon& c, cudaStream_t s);
+cudaError_t gemm_wgrad_mx(const void* AT_q, const uint8_t* AT_sf, int M, const void* BT_q, const uint8_t* BT_sf,
+                          int N, int E, const int32_t* counts, int64_t rows_pad, void* out0, void* out1,
+                          int split_col, const GemmCommon& c, cudaStream_t s);
 // BF16 inference forward with the operands swapped (gemm_swap.cuh): weight
 // rows as the M side of 2-SM pair tiles, token tiles of any multiple of 32
 // rows as N. h [a_rows, I] (rows of the padded layout; only routed rows are
@@ -86,6 +105,13 @@ cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, 
 // MXFP8 quantisation of each row of x [T, H] (the codes the dispatch writes):
 // x_q [T, H] E4M3, x_sf [T, H/32] E8M0 bytes.
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s);
+// MXFP8 quantisation of a row-major [R, K] BF16 matrix along K with scales in
+// the tensor-core chunk order (K % 128 == 0).
+cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s);
+// MXFP8 quantisation of the columns of a row-major [R, F] BF16 matrix along R
+// (blocks of 32 rows), written transposed as a K-major [F, R] operand with
+// chunk-ordered scales (R % 128 == 0, F % 128 == 0).
+cudaError_t launch_quantize_cols_tiled(const void* src, int64_t R, int F, void* qT, void* sfT, cudaStream_t s);
 // MXFP8 pull-dispatch of rows quantised by launch_quantize_rows (same bytes
 // as launch_dispatch; pad rows left unwritten).
 cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, int E, int k, const int32_t* counts,

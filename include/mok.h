@@ -49,7 +49,7 @@ typedef enum {
     MOK_ERR_CUDA = 2,        /* CUDA runtime/driver error */
     MOK_ERR_TIMEOUT = 3,     /* a device-side bounded wait gave up */
     MOK_ERR_CAPACITY = 4,    /* ring buffer smaller than one minibatch */
-    MOK_ERR_UNSUPPORTED = 5  /* valid but not built (e.g. MXFP8 backward) */
+    MOK_ERR_UNSUPPORTED = 5  /* valid but not built (e.g. a backward with a shared expert) */
 } mok_status;
 
 /* Shapes of one layer. T tokens, hidden H, expert intermediate I, E routed
@@ -242,8 +242,9 @@ size_t mok_saved_size(const mok_problem* p);
  * divide H and 2I (256 for BF16, 128 for MXFP8); other shapes use the stage
  * kernels. The device status reports MOK_ERR_CAPACITY if a ring region
  * cannot hold the padded rows of 16 tokens. `saved` != NULL (training) keeps
- * the activations the backward needs (BF16 only; MOK_ERR_UNSUPPORTED for
- * MXFP8). */
+ * the activations the backward needs: the gathered rows (BF16), the fp32
+ * gate/up pre-activations, h (BF16) and the partials; MXFP8 training keeps
+ * the same BF16 values and runs its GEMMs on MXFP8 copies in the workspace. */
 mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a,
                            const mok_config* cfg, mok_stream_t stream);
 
@@ -311,7 +312,7 @@ mok_status mok_combine(const mok_problem* p, const void* partials, const float* 
                        const float* shared, void* out, mok_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
-/* Backward (BF16)                                                              */
+/* Backward (BF16 and MXFP8)                                                    */
 /* ------------------------------------------------------------------------- */
 
 typedef struct {
@@ -343,7 +344,15 @@ typedef struct {
  * w_j (gw_j - sum_i w_i gw_i), dW_r = x^T dl, and dX[t] = sum_j da[t,j] +
  * sum_j dl_j W_r[:, e_j] in fixed order. The bias gets no gradient.
  * Bitwise deterministic. dW_gate, dW_up and dW_down must be 16-B aligned
- * (written by TMA stores), workspace and saved 1024-B aligned. */
+ * (written by TMA stores), workspace and saved 1024-B aligned.
+ * MXFP8 (p->dtype == MOK_MXFP8, after an MXFP8 training forward; [K-ja] 03
+ * and [RW] report an MXFP8 backward): every backward GEMM takes MXFP8
+ * operands blocked by 32 along its own reduction dimension - dy and W_down
+ * along H for dh, dG|dU and W_gate, W_up along I for da, and x, h, dy, dG,
+ * dU along each expert's rows for the weight gradients (quantised from the
+ * BF16 values, transposed so the tokens are the K dimension). The weights'
+ * backward copies are quantised in each call (into the workspace). A shared
+ * expert (I_shared > 0) has no backward here: MOK_ERR_UNSUPPORTED. */
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
                             const mok_config* cfg, mok_stream_t stream);
 

@@ -68,3 +68,54 @@ def test_router_gradient_rows_sum_to_zero():
     dWr = g["dW_r"].double().cpu().numpy()
     scale = np.abs(dWr).max()
     assert np.max(np.abs(dWr.sum(1))) <= 1e-4 * scale * wl.E
+
+
+MX_BWD_CASES = [
+    synth.small("mxbwd_small", T=256, H=256, I=128, E=4, k=2, dtype="mxfp8", backward=True),
+    synth.small("mxbwd_ragged", T=500, H=512, I=256, E=4, k=2, dtype="mxfp8", zipf_s=1.2, backward=True),
+    synth.small("mxbwd_all_experts", T=96, H=256, I=128, E=4, k=4, dtype="mxfp8", backward=True),
+]
+
+
+def _run_mx(wl, seed=0):
+    inp = synth.make_inputs(wl, seed=seed)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    dY = to_dev_bf16(inp.dY)
+    out_inf = layer.forward(x).clone()
+    out = layer.forward(x, training=True).clone()
+    g = layer.backward(x, dY)
+    torch.cuda.synchronize()
+    assert layer.status(wl.T, training=True) == (mok.OK, 0)
+    return inp, layer, x, dY, out_inf, out, g
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", MX_BWD_CASES, ids=[w.name for w in MX_BWD_CASES])
+def test_mxfp8_backward_matches_oracle(wl):
+    """MXFP8 backward (every backward GEMM on MXFP8 operands blocked along
+    its own reduction dimension) against the oracle's MXFP8 mode; the MXFP8
+    training forward gives the inference forward's bits."""
+    inp, layer, x, dY, out_inf, out, g = _run_mx(wl)
+    assert torch.equal(out.view(torch.int16), out_inf.view(torch.int16))
+    r = oracle.route(inp.x, inp.W_r, wl.k, inp.bias)
+    dX, dWg, dWu, dWd, dWr = oracle.moe_backward(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r,
+                                                  mode=oracle.MODE_MXFP8)
+    c = TOL[mok.MXFP8]
+    assert_close(host_bf16_f64(g["dX"]), dX, c, "dX (MXFP8)")
+    assert_close(host_bf16_f64(g["dW_gate"]), dWg, c, "dW_gate (MXFP8)")
+    assert_close(host_bf16_f64(g["dW_up"]), dWu, c, "dW_up (MXFP8)")
+    assert_close(host_bf16_f64(g["dW_down"]), dWd, c, "dW_down (MXFP8)")
+    assert_close(g["dW_r"].cpu().numpy().astype(np.float64), dWr, c, "dW_r (MXFP8)", bf16_out=False)
+
+
+@pytest.mark.gpu
+def test_mxfp8_backward_bitwise_deterministic():
+    wl = MX_BWD_CASES[1]
+    inp, layer, x, dY, out_inf, out, g = _run_mx(wl, seed=2)
+    first = {n: t.clone() for n, t in g.items()}
+    for _ in range(9):
+        layer.forward(x, training=True)
+        again = layer.backward(x, dY)
+        for n in first:
+            assert torch.equal(again[n].view(torch.uint8), first[n].view(torch.uint8)), n

@@ -191,9 +191,12 @@ def test_invalid_arguments_rejected_on_host():
     with pytest.raises(mok.MokError) as ei:
         mok.moe_forward(layer.problem(wl.T), x, layer.packed, b["routing"], b["out"], small_ws)
     assert ei.value.code == mok.ERR_INVALID
-    p_mx = mok.make_problem(wl.T, wl.H, wl.I, wl.E, wl.k, mok.MXFP8)
+    # a backward with a shared expert is not built
+    p_sh = mok.make_problem(wl.T, wl.H, wl.I, wl.E, wl.k, mok.BF16, 128)
+    g = {n: torch.empty(1, device="cuda") for n in ("dX", "dW_gate", "dW_up", "dW_down", "dW_r")}
     with pytest.raises(mok.MokError) as ei:
-        mok.moe_forward(p_mx, x, layer.packed, b["routing"], b["out"], b["ws"], saved=b["ws"])
+        mok.moe_backward(p_sh, x, layer.W_r, layer.Wg, layer.Wu, layer.Wd, layer.packed, x, b["routing"], b["ws"], g,
+                         b["ws"])
     assert ei.value.code == mok.ERR_UNSUPPORTED
 
 
