@@ -332,7 +332,8 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
         launches_per_step = 3 + 4 + 12
         status_ws = b["ws"]
         flops = 18.0 * H * wl.I * T * wl.k
-        kern = "layer GEMMs fwd+bwd (staged; 2 fwd + 4 bwd grouped GEMM launches)"
+        kern = ("layer GEMMs fwd+bwd (staged; 2 fwd + 4 bwd grouped GEMM launches" +
+                (", MXFP8 operands and quantisation passes)" if dtype == mok.MXFP8 else ")"))
     elif len(xs) > 1:
         routings = [{n: v.clone() for n, v in rt.items()} for _ in xs]
         outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs]
@@ -682,8 +683,8 @@ def measure_torch_composed(wl, inp, dev, steps, warmup):
 
 
 # Sub-measurements of the default line: the metric's other halves ("fwd+bwd"
-# and MXFP8), on the same GPU in the same run.
-EXTRA_WORKLOADS = ("bf16_bwd_T4096", "mxfp8_zipf_T2560")
+# and MXFP8, forward and training), on the same GPU in the same run.
+EXTRA_WORKLOADS = ("bf16_bwd_T4096", "mxfp8_zipf_T2560", "mxfp8_bwd_T4096")
 
 
 def main():
@@ -723,8 +724,8 @@ def main():
     extras = []
     if (args.workload == "bf16_fwd_T2560" and not args.no_extra and not args.megakernel and not args.gemm_pairs
             and ws == 1):
-        # the same experts (same weight draw): BF16 fwd+bwd at T=4096 and the
-        # MXFP8 forward with Zipf-skewed routing at T=2560
+        # the same experts (same weight draw): BF16 fwd+bwd at T=4096, the
+        # MXFP8 forward with Zipf-skewed routing at T=2560, MXFP8 fwd+bwd at T=4096
         del layer
         torch.cuda.empty_cache()
         for name in EXTRA_WORKLOADS:

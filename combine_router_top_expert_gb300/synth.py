@@ -71,6 +71,9 @@ WORKLOADS = {
                                     ring_rows=16384),
     "bf16_bwd_T4096": Workload("bf16_bwd_T4096", T=4096, H=7168, I=2048, E=32, k=8,
                                backward=True),
+    # the same training step with MXFP8 routed experts (forward and backward)
+    "mxfp8_bwd_T4096": Workload("mxfp8_bwd_T4096", T=4096, H=7168, I=2048, E=32, k=8, dtype="mxfp8",
+                                backward=True),
     # profiling case: the same expert shape with 8 experts (about 1 GB of
     # weights, still well above the 129 MB L2) for counter captures
     "bf16_fwd_E8_T2560": Workload("bf16_fwd_E8_T2560", T=2560, H=7168, I=2048, E=8, k=2),

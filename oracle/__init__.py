@@ -58,6 +58,8 @@ def lib():
                                            P, P, P, P, P]
             L.orc_moe_backward_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, I, P, I, P, P, I,
                                                    P, P, P, P]
+            L.orc_moe_backward_sampled_mx.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, P, P, P, I, P, P, I,
+                                                      P, P, P, P]
             L.orc_router_grad_columns.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P, P, I, P, I, P]
             L.orc_mx_quantize_rows.argtypes = [P, I64, I64, P, P]
             L.orc_mx_quantize_bf16_rows.argtypes = [P, I64, I64, P, P]
@@ -273,6 +275,16 @@ def moe_backward_sampled(x, W_r, Wg, Wu, Wd, dY, routing, tokens, cols, mode=MOD
     dWg = np.empty((len(cols), H))
     dWu = np.empty((len(cols), H))
     dWd = np.empty((len(cols), H))
+    if mode == MODE_MXFP8:
+        rc = lib().orc_moe_backward_sampled_mx(
+            _p(x), _p(W_r), _p(Wg), _p(Wu), _p(Wd), _p(dY), T, H, I, E, k,
+            _p(np.ascontiguousarray(routing["idx"], dtype=np.int32)),
+            _p(np.ascontiguousarray(routing["w"], dtype=np.float64)),
+            _p(np.ascontiguousarray(routing["offsets"], dtype=np.int32)),
+            _p(np.ascontiguousarray(routing["row_src"], dtype=np.int32)),
+            _p(tok), len(tok), _p(ce), _p(ci), len(cols), _p(dX), _p(dWg), _p(dWu), _p(dWd))
+        _check(rc, "moe_backward_sampled_mx")
+        return dX, dWg, dWu, dWd
     rc = lib().orc_moe_backward_sampled(
         _p(x), _p(W_r), _p(Wg), _p(Wu), _p(Wd), _p(dY), T, H, I, E, k,
         _p(np.ascontiguousarray(routing["idx"], dtype=np.int32)),

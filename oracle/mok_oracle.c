@@ -929,6 +929,166 @@ int orc_moe_backward_sampled(const uint16_t* x, const float* W_r, const uint16_t
     return ORC_OK;
 }
 
+/* The sampled outputs of orc_moe_backward_sampled in the MXFP8 mode of
+ * orc_moe_backward (same arguments and outputs, BF16 inputs). Experts are
+ * visited once each; an expert used by a sampled token or column has its
+ * forward weights (W_gate, W_up blocked along H, W_down along I) and its
+ * backward copies (W_down along H, W_gate and W_up along I) quantised once.
+ * dX rows need only the token's own k rows; a weight-gradient column needs
+ * the whole column of its operands over the expert's rows, blocked along
+ * those rows 32 at a time from the expert's first row. */
+int orc_moe_backward_sampled_mx(const uint16_t* x, const float* W_r, const uint16_t* Wg, const uint16_t* Wu,
+                                const uint16_t* Wd, const uint16_t* dY, int T, int H, int I, int E, int k,
+                                const int32_t* idx, const double* w, const int32_t* offsets, const int32_t* row_src,
+                                const int32_t* tok, int n_tok, const int32_t* col_e, const int32_t* col_i, int n_col,
+                                double* dX_s, double* dWg_s, double* dWu_s, double* dWd_s) {
+    if (H % 32 || I % 32) return ORC_ERR;
+    for (int q = 0; q < n_tok; ++q) if (tok[q] < 0 || tok[q] >= T) return ORC_ERR;
+    for (int q = 0; q < n_col; ++q) if (col_e[q] < 0 || col_e[q] >= E || col_i[q] < 0 || col_i[q] >= I) return ORC_ERR;
+    long HI = (long)H * I;
+    double* gw = (double*)calloc((size_t)n_tok * k + 1, sizeof(double));
+    double* da = (double*)calloc((size_t)n_tok * k * H + 1, sizeof(double));
+    expert_w W, WB;
+    if (!gw || !da || alloc_expert(&W, HI) || alloc_expert(&WB, HI)) return ORC_ERR;
+    for (int e = 0; e < E; ++e) {
+        int used = 0;
+        for (int q = 0; q < n_tok && !used; ++q)
+            for (int j = 0; j < k; ++j) used |= idx[(long)tok[q] * k + j] == e;
+        for (int q = 0; q < n_col && !used; ++q) used |= col_e[q] == e;
+        if (!used) continue;
+        load_expert(Wg, Wu, Wd, 0, e, H, I, ORC_MXFP8, &W);
+        load_expert(Wg, Wu, Wd, 0, e, H, I, ORC_BF16, &WB);
+        mx_roundtrip_rows(WB.g, H, I);
+        mx_roundtrip_rows(WB.u, H, I);
+        mx_roundtrip_rows(WB.d, I, H);
+        /* ---- the sampled tokens' rows through this expert */
+        for (int q = 0; q < n_tok; ++q) {
+            int t = tok[q];
+            for (int j = 0; j < k; ++j) {
+                if (idx[(long)t * k + j] != e) continue;
+                double* af = (double*)malloc(sizeof(double) * H);
+                double* G = (double*)malloc(sizeof(double) * I);
+                double* U = (double*)malloc(sizeof(double) * I);
+                double* hq = (double*)malloc(sizeof(double) * I);
+                double* y = (double*)malloc(sizeof(double) * H);
+                double* dyq = (double*)malloc(sizeof(double) * H);
+                double* dg = (double*)malloc(sizeof(double) * I);
+                double* du = (double*)malloc(sizeof(double) * I);
+                act_row(x, 0, t, H, ORC_MXFP8, af);
+                ffn_row(af, &W, H, I, ORC_MXFP8, G, U, hq, y);
+                double wj = w[(long)t * k + j], g = 0.0;
+                for (int c = 0; c < H; ++c) {
+                    double dYv = bf16_to_f64(dY[(long)t * H + c]);
+                    g += dYv * y[c];
+                    dyq[c] = orc_round_bf16(wj * dYv);
+                }
+                gw[(long)q * k + j] = g;
+                mx_roundtrip_vec(dyq, H);
+#pragma omp parallel for schedule(static)
+                for (int i = 0; i < I; ++i) {
+                    double dh = 0.0;
+                    const double* dr = WB.d + (long)i * H;
+                    for (int c = 0; c < H; ++c) dh += dyq[c] * dr[c];
+                    double sg = 1.0 / (1.0 + exp(-G[i]));
+                    dg[i] = orc_round_bf16(dh * U[i] * sg * (1.0 + G[i] * (1.0 - sg)));
+                    du[i] = orc_round_bf16(dh * G[i] * sg);
+                }
+                mx_roundtrip_vec(dg, I);
+                mx_roundtrip_vec(du, I);
+                double* dar = da + ((long)q * k + j) * H;
+#pragma omp parallel for schedule(static)
+                for (int c = 0; c < H; ++c) {
+                    const double* gr = WB.g + (long)c * I;
+                    const double* ur = WB.u + (long)c * I;
+                    double sacc = 0.0;
+                    for (int i = 0; i < I; ++i) sacc += dg[i] * gr[i] + du[i] * ur[i];
+                    dar[c] = sacc;
+                }
+                free(af); free(G); free(U); free(hq); free(y); free(dyq); free(dg); free(du);
+            }
+        }
+        /* ---- the sampled weight-gradient columns of this expert */
+        int r0 = offsets[e], nr = offsets[e + 1] - offsets[e];
+        for (int qc = 0; qc < n_col; ++qc) {
+            if (col_e[qc] != e) continue;
+            int i = col_i[qc];
+            double* og = dWg_s + (long)qc * H;
+            double* ou = dWu_s + (long)qc * H;
+            double* od = dWd_s + (long)qc * H;
+            for (int c = 0; c < H; ++c) { og[c] = 0.0; ou[c] = 0.0; od[c] = 0.0; }
+            if (nr == 0) continue;
+            double* A = (double*)malloc(sizeof(double) * (size_t)nr * H);
+            double* DY = (double*)malloc(sizeof(double) * (size_t)nr * H);
+            double* DGc = (double*)malloc(sizeof(double) * nr);
+            double* DUc = (double*)malloc(sizeof(double) * nr);
+            double* HBc = (double*)malloc(sizeof(double) * nr);
+            if (!A || !DY || !DGc || !DUc || !HBc) return ORC_ERR;
+#pragma omp parallel
+            {
+                double* af = (double*)malloc(sizeof(double) * H);
+                double* dyq = (double*)malloc(sizeof(double) * H);
+#pragma omp for schedule(static)
+                for (int rr = 0; rr < nr; ++rr) {
+                    int slot = row_src[r0 + rr];
+                    int t = slot / k;
+                    act_row(x, 0, t, H, ORC_BF16, A + (long)rr * H);
+                    act_row(x, 0, t, H, ORC_MXFP8, af);
+                    double Gv = 0.0, Uv = 0.0;
+                    for (int hh = 0; hh < H; ++hh) {
+                        Gv += af[hh] * W.g[(long)hh * I + i];
+                        Uv += af[hh] * W.u[(long)hh * I + i];
+                    }
+                    HBc[rr] = orc_round_bf16(silu(Gv) * Uv);
+                    for (int c = 0; c < H; ++c) {
+                        DY[(long)rr * H + c] = orc_round_bf16(w[slot] * bf16_to_f64(dY[(long)t * H + c]));
+                        dyq[c] = DY[(long)rr * H + c];
+                    }
+                    mx_roundtrip_vec(dyq, H);
+                    double dh = 0.0;
+                    for (int c = 0; c < H; ++c) dh += dyq[c] * WB.d[(long)i * H + c];
+                    double sg = 1.0 / (1.0 + exp(-Gv));
+                    DGc[rr] = orc_round_bf16(dh * Uv * sg * (1.0 + Gv * (1.0 - sg)));
+                    DUc[rr] = orc_round_bf16(dh * Gv * sg);
+                }
+                free(af); free(dyq);
+            }
+            mx_roundtrip_cols(A, nr, H);
+            mx_roundtrip_cols(DY, nr, H);
+            mx_roundtrip_cols(DGc, nr, 1);
+            mx_roundtrip_cols(DUc, nr, 1);
+            mx_roundtrip_cols(HBc, nr, 1);
+            for (int rr = 0; rr < nr; ++rr)
+                for (int c = 0; c < H; ++c) {
+                    og[c] += A[(long)rr * H + c] * DGc[rr];
+                    ou[c] += A[(long)rr * H + c] * DUc[rr];
+                    od[c] += HBc[rr] * DY[(long)rr * H + c];
+                }
+            free(A); free(DY); free(DGc); free(DUc); free(HBc);
+        }
+    }
+    free_expert(&W);
+    free_expert(&WB);
+    /* ---- dX rows: the token's da rows plus the router term */
+    for (int q = 0; q < n_tok; ++q) {
+        int t = tok[q];
+        double m = 0.0;
+        for (int j = 0; j < k; ++j) m += w[(long)t * k + j] * gw[(long)q * k + j];
+        double* o = dX_s + (long)q * H;
+        for (int c = 0; c < H; ++c) {
+            double sacc = 0.0;
+            for (int j = 0; j < k; ++j) sacc += da[((long)q * k + j) * H + c];
+            for (int j = 0; j < k; ++j) {
+                double dl = w[(long)t * k + j] * (gw[(long)q * k + j] - m);
+                sacc += dl * (double)W_r[(long)c * E + idx[(long)t * k + j]];
+            }
+            o[c] = sacc;
+        }
+    }
+    free(gw);
+    free(da);
+    return ORC_OK;
+}
+
 /* Columns dW_r[:, e] of the router gradient for the experts listed in
  * `col_e` (n_col of them), computed for inputs too large for the full
  * backward. The column of expert e sums x[t] * dl[t, j] over the tokens t

@@ -135,3 +135,39 @@ def test_fullsize_ring_stream_16x4096():
     r = oracle.route(xcat, inp.W_r, wl.k, inp.bias)
     ref = oracle.moe_forward(xcat, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_MXFP8, shared=inp.shared)
     assert_close(np.concatenate(got), ref, TOL[mok.MXFP8], "ring stream, batches 0 and 15")
+
+
+@pytest.mark.gpu
+def test_fullsize_mxfp8_backward_T4096():
+    """The MXFP8 training step at T=4096 (H=7168, I=2048, E=32, k=8): sampled
+    dX rows and weight-gradient columns against the oracle's MXFP8 backward,
+    and ten bitwise reruns."""
+    wl = synth.WORKLOADS["mxfp8_bwd_T4096"]
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    dY = to_dev_bf16(inp.dY)
+    layer.forward(x, training=True)
+    g = layer.backward(x, dY)
+    torch.cuda.synchronize()
+    assert layer.status(wl.T, training=True) == (mok.OK, 0)
+    r = oracle.route(inp.x, inp.W_r, wl.k)
+    toks = _sample_tokens(wl.T, n=4, seed=3)
+    rng = np.random.default_rng(4)
+    cols = [(int(e), int(i)) for e, i in zip(rng.integers(0, wl.E, 4), rng.integers(0, wl.I, 4))]
+    sX, sG, sU, sD = oracle.moe_backward_sampled(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, toks, cols,
+                                                 mode=oracle.MODE_MXFP8)
+    c = TOL[mok.MXFP8]
+    assert_close(host_bf16_f64(g["dX"][toks]), sX, c, "dX (MXFP8)")
+    gG = np.stack([host_bf16_f64(g["dW_gate"][e, :, i]) for e, i in cols])
+    gU = np.stack([host_bf16_f64(g["dW_up"][e, :, i]) for e, i in cols])
+    gD = np.stack([host_bf16_f64(g["dW_down"][e, i, :]) for e, i in cols])
+    assert_close(gG, sG, c, "dW_gate columns (MXFP8)")
+    assert_close(gU, sU, c, "dW_up columns (MXFP8)")
+    assert_close(gD, sD, c, "dW_down rows (MXFP8)")
+    first = {n: t.clone() for n, t in g.items()}
+    for _ in range(9):
+        layer.forward(x, training=True)
+        again = layer.backward(x, dY)
+        for n in first:
+            assert torch.equal(again[n].view(torch.uint8), first[n].view(torch.uint8)), n

@@ -638,3 +638,22 @@ def test_mxfp8_backward_exact_operands_equal_bf16_backward():
     for a, b in zip(mx, bf):
         assert np.array_equal(a, b)
     assert np.abs(mx[1]).max() > 0 and np.abs(mx[3]).max() > 0
+
+
+def test_sampled_mxfp8_backward_equals_full_mxfp8_backward():
+    """The one-by-one MXFP8 backward (dX rows, weight-gradient columns) gives
+    the full MXFP8 backward's numbers."""
+    wl = synth.small("t", T=70, H=64, I=64, E=4, k=2, backward=True)
+    inp = synth.make_inputs(wl, seed=43)
+    r = oracle.route(inp.x, inp.W_r, 2)
+    dX, dWg, dWu, dWd, dWr = oracle.moe_backward(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r,
+                                                  mode=oracle.MODE_MXFP8)
+    toks = [0, 33, 69]
+    cols = [(0, 3), (3, 63), (1, 0)]
+    sX, sG, sU, sD = oracle.moe_backward_sampled(inp.x, inp.W_r, inp.Wg, inp.Wu, inp.Wd, inp.dY, r, toks, cols,
+                                                 mode=oracle.MODE_MXFP8)
+    assert np.allclose(sX, dX[toks], rtol=1e-12, atol=1e-14 * np.abs(dX).max())
+    for q, (e, i) in enumerate(cols):
+        assert np.allclose(sG[q], dWg[e][:, i], rtol=1e-12, atol=1e-14 * np.abs(dWg).max())
+        assert np.allclose(sU[q], dWu[e][:, i], rtol=1e-12, atol=1e-14 * np.abs(dWu).max())
+        assert np.allclose(sD[q], dWd[e][i, :], rtol=1e-12, atol=1e-14 * np.abs(dWd).max())
