@@ -60,6 +60,35 @@ PackedLayout packed_layout(int E, int H, int I, int dtype) {
     return L;
 }
 
+// The MXFP8 backward's weight copies: W_down as [E*I, H] blocked along H,
+// W_gate and W_up as [E*H, I] blocked along I (codes, then chunk-ordered
+// scales).
+struct PackedBwdLayout {
+    size_t wd, wdsf, wg, wgsf, wu, wusf, total;
+};
+
+PackedBwdLayout packed_bwd_layout(int E, int H, int I) {
+    PackedBwdLayout L{};
+    const int64_t n = (int64_t)E * H * I;
+    size_t o = 0;
+    L.wd = o; o += align_up(n, 1024);
+    L.wdsf = o; o += align_up(n / 32, 1024);
+    L.wg = o; o += align_up(n, 1024);
+    L.wgsf = o; o += align_up(n / 32, 1024);
+    L.wu = o; o += align_up(n, 1024);
+    L.wusf = o; o += align_up(n / 32, 1024);
+    L.total = o;
+    return L;
+}
+
+cudaError_t pack_bwd(const void* Wg, const void* Wu, const void* Wd, int E, int H, int I, char* b, cudaStream_t s) {
+    PackedBwdLayout L = packed_bwd_layout(E, H, I);
+    cudaError_t e = launch_quantize_rows_tiled(Wd, (int64_t)E * I, H, b + L.wd, b + L.wdsf, s);
+    if (e == cudaSuccess) e = launch_quantize_rows_tiled(Wg, (int64_t)E * H, I, b + L.wg, b + L.wgsf, s);
+    if (e == cudaSuccess) e = launch_quantize_rows_tiled(Wu, (int64_t)E * H, I, b + L.wu, b + L.wusf, s);
+    return e;
+}
+
 // Forward buffers. When `saved` is given (BF16 training), A, GU, h and the
 // partials live there so the backward can read them.
 struct FwdLayout {
@@ -129,9 +158,8 @@ BwdLayout bwd_layout(const mok_problem* p) {
         };
         q(L.dyq, L.dysf, rows, H);
         q(L.dguq, L.dgusf, rows, 2 * I);
-        q(L.wdq, L.wdsf, E * I, H);
-        q(L.wgq, L.wgsf, E * H, I);
-        q(L.wuq, L.wusf, E * H, I);
+        L.wdq = o;   // the weights' backward copies when the caller passes none
+        o += packed_bwd_layout((int)E, (int)H, (int)I).total;
         q(L.atq, L.atsf, H, rows);
         q(L.gutq, L.gutsf, 2 * I, rows);
         q(L.htq, L.htsf, I, rows);
@@ -267,6 +295,20 @@ mok_status mok_route_layout(const void* x, const float* W_r, const float* bias, 
     if (!device_ok()) return MOK_ERR_CUDA;
     return cuda_status(launch_route_layout(x, W_r, bias, T, H, E, k, topk_idx, topk_w, counts, offsets, row_src,
                                            slot_row, workspace, (cudaStream_t)stream));
+}
+
+size_t mok_packed_weights_bwd_size(int32_t E, int32_t H, int32_t I, int32_t dtype) {
+    if (dtype != MOK_MXFP8 || !dims_ok(E, H, I, dtype)) return 0;
+    return packed_bwd_layout(E, H, I).total;
+}
+
+mok_status mok_pack_weights_bwd(int32_t E, int32_t H, int32_t I, int32_t dtype, const void* W_gate, const void* W_up,
+                                const void* W_down, void* packed_bwd, size_t bytes, mok_stream_t stream) {
+    if (dtype != MOK_MXFP8 || !dims_ok(E, H, I, dtype) || !W_gate || !W_up || !W_down || !packed_bwd)
+        return MOK_ERR_INVALID;
+    if (bytes < packed_bwd_layout(E, H, I).total || !aligned(packed_bwd, 256)) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(pack_bwd(W_gate, W_up, W_down, E, H, I, static_cast<char*>(packed_bwd), (cudaStream_t)stream));
 }
 
 size_t mok_packed_weights_size(int32_t E, int32_t H, int32_t I, int32_t dtype) {
@@ -547,6 +589,7 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
         !a->dW_r || !a->workspace)
         return MOK_ERR_INVALID;
     if (p->T > 0 && (!a->x || !a->dY || !a->dX)) return MOK_ERR_INVALID;   // token arrays may be empty
+    if (a->packed_bwd && (p->dtype != MOK_MXFP8 || !aligned(a->packed_bwd, 256))) return MOK_ERR_INVALID;
     if (a->ws_bytes < mok_workspace_size(p, cfg) || !aligned(a->workspace, 1024) || !aligned(a->saved, 1024) ||
         !aligned(a->dW_gate, 16) || !aligned(a->dW_up, 16) || !aligned(a->dW_down, 16))
         return MOK_ERR_INVALID;
@@ -591,19 +634,26 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
         auto Q = [&](size_t off) { return ws + off; };
         auto QS = [&](size_t off) { return reinterpret_cast<uint8_t*>(ws + off); };
         const int64_t rp = rows_tiles(p);
-        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_down, (int64_t)E * I, H, Q(L.wdq), QS(L.wdsf), s);
-        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_gate, (int64_t)E * H, I, Q(L.wgq), QS(L.wgsf), s);
-        if (e == cudaSuccess) e = launch_quantize_rows_tiled(a->W_up, (int64_t)E * H, I, Q(L.wuq), QS(L.wusf), s);
+        // the weights' backward copies: packed once by the caller
+        // (mok_pack_weights_bwd), or made here into the workspace
+        const PackedBwdLayout PB = packed_bwd_layout(E, H, I);
+        char* pb = a->packed_bwd ? static_cast<char*>(const_cast<void*>(a->packed_bwd)) : nullptr;
+        if (!pb && e == cudaSuccess) {
+            pb = ws + L.wdq;   // the workspace's weight-copy region has the same layout
+            e = pack_bwd(a->W_gate, a->W_up, a->W_down, E, H, I, pb, s);
+        }
+        auto WQ = [&](size_t off) { return pb + off; };
+        auto WS = [&](size_t off) { return reinterpret_cast<uint8_t*>(pb + off); };
         // dh = dy W_down^T (K = H), dSwiGLU -> dG|dU (BF16)
         if (e == cudaSuccess) e = launch_quantize_rows_tiled(dy, rp, H, Q(L.dyq), QS(L.dysf), s);
         if (e == cudaSuccess)
-            e = gemm_dgrad_h_mx(Q(L.dyq), QS(L.dysf), Q(L.wdq), QS(L.wdsf), E, H, I, r.counts, rows, sv + FL.sGU, dgu,
-                                c, s);
+            e = gemm_dgrad_h_mx(Q(L.dyq), QS(L.dysf), WQ(PB.wd), WS(PB.wdsf), E, H, I, r.counts, rows, sv + FL.sGU,
+                                dgu, c, s);
         // da = dG W_gate^T + dU W_up^T (K = I), pushed to the slots
         if (e == cudaSuccess) e = launch_quantize_rows_tiled(dgu, rp, 2 * I, Q(L.dguq), QS(L.dgusf), s);
         if (e == cudaSuccess)
-            e = gemm_dgrad_a_mx(Q(L.dguq), QS(L.dgusf), Q(L.wgq), QS(L.wgsf), Q(L.wuq), QS(L.wusf), E, H, I, r.counts,
-                                r.offsets, r.row_src, rows, da, c, s);
+            e = gemm_dgrad_a_mx(Q(L.dguq), QS(L.dgusf), WQ(PB.wg), WS(PB.wgsf), WQ(PB.wu), WS(PB.wusf), E, H, I,
+                                r.counts, r.offsets, r.row_src, rows, da, c, s);
         // weight gradients over each expert's tokens: operands blocked along the tokens
         if (e == cudaSuccess) e = launch_quantize_cols_tiled(sv + FL.sA, rp, H, Q(L.atq), QS(L.atsf), s);
         if (e == cudaSuccess) e = launch_quantize_cols_tiled(dgu, rp, 2 * I, Q(L.gutq), QS(L.gutsf), s);

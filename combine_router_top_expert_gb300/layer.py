@@ -30,6 +30,8 @@ class MoELayer:
         self.bias = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias, dtype=np.float32)).to(device)
         Wg_d, Wu_d, Wd_d = (to_dev_bf16(a, device) for a in (Wg, Wu, Wd))
         self.packed = mok.pack_weights(Wg_d, Wu_d, Wd_d, dtype)
+        # MXFP8 training: the backward's weight copies, packed once like the forward's
+        self.packed_bwd = mok.pack_weights_bwd(Wg_d, Wu_d, Wd_d, dtype) if keep_unpacked else None
         self.Wg, self.Wu, self.Wd = (Wg_d, Wu_d, Wd_d) if keep_unpacked else (None, None, None)
         self.I_shared = 0
         self.packed_shared = None
@@ -89,7 +91,7 @@ class MoELayer:
                          dW_down=torch.empty_like(self.Wd),
                          dW_r=torch.empty((self.H, self.E), dtype=torch.float32, device=self.device))
         mok.moe_backward(self.problem(T), x, self.W_r, self.Wg, self.Wu, self.Wd, self.packed, dY, b["routing"],
-                         b["saved"], grads, b["ws"], cfg=cfg, stream=stream)
+                         b["saved"], grads, b["ws"], cfg=cfg, stream=stream, packed_bwd=self.packed_bwd)
         return grads
 
     def status(self, T, training=False):

@@ -27,7 +27,7 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches",
            "mok_quantize_rows", "mok_dispatch_quantized", "mok_route_test_hook", "mok_ep_workspace_size",
-           "mok_ep_dispatch", "mok_ep_push"]
+           "mok_ep_dispatch", "mok_ep_push", "mok_packed_weights_bwd_size", "mok_pack_weights_bwd"]
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
@@ -74,7 +74,7 @@ class BwdArgs(ctypes.Structure):
                 ("dY", ctypes.c_void_p), ("routing", Routing), ("saved", ctypes.c_void_p),
                 ("dX", ctypes.c_void_p), ("dW_gate", ctypes.c_void_p), ("dW_up", ctypes.c_void_p),
                 ("dW_down", ctypes.c_void_p), ("dW_r", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("ws_bytes", ctypes.c_size_t)]
+                ("ws_bytes", ctypes.c_size_t), ("packed_bwd", ctypes.c_void_p)]
 
 
 class EpPeer(ctypes.Structure):
@@ -106,6 +106,9 @@ def lib():
             L.mok_packed_weights_size.argtypes = [I32] * 4
             L.mok_packed_weights_size.restype = SZ
             L.mok_pack_weights.argtypes = [I32, I32, I32, I32, P, P, P, P, SZ, P]
+            L.mok_packed_weights_bwd_size.argtypes = [I32] * 4
+            L.mok_packed_weights_bwd_size.restype = SZ
+            L.mok_pack_weights_bwd.argtypes = [I32, I32, I32, I32, P, P, P, P, SZ, P]
             L.mok_workspace_size.argtypes = [PP, PC]
             L.mok_workspace_size.restype = SZ
             L.mok_saved_size.argtypes = [PP]
@@ -135,7 +138,7 @@ def lib():
             for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
                          "mok_moe_forward_batches", "mok_dispatch", "mok_quantize_rows", "mok_dispatch_quantized",
                          "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_route_test_hook",
-                         "mok_ep_dispatch", "mok_ep_push"):
+                         "mok_ep_dispatch", "mok_ep_push", "mok_pack_weights_bwd"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -273,6 +276,20 @@ def pack_weights(Wg, Wu, Wd, dtype, packed=None, stream=None):
     return packed
 
 
+def pack_weights_bwd(Wg, Wu, Wd, dtype, packed_bwd=None, stream=None):
+    """The MXFP8 backward's weight copies (None for BF16)."""
+    E, H, I = Wg.shape
+    n = int(lib().mok_packed_weights_bwd_size(E, H, I, dtype))
+    if n == 0:
+        return None
+    if packed_bwd is None:
+        packed_bwd = alloc_bytes(n, Wg.device)
+    rc = lib().mok_pack_weights_bwd(E, H, I, dtype, _ptr(_bf16(Wg)), _ptr(_bf16(Wu)), _ptr(_bf16(Wd)),
+                                    _ptr(packed_bwd), packed_bwd.numel(), _stream(stream))
+    _check(rc, "mok_pack_weights_bwd")
+    return packed_bwd
+
+
 def moe_forward(p: Problem, x, packed, routing, out, workspace, saved=None, packed_shared=None,
                 cfg: Config | None = None, stream=None):
     a = FwdArgs(x.data_ptr(), packed.data_ptr(), packed_shared.data_ptr() if packed_shared is not None else None,
@@ -299,12 +316,13 @@ def moe_forward_batches(p: Problem, xs, packed, routings, outs, workspace, packe
 
 
 def moe_backward(p: Problem, x, W_r, Wg, Wu, Wd, packed, dY, routing, saved, grads, workspace,
-                 cfg: Config | None = None, stream=None):
+                 cfg: Config | None = None, stream=None, packed_bwd=None):
     """grads: dict with dX, dW_gate, dW_up, dW_down, dW_r (preallocated)."""
     a = BwdArgs(x.data_ptr(), W_r.data_ptr(), Wg.data_ptr(), Wu.data_ptr(), Wd.data_ptr(), packed.data_ptr(),
                 dY.data_ptr(), routing_struct(routing), saved.data_ptr(), grads["dX"].data_ptr(),
                 grads["dW_gate"].data_ptr(), grads["dW_up"].data_ptr(), grads["dW_down"].data_ptr(),
-                grads["dW_r"].data_ptr(), workspace.data_ptr(), workspace.numel())
+                grads["dW_r"].data_ptr(), workspace.data_ptr(), workspace.numel(),
+                packed_bwd.data_ptr() if packed_bwd is not None else None)
     rc = lib().mok_moe_backward(ctypes.byref(p), ctypes.byref(a), ctypes.byref(cfg) if cfg else None,
                                 _stream(stream))
     _check(rc, "mok_moe_backward")

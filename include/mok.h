@@ -332,7 +332,21 @@ typedef struct {
     float* dW_r;            /* [H,E] f32 */
     void* workspace;
     size_t ws_bytes;
+    const void* packed_bwd; /* MXFP8: the weights' backward copies from mok_pack_weights_bwd, or NULL
+                               (then they are made in each call, in the workspace); NULL for BF16 */
 } mok_bwd_args;
+
+/* Bytes of the MXFP8 backward's weight copies (0 unless dtype == MOK_MXFP8). */
+size_t mok_packed_weights_bwd_size(int32_t E, int32_t H, int32_t I, int32_t dtype);
+
+/* The MXFP8 backward's weight copies, made once per weight update like the
+ * forward's packing: W_down [E,I,H] quantised along H (for dh = dy W_down^T)
+ * and W_gate, W_up [E,H,I] along I (for da), E4M3 codes with E8M0 scales in
+ * the tensor-core chunk order. packed_bwd: mok_packed_weights_bwd_size bytes,
+ * 256-B aligned. */
+mok_status mok_pack_weights_bwd(int32_t E, int32_t H, int32_t I, int32_t dtype, const void* W_gate,
+                                const void* W_up, const void* W_down, void* packed_bwd, size_t bytes,
+                                mok_stream_t stream);
 
 /* Backward of the layer ([K-ja] 02: pull on reverse-combine, push on
  * reverse-dispatch). Reverse-combine pulls dy[row] = w[t,j] * dY[t] into
@@ -351,7 +365,8 @@ typedef struct {
  * along H for dh, dG|dU and W_gate, W_up along I for da, and x, h, dy, dG,
  * dU along each expert's rows for the weight gradients (quantised from the
  * BF16 values, transposed so the tokens are the K dimension). The weights'
- * backward copies are quantised in each call (into the workspace). A shared
+ * backward copies come from a->packed_bwd (mok_pack_weights_bwd), or are
+ * quantised in the call into the workspace when it is NULL. A shared
  * expert (I_shared > 0) has no backward here: MOK_ERR_UNSUPPORTED. */
 mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a,
                             const mok_config* cfg, mok_stream_t stream);

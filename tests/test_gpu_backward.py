@@ -119,3 +119,19 @@ def test_mxfp8_backward_bitwise_deterministic():
         again = layer.backward(x, dY)
         for n in first:
             assert torch.equal(again[n].view(torch.uint8), first[n].view(torch.uint8)), n
+
+
+@pytest.mark.gpu
+def test_mxfp8_backward_weight_copies_packed_or_per_call():
+    """The weights' MXFP8 backward copies packed once (mok_pack_weights_bwd)
+    or quantised inside the call (packed_bwd NULL) give the same bits."""
+    wl = MX_BWD_CASES[0]
+    inp, layer, x, dY, out_inf, out, g = _run_mx(wl, seed=4)
+    first = {n: t.clone() for n, t in g.items()}
+    b = layer.buffers(wl.T, True)
+    grads = {n: torch.empty_like(t) for n, t in first.items()}
+    mok.moe_backward(layer.problem(wl.T), x, layer.W_r, layer.Wg, layer.Wu, layer.Wd, layer.packed, dY,
+                     b["routing"], b["saved"], grads, b["ws"], packed_bwd=None)
+    torch.cuda.synchronize()
+    for n in first:
+        assert torch.equal(grads[n].view(torch.uint8), first[n].view(torch.uint8)), n
