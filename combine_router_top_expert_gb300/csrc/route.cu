@@ -93,17 +93,15 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
 // L owns summation chain L (h = 256*i + 8*L + m). The chunks (c, g) of the
 // router weights (one 32 KB bulk copy each, from the layout above) and the
 // matching raw x rows (one bulk copy per token) stream through a STAGES-deep
-// shared-memory ring with a full and an empty mbarrier per slot; thread 0
-// issues the copies of a slot once every warp has released it. Each warp
-// reads its tokens' raw BF16 x straight from the ring (16 bytes per lane:
-// its chain's 8 h values in order) and widens them in registers, so no
-// CTA-wide barrier orders the chunks. Every wait is bounded: after a timeout
-// the status block records it, no thread waits again, and the CTA runs to
-// its end (its logits are then replaced by zeros; the caller sees
-// MOK_ERR_TIMEOUT).
+// shared-memory ring, one mbarrier per slot; thread 0 issues the copies. x
+// is converted to fp32 once per CTA, one chunk ahead, into a double buffer,
+// so the inner loop is fused multiply-adds fed by conflict-free 16-byte
+// shared loads. Every wait is bounded: after a timeout the status block
+// records it, no thread waits again, and the CTA runs to its end (its
+// results are then garbage; the caller sees MOK_ERR_TIMEOUT).
 // Dynamic shared memory:
-//   bars [2][STAGES] u64 (256 B) | ws [STAGES][32][256] f32 | xr [STAGES][TT][256] bf16 |
-//   lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
+//   bars [STAGES] u64 (128 B) | ws [STAGES][32][256] f32 | xr [STAGES][TT][256] bf16 |
+//   xf [2][TT][256] f32 | lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
 template <int TW, int STAGES>
 __global__ void __launch_bounds__(kTopkThreads)
 route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr_copies, int wr_copies,
@@ -112,14 +110,13 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
                   int withhold) {
     constexpr int TT = 2 * TW;
     constexpr int NT = kTopkThreads;
-    constexpr int NWARPS = NT / 32;
     static_assert(TT <= kRouteTTMax && TT >= kRouteTTMin && STAGES >= 3 && STAGES <= 16, "router tile");
     extern __shared__ __align__(128) unsigned char route_smem[];
-    const uint32_t full0 = tc::smem_u32(route_smem);
-    const uint32_t empty0 = full0 + 8u * 16u;
-    float* ws = reinterpret_cast<float*>(route_smem + 256);
+    const uint32_t bar0 = tc::smem_u32(route_smem);
+    float* ws = reinterpret_cast<float*>(route_smem + 128);
     __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(ws + STAGES * 32 * kRouteChunk);
-    float* lg = reinterpret_cast<float*>(xr + STAGES * TT * kRouteChunk);
+    float* xf = reinterpret_cast<float*>(xr + STAGES * TT * kRouteChunk);
+    float* lg = xf + 2 * TT * kRouteChunk;
     float* slog = lg + TT * E;
     int32_t* cnt = reinterpret_cast<int32_t*>(slog + TT * k);
 
@@ -133,35 +130,25 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
     const float* __restrict__ Wr = Wr_copies + (int64_t)(blockIdx.x % wr_copies) * total * router_chunk_floats();
 
     for (int e = tid; e < E; e += NT) cnt[e] = 0;
-    for (int i = tid; i < TT * E; i += NT) lg[i] = 0.f;
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            tc::mbar_init(full0 + 8u * s, 1);
-            tc::mbar_init(empty0 + 8u * s, NWARPS);
-        }
+        for (int s = 0; s < STAGES; ++s) tc::mbar_init(bar0 + 8u * s, 1);
         tc::fence_mbar_init();
     }
     __syncthreads();
 
     bool ok = true;
     int issued = 0, seen = 0;   // thread 0: chunks issued / chunks it has seen land
+    // thread 0: the copies of chunk n into slot n % STAGES (nothing more
+    // once one of its waits gave up)
     // withhold (test hook): CTA 0 never issues chunk 1, so its wait runs out
     const bool hold = withhold != 0 && blockIdx.x == 0;
-    // thread 0: the copies of chunk n into slot n % STAGES, once every warp
-    // has released the slot's previous chunk (nothing more once a wait gave up)
     auto issue = [&](int n) {
         if (!ok || n >= total) return;
-        const int slot = n % STAGES;
-        if (n >= STAGES &&
-            !tc::mbar_wait(empty0 + 8u * slot, (uint32_t)(((n - STAGES) / STAGES) & 1), st, tmo, kSiteRouterChunk)) {
-            ok = false;
-            return;
-        }
         issued = n + 1;
         if (hold && n == 1) return;
-        const int g = n / nchunks, c = n % nchunks;
+        const int g = n / nchunks, c = n % nchunks, slot = n % STAGES;
         const int h0 = c * kRouteChunk, hw = min(kRouteChunk, H - h0);
-        const uint32_t bar = full0 + 8u * slot;
+        const uint32_t bar = bar0 + 8u * slot;
         tc::mbar_expect_tx(bar, (uint32_t)(router_chunk_floats() * 4 + (int64_t)ntok * hw * 2));
         tc::bulk_load(tc::smem_u32(ws + slot * 32 * kRouteChunk),
                       Wr + ((int64_t)c * EG + g) * router_chunk_floats(), (uint32_t)(router_chunk_floats() * 4), bar);
@@ -169,14 +156,34 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         for (int t = 0; t < ntok; ++t)
             tc::bulk_load(xd + t * kRouteChunk * 2, x + (int64_t)(t0 + t) * H + h0, (uint32_t)hw * 2, bar);
     };
+    auto wait = [&](int n) {
+        if (ok && n < total) {
+            ok = tc::mbar_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1), st, tmo, kSiteRouterChunk);
+            if (ok) seen = n + 1;
+        }
+    };
+    // raw x of slot b -> fp32 buffer d (the h order above)
+    auto convert_x = [&](int b, int d) {
+        const __nv_bfloat16* xb = xr + b * TT * kRouteChunk;
+        for (int v = tid; v < TT * (kRouteChunk / 8); v += NT) {
+            const int t = v / (kRouteChunk / 8), L = v % (kRouteChunk / 8);
+            const uint4 r = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * L);
+            float* o = xf + (d * TT + t) * kRouteChunk + 4 * L;
+            *reinterpret_cast<float4*>(o) = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
+            *reinterpret_cast<float4*>(o + 128) = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
+        }
+    };
 
     if (tid == 0)
         for (int n = 0; n < STAGES - 1; ++n) issue(n);
+    wait(0);
+    convert_x(0, 0);
     float acc[TW][4];
     for (int n = 0; n < total; ++n) {
-        const int slot = n % STAGES;
-        if (ok && !tc::mbar_wait(full0 + 8u * slot, (uint32_t)((n / STAGES) & 1), st, tmo, kSiteRouterChunk)) ok = false;
-        if (tid == 0 && ok) seen = n + 1;
+        wait(n + 1);       // its x is converted below
+        __syncthreads();   // x(n) converted by every thread; chunk n - 1 consumed
+        if (tid == 0) issue(n + STAGES - 1);   // into slot (n - 1) % STAGES
+        if (n + 1 < total) convert_x((n + 1) % STAGES, (n + 1) & 1);
         const int g = n / nchunks, c = n % nchunks;
         if (c == 0) {
 #pragma unroll
@@ -184,8 +191,8 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
         }
-        const float* wb = ws + slot * 32 * kRouteChunk;
-        const __nv_bfloat16* xb = xr + (slot * TT + tg * TW) * kRouteChunk;
+        const float* wb = ws + (n % STAGES) * 32 * kRouteChunk;
+        const float* xb = xf + ((n & 1) * TT + tg * TW) * kRouteChunk;
         if (c * kRouteChunk + 8 * lane < H) {
             float wv[4][8];
 #pragma unroll
@@ -205,11 +212,11 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     if (t2 + u < TW) {
-                        const uint4 r = *reinterpret_cast<const uint4*>(xb + (t2 + u) * kRouteChunk + 8 * lane);
-                        xv[u][0] = bf16_lo(r.x); xv[u][1] = bf16_hi(r.x);
-                        xv[u][2] = bf16_lo(r.y); xv[u][3] = bf16_hi(r.y);
-                        xv[u][4] = bf16_lo(r.z); xv[u][5] = bf16_hi(r.z);
-                        xv[u][6] = bf16_lo(r.w); xv[u][7] = bf16_hi(r.w);
+                        const float* xr2 = xb + (t2 + u) * kRouteChunk + 4 * lane;
+                        const float4 a = *reinterpret_cast<const float4*>(xr2);
+                        const float4 b = *reinterpret_cast<const float4*>(xr2 + 128);
+                        xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
+                        xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
                     }
                 }
 #pragma unroll
@@ -222,30 +229,26 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
                         }
             }
         }
-        // this warp is done with the slot: release it to the producer
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(empty0 + 8u * slot);
         if (c == nchunks - 1) {
             // butterfly across the 32 chains, then the bias
 #pragma unroll
             for (int t = 0; t < TW; ++t)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    float sum = acc[t][q];
+                    float s = acc[t][q];
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) sum = sum + __shfl_xor_sync(0xffffffffu, sum, off);
+                    for (int off = 16; off >= 1; off >>= 1) s = s + __shfl_xor_sync(0xffffffffu, s, off);
                     const int e = 32 * g + 4 * quad + q, tt = tg * TW + t;
-                    if (lane == 0 && e < E && tt < ntok) lg[tt * E + e] = bias ? sum + bias[e] : sum;
+                    if (lane == 0 && e < E && tt < ntok) lg[tt * E + e] = bias ? s + bias[e] : s;
                 }
         }
-        if (tid == 0) issue(n + STAGES - 1);   // into the slot chunk n - 1 used
     }
     if (tid == 0 && seen < issued) {
         // a wait gave up: let the copies still in flight (at most one per
         // slot) land before the CTA exits, within the same time bound
         const uint64_t start = globaltimer_ns();
         for (int n = seen; n < issued; ++n)
-            while (!(hold && n == 1) && !tc::mbar_try_wait(full0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1)) &&
+            while (!(hold && n == 1) && !tc::mbar_try_wait(bar0 + 8u * (n % STAGES), (uint32_t)((n / STAGES) & 1)) &&
                    globaltimer_ns() - start < tmo) {
             }
     }
@@ -306,8 +309,8 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 }
 
 size_t route_topk_smem_bytes(int TT, int STAGES, int E, int k) {
-    return (size_t)256 + (size_t)STAGES * 32 * kRouteChunk * 4 + (size_t)STAGES * TT * kRouteChunk * 2 +
-           (size_t)TT * E * 4 + (size_t)TT * k * 4 + (size_t)E * 4;
+    return (size_t)128 + (size_t)STAGES * 32 * kRouteChunk * 4 + (size_t)STAGES * TT * kRouteChunk * 2 +
+           (size_t)2 * TT * kRouteChunk * 4 + (size_t)TT * E * 4 + (size_t)TT * k * 4 + (size_t)E * 4;
 }
 
 // Counts, offsets and the stable (expert, token) permutation. CTA b handles
@@ -419,7 +422,7 @@ cudaError_t launch_topk_variant(const __nv_bfloat16* x, const float* Wr, int wr_
 // is about (fixed cost of streaming every weight chunk, worth ~5 tokens per
 // warp) + TW, so the kernel takes about rounds x (TW + 5), rounds = CTAs
 // over SMs. Pick the cheapest that fits shared memory, larger tiles on ties.
-constexpr int kRouteStages(int tw) { return tw == 14 ? 4 : tw == 9 ? 5 : 6; }
+constexpr int kRouteStages(int tw) { return tw == 14 ? 3 : 4; }
 int route_tokens_per_cta(int T, int num_sms, int E, int k) {
     const int tws[4] = {14, 9, 4, 2};
     int best = 2;
@@ -439,15 +442,9 @@ cudaError_t launch_route_topk(const __nv_bfloat16* x, const float* Wr, const flo
     const int r = route_wr_copies(E, H);
     if (tt == 28) return launch_topk_variant<14, kRouteStages(14)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist,
                                                                    st, tmo, hold, s);
-    if (tt == 18)
-        return launch_topk_variant<9, kRouteStages(9)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo,
-                                                       hold, s);
-    if (tt == 8)
-        return launch_topk_variant<4, kRouteStages(4)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo,
-                                                       hold, s);
-    if (tt == 4)
-        return launch_topk_variant<2, kRouteStages(2)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo,
-                                                       hold, s);
+    if (tt == 18) return launch_topk_variant<9, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
+    if (tt == 8) return launch_topk_variant<4, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
+    if (tt == 4) return launch_topk_variant<2, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
     return cudaErrorInvalidValue;
 }
 
