@@ -364,18 +364,15 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
         part = torch.empty((T * wl.k, H), dtype=torch.bfloat16, device=dev)
         out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         status_ws = b["ws"]
-        mx_once = dtype == mok.MXFP8   # MXFP8: quantise each token once, then gather its bytes
-        xq = mok.alloc_bytes(T * H, dev) if mx_once else None
-        xsf = mok.alloc_bytes(T * H // 32, dev) if mx_once else None
+        mx_once = dtype == mok.MXFP8   # MXFP8: one token-major pass quantises each token once
 
         def step(ev=None):
-            # route/layout, dispatch, grouped GEMMs, combine (7 launches; MXFP8 8)
+            # route/layout, dispatch, grouped GEMMs, combine (7 launches)
             layer.route(x, stream=stream)
             if ev is not None:
                 ev[2].record(stream)
             if mx_once:
-                mok.quantize_rows(x, xq, xsf, stream=stream)
-                mok.dispatch_quantized(p, xq, xsf, rt, A, A_sf, stream=stream)
+                mok.dispatch_tokens(p, x, rt, A, A_sf, stream=stream)
             else:
                 mok.dispatch(p, x, rt, A, A_sf, stream=stream)
             if ev is not None:
@@ -384,7 +381,7 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
             if ev is not None:
                 ev[1].record(stream)
             mok.combine(p, part, rt["topk_w"], out, stream=stream)
-        launches_per_step = 8 if mx_once else 7
+        launches_per_step = 7
         flops = 6.0 * H * wl.I * T * wl.k
         kern = "grouped expert GEMMs (gate/up+SwiGLU, down+push; 2 launches)"
     else:

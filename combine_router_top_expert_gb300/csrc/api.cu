@@ -382,6 +382,16 @@ mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const v
                                          static_cast<uint8_t*>(A_sf), (cudaStream_t)stream));
 }
 
+mok_status mok_dispatch_tokens(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
+                               mok_stream_t stream) {
+    if (!problem_ok(p) || p->dtype != MOK_MXFP8 || !routing_ok(r, p->T) || !A || !A_sf || !aligned(A, 16))
+        return MOK_ERR_INVALID;
+    if (p->T > 0 && (!x || !aligned(x, 16))) return MOK_ERR_INVALID;
+    if (!device_ok()) return MOK_ERR_CUDA;
+    return cuda_status(launch_dispatch_tokens(x, p->T, p->H, p->E, p->k, r->topk_idx, r->slot_row, r->counts,
+                                              r->offsets, A, static_cast<uint8_t*>(A_sf), (cudaStream_t)stream));
+}
+
 mok_status mok_expert_ffn(const mok_problem* p, const void* A, const void* A_sf, const void* packed,
                           const mok_routing* r, void* h, void* h_sf, void* partials, const mok_config* cfg,
                           void* workspace, mok_stream_t stream) {
@@ -539,7 +549,8 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
         // pad rows stay unwritten for inference (their GEMM rows are never
         // stored); training keeps them zero for the weight gradients
         if (mx && !training)
-            e = launch_quantize_rows(a->x, p->T, p->H, ws + L.xq, ws + L.xsf, s);
+            e = launch_dispatch_tokens(a->x, p->T, p->H, p->E, p->k, r.topk_idx, r.slot_row, r.counts, r.offsets, A,
+                                       A_sf, s);
         else if (mx)   // MXFP8 training: BF16 rows saved for the weight gradients, quantised for the GEMM
             e = launch_dispatch(false, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, sv + L.sA,
                                 nullptr, nullptr, nullptr, s, true);
@@ -547,9 +558,6 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
             e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
                                 nullptr, s, training);
     }
-    if (e == cudaSuccess && mx && !training)
-        e = launch_dispatch_q(ws + L.xq, ws + L.xsf, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A,
-                              A_sf, s);
     if (e == cudaSuccess && mx && training) e = launch_quantize_rows_tiled(sv + L.sA, rows_tiles(p), p->H, A, A_sf, s);
     if (e == cudaSuccess && use_swap(p, cfg, training)) {
         e = gemm_gateup_swap(A, pk + PL.gu, p->E, p->H, p->I, r.counts, rows, h, swap_policy(cfg), c, s);

@@ -131,6 +131,48 @@ dispatch_q_kernel(const uint8_t* __restrict__ xq, const uint32_t* __restrict__ x
     }
 }
 
+// MXFP8 pull-dispatch in one token-major pass: a warp takes a token, each
+// lane quantises 128-wide chunks of its row once (four 32-element blocks,
+// the same encoder as quantize_rows) and writes the codes and the chunk's
+// scale word to each of the token's k rows of the padded expert-contiguous
+// layout. Every token row is read once from HBM and no quantised copy of x
+// is written and read back. Pad rows are not written. The bytes equal those
+// of quantize_rows + dispatch_q.
+__global__ void __launch_bounds__(256)
+dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E, int k,
+                       const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_row,
+                       const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
+                       uint8_t* __restrict__ A, uint8_t* __restrict__ A_sf) {
+    __shared__ int32_t poff[kMaxE + 1];
+    padded_offsets(counts, E, poff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kc_row = H / 128;
+    for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < T; t += (int64_t)gridDim.x * 8) {
+        // padded destination row of slot j (lane j holds it when k <= 32)
+        auto dest = [&](int j) {
+            const int64_t sl = t * k + j;
+            const int e = topk_idx[sl];
+            return poff[e] + slot_row[sl] - offsets[e];
+        };
+        const int my_pr = (k <= 32 && lane < k) ? dest(lane) : 0;
+        for (int q = lane; q < kc_row; q += 32) {
+            uint4 o[8];
+            uint32_t word = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                word |= quantize_block32(x + t * H + q * 128 + 32 * b, o[2 * b], o[2 * b + 1]) << (8 * b);
+            for (int j = 0; j < k; ++j) {
+                const int pr = k <= 32 ? __shfl_sync(__activemask(), my_pr, j) : dest(j);
+                uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H + q * 128);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) __stcs(dst + i, o[i]);
+                *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)(pr / kTileM) * kc_row + q) * 512 +
+                                             sf_chunk_offset(pr % kTileM, 0)) = word;
+            }
+        }
+    }
+}
+
 template <bool MX>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
@@ -489,6 +531,16 @@ cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, 
                                                       offsets, row_src, A, nullptr,
                                                       static_cast<const __nv_bfloat16*>(scale_src), wslot,
                                                       zero_pads ? 1 : 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, const int32_t* topk_idx,
+                                   const int32_t* slot_row, const int32_t* counts, const int32_t* offsets, void* A,
+                                   uint8_t* A_sf, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int blocks = (int)std::min<int64_t>(ceil_div(T, 8), (int64_t)sm_count() * 8);
+    dispatch_tokens_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx,
+                                                  slot_row, counts, offsets, static_cast<uint8_t*>(A), A_sf);
     return cudaGetLastError();
 }
 

@@ -105,6 +105,11 @@ cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, 
 // MXFP8 quantisation of each row of x [T, H] (the codes the dispatch writes):
 // x_q [T, H] E4M3, x_sf [T, H/32] E8M0 bytes.
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s);
+// MXFP8 pull-dispatch in one token-major pass (each token quantised once,
+// its k rows written from registers); pad rows are not written.
+cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, const int32_t* topk_idx,
+                                   const int32_t* slot_row, const int32_t* counts, const int32_t* offsets, void* A,
+                                   uint8_t* A_sf, cudaStream_t s);
 // MXFP8 quantisation of a row-major [R, K] BF16 matrix along K with scales in
 // the tensor-core chunk order (K % 128 == 0).
 cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s);

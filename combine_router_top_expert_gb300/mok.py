@@ -27,7 +27,8 @@ EXPORTS = ["mok_route_workspace_size", "mok_route_layout", "mok_packed_weights_s
            "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_status_string",
            "mok_version", "mok_route_layout_static", "mok_workspace_size_batches", "mok_moe_forward_batches",
            "mok_quantize_rows", "mok_dispatch_quantized", "mok_route_test_hook", "mok_ep_workspace_size",
-           "mok_ep_dispatch", "mok_ep_push", "mok_packed_weights_bwd_size", "mok_pack_weights_bwd"]
+           "mok_ep_dispatch", "mok_ep_push", "mok_packed_weights_bwd_size", "mok_pack_weights_bwd",
+           "mok_dispatch_tokens"]
 
 FLAG_MEGAKERNEL = 1
 FLAG_GEMM_PAIRS = 2
@@ -121,6 +122,7 @@ def lib():
             L.mok_padded_rows_max.restype = ctypes.c_int64
             L.mok_dispatch.argtypes = [PP, P, PR, P, P, P]
             L.mok_quantize_rows.argtypes = [P, I32, I32, P, P, P]
+            L.mok_dispatch_tokens.argtypes = [PP, P, PR, P, P, P]
             L.mok_dispatch_quantized.argtypes = [PP, P, P, PR, P, P, P]
             L.mok_expert_ffn.argtypes = [PP, P, P, P, PR, P, P, P, PC, P, P]
             L.mok_combine.argtypes = [PP, P, P, P, P, P]
@@ -138,7 +140,7 @@ def lib():
             for name in ("mok_route_layout", "mok_route_layout_static", "mok_pack_weights", "mok_moe_forward",
                          "mok_moe_forward_batches", "mok_dispatch", "mok_quantize_rows", "mok_dispatch_quantized",
                          "mok_expert_ffn", "mok_combine", "mok_moe_backward", "mok_device_status", "mok_route_test_hook",
-                         "mok_ep_dispatch", "mok_ep_push", "mok_pack_weights_bwd"):
+                         "mok_ep_dispatch", "mok_ep_push", "mok_pack_weights_bwd", "mok_dispatch_tokens"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -333,6 +335,12 @@ def dispatch(p: Problem, x, routing, A, A_sf=None, stream=None):
     rs = routing_struct(routing)
     rc = lib().mok_dispatch(ctypes.byref(p), _ptr(x), ctypes.byref(rs), _ptr(A), _ptr(A_sf), _stream(stream))
     _check(rc, "mok_dispatch")
+
+
+def dispatch_tokens(p: Problem, x, routing, A, A_sf, stream=None):
+    rs = routing_struct(routing)
+    rc = lib().mok_dispatch_tokens(ctypes.byref(p), _ptr(x), ctypes.byref(rs), _ptr(A), _ptr(A_sf), _stream(stream))
+    _check(rc, "mok_dispatch_tokens")
 
 
 def quantize_rows(x, x_q, x_sf, stream=None):

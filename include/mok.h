@@ -294,6 +294,15 @@ mok_status mok_quantize_rows(const void* x, int32_t T, int32_t H, void* x_q, voi
 mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const void* x_sf,
                                   const mok_routing* r, void* A, void* A_sf, mok_stream_t stream);
 
+/* MXFP8 pull-dispatch in one token-major pass, as mok_moe_forward runs it:
+ * each token's row is quantised once (the rule of mok_quantize_rows) and its
+ * codes and scale words are written to each of its k routed rows (the bytes
+ * of mok_dispatch for routed rows); pad rows are left unwritten. Uses
+ * topk_idx, slot_row, counts and offsets of the routing. p->dtype must be
+ * MOK_MXFP8; x and A 16-B aligned. */
+mok_status mok_dispatch_tokens(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
+                               mok_stream_t stream);
+
 /* Grouped expert FFN on the dispatched rows: h = SwiGLU(A W_gate[e], A W_up[e])
  * (BF16 or MXFP8 as dtype), y = h W_down[e], y row pushed to partials[t*k+j]
  * ([T*k, H] bf16, unweighted). h/h_sf are caller scratch of

@@ -146,8 +146,40 @@ def test_quantize_once_then_gather():
     sf1 = untile_sf(S1.cpu().numpy(), poff[-1], wl.H)
     sf2 = untile_sf(S2.cpu().numpy(), poff[-1], wl.H)
     assert np.array_equal(sf2[live], sf1[live])
+    # the one-pass token-major dispatch writes the same routed bytes and scales
+    A3, S3 = mok.alloc_bytes(rows * wl.H).view(rows, wl.H), mok.alloc_bytes(rows * wl.H // 32)
+    mok.dispatch_tokens(p, x, rt, A3, S3)
+    torch.cuda.synchronize()
+    assert np.array_equal(A3[:poff[-1]].cpu().numpy()[live], A1[:poff[-1]].cpu().numpy()[live])
+    assert np.array_equal(untile_sf(S3.cpu().numpy(), poff[-1], wl.H)[live], sf1[live])
     with pytest.raises(mok.MokError):
         mok.quantize_rows(x[:, :1000], xq, xsf)     # H % 128 != 0
+
+
+@pytest.mark.gpu
+def test_token_major_dispatch_many_slots():
+    """k = 40 > 32 slots per token (each slot's row looked up directly rather
+    than shuffled from lane j): the same routed bytes as mok_dispatch."""
+    wl = synth.small("disp_k40", T=50, H=256, I=128, E=64, k=40)
+    inp = synth.make_inputs(wl, seed=3)
+    layer = layer_for(inp, mok.MXFP8)
+    x = to_dev_bf16(inp.x)
+    rt = layer.route(x)
+    p = layer.problem(wl.T)
+    rows = mok.padded_rows_max(wl.T, wl.E, wl.k)
+    A1, A3 = mok.alloc_bytes(rows * wl.H).view(rows, wl.H), mok.alloc_bytes(rows * wl.H).view(rows, wl.H)
+    S1, S3 = mok.alloc_bytes(rows * wl.H // 32), mok.alloc_bytes(rows * wl.H // 32)
+    mok.dispatch(p, x, rt, A1, S1)
+    mok.dispatch_tokens(p, x, rt, A3, S3)
+    torch.cuda.synchronize()
+    counts = rt["counts"].cpu().numpy()
+    poff = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)])
+    live = np.zeros(poff[-1], bool)
+    for e in range(wl.E):
+        live[poff[e]:poff[e] + counts[e]] = True
+    assert np.array_equal(A3[:poff[-1]].cpu().numpy()[live], A1[:poff[-1]].cpu().numpy()[live])
+    assert np.array_equal(untile_sf(S3.cpu().numpy(), poff[-1], wl.H)[live],
+                          untile_sf(S1.cpu().numpy(), poff[-1], wl.H)[live])
 
 
 @pytest.mark.gpu
