@@ -155,14 +155,21 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
             return poff[e] + slot_row[sl] - offsets[e];
         };
         const int my_pr = (k <= 32 && lane < k) ? dest(lane) : 0;
-        for (int q = lane; q < kc_row; q += 32) {
+        // every lane runs the same trip counts (the shuffles need the whole
+        // warp); lanes without a chunk in this round only pass rows along
+        for (int q0 = 0; q0 < kc_row; q0 += 32) {
+            const int q = q0 + lane;
+            const bool act = q < kc_row;
             uint4 o[8];
             uint32_t word = 0;
+            if (act) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                word |= quantize_block32(x + t * H + q * 128 + 32 * b, o[2 * b], o[2 * b + 1]) << (8 * b);
+                for (int b = 0; b < 4; ++b)
+                    word |= quantize_block32(x + t * H + q * 128 + 32 * b, o[2 * b], o[2 * b + 1]) << (8 * b);
+            }
             for (int j = 0; j < k; ++j) {
-                const int pr = k <= 32 ? __shfl_sync(__activemask(), my_pr, j) : dest(j);
+                const int pr = k <= 32 ? __shfl_sync(0xffffffffu, my_pr, j) : dest(j);
+                if (!act) continue;
                 uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H + q * 128);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) __stcs(dst + i, o[i]);
