@@ -384,7 +384,7 @@ mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const v
 
 mok_status mok_dispatch_tokens(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
                                mok_stream_t stream) {
-    if (!problem_ok(p) || p->dtype != MOK_MXFP8 || !routing_ok(r, p->T) || !A || !A_sf || !aligned(A, 16))
+    if (!problem_ok(p) || p->dtype != MOK_MXFP8 || !routing_ok(r, p->T) || !A || !A_sf || !aligned(A, 32))
         return MOK_ERR_INVALID;
     if (p->T > 0 && (!x || !aligned(x, 16))) return MOK_ERR_INVALID;
     if (!device_ok()) return MOK_ERR_CUDA;

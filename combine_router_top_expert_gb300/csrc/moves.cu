@@ -13,6 +13,7 @@
 
 #include "common.cuh"
 #include "moves.cuh"
+#include "tc.cuh"
 
 namespace mok {
 
@@ -131,13 +132,15 @@ dispatch_q_kernel(const uint8_t* __restrict__ xq, const uint32_t* __restrict__ x
     }
 }
 
-// MXFP8 pull-dispatch in one token-major pass: a warp takes a token, each
-// lane quantises 128-wide chunks of its row once (four 32-element blocks,
-// the same encoder as quantize_rows) and writes the codes and the chunk's
-// scale word to each of the token's k rows of the padded expert-contiguous
-// layout. Every token row is read once from HBM and no quantised copy of x
-// is written and read back. Pad rows are not written. The bytes equal those
-// of quantize_rows + dispatch_q.
+// MXFP8 pull-dispatch in one token-major pass: a warp takes a token and
+// lane L quantises the 32-element blocks L, L + 32, ... of its row once (the
+// encoder of quantize_rows), then writes each block's 32 codes with one
+// 32-byte store to each of the token's k rows of the padded expert-contiguous
+// layout (a warp store covers 1 KB of a row); the four scale codes of a
+// 128-wide chunk, held by four neighbouring lanes, leave as one word. Every
+// token row is read once and no quantised copy of x is written and read
+// back. Pad rows are not written. The bytes equal those of quantize_rows +
+// dispatch_q.
 __global__ void __launch_bounds__(256)
 dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E, int k,
                        const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_row,
@@ -146,7 +149,7 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
     __shared__ int32_t poff[kMaxE + 1];
     padded_offsets(counts, E, poff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kc_row = H / 128;
+    const int nb = H / 32, kc_row = H / 128;
     for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < T; t += (int64_t)gridDim.x * 8) {
         // padded destination row of slot j (lane j holds it when k <= 32)
         auto dest = [&](int j) {
@@ -156,25 +159,27 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
         };
         const int my_pr = (k <= 32 && lane < k) ? dest(lane) : 0;
         // every lane runs the same trip counts (the shuffles need the whole
-        // warp); lanes without a chunk in this round only pass rows along
-        for (int q0 = 0; q0 < kc_row; q0 += 32) {
-            const int q = q0 + lane;
-            const bool act = q < kc_row;
-            uint4 o[8];
-            uint32_t word = 0;
-            if (act) {
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    word |= quantize_block32(x + t * H + q * 128 + 32 * b, o[2 * b], o[2 * b + 1]) << (8 * b);
-            }
+        // warp); nb % 4 == 0, so the four lanes of a chunk are all active or
+        // all idle
+        for (int b0 = 0; b0 < nb; b0 += 32) {
+            const int b = b0 + lane;
+            const bool act = b < nb;
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+            uint32_t code = 0;
+            if (act) code = quantize_block32(x + t * H + b * 32, o0, o1);
+            // the chunk's four codes, byte j = block 4c + j, in the chunk's first lane
+            uint32_t word = code;
+            word |= __shfl_down_sync(0xffffffffu, code, 1) << 8;
+            word |= __shfl_down_sync(0xffffffffu, code, 2) << 16;
+            word |= __shfl_down_sync(0xffffffffu, code, 3) << 24;
+            const uint32_t w8[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
             for (int j = 0; j < k; ++j) {
                 const int pr = k <= 32 ? __shfl_sync(0xffffffffu, my_pr, j) : dest(j);
                 if (!act) continue;
-                uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H + q * 128);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) __stcs(dst + i, o[i]);
-                *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)(pr / kTileM) * kc_row + q) * 512 +
-                                             sf_chunk_offset(pr % kTileM, 0)) = word;
+                tc::stg_v8(A + (int64_t)pr * H + b * 32, w8);
+                if ((lane & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)(pr / kTileM) * kc_row + b / 4) * 512 +
+                                                 sf_chunk_offset(pr % kTileM, 0)) = word;
             }
         }
     }

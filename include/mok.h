@@ -299,7 +299,7 @@ mok_status mok_dispatch_quantized(const mok_problem* p, const void* x_q, const v
  * codes and scale words are written to each of its k routed rows (the bytes
  * of mok_dispatch for routed rows); pad rows are left unwritten. Uses
  * topk_idx, slot_row, counts and offsets of the routing. p->dtype must be
- * MOK_MXFP8; x and A 16-B aligned. */
+ * MOK_MXFP8; x 16-B and A 32-B aligned. */
 mok_status mok_dispatch_tokens(const mok_problem* p, const void* x, const mok_routing* r, void* A, void* A_sf,
                                mok_stream_t stream);
 
