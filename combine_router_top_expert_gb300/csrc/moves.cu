@@ -593,12 +593,14 @@ quantize_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int
 // column f, so a GEMM reducing over R reads it K-major) and scales in the
 // tensor-core chunk order of that [F, R] operand (chunk (f / 128, r / 128),
 // byte sf_chunk_offset(f % 128, (r / 32) % 4)). R % 128 == 0, F % 128 == 0.
-// A CTA takes 32 rows x 128 columns: the tile goes through shared memory and
-// each thread quantises one column block and stores its 32 codes at once.
+// A CTA takes 32 rows x 128 columns: the tile arrives in 16-byte loads into
+// shared memory (raw BF16, rows padded by 16 bytes), then each thread
+// quantises one column block and stores its 32 codes at once.
 __global__ void __launch_bounds__(128)
 quantize_cols_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int F, uint8_t* __restrict__ qT,
                            uint8_t* __restrict__ sfT) {
-    __shared__ float tile[32][129];
+    constexpr int kPitch = 136;   // bf16 per shared row (128 + 8)
+    __shared__ __align__(16) __nv_bfloat16 tile[32 * kPitch];
     const int tid = threadIdx.x;
     const int64_t nrb = R / 32;
     const int nfc = F / 128;
@@ -607,18 +609,33 @@ quantize_cols_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int
         const int64_t r0 = (blk / nfc) * 32;
         const int f0 = (int)(blk % nfc) * 128;
         __syncthreads();
-        for (int i = 0; i < 32; ++i) tile[i][tid] = __bfloat162float(src[(r0 + i) * F + f0 + tid]);
+        // 32 rows x 16 chunks of 8 values: four 16-byte loads per thread
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = tid / 16 + 8 * u, c = tid % 16;
+            v[u] = __ldg(reinterpret_cast<const uint4*>(src + (r0 + r) * F + f0 + 8 * c));
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int r = tid / 16 + 8 * u, c = tid % 16;
+            *reinterpret_cast<uint4*>(tile + r * kPitch + 8 * c) = v[u];
+        }
         __syncthreads();
+        float col[32];
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(tile[i][tid]));
+        for (int i = 0; i < 32; ++i) {
+            col[i] = __bfloat162float(tile[i * kPitch + tid]);
+            amax = fmaxf(amax, fabsf(col[i]));
+        }
         const uint32_t code = e8m0_code(amax);
         const float inv = e8m0_inv_scale(code);
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            w[i] = f32x2_to_e4m3x2(tile[4 * i][tid] * inv, tile[4 * i + 1][tid] * inv) |
-                   (f32x2_to_e4m3x2(tile[4 * i + 2][tid] * inv, tile[4 * i + 3][tid] * inv) << 16);
+            w[i] = f32x2_to_e4m3x2(col[4 * i] * inv, col[4 * i + 1] * inv) |
+                   (f32x2_to_e4m3x2(col[4 * i + 2] * inv, col[4 * i + 3] * inv) << 16);
         const int f = f0 + tid;
         uint4* dst = reinterpret_cast<uint4*>(qT + (int64_t)f * R + r0);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
