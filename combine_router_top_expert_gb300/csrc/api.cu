@@ -224,22 +224,18 @@ GemmCommon make_common(void* ws, const mok_config* cfg) {
 
 // BF16 inference GEMMs: swapped-operand pair tiles (weight rows as M, token
 // tiles of 256 rows plus a remainder as N) or the 128-row token tiles.
-// Measured on the 32-expert H=7168/I=2048 layer: a pair tile's time follows
-// the bytes its stages load, so a remainder tile of about half the width
-// costs most of a full one; with 640 rows per expert (two full tiles and a
-// 128-row remainder) the token tiles were as fast or faster, with 512, 768
-// or 1024 rows the swapped tiles 7-17 % faster. Default: swapped tiles when
-// the average rows per expert leave no remainder or one of at least 192
-// rows; MOK_FLAG_SWAPPED_TILES / MOK_FLAG_ROW_TILES force either.
+// Measured on the 32-expert H=7168/I=2048 layer (GEMM pair alone, L2
+// flushed, three interleaved repeats): the token tiles were as fast or
+// faster at 512, 640, 768 and 1024 rows per expert, with exact and with
+// random routing (random, 640 rows: 1430 against 1390 TFLOP/s; 1024 rows:
+// 1540 against 1397), so they are the default; MOK_FLAG_SWAPPED_TILES selects
+// the swapped tiles (the autotuner times both).
 bool use_swap(const mok_problem* p, const mok_config* cfg, bool training) {
     if (p->dtype != MOK_BF16 || training) return false;
     if (!swap_supported(p->H, p->I)) return false;
     const int flags = cfg ? cfg->flags : 0;
     if (flags & (MOK_FLAG_ROW_TILES | MOK_FLAG_GEMM_PAIRS)) return false;
-    if (flags & MOK_FLAG_SWAPPED_TILES) return true;
-    const int64_t rows = (int64_t)p->T * p->k / p->E;
-    const int64_t rem = rows % 256;
-    return rows >= 256 && (rem == 0 || rem >= 192);
+    return (flags & MOK_FLAG_SWAPPED_TILES) != 0;
 }
 int swap_policy(const mok_config* cfg) { return (cfg && (cfg->flags & MOK_FLAG_TOKEN_TILES_BALANCED)) ? 1 : 0; }
 

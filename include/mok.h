@@ -118,12 +118,11 @@ typedef struct {
  * pair tiles (256 rows over two CTAs) and an expert's tokens cut into tiles
  * of 256 rows and one remainder tile (a multiple of 32 rows) as the N side,
  * so little tensor work is spent on padded rows and no CTA of a pair idles
- * (needs I % 128 == 0 and H % 256 == 0). By default the swapped tiles run
- * when the average rows per expert, T*k/E, is at least 256 and leaves no
- * remainder modulo 256 or one of at least 192 rows (measured faster there;
- * a narrow remainder tile costs most of a full one). MOK_FLAG_ROW_TILES forces
- * the token tiles, MOK_FLAG_SWAPPED_TILES the swapped ones. The training
- * forward (saved != NULL) and MXFP8 use the token tiles. */
+ * (needs I % 128 == 0 and H % 256 == 0). The token tiles are the default
+ * (measured as fast or faster from 512 to 1024 rows per expert);
+ * MOK_FLAG_SWAPPED_TILES selects the swapped ones, MOK_FLAG_ROW_TILES states
+ * the default explicitly. The training forward (saved != NULL) and MXFP8
+ * always use the token tiles. */
 #define MOK_FLAG_ROW_TILES 16
 #define MOK_FLAG_SWAPPED_TILES 128
 /* Swapped-operand tiles: cut each expert's tokens into ceil(n/256) tiles of
