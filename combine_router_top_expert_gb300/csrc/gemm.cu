@@ -462,10 +462,16 @@ cudaError_t gemm_wgrad_mx(const void* AT_q, const uint8_t* AT_sf, int M, const v
     p.b_sf = BT_sf;
     p.sf_kchunks = (int)(rows_pad / 128);
     p.sf_kchunks_b = (int)(rows_pad / 128);
-    p.n_tiles = N / 128;
+    // 256-wide tiles (one accumulator, 8 epilogue warps storing 32-byte row
+    // segments) halve the A bytes loaded per FLOP against 128-wide ones; they
+    // need 32-byte aligned outputs
+    const bool wide = N % 256 == 0 && (reinterpret_cast<uintptr_t>(out0) & 31) == 0 &&
+                      (split_col >= N || (reinterpret_cast<uintptr_t>(out1) & 31) == 0);
+    const int BN = wide ? 256 : 128;
+    p.n_tiles = N / BN;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, AT_q, M, rows_pad, 1, 128, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, BT_q, N, rows_pad, 1, 128, 128)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, BT_q, N, rows_pad, 1, 128, BN)) return cudaErrorInvalidValue;
     CUtensorMap to0, to1;
     if (!make_tmap_out3d(&to0, out0, E, M, p.ldo, p.ldo)) return cudaErrorInvalidValue;
     if (split_col < N) {
@@ -474,6 +480,7 @@ cudaError_t gemm_wgrad_mx(const void* AT_q, const uint8_t* AT_sf, int M, const v
         to1 = to0;
     }
     const int64_t tub = (int64_t)E * (M / kTileM) * p.n_tiles;
+    if (wide) return run<256, true, false, kEpiDense, 4, 1>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
     return run<128, true, false, kEpiDense, 6, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
 }
 

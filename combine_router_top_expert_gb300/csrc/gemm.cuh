@@ -74,7 +74,8 @@ struct GemmCfg {
     // MXFP8 tiles 256 wide keep one accumulator (their scales take the rest
     // of TMEM) and hide the epilogue behind the next tile with 8 epilogue
     // warps.
-    static constexpr bool kWideEpi = MX && (EPI == kEpiSwiGLU || EPI == kEpiScatter) && ACC_STAGES == 1;
+    static constexpr bool kWideEpi = MX && (EPI == kEpiSwiGLU || EPI == kEpiScatter || EPI == kEpiDense) &&
+                                     ACC_STAGES == 1;
     static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // BF16 grouped-row forward tiles: an expert's last tile with at most 64
@@ -107,7 +108,8 @@ struct GemmCfg {
     // dense epilogue: per epilogue warp two 32 x 32 BF16 staging blocks for
     // its TMA stores, 1 KB past the barriers
     static constexpr int kEpiStageOffset = kBarOffset + 1024;
-    static constexpr int kEpiStageBytes = EPI == kEpiDense ? 4 * 2 * 2048 : 0;
+    // (the wide MXFP8 dense epilogue stores from registers and stages nothing)
+    static constexpr int kEpiStageBytes = (EPI == kEpiDense && !kWideEpi) ? 4 * 2 * 2048 : 0;
     static constexpr int kSmemBytes = 1024 /*align slack*/ + kBarOffset + (EPI == kEpiDense ? 1024 : 256) + kEpiStageBytes;
     static_assert(kTmemNeed <= 512, "tensor memory budget");
     static_assert(BN % 32 == 0 && BN <= 256, "BN");
@@ -519,7 +521,53 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
 
-            if constexpr (C::kWideEpi && EPI == kEpiScatter) {
+            if constexpr (C::kWideEpi && EPI == kEpiDense) {
+                // weight gradients, 256 columns: this warp's 32-column chunks
+                // eg, eg+2, eg+4, eg+6 to registers (packed to BF16), the
+                // accumulator released, then each row segment written with
+                // 32-byte stores (whole sectors); an expert without tokens
+                // writes zeros
+                static_assert(CLN == 1, "dense wide epilogue: single CTAs");
+                const int eg = (warp - 2) >> 2;
+                uint32_t w0[16], w1[16], w2[16], w3[16];
+                if (has_acc) {
+                    auto load_pair = [&](int c, uint32_t(&wa)[16], uint32_t(&wb)[16]) {
+                        uint32_t ra[32], rb[32];
+                        tc::tmem_ld_32x32b_x32(tbase + 32 * c, ra);
+                        tc::tmem_ld_32x32b_x32(tbase + 32 * (c + 2), rb);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            wa[i] = pack_bf16x2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1]));
+                            wb[i] = pack_bf16x2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1]));
+                        }
+                    };
+                    load_pair(eg, w0, w1);
+                    load_pair(eg + 4, w2, w3);
+                    tc::fence_before_sync();
+                    tc::mbar_arrive(acce_bar(acc));
+                    if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w0[i] = w1[i] = w2[i] = w3[i] = 0u;
+                }
+                const int mrow = ti.row_base + row;
+                if (mrow < p.m_fixed) {
+                    auto store_chunk = [&](int c, const uint32_t(&w)[16]) {
+                        const int col = ti.n * BN + 32 * c;
+                        __nv_bfloat16* o = col < p.split_col
+                            ? static_cast<__nv_bfloat16*>(p.out0) + ((int64_t)ti.e * p.m_fixed + mrow) * p.ldo + col
+                            : static_cast<__nv_bfloat16*>(p.out1) + ((int64_t)ti.e * p.m_fixed + mrow) * p.ldo +
+                                  (col - p.split_col);
+                        tc::stg_v8(o, w);
+                        tc::stg_v8(o + 16, w + 8);
+                    };
+                    store_chunk(eg, w0);
+                    store_chunk(eg + 2, w1);
+                    store_chunk(eg + 4, w2);
+                    store_chunk(eg + 6, w3);
+                }
+            } else if constexpr (C::kWideEpi && EPI == kEpiScatter) {
                 // this warp's 32-column chunks eg, eg+2, eg+4, eg+6 to
                 // registers (packed to BF16 two at a time), accumulator
                 // released, then pushed to the row's slot
@@ -561,7 +609,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (eg + 4 < nch) store_chunk(eg + 4, w2);
                     if (eg + 6 < nch) store_chunk(eg + 6, w3);
                 }
-            } else if constexpr (C::kWideEpi) {
+            } else if constexpr (C::kWideEpi && EPI == kEpiSwiGLU) {
                 // this warp's 64 h columns: gate and up pre-activations to
                 // registers, accumulator released, then SwiGLU and two
                 // 32-element MXFP8 blocks (scale codes 2*eg and 2*eg+1 of the

@@ -74,6 +74,9 @@ MX_BWD_CASES = [
     synth.small("mxbwd_small", T=256, H=256, I=128, E=4, k=2, dtype="mxfp8", backward=True),
     synth.small("mxbwd_ragged", T=500, H=512, I=256, E=4, k=2, dtype="mxfp8", zipf_s=1.2, backward=True),
     synth.small("mxbwd_all_experts", T=96, H=256, I=128, E=4, k=4, dtype="mxfp8", backward=True),
+    # H = 384: the down weight gradient's 384 columns take the 128-wide tiles,
+    # the gate/up one's 256 columns the 256-wide tiles
+    synth.small("mxbwd_h384", T=200, H=384, I=128, E=4, k=2, dtype="mxfp8", zipf_s=1.2, backward=True),
 ]
 
 
