@@ -74,8 +74,7 @@ struct GemmCfg {
     // MXFP8 tiles 256 wide keep one accumulator (their scales take the rest
     // of TMEM) and hide the epilogue behind the next tile with 8 epilogue
     // warps.
-    static constexpr bool kWideEpi = MX && (EPI == kEpiSwiGLU || EPI == kEpiScatter || EPI == kEpiDense) &&
-                                     ACC_STAGES == 1;
+    static constexpr bool kWideEpi = MX && ACC_STAGES == 1;
     static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // BF16 grouped-row forward tiles: an expert's last tile with at most 64
@@ -566,6 +565,58 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     store_chunk(eg + 2, w1);
                     store_chunk(eg + 4, w2);
                     store_chunk(eg + 6, w3);
+                }
+            } else if constexpr (C::kWideEpi && EPI == kEpiDSwiGLU) {
+                // dgrad of h, 256 columns: this warp's 32-column chunks eg,
+                // eg+2, eg+4, eg+6 of dh (fp32) to registers, the accumulator
+                // released, then dG = dh U silu'(G) and dU = dh silu(G) from
+                // the saved fp32 pre-activations, 8 columns at a time
+                static_assert(CLN == 1, "dSwiGLU wide epilogue: single CTAs");
+                const int eg = (warp - 2) >> 2;
+                const int I = p.split_col;
+                const int64_t prow = ti.row_base + row;
+                uint32_t r[4][32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tc::tmem_ld_32x32b_x32(tbase + 32 * (eg + 2 * j), r[j]);
+                tc::tmem_ld_wait();
+                tc::fence_before_sync();
+                tc::mbar_arrive(acce_bar(acc));
+                if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
+                if (ti.valid) {
+                    const float* gb = static_cast<const float*>(p.gu) + prow * (int64_t)(2 * I);
+                    __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)(2 * I);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = ti.n * BN + 32 * (eg + 2 * j);
+#pragma unroll
+                        for (int h16 = 0; h16 < 2; ++h16) {
+                            uint32_t dgw[8], duw[8];
+#pragma unroll
+                            for (int g8 = 0; g8 < 2; ++g8) {
+                                const int c8 = 16 * h16 + 8 * g8;
+                                uint32_t gw[8], uw[8];
+                                tc::ldg_v8(gb + col + c8, gw);
+                                tc::ldg_v8(gb + I + col + c8, uw);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    float dg2[2], du2[2];
+#pragma unroll
+                                    for (int q2 = 0; q2 < 2; ++q2) {
+                                        const float G = __uint_as_float(gw[2 * i + q2]);
+                                        const float U = __uint_as_float(uw[2 * i + q2]);
+                                        const float dh = __uint_as_float(r[j][c8 + 2 * i + q2]);
+                                        const float sg = 1.0f / (1.0f + expf(-G));
+                                        dg2[q2] = dh * U * (sg * (1.0f + G * (1.0f - sg)));
+                                        du2[q2] = dh * (G * sg);
+                                    }
+                                    dgw[4 * g8 + i] = pack_bf16x2(dg2[0], dg2[1]);
+                                    duw[4 * g8 + i] = pack_bf16x2(du2[0], du2[1]);
+                                }
+                            }
+                            tc::stg_v8(ob + col + 16 * h16, dgw);
+                            tc::stg_v8(ob + I + col + 16 * h16, duw);
+                        }
+                    }
                 }
             } else if constexpr (C::kWideEpi && EPI == kEpiScatter) {
                 // this warp's 32-column chunks eg, eg+2, eg+4, eg+6 to
