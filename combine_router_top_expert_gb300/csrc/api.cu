@@ -649,20 +649,21 @@ mok_status mok_moe_backward(const mok_problem* p, const mok_bwd_args* a, const m
         auto WQ = [&](size_t off) { return pb + off; };
         auto WS = [&](size_t off) { return reinterpret_cast<uint8_t*>(pb + off); };
         // dh = dy W_down^T (K = H), dSwiGLU -> dG|dU (BF16)
-        if (e == cudaSuccess) e = launch_quantize_rows_tiled(dy, rp, H, Q(L.dyq), QS(L.dysf), s);
+        // dy and dG|dU: quantised along both of their GEMMs' reduction dimensions in one read each
+        if (e == cudaSuccess)
+            e = launch_quantize_rows_cols_tiled(dy, rp, H, Q(L.dyq), QS(L.dysf), Q(L.dytq), QS(L.dytsf), s);
         if (e == cudaSuccess)
             e = gemm_dgrad_h_mx(Q(L.dyq), QS(L.dysf), WQ(PB.wd), WS(PB.wdsf), E, H, I, r.counts, rows, sv + FL.sGU,
                                 dgu, c, s);
         // da = dG W_gate^T + dU W_up^T (K = I), pushed to the slots
-        if (e == cudaSuccess) e = launch_quantize_rows_tiled(dgu, rp, 2 * I, Q(L.dguq), QS(L.dgusf), s);
+        if (e == cudaSuccess)
+            e = launch_quantize_rows_cols_tiled(dgu, rp, 2 * I, Q(L.dguq), QS(L.dgusf), Q(L.gutq), QS(L.gutsf), s);
         if (e == cudaSuccess)
             e = gemm_dgrad_a_mx(Q(L.dguq), QS(L.dgusf), WQ(PB.wg), WS(PB.wgsf), WQ(PB.wu), WS(PB.wusf), E, H, I,
                                 r.counts, r.offsets, r.row_src, rows, da, c, s);
         // weight gradients over each expert's tokens: operands blocked along the tokens
         if (e == cudaSuccess) e = launch_quantize_cols_tiled(sv + FL.sA, rp, H, Q(L.atq), QS(L.atsf), s);
-        if (e == cudaSuccess) e = launch_quantize_cols_tiled(dgu, rp, 2 * I, Q(L.gutq), QS(L.gutsf), s);
         if (e == cudaSuccess) e = launch_quantize_cols_tiled(sv + FL.sh, rp, I, Q(L.htq), QS(L.htsf), s);
-        if (e == cudaSuccess) e = launch_quantize_cols_tiled(dy, rp, H, Q(L.dytq), QS(L.dytsf), s);
         if (e == cudaSuccess)
             e = gemm_wgrad_mx(Q(L.atq), QS(L.atsf), H, Q(L.gutq), QS(L.gutsf), 2 * I, E, r.counts, rp, a->dW_gate,
                               a->dW_up, I, c, s);

@@ -567,101 +567,133 @@ cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, i
     return cudaGetLastError();
 }
 
-// MXFP8 quantisation of the rows of a row-major [R, K] BF16 matrix along K
-// (K % 128 == 0): codes [R, K] E4M3, scales in the tensor-core chunk order
-// (chunk (r / 128, c / 128) of 512 bytes at ((r / 128) * (K / 128) + c / 128)
-// * 512, byte sf_chunk_offset(r % 128, (c / 32) % 4)). One warp per row.
-__global__ void __launch_bounds__(256)
-quantize_rows_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int K, uint8_t* __restrict__ q,
-                           uint8_t* __restrict__ sf) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nb = K / 32, nkc = K / 128;
-    for (int64_t r = (int64_t)blockIdx.x * 8 + warp; r < R; r += (int64_t)gridDim.x * 8) {
-        for (int b = lane; b < nb; b += 32) {
-            uint4 o0, o1;
-            const uint32_t code = quantize_block32(src + r * K + b * 32, o0, o1);
-            uint4* dst = reinterpret_cast<uint4*>(q + r * K + b * 32);
-            dst[0] = o0;
-            dst[1] = o1;
-            sf[((r / kTileM) * nkc + b / 4) * 512 + sf_chunk_offset((int)(r % kTileM), b % 4)] = (uint8_t)code;
-        }
-    }
+// MXFP8 quantisation of a row-major [R, F] BF16 matrix (R % 128 == 0,
+// F % 128 == 0) in tiles of 32 rows x 128 columns, in one read of the source:
+//  ROWS: along F, codes [R, F] E4M3 and scales in the tensor-core chunk order
+//        of that [R, F] operand (chunk (r / 128, c / 128) of 512 bytes at
+//        ((r / 128) * (F / 128) + c / 128) * 512, byte
+//        sf_chunk_offset(r % 128, (c / 32) % 4));
+//  COLS: along R in blocks of 32 rows, written transposed: codes [F, R] (row
+//        f holds column f, so a GEMM reducing over R reads it K-major) and
+//        scales in the chunk order of that [F, R] operand (chunk
+//        (f / 128, r / 128), byte sf_chunk_offset(f % 128, (r / 32) % 4)).
+// A CTA of 128 threads takes tile after tile: the tile arrives in 16-byte
+// loads into shared memory (raw BF16, rows padded by 16 bytes), the next
+// tile's loads are issued before this one is quantised, then thread t
+// quantises column t (COLS) and row t / 4's 32-column block t % 4 (ROWS).
+// Every block goes through quantize32, so both layouts hold the codes of the
+// same rule as the other quantisers.
+__device__ __forceinline__ uint32_t quantize32(const float (&f)[32], uint4& o0, uint4& o1) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const uint32_t code = e8m0_code(amax);
+    const float inv = e8m0_inv_scale(code);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+    o0 = make_uint4(w[0], w[1], w[2], w[3]);
+    o1 = make_uint4(w[4], w[5], w[6], w[7]);
+    return code;
 }
 
-// MXFP8 quantisation of the columns of a row-major [R, F] BF16 matrix along
-// R in blocks of 32 rows, written transposed: codes [F, R] E4M3 (row f holds
-// column f, so a GEMM reducing over R reads it K-major) and scales in the
-// tensor-core chunk order of that [F, R] operand (chunk (f / 128, r / 128),
-// byte sf_chunk_offset(f % 128, (r / 32) % 4)). R % 128 == 0, F % 128 == 0.
-// A CTA takes 32 rows x 128 columns: the tile arrives in 16-byte loads into
-// shared memory (raw BF16, rows padded by 16 bytes), then each thread
-// quantises one column block and stores its 32 codes at once.
+template <bool ROWS, bool COLS>
 __global__ void __launch_bounds__(128)
-quantize_cols_tiled_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int F, uint8_t* __restrict__ qT,
-                           uint8_t* __restrict__ sfT) {
+quantize_tiles_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int F, uint8_t* __restrict__ q,
+                      uint8_t* __restrict__ sf, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT) {
     constexpr int kPitch = 136;   // bf16 per shared row (128 + 8)
     __shared__ __align__(16) __nv_bfloat16 tile[32 * kPitch];
     const int tid = threadIdx.x;
-    const int64_t nrb = R / 32;
     const int nfc = F / 128;
+    const int64_t ntiles = (R / 32) * nfc;
     const int64_t nkc = R / 128;
-    for (int64_t blk = blockIdx.x; blk < nrb * nfc; blk += gridDim.x) {
+    uint4 v[4];
+    auto load = [&](int64_t blk) {
         const int64_t r0 = (blk / nfc) * 32;
         const int f0 = (int)(blk % nfc) * 128;
-        __syncthreads();
-        // 32 rows x 16 chunks of 8 values: four 16-byte loads per thread
-        uint4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int r = tid / 16 + 8 * u, c = tid % 16;
             v[u] = __ldg(reinterpret_cast<const uint4*>(src + (r0 + r) * F + f0 + 8 * c));
         }
+    };
+    int64_t blk = blockIdx.x;
+    if (blk < ntiles) load(blk);
+    for (; blk < ntiles; blk += gridDim.x) {
+        const int64_t r0 = (blk / nfc) * 32;
+        const int f0 = (int)(blk % nfc) * 128;
+        __syncthreads();   // the previous tile's shared reads are done
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int r = tid / 16 + 8 * u, c = tid % 16;
             *reinterpret_cast<uint4*>(tile + r * kPitch + 8 * c) = v[u];
         }
         __syncthreads();
-        float col[32];
-        float amax = 0.f;
+        if (blk + gridDim.x < ntiles) load(blk + gridDim.x);
+        if constexpr (COLS) {
+            float f[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            col[i] = __bfloat162float(tile[i * kPitch + tid]);
-            amax = fmaxf(amax, fabsf(col[i]));
+            for (int i = 0; i < 32; ++i) f[i] = __bfloat162float(tile[i * kPitch + tid]);
+            uint4 o0, o1;
+            const uint32_t code = quantize32(f, o0, o1);
+            const int fc = f0 + tid;
+            uint4* dst = reinterpret_cast<uint4*>(qT + (int64_t)fc * R + r0);
+            dst[0] = o0;
+            dst[1] = o1;
+            sfT[((int64_t)(fc / kTileM) * nkc + r0 / 128) * 512 + sf_chunk_offset(fc % kTileM, (int)((r0 / 32) % 4))] =
+                (uint8_t)code;
         }
-        const uint32_t code = e8m0_code(amax);
-        const float inv = e8m0_inv_scale(code);
-        uint32_t w[8];
+        if constexpr (ROWS) {
+            const int r = tid >> 2, b = tid & 3;
+            float f[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = f32x2_to_e4m3x2(col[4 * i] * inv, col[4 * i + 1] * inv) |
-                   (f32x2_to_e4m3x2(col[4 * i + 2] * inv, col[4 * i + 3] * inv) << 16);
-        const int f = f0 + tid;
-        uint4* dst = reinterpret_cast<uint4*>(qT + (int64_t)f * R + r0);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        sfT[((int64_t)(f / kTileM) * nkc + r0 / 128) * 512 + sf_chunk_offset(f % kTileM, (int)((r0 / 32) % 4))] =
-            (uint8_t)code;
+            for (int i = 0; i < 4; ++i) {
+                const uint4 w = *reinterpret_cast<const uint4*>(tile + r * kPitch + 32 * b + 8 * i);
+                f[8 * i + 0] = bf16_lo(w.x); f[8 * i + 1] = bf16_hi(w.x);
+                f[8 * i + 2] = bf16_lo(w.y); f[8 * i + 3] = bf16_hi(w.y);
+                f[8 * i + 4] = bf16_lo(w.z); f[8 * i + 5] = bf16_hi(w.z);
+                f[8 * i + 6] = bf16_lo(w.w); f[8 * i + 7] = bf16_hi(w.w);
+            }
+            uint4 o0, o1;
+            const uint32_t code = quantize32(f, o0, o1);
+            const int64_t rg = r0 + r;
+            uint4* dst = reinterpret_cast<uint4*>(q + rg * F + f0 + 32 * b);
+            dst[0] = o0;
+            dst[1] = o1;
+            sf[((rg / kTileM) * nfc + f0 / 128) * 512 + sf_chunk_offset((int)(rg % kTileM), b)] = (uint8_t)code;
+        }
     }
 }
 
-cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s) {
+namespace {
+template <bool ROWS, bool COLS>
+cudaError_t launch_quantize_tiles(const void* src, int64_t R, int F, void* q, void* sf, void* qT, void* sfT,
+                                  cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    if (K % 128) return cudaErrorInvalidValue;
-    const int blocks = (int)std::min<int64_t>(ceil_div(R, 8), (int64_t)sm_count() * 8);
-    quantize_rows_tiled_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(src), R, K,
-                                                      static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf));
-    return cudaGetLastError();
-}
-
-cudaError_t launch_quantize_cols_tiled(const void* src, int64_t R, int F, void* qT, void* sfT, cudaStream_t s) {
-    if (R <= 0) return cudaSuccess;
+    // whole 128-row scale chunks on both sides
     if (R % 128 || F % 128) return cudaErrorInvalidValue;
     const int64_t n = (R / 32) * (F / 128);
     const int blocks = (int)std::min<int64_t>(n, (int64_t)sm_count() * 16);
-    quantize_cols_tiled_kernel<<<blocks, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(src), R, F,
-                                                      static_cast<uint8_t*>(qT), static_cast<uint8_t*>(sfT));
+    quantize_tiles_kernel<ROWS, COLS><<<blocks, 128, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(src), R, F, static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf),
+        static_cast<uint8_t*>(qT), static_cast<uint8_t*>(sfT));
     return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s) {
+    return launch_quantize_tiles<true, false>(src, R, K, q, sf, nullptr, nullptr, s);
+}
+
+cudaError_t launch_quantize_cols_tiled(const void* src, int64_t R, int F, void* qT, void* sfT, cudaStream_t s) {
+    return launch_quantize_tiles<false, true>(src, R, F, nullptr, nullptr, qT, sfT, s);
+}
+
+cudaError_t launch_quantize_rows_cols_tiled(const void* src, int64_t R, int F, void* q, void* sf, void* qT, void* sfT,
+                                            cudaStream_t s) {
+    return launch_quantize_tiles<true, true>(src, R, F, q, sf, qT, sfT, s);
 }
 
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s) {

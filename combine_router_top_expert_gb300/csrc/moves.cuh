@@ -111,12 +111,15 @@ cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, co
                                    const int32_t* slot_row, const int32_t* counts, const int32_t* offsets, void* A,
                                    uint8_t* A_sf, cudaStream_t s);
 // MXFP8 quantisation of a row-major [R, K] BF16 matrix along K with scales in
-// the tensor-core chunk order (K % 128 == 0).
+// the tensor-core chunk order (R % 128 == 0, K % 128 == 0).
 cudaError_t launch_quantize_rows_tiled(const void* src, int64_t R, int K, void* q, void* sf, cudaStream_t s);
 // MXFP8 quantisation of the columns of a row-major [R, F] BF16 matrix along R
 // (blocks of 32 rows), written transposed as a K-major [F, R] operand with
 // chunk-ordered scales (R % 128 == 0, F % 128 == 0).
 cudaError_t launch_quantize_cols_tiled(const void* src, int64_t R, int F, void* qT, void* sfT, cudaStream_t s);
+// Both of the above from one read of the source (same bytes).
+cudaError_t launch_quantize_rows_cols_tiled(const void* src, int64_t R, int F, void* q, void* sf, void* qT, void* sfT,
+                                            cudaStream_t s);
 // MXFP8 pull-dispatch of rows quantised by launch_quantize_rows (same bytes
 // as launch_dispatch; pad rows left unwritten).
 cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, int E, int k, const int32_t* counts,
