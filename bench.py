@@ -314,7 +314,8 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
     rt = b["routing"]
     routings = ws_b = None
     mode = ("fwd+bwd (staged)" if wl.backward else
-            f"{len(xs)} macro-batches, megakernel" if len(xs) > 1 else
+            f"{len(xs)} macro-batches, megakernel" if len(xs) > 1 and not staged else
+            f"{len(xs)} macro-batches, staged kernels batch by batch" if len(xs) > 1 else
             "staged kernels" if staged else "megakernel")
 
     if wl.backward:
@@ -335,6 +336,24 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
         flops = 18.0 * H * wl.I * T * wl.k
         kern = ("layer GEMMs fwd+bwd (staged; 2 fwd + 4 bwd grouped GEMM launches" +
                 (", MXFP8 operands and quantisation passes)" if dtype == mok.MXFP8 else ")"))
+    elif len(xs) > 1 and staged:
+        outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs]
+        status_ws = b["ws"]
+
+        def step(ev=None):
+            # batch by batch: route/layout, dispatch, grouped GEMMs, shared
+            # expert, weighted sum
+            if ev is not None:
+                ev[0].record(stream)
+            for xb, ob in zip(xs, outs):
+                layer.route(xb, stream=stream)
+                layer.forward(xb, cfg=cfg, stream=stream, route=False, out=ob)
+            if ev is not None:
+                ev[1].record(stream)
+        # per batch: route 3, dispatch 1, grouped GEMMs 2, shared expert 2, weighted sum 1
+        launches_per_step = len(xs) * (3 + 1 + 2 + (2 if wl.shared_I else 0) + 1)
+        flops = wl.fwd_flops()
+        kern = "every launch of the batch-by-batch stage kernels (routing, dispatch, GEMMs, shared expert, sum)"
     elif len(xs) > 1:
         routings = [{n: v.clone() for n, v in rt.items()} for _ in xs]
         outs = [torch.empty((T, H), dtype=torch.bfloat16, device=dev) for _ in xs]
@@ -459,12 +478,12 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
         raise SystemExit(f"{wl.name}: device status after timed steps: {st}")
 
     sm_partition = None
-    if trace and (not staged or len(xs) > 1):
+    if trace and not staged:
         sm_partition = trace_step(args, mok, layer, x, xs, p, cfg, b, wl, stream, routings, ws_b)
 
     e2e = None
     if with_e2e:
-        e2e = measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps)
+        e2e = measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps, staged)
 
     # aggregate over ranks: the slowest rank's times
     t_max, e2e_max = max_over_ranks([total_ms, e2e["ms"] if e2e else 0.0], dev)
@@ -474,7 +493,7 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
                 staged=staged, tokens_per_step=T * len(xs), batches=len(xs))
 
 
-def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps):
+def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, status_ws, steps, staged):
     """End to end through the public API with host buffers: every step copies
     its inputs in from pinned host memory and its result back out; steps are
     pipelined the way a serving loop would run them (copy streams in and out
@@ -494,7 +513,8 @@ def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, stat
         grads_slot = [dict(dX=out_slot[i][0], dW_gate=torch.empty_like(layer.Wg), dW_up=torch.empty_like(layer.Wu),
                            dW_down=torch.empty_like(layer.Wd),
                            dW_r=torch.empty((H, wl.E), dtype=torch.float32, device=dev)) for i in range(2)]
-    route_e2e = [layer.buffers(T, wl.backward)["routing"]] if len(xs) == 1 else routings
+    batched = len(xs) > 1 and not staged   # one megakernel launch over all macro-batches
+    route_e2e = routings if batched else [layer.buffers(T, wl.backward)["routing"]]
     c_in, c_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -517,15 +537,18 @@ def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, stat
             if wl.backward:
                 layer.forward(xsl[0], training=True, cfg=cfg, stream=stream)
                 layer.backward(xsl[0], dY_slot[sl], cfg=cfg, stream=stream, grads=grads_slot[sl])
-            else:
+            elif batched:
                 for xd, rb in zip(xsl, route_e2e):
                     mok.route_layout(xd, layer.W_r, wl.k, layer.bias, out=rb, workspace=b["route_ws"],
                                      stream=stream)
-                if len(xs) > 1:
-                    mok.moe_forward_batches(p, xsl, layer.packed, route_e2e, out_slot[sl], ws_b,
-                                            packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
-                else:
-                    mok.moe_forward(p, xsl[0], layer.packed, route_e2e[0], out_slot[sl][0], b["ws"],
+                mok.moe_forward_batches(p, xsl, layer.packed, route_e2e, out_slot[sl], ws_b,
+                                        packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
+            else:
+                # batch by batch (one batch: the single-step path)
+                for xd, od in zip(xsl, out_slot[sl]):
+                    mok.route_layout(xd, layer.W_r, wl.k, layer.bias, out=route_e2e[0], workspace=b["route_ws"],
+                                     stream=stream)
+                    mok.moe_forward(p, xd, layer.packed, route_e2e[0], od, b["ws"],
                                     packed_shared=layer.packed_shared, cfg=cfg, stream=stream)
         ev_done[sl].record(stream)
         c_out.wait_event(ev_done[sl])
@@ -550,7 +573,7 @@ def measure_e2e(wl, inp, layer, dev, stream, cfg, b, p, xs, routings, ws_b, stat
     return dict(ms=a0.elapsed_time(a1), steps=n_e2e,
                 h2d=len(xs) * T * H * 2 * (2 if wl.backward else 1), d2h=len(xs) * T * H * 2,
                 api="mok_route_layout + " + ("mok_moe_forward(training) + mok_moe_backward" if wl.backward else
-                                             "mok_moe_forward_batches" if len(xs) > 1 else "mok_moe_forward"))
+                                             "mok_moe_forward_batches" if batched else "mok_moe_forward"))
 
 
 def roofline(m, args):

@@ -603,19 +603,19 @@ __device__ void combine_tokens(const MegaParams& p, const MegaBatch& bt, int t0,
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            // up to 4 slots' loads in flight, then their products in j order
-            for (int j0 = 0; j0 < k; j0 += 4) {
-                uint4 u[4];
-                float wj[4];
+            // up to 8 slots' loads in flight, then their products in j order
+            for (int j0 = 0; j0 < k; j0 += 8) {
+                uint4 u[8];
+                float wj[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     if (j0 + q < k) {
                         wj[q] = bt.topk_w[(int64_t)t * k + j0 + q];
                         u[q] = __ldcs(reinterpret_cast<const uint4*>(bt.partials + ((int64_t)t * k + j0 + q) * H) + c);
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 8; ++q) {
                     if (j0 + q < k) {
                         acc[0] = fmaf(wj[q], bf16_lo(u[q].x), acc[0]); acc[1] = fmaf(wj[q], bf16_hi(u[q].x), acc[1]);
                         acc[2] = fmaf(wj[q], bf16_lo(u[q].y), acc[2]); acc[3] = fmaf(wj[q], bf16_hi(u[q].y), acc[3]);

@@ -70,18 +70,19 @@ class MoELayer:
         return mok.route_layout(x, self.W_r, self.k, self.bias, out=b["routing"], workspace=b["route_ws"],
                                 stream=stream)
 
-    def forward(self, x, training=False, cfg=None, stream=None, route=True):
-        """out [T, H] bf16 (a view of a reused buffer). The stage kernels run
-        unless cfg has FLAG_MEGAKERNEL (inference only); training keeps the
-        activations the backward needs."""
+    def forward(self, x, training=False, cfg=None, stream=None, route=True, out=None):
+        """out [T, H] bf16 (a view of a reused buffer unless `out` is given).
+        The stage kernels run unless cfg has FLAG_MEGAKERNEL (inference only);
+        training keeps the activations the backward needs."""
         T = x.shape[0]
         b = self.buffers(T, training, cfg)
         if route:
             self.route(x, training, stream)
-        mok.moe_forward(self.problem(T), x, self.packed, b["routing"], b["out"], b["ws"],
+        dst = b["out"] if out is None else out
+        mok.moe_forward(self.problem(T), x, self.packed, b["routing"], dst, b["ws"],
                         saved=b.get("saved") if training else None, packed_shared=self.packed_shared, cfg=cfg,
                         stream=stream)
-        return b["out"][:T]
+        return dst[:T]
 
     def backward(self, x, dY, cfg=None, stream=None, grads=None):
         T = x.shape[0]
