@@ -77,11 +77,13 @@ WORKLOADS = {
     # profiling case: the same expert shape with 8 experts (about 1 GB of
     # weights, still well above the 129 MB L2) for counter captures
     "bf16_fwd_E8_T2560": Workload("bf16_fwd_E8_T2560", T=2560, H=7168, I=2048, E=8, k=2),
-    # 1024 rows per expert as at T=4096 with 32 experts: the swapped-operand GEMM tiles
+    # 1024 rows per expert as at T=4096 with 32 experts
     "bf16_fwd_E8_T4096": Workload("bf16_fwd_E8_T4096", T=4096, H=7168, I=2048, E=8, k=2),
     "mxfp8_fwd_E8_T2560": Workload("mxfp8_fwd_E8_T2560", T=2560, H=7168, I=2048, E=8, k=2, dtype="mxfp8"),
     # backward profiling case: 1024 rows per expert, as in the 32-expert T=4096 backward
     "bf16_bwd_E8_T4096": Workload("bf16_bwd_E8_T4096", T=4096, H=7168, I=2048, E=8, k=2, backward=True),
+    "mxfp8_bwd_E8_T4096": Workload("mxfp8_bwd_E8_T4096", T=4096, H=7168, I=2048, E=8, k=2, dtype="mxfp8",
+                                   backward=True),
 }
 
 
