@@ -472,10 +472,21 @@ cudaError_t gemm_wgrad_mx(const void* AT_q, const uint8_t* AT_sf, int M, const v
     const bool wide = N % 256 == 0 && (reinterpret_cast<uintptr_t>(out0) & 31) == 0 &&
                       (split_col >= N || (reinterpret_cast<uintptr_t>(out1) & 31) == 0);
     const int BN = wide ? 256 : 128;
+    // 2-SM pairs over two 128-row M tiles: each CTA loads its 128 weight rows
+    // and half of the 256 B rows per K block (a third less per FLOP)
+    const bool pair = wide && M % 256 == 0;
     p.n_tiles = N / BN;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, AT_q, M, rows_pad, 1, 128, 128)) return cudaErrorInvalidValue;
-    if (!make_tmap(&tb, BT_q, N, rows_pad, 1, 128, BN)) return cudaErrorInvalidValue;
+    if (!make_tmap(&tb, BT_q, N, rows_pad, 1, 128, pair ? BN / 2 : BN)) return cudaErrorInvalidValue;
+    if (pair) {
+        CUtensorMap tsa, tsb;
+        if (!make_tmap_chunks(&tsa, AT_sf, (int64_t)(M / kTileM) * p.sf_kchunks) ||
+            !make_tmap_chunks(&tsb, BT_sf, (int64_t)(N / kTileM) * p.sf_kchunks_b))
+            return cudaErrorInvalidValue;
+        const int64_t tub = (int64_t)E * (M / kTileM) * p.n_tiles;   // in 128-row tiles, two per pair
+        return run<256, true, false, kEpiDense, 6, 1, 2>(ta, tb, tb, tsa, tsb, p, tub, c.num_sms, s);
+    }
     CUtensorMap to0, to1;
     if (!make_tmap_out3d(&to0, out0, E, M, p.ldo, p.ldo)) return cudaErrorInvalidValue;
     if (split_col < N) {

@@ -146,7 +146,7 @@ __device__ __forceinline__ void build_sched(const GemmParams& p, Sched& s) {
             s.poff[e] = rows;
             s.toff[e] = tiles;
             rows += p.identity_rows > 0 ? cnt : mt * kTileM;
-            tiles += p.m_fixed > 0 ? ceil_div(p.m_fixed, kTileM) * p.n_tiles : ceil_div(mt, CLN) * p.n_tiles;
+            tiles += p.m_fixed > 0 ? ceil_div(p.m_fixed, kTileM * CLN) * p.n_tiles : ceil_div(mt, CLN) * p.n_tiles;
         }
         s.poff[p.E] = rows;
         s.toff[p.E] = tiles;
@@ -222,6 +222,7 @@ __device__ __forceinline__ void load_gate_up(uint32_t tbase, int c0, uint32_t (&
 // 2mp + rank. An expert with an odd number of m-tiles leaves the last pair's
 // second half outside its segment: that CTA's rows are not valid (valid = 0)
 // and its epilogue stores nothing.
+template <int BK>
 __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const Sched& s, int g, int rank) {
     TileInfo ti;
     int lo = 0, hi = p.E - 1;  // last e with toff[e] <= g
@@ -231,6 +232,22 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
     }
     const int e = lo;
     const int cnt = p.counts[e];
+    if (p.m_fixed > 0) {
+        // weight gradients: M = the fixed weight rows (a multiple of 256), in
+        // pairs of 128-row tiles; K = the expert's padded token segment
+        const int mp = p.m_fixed / (2 * kTileM);
+        const int local = g - s.toff[e];
+        ti.e = e;
+        ti.n = local / mp;
+        ti.m = 2 * (local % mp) + rank;
+        ti.a_row0 = s.poff[e];
+        ti.num_kb = (ceil_div(cnt, kTileM) * kTileM) / BK;
+        ti.row_base = ti.m * kTileM;
+        ti.local_row0 = ti.m * kTileM;
+        ti.valid = 1;
+        ti.half = 0;
+        return ti;
+    }
     const int mt = ceil_div(cnt, kTileM);
     const int mp = ceil_div(mt, 2);
     const int local = g - s.toff[e];
@@ -264,7 +281,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // rows; dense epilogue - the outputs out0 / out1 as [E, m_fixed, width]
     // BF16 (boxes of 32 x 32 x 1); unused otherwise
     using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>;
-    static_assert(CLN == 1 || (CLN == 2 && EPI != kEpiDense), "2-SM pairs: grouped-row GEMMs");
+    static_assert(CLN == 1 || (CLN == 2 && (EPI != kEpiDense || MX)),
+                  "2-SM pairs: grouped-row GEMMs and the MXFP8 K-major weight gradients");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Sched sched;
     __shared__ uint32_t s_tmem_base;
@@ -332,7 +350,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                          (EPI != kEpiSwiGLU || p.gu == nullptr);
     auto decode = [&](int gi) {
         if constexpr (CLN == 2) {
-            return decode_pair_tile(p, sched, gi, rank);
+            return decode_pair_tile<C::kBK>(p, sched, gi, rank);
         } else {
             TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, gi);
             ti.half = half_ok && p.counts[ti.e] - ti.local_row0 <= 64 ? 1 : 0;
@@ -356,20 +374,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         // both halves signal the leader's full barrier, which expects both
                         const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
                         if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2 * (C::kStageBytes + C::kSfStage));
-                        tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, kb * C::kBK, ti.a_row0);
-                        const bool b1 = kb < p.b_split_kb;
-                        const int brow = ti.e * p.b_rows_per_expert + ti.n * BN;
+                        // K-major weight gradients: K is the expert's token range, A rows
+                        // this CTA's 128 weight rows, B rows the tile's N columns
+                        const bool kw = p.kmajor_wgrad != 0;
+                        const int ax = kw ? ti.a_row0 + kb * C::kBK : kb * C::kBK;
+                        const int ay = kw ? ti.m * kTileM : ti.a_row0;
+                        tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, ax, ay);
+                        const bool b1 = kw || kb < p.b_split_kb;
+                        const int brow = kw ? ti.n * BN : ti.e * p.b_rows_per_expert + ti.n * BN;
                         tc::tma_load_2d_2sm(b_tile(stage), b1 ? (const void*)&tmB : (const void*)&tmB2, lead_full,
-                                            (b1 ? kb : kb - p.b_split_kb) * C::kBK, brow + rank * (BN / 2));
+                                            kw ? ax : (b1 ? kb : kb - p.b_split_kb) * C::kBK, brow + rank * (BN / 2));
                         if constexpr (MX) {
                             // scale chunks (512 B = two 256-byte rows of tmX0 / tmX1): this CTA's A
                             // rows, and all BN rows of B (the pair MMA reads B's scales in each CTA)
-                            tc::tma_load_2d_2sm(sf_tile(stage), &tmX0, lead_full, 0,
-                                                2 * ((ti.a_row0 / kTileM) * p.sf_kchunks + kb));
+                            const int akc = kw ? ax / 128 : kb;
+                            const int art = kw ? ti.m : ti.a_row0 / kTileM;
+                            const int bkn = kw ? p.sf_kchunks_b : p.sf_kchunks;
+                            tc::tma_load_2d_2sm(sf_tile(stage), &tmX0, lead_full, 0, 2 * (art * p.sf_kchunks + akc));
 #pragma unroll
                             for (int j = 0; j < C::kNChunks; ++j)
                                 tc::tma_load_2d_2sm(sf_tile(stage) + 512 * (1 + j), &tmX1, lead_full, 0,
-                                                    2 * ((brow / kTileM + j) * p.sf_kchunks + kb));
+                                                    2 * ((brow / kTileM + j) * bkn + akc));
                         }
                         last_par[stage] = (int)ph;
                         if (++stage == STAGES) { stage = 0; ph ^= 1u; }
@@ -526,7 +551,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // accumulator released, then each row segment written with
                 // 32-byte stores (whole sectors); an expert without tokens
                 // writes zeros
-                static_assert(CLN == 1, "dense wide epilogue: single CTAs");
                 const int eg = (warp - 2) >> 2;
                 uint32_t w0[16], w1[16], w2[16], w3[16];
                 if (has_acc) {
@@ -544,7 +568,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     load_pair(eg, w0, w1);
                     load_pair(eg + 4, w2, w3);
                     tc::fence_before_sync();
-                    tc::mbar_arrive(acce_bar(acc));
+                    if constexpr (CLN == 2) tc::mbar_arrive_cluster(tc::mapa_shared(acce_bar(acc), 0));
+                    else tc::mbar_arrive(acce_bar(acc));
                     if (++acc == ACC_STAGES) { acc = 0; acc_ph ^= 1u; }
                 } else {
 #pragma unroll
