@@ -44,19 +44,8 @@ __device__ __forceinline__ int find_expert(const int32_t* poff, int E, int pr) {
 // Pull-dispatch: one warp per padded row.
 // ---------------------------------------------------------------------------
 // One 32-element MXFP8 block: E8M0 code of its amax, E4M3 bytes of x / scale.
-__device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* src, uint4& o0, uint4& o1) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4 v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __ldg(s4 + i);
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[8 * i + 0] = bf16_lo(v[i].x); f[8 * i + 1] = bf16_hi(v[i].x);
-        f[8 * i + 2] = bf16_lo(v[i].y); f[8 * i + 3] = bf16_hi(v[i].y);
-        f[8 * i + 4] = bf16_lo(v[i].z); f[8 * i + 5] = bf16_hi(v[i].z);
-        f[8 * i + 6] = bf16_lo(v[i].w); f[8 * i + 7] = bf16_hi(v[i].w);
-    }
+// Every quantiser of the library goes through quantize32.
+__device__ __forceinline__ uint32_t quantize32(const float (&f)[32], uint4& o0, uint4& o1) {
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -70,6 +59,27 @@ __device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* src, u
     o0 = make_uint4(w[0], w[1], w[2], w[3]);
     o1 = make_uint4(w[4], w[5], w[6], w[7]);
     return code;
+}
+
+// 32 BF16 values (four 16-byte words) to fp32.
+__device__ __forceinline__ void unpack32(const uint4 (&v)[4], float (&f)[32]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[8 * i + 0] = bf16_lo(v[i].x); f[8 * i + 1] = bf16_hi(v[i].x);
+        f[8 * i + 2] = bf16_lo(v[i].y); f[8 * i + 3] = bf16_hi(v[i].y);
+        f[8 * i + 4] = bf16_lo(v[i].z); f[8 * i + 5] = bf16_hi(v[i].z);
+        f[8 * i + 6] = bf16_lo(v[i].w); f[8 * i + 7] = bf16_hi(v[i].w);
+    }
+}
+
+__device__ __forceinline__ uint32_t quantize_block32(const __nv_bfloat16* src, uint4& o0, uint4& o1) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __ldg(s4 + i);
+    float f[32];
+    unpack32(v, f);
+    return quantize32(f, o0, o1);
 }
 
 // Row-wise MXFP8 quantisation of x (warp per row; the codes the dispatch
@@ -132,17 +142,18 @@ dispatch_q_kernel(const uint8_t* __restrict__ xq, const uint32_t* __restrict__ x
     }
 }
 
-// MXFP8 pull-dispatch in one token-major pass: a warp takes a token and
-// lane L quantises the 32-element blocks L, L + 32, ... of its row once (the
-// encoder of quantize_rows), then writes each block's 32 codes with one
-// 32-byte store to each of the token's k rows of the padded expert-contiguous
-// layout (a warp store covers 1 KB of a row); the four scale codes of a
-// 128-wide chunk, held by four neighbouring lanes, leave as one word. Every
-// token row is read once and no quantised copy of x is written and read
-// back. Pad rows are not written. The bytes equal those of quantize_rows +
-// dispatch_q.
+// MXFP8 pull-dispatch in one token-major pass: W warps (1 or 2) take a token
+// and lane L of warp w quantises the 32-element blocks 32w + L, 32w + L + 32W,
+// ... of its row once (the encoder of quantize_rows), then writes each
+// block's 32 codes with one 32-byte store to each of the token's k rows of
+// the padded expert-contiguous layout (a warp store covers 1 KB of a row);
+// the four scale codes of a 128-wide chunk, held by four neighbouring lanes,
+// leave as one word. Every token row is read once and no quantised copy of x
+// is written and read back. Pad rows are not written. The bytes equal those
+// of quantize_rows + dispatch_q. Two warps per token keep twice the loads in
+// flight when there are too few tokens to fill the GPU with one each.
 __global__ void __launch_bounds__(256)
-dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E, int k,
+dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E, int k, int W,
                        const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_row,
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                        uint8_t* __restrict__ A, uint8_t* __restrict__ A_sf) {
@@ -150,7 +161,10 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
     padded_offsets(counts, E, poff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = H / 32, kc_row = H / 128;
-    for (int64_t t = (int64_t)blockIdx.x * 8 + warp; t < T; t += (int64_t)gridDim.x * 8) {
+    const int64_t units = (int64_t)T * W;
+    for (int64_t u = (int64_t)blockIdx.x * 8 + warp; u < units; u += (int64_t)gridDim.x * 8) {
+        const int64_t t = u / W;
+        const int bw = (int)(u % W) * 32;   // this warp's first block
         // padded destination row of slot j (lane j holds it when k <= 32)
         auto dest = [&](int j) {
             const int64_t sl = t * k + j;
@@ -158,15 +172,31 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
             return poff[e] + slot_row[sl] - offsets[e];
         };
         const int my_pr = (k <= 32 && lane < k) ? dest(lane) : 0;
+        // lane L quantises blocks L, L + 32, ...; the next round's four
+        // 16-byte loads are issued before this round is quantised and stored
+        const uint4* xs = reinterpret_cast<const uint4*>(x + t * H);
+        const int step = 32 * W;
+        uint4 nv[4];
+        if (bw + lane < nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) nv[i] = __ldg(xs + (bw + lane) * 4 + i);
         // every lane runs the same trip counts (the shuffles need the whole
         // warp); nb % 4 == 0, so the four lanes of a chunk are all active or
         // all idle
-        for (int b0 = 0; b0 < nb; b0 += 32) {
+        for (int b0 = bw; b0 < nb; b0 += step) {
             const int b = b0 + lane;
             const bool act = b < nb;
+            const uint4 cv[4] = {nv[0], nv[1], nv[2], nv[3]};
+            if (b + step < nb)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) nv[i] = __ldg(xs + (b + step) * 4 + i);
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
             uint32_t code = 0;
-            if (act) code = quantize_block32(x + t * H + b * 32, o0, o1);
+            if (act) {
+                float f[32];
+                unpack32(cv, f);
+                code = quantize32(f, o0, o1);
+            }
             // the chunk's four codes, byte j = block 4c + j, in the chunk's first lane
             uint32_t word = code;
             word |= __shfl_down_sync(0xffffffffu, code, 1) << 8;
@@ -550,8 +580,12 @@ cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, co
                                    const int32_t* slot_row, const int32_t* counts, const int32_t* offsets, void* A,
                                    uint8_t* A_sf, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const int blocks = (int)std::min<int64_t>(ceil_div(T, 8), (int64_t)sm_count() * 8);
-    dispatch_tokens_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H, E, k, topk_idx,
+    // two warps per token while one each would leave the GPU short of loads in
+    // flight (fewer tokens than about 27 per SM: a warp per token then fills
+    // at most 27 of the ~32 warp slots an SM holds at this register count)
+    const int W = (int64_t)T < (int64_t)sm_count() * 27 ? 2 : 1;
+    const int blocks = (int)std::min<int64_t>(ceil_div((int64_t)T * W, 8), (int64_t)sm_count() * 8);
+    dispatch_tokens_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H, E, k, W, topk_idx,
                                                   slot_row, counts, offsets, static_cast<uint8_t*>(A), A_sf);
     return cudaGetLastError();
 }
@@ -583,22 +617,6 @@ cudaError_t launch_dispatch_q(const void* x_q, const void* x_sf, int T, int H, i
 // quantises column t (COLS) and row t / 4's 32-column block t % 4 (ROWS).
 // Every block goes through quantize32, so both layouts hold the codes of the
 // same rule as the other quantisers.
-__device__ __forceinline__ uint32_t quantize32(const float (&f)[32], uint4& o0, uint4& o1) {
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    const uint32_t code = e8m0_code(amax);
-    const float inv = e8m0_inv_scale(code);
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        w[i] = f32x2_to_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
-               (f32x2_to_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
-    o0 = make_uint4(w[0], w[1], w[2], w[3]);
-    o1 = make_uint4(w[4], w[5], w[6], w[7]);
-    return code;
-}
-
 template <bool ROWS, bool COLS>
 __global__ void __launch_bounds__(128)
 quantize_tiles_kernel(const __nv_bfloat16* __restrict__ src, int64_t R, int F, uint8_t* __restrict__ q,
