@@ -250,7 +250,12 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
         return run<256, true, false, kEpiSwiGLU, 4, 1>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
-        if (cl) return run<256, false, false, kEpiSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        if (cl) {
+            // the odd last 128-row tile of an expert runs as an M=128 pair: 64-row A boxes
+            CUtensorMap ta64;
+            if (!make_tmap(&ta64, A, a_rows, H, 2, 64, 64)) return cudaErrorInvalidValue;
+            return run<256, false, false, kEpiSwiGLU, 6, 2, 2>(ta, tb, tb, ta64, ta64, p, tub, c.num_sms, s);
+        }
         return run<256, false, false, kEpiSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     return run<128, false, false, kEpiSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -293,7 +298,11 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
         return run<128, true, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     if (BN == 256) {
-        if (cl) return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+        if (cl) {
+            CUtensorMap ta64;
+            if (!make_tmap(&ta64, h, a_rows, I, 2, 64, 64)) return cudaErrorInvalidValue;
+            return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb, ta64, ta64, p, tub, c.num_sms, s);
+        }
         return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     }
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -359,7 +368,11 @@ cudaError_t gemm_dgrad_h(const void* dy, const void* W_down, int E, int H, int I
     if (!make_tmap(&ta, dy, a_rows, H, 2, 64, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, W_down, (int64_t)E * I, H, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
-    if (cl) return run<256, false, false, kEpiDSwiGLU, 6, 2, 2>(ta, tb, tb, p, tub, c.num_sms, s);
+    if (cl) {
+        CUtensorMap ta64;
+        if (!make_tmap(&ta64, dy, a_rows, H, 2, 64, 64)) return cudaErrorInvalidValue;
+        return run<256, false, false, kEpiDSwiGLU, 6, 2, 2>(ta, tb, tb, ta64, ta64, p, tub, c.num_sms, s);
+    }
     if (BN == 256) return run<256, false, false, kEpiDSwiGLU, 4, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     if (BN == 128) return run<128, false, false, kEpiDSwiGLU, 6, 2>(ta, tb, tb, p, tub, c.num_sms, s);
     return run<64, false, false, kEpiDSwiGLU, 8, 2>(ta, tb, tb, p, tub, c.num_sms, s);
@@ -386,7 +399,11 @@ cudaError_t gemm_dgrad_a(const void* dgu, const void* W_gate, const void* W_up, 
     if (!make_tmap(&tb, W_gate, (int64_t)E * H, I, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb2, W_up, (int64_t)E * H, I, 2, 64, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
     const int64_t tub = mtiles_ub(a_rows, E) * p.n_tiles;
-    if (cl) return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
+    if (cl) {
+        CUtensorMap ta64;
+        if (!make_tmap(&ta64, dgu, a_rows, 2 * I, 2, 64, 64)) return cudaErrorInvalidValue;
+        return run<256, false, false, kEpiScatter, 6, 2, 2>(ta, tb, tb2, ta64, ta64, p, tub, c.num_sms, s);
+    }
     if (BN == 256) return run<256, false, false, kEpiScatter, 4, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
     return run<128, false, false, kEpiScatter, 6, 2>(ta, tb, tb2, p, tub, c.num_sms, s);
 }

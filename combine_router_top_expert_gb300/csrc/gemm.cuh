@@ -76,6 +76,9 @@ struct GemmCfg {
     // warps.
     static constexpr bool kWideEpi = MX && ACC_STAGES == 1;
     static constexpr int kEpiWarps = kWideEpi ? 8 : 4;
+    // BF16 2-SM pairs run an expert's odd last 128-row tile as an M=128 pair
+    // (64 rows per CTA; tmX0 then maps A in boxes of 64 rows)
+    static constexpr bool kPairTails = CLN == 2 && !MX && !MN_MAJOR && EPI != kEpiDense;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
     // BF16 grouped-row forward tiles: an expert's last tile with at most 64
     // rows runs M=64 MMAs (rows 16q..16q+15 land in TMEM lanes 32q..32q+15)
@@ -127,6 +130,7 @@ struct TileInfo {
     int local_row0;  // first expert-local row of the tile
     int valid;       // 0: skip
     int half;        // 1: the expert's last tile holds at most 64 rows; one M=64 MMA per K step
+    int m128;        // 2-SM pairs: the pair shares one 128-row tile, 64 rows per CTA, M=128 MMAs
 };
 
 // Per-CTA copy of the group schedule.
@@ -185,6 +189,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, const Sched
     }
     ti.valid = 1;
     ti.half = 0;
+    ti.m128 = 0;
     return ti;
 }
 
@@ -219,10 +224,11 @@ __device__ __forceinline__ void load_gate_up(uint32_t tbase, int c0, uint32_t (&
 
 // 2-SM pairs: pair tile g covers m-tiles 2mp and 2mp+1 of one expert (n
 // fastest-varying after mp, as for single tiles); CTA `rank` takes m-tile
-// 2mp + rank. An expert with an odd number of m-tiles leaves the last pair's
-// second half outside its segment: that CTA's rows are not valid (valid = 0)
-// and its epilogue stores nothing.
-template <int BK>
+// 2mp + rank. An expert with an odd number of m-tiles: with TAILS its last
+// pair shares the single last m-tile, CTA `rank` taking its rows 64*rank ..
+// 64*rank+63, and runs M=128 MMAs (m128); without, the second CTA's rows lie
+// outside the segment (valid = 0) and its epilogue stores nothing.
+template <int BK, bool TAILS = false>
 __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const Sched& s, int g, int rank) {
     TileInfo ti;
     int lo = 0, hi = p.E - 1;  // last e with toff[e] <= g
@@ -246,6 +252,7 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
         ti.local_row0 = ti.m * kTileM;
         ti.valid = 1;
         ti.half = 0;
+        ti.m128 = 0;
         return ti;
     }
     const int mt = ceil_div(cnt, kTileM);
@@ -253,11 +260,14 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
     const int local = g - s.toff[e];
     ti.e = e;
     ti.n = local / mp;
-    ti.m = 2 * (local % mp) + rank;
-    ti.a_row0 = s.poff[e] + ti.m * kTileM;
+    const int pp = local % mp;
+    ti.m128 = (TAILS && (mt & 1) && pp == mp - 1) ? 1 : 0;
+    ti.m = ti.m128 ? mt - 1 : 2 * pp + rank;
+    const int r0 = ti.m * kTileM + (ti.m128 ? 64 * rank : 0);   // first expert-local row of this CTA
+    ti.a_row0 = s.poff[e] + r0;
     ti.num_kb = p.num_kb;
     ti.row_base = ti.a_row0;
-    ti.local_row0 = ti.m * kTileM;
+    ti.local_row0 = r0;
     ti.valid = ti.m < mt ? 1 : 0;
     ti.half = 0;
     return ti;
@@ -350,7 +360,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                          (EPI != kEpiSwiGLU || p.gu == nullptr);
     auto decode = [&](int gi) {
         if constexpr (CLN == 2) {
-            return decode_pair_tile<C::kBK>(p, sched, gi, rank);
+            return decode_pair_tile<C::kBK, C::kPairTails>(p, sched, gi, rank);
         } else {
             TileInfo ti = decode_tile<BN, MN_MAJOR, C::kBK>(p, sched, gi);
             ti.half = half_ok && p.counts[ti.e] - ti.local_row0 <= 64 ? 1 : 0;
@@ -373,13 +383,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if constexpr (CLN == 2) {
                         // both halves signal the leader's full barrier, which expects both
                         const uint32_t lead_full = tc::mapa_shared(full_bar(stage), 0);
-                        if (rank == 0) tc::mbar_expect_tx(full_bar(stage), 2 * (C::kStageBytes + C::kSfStage));
+                        // an M=128 pair tile stages 64 A rows per CTA
+                        const uint32_t abytes = (C::kPairTails && ti.m128) ? C::kBytesA / 2 : C::kBytesA;
+                        if (rank == 0)
+                            tc::mbar_expect_tx(full_bar(stage), 2 * (abytes + C::kBytesB + C::kSfStage));
                         // K-major weight gradients: K is the expert's token range, A rows
                         // this CTA's 128 weight rows, B rows the tile's N columns
                         const bool kw = p.kmajor_wgrad != 0;
                         const int ax = kw ? ti.a_row0 + kb * C::kBK : kb * C::kBK;
                         const int ay = kw ? ti.m * kTileM : ti.a_row0;
-                        tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, ax, ay);
+                        if (C::kPairTails && ti.m128) tc::tma_load_2d_2sm(a_tile(stage), &tmX0, lead_full, ax, ay);
+                        else tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, ax, ay);
                         const bool b1 = kw || kb < p.b_split_kb;
                         const int brow = kw ? ti.n * BN : ti.e * p.b_rows_per_expert + ti.n * BN;
                         tc::tma_load_2d_2sm(b_tile(stage), b1 ? (const void*)&tmB : (const void*)&tmB2, lead_full,
@@ -507,7 +521,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         } else if constexpr (MX) {
                             tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
                         } else if constexpr (CLN == 2) {
-                            tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(256, BN, false, false), accum);
+                            tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(ti.m128 ? 128 : 256, BN, false, false), accum);
                         } else {
                             tc::mma_bf16(d, ad, bd, tc::idesc_bf16(ti.half ? 64 : 128, BN, MN_MAJOR, MN_MAJOR), accum);
                         }
@@ -537,7 +551,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int gi = gstart; gi < gtotal; gi += gstep) {
             TileInfo ti = decode(gi);
             // tile row owned by this thread (-1: none, in the empty lanes of an M=64 tile)
-            const int row = ti.half ? (lane < 16 ? q * 16 + lane : -1) : q * 32 + lane;
+            // (an M=128 pair tile: lanes 32q.. hold rows 32(q%2).. of this CTA's 64 for the
+            // tile columns (q/2)*BN/2 .. +BN/2, in tensor-memory columns 0 .. BN/2)
+            const int row = ti.m128 ? 32 * (q & 1) + lane : ti.half ? (lane < 16 ? q * 16 + lane : -1) : q * 32 + lane;
+            const int cbeg = ti.m128 ? (q >> 1) * (BN / 2) : 0;   // first tile column of this warp
+            const int cspan = ti.m128 ? BN / 2 : BN;              // its tile columns
             const bool has_acc = ti.num_kb > 0;
             if (has_acc) {
                 if (!tc::mbar_wait(accf_bar(acc), acc_ph, st, tmo, kSiteEpiAccFull)) break;
@@ -761,10 +779,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const bool live = (p.identity_rows > 0 ? (prow < p.identity_rows) : true) && ti.valid && row >= 0;
                 uint32_t sfw = 0;   // MXFP8: scale codes of the current 128-wide chunk of h
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+                for (int c0 = 0; c0 < cspan / 2; c0 += 32) {
                     uint32_t gr[32], ur[32];
                     load_gate_up<BN, !MX>(tbase, c0, gr, ur);
-                    const int hc = ti.n * (BN / 2) + c0;
+                    const int hc = ti.n * (BN / 2) + cbeg / 2 + c0;
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -823,12 +841,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     dest = p.row_src[p.offsets[ti.e] + lrow];
                 }
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 32) {
+                for (int c0 = 0; c0 < cspan; c0 += 32) {
                     uint32_t r[32];
                     tc::tmem_ld_32x32b_x32(tbase + c0, r);
                     tc::tmem_ld_wait();
                     if (dest < 0) continue;
-                    const int col = ti.n * BN + c0;
+                    const int col = ti.n * BN + cbeg + c0;
                     if (p.out_f32) {
                         float* dst = static_cast<float*>(p.out0) + dest * p.ldo + col;
 #pragma unroll
@@ -848,11 +866,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const float* gb = static_cast<const float*>(p.gu) + prow * (int64_t)(2 * I);
                 __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(p.out0) + prow * (int64_t)(2 * I);
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN && ti.valid; c0 += 32) {   // pairs: no rows outside the expert
+                for (int c0 = 0; c0 < cspan && ti.valid; c0 += 32) {   // pairs: no rows outside the expert
                     uint32_t r[32];
                     tc::tmem_ld_32x32b_x32(tbase + c0, r);
                     tc::tmem_ld_wait();
-                    const int col = ti.n * BN + c0;
+                    const int col = ti.n * BN + cbeg + c0;
                     uint32_t dgw[16], duw[16];
                     uint32_t gw32[32], uw32[32];
 #pragma unroll

@@ -85,14 +85,16 @@ typedef struct {
  * SM split, GPU-local counters, ring) instead of the stage kernels
  * (dispatch, grouped GEMMs, combine). */
 #define MOK_FLAG_MEGAKERNEL 1
-/* Run the staged grouped GEMMs (BF16 forward gate/up and down, backward
- * dgrad; MXFP8 gate/up) as 2-SM CTA pairs: tcgen05 cta_group::2 MMAs of 256
- * rows over two CTAs, each staging its own 128 A rows and half of the B rows
+/* 2-SM CTA pairs for the staged grouped GEMMs (BF16 forward gate/up and
+ * down, backward dgrad; MXFP8 gate/up): tcgen05 cta_group::2 MMAs of 256 rows
+ * over two CTAs, each staging its own 128 A rows and half of the B rows
  * (MXFP8: its A rows' block scales and all B rows' scales). Results are
- * bit-identical to the default single-CTA kernels; experts whose row count
- * is an odd number of 128-row tiles leave half of their last pair idle. The
- * shared expert and the MXFP8 down GEMM run single CTAs. Off by default
- * (measured no faster). */
+ * bit-identical to single-CTA kernels; an expert whose row count is an odd
+ * number of 128-row tiles leaves half of its last pair idle. The BF16 GEMMs
+ * run as pairs by default (measured faster); this flag also puts the MXFP8
+ * gate/up GEMM on pairs (measured slower). The shared expert and the MXFP8
+ * down GEMM always run single CTAs; the MXFP8 weight gradients always run as
+ * pairs when the weight rows are a multiple of 256. */
 #define MOK_FLAG_GEMM_PAIRS 2
 /* Megakernel trace: the launch writes one record of eight uint64 per CTA
  * (CTA i at byte offset 256 + 64*i of the workspace): [0] role (0 mover,
@@ -119,10 +121,10 @@ typedef struct {
  * of 256 rows and one remainder tile (a multiple of 32 rows) as the N side,
  * so little tensor work is spent on padded rows and no CTA of a pair idles
  * (needs I % 128 == 0 and H % 256 == 0). The token tiles are the default
- * (measured as fast or faster from 512 to 1024 rows per expert);
- * MOK_FLAG_SWAPPED_TILES selects the swapped ones, MOK_FLAG_ROW_TILES states
- * the default explicitly. The training forward (saved != NULL) and MXFP8
- * always use the token tiles. */
+ * (measured as fast or faster from 512 to 1024 rows per expert), as 2-SM
+ * pairs for BF16 (MOK_FLAG_GEMM_PAIRS); MOK_FLAG_SWAPPED_TILES selects the
+ * swapped tiles, MOK_FLAG_ROW_TILES the token tiles on single CTAs. The
+ * training forward (saved != NULL) and MXFP8 always use the token tiles. */
 #define MOK_FLAG_ROW_TILES 16
 #define MOK_FLAG_SWAPPED_TILES 128
 /* Swapped-operand tiles: cut each expert's tokens into ceil(n/256) tiles of

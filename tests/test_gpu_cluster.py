@@ -1,10 +1,12 @@
 """Grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2: one M=256 MMA over
 two CTAs' 128-row A halves and 128-row B halves) against the single-CTA
 kernels. Every output element is still one K-ordered tensor-core dot product
-with fp32 accumulation, so the results must be bit-identical; experts with
-an odd number of 128-row tiles exercise the pair whose second half lies
-outside the expert (its rows must not be written). MXFP8 runs single CTAs
-either way."""
+with fp32 accumulation, so the results must be bit-identical. Experts with
+an odd number of 128-row tiles exercise the last pair: in BF16 it shares the
+expert's last tile as an M=128 pair MMA (64 rows per CTA, the accumulator
+spread over all 128 lanes with half the columns each); the MXFP8 gate/up
+pairs leave its second half idle (rows outside the expert must not be
+written)."""
 import pytest
 import torch
 
@@ -42,13 +44,15 @@ def test_cluster_pairs_forward_bitwise(wl):
 
 @pytest.mark.gpu
 def test_cluster_pairs_backward_bitwise():
-    wl = synth.small("cl_bwd", T=400, H=512, I=512, E=4, k=2, backward=True)
+    # about 300 rows per expert: three 128-row tiles, so the last pair of every
+    # GEMM (training gate/up with G|U saved, down, both dgrads) is an M=128 pair
+    wl = synth.small("cl_bwd", T=600, H=512, I=512, E=4, k=2, backward=True)
     inp = synth.make_inputs(wl)
     layer = layer_for(inp, mok.BF16)
     x = to_dev_bf16(inp.x)
     dY = to_dev_bf16(inp.dY)
     res = []
-    for flags in (mok.FLAG_GEMM_PAIRS, 0):
+    for flags in (mok.FLAG_GEMM_PAIRS, mok.FLAG_ROW_TILES):
         cfg = mok.make_config(flags=flags)
         layer.forward(x, training=True, cfg=cfg)
         g = layer.backward(x, dY, cfg=cfg)
