@@ -307,6 +307,7 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
     staged = not args.megakernel or wl.backward
     flags = ((0 if staged else mok.FLAG_MEGAKERNEL) | (mok.FLAG_GEMM_PAIRS if args.gemm_pairs else 0) |
              (mok.FLAG_SWAPPED_TILES if args.swapped_tiles else 0) |
+             (mok.FLAG_ROW_TILES if args.single_cta else 0) |
              (mok.FLAG_MB_TOKEN_RANGES if args.mb_token_ranges else 0))
     cfg = mok.make_config(flags=flags, ring_rows=wl.ring_rows, mover_ctas=args.movers,
                           minibatch_tokens=args.minibatch)
@@ -584,7 +585,7 @@ def roofline(m, args):
     H = wl.H
     # captured traffic belongs to the single-CTA stage kernels only
     traffic, traffic_note = (captured_traffic(wl.name) if (m["staged"] and m["batches"] == 1 and not args.gemm_pairs
-                                                           and not args.swapped_tiles)
+                                                           and not args.swapped_tiles and not args.single_cta)
                              else (None, "not captured for this path"))
     fl = m["flops"]
     g_ms = statistics.mean(m["gemm_ms"])
@@ -721,6 +722,8 @@ def main():
                     help="skip the fwd+bwd and MXFP8 sub-measurements of the default workload")
     ap.add_argument("--megakernel", action="store_true", help="time the persistent megakernel forward")
     ap.add_argument("--gemm-pairs", action="store_true", help="BF16 grouped GEMMs as 2-SM CTA pairs (tcgen05 cta_group::2)")
+    ap.add_argument("--single-cta", action="store_true",
+                    help="BF16 grouped GEMMs on single CTAs (128-row token tiles) instead of 2-SM pairs")
     ap.add_argument("--swapped-tiles", action="store_true",
                     help="BF16 inference GEMMs with swapped operands (weight rows as M of 2-SM pair tiles)")
     ap.add_argument("--movers", type=int, default=0, help="megakernel mover CTAs (0 = library default)")
@@ -747,7 +750,7 @@ def main():
     m = measure(args, wl, inp, layer, dev, args.steps, args.warmup, trace=args.trace)
     extras = []
     if (args.workload == "bf16_fwd_T2560" and not args.no_extra and not args.megakernel and not args.gemm_pairs
-            and not args.swapped_tiles and ws == 1):
+            and not args.swapped_tiles and not args.single_cta and ws == 1):
         # the same experts (same weight draw): BF16 fwd+bwd at T=4096, the
         # MXFP8 forward with Zipf-skewed routing at T=2560, MXFP8 fwd+bwd at T=4096
         del layer
@@ -774,6 +777,7 @@ def main():
         "config": config_of(m, args, ws),
         "gemm_cta_pairs": bool(args.gemm_pairs),
         "gemm_swapped_tiles": bool(args.swapped_tiles),
+        "gemm_single_cta": bool(args.single_cta),
         "roofline": roofline(m, args),
         "e2e": e2e_of(m, ws),
         "stage_rooflines": m["stage_lines"],

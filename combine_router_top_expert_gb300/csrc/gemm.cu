@@ -540,6 +540,10 @@ cudaError_t gemm_wgrad(const void* Aact, int M, const void* B, int N, int E, con
         to1 = to0;
     }
     const int64_t tub = (int64_t)E * ((M + kTileM - 1) / kTileM) * p.n_tiles;
+    // 2-SM pairs over two 128-row weight tiles (each CTA: its 128 weight rows,
+    // half of the 256 columns; 32 KB per K block, 6 stages)
+    if (BN == 256 && c.cluster == 2 && M % 256 == 0)
+        return run<256, false, true, kEpiDense, 6, 2, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
     if (BN == 256) return run<256, false, true, kEpiDense, 4, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
     if (BN == 128) return run<128, false, true, kEpiDense, 6, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);
     return run<64, false, true, kEpiDense, 8, 2>(ta, tb, tb, to0, to1, p, tub, c.num_sms, s);

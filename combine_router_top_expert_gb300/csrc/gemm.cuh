@@ -70,7 +70,9 @@ struct GemmParams {
 // the BN B rows of the pair's 256 x BN tile.
 template <int BN, bool MX, bool MN_MAJOR, int EPI, int STAGES, int ACC_STAGES, int CLN = 1>
 struct GemmCfg {
-    static_assert(CLN == 1 || (CLN == 2 && !MN_MAJOR && BN % 32 == 0 && (!MX || BN == 256)), "2-SM pairs: K-major");
+    static_assert(CLN == 1 || (CLN == 2 && BN % 32 == 0 && (!MX || BN == 256) &&
+                               (!MN_MAJOR || (!MX && EPI == kEpiDense && BN == 256))),
+                  "2-SM pairs: K-major, or the BF16 MN-major weight gradients");
     // MXFP8 tiles 256 wide keep one accumulator (their scales take the rest
     // of TMEM) and hide the epilogue behind the next tile with 8 epilogue
     // warps.
@@ -291,8 +293,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // rows; dense epilogue - the outputs out0 / out1 as [E, m_fixed, width]
     // BF16 (boxes of 32 x 32 x 1); unused otherwise
     using C = GemmCfg<BN, MX, MN_MAJOR, EPI, STAGES, ACC_STAGES, CLN>;
-    static_assert(CLN == 1 || (CLN == 2 && (EPI != kEpiDense || MX)),
-                  "2-SM pairs: grouped-row GEMMs and the MXFP8 K-major weight gradients");
+    static_assert(CLN == 1 || (CLN == 2 && (EPI != kEpiDense || MX || MN_MAJOR)),
+                  "2-SM pairs: grouped-row GEMMs and the weight gradients");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Sched sched;
     __shared__ uint32_t s_tmem_base;
@@ -387,6 +389,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint32_t abytes = (C::kPairTails && ti.m128) ? C::kBytesA / 2 : C::kBytesA;
                         if (rank == 0)
                             tc::mbar_expect_tx(full_bar(stage), 2 * (abytes + C::kBytesB + C::kSfStage));
+                        if constexpr (MN_MAJOR) {
+                            // BF16 weight gradients: K rows of the expert's token range; A
+                            // this CTA's 128 weight columns, B its half of the tile's columns
+                            const int krow = ti.a_row0 + kb * 64;
+                            const int m0 = ti.m * kTileM;
+                            tc::tma_load_2d_2sm(a_tile(stage), &tmA, lead_full, m0, krow);
+                            tc::tma_load_2d_2sm(a_tile(stage) + 8192, &tmA, lead_full, m0 + 64, krow);
+#pragma unroll
+                            for (int j = 0; j < BN / 128; ++j)
+                                tc::tma_load_2d_2sm(b_tile(stage) + 8192 * j, &tmB, lead_full,
+                                                    ti.n * BN + rank * (BN / 2) + 64 * j, krow);
+                            last_par[stage] = (int)ph;
+                            if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                            continue;
+                        }
                         // K-major weight gradients: K is the expert's token range, A rows
                         // this CTA's 128 weight rows, B rows the tile's N columns
                         const bool kw = p.kmajor_wgrad != 0;
@@ -521,7 +538,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         } else if constexpr (MX) {
                             tc::mma_mxf8(d, ad, bd, tc::idesc_mxf8(128, BN, kk, kk), sfa_t, sfb_t, accum);
                         } else if constexpr (CLN == 2) {
-                            tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(ti.m128 ? 128 : 256, BN, false, false), accum);
+                            tc::mma_bf16_2sm(d, ad, bd, tc::idesc_bf16(ti.m128 ? 128 : 256, BN, MN_MAJOR, MN_MAJOR),
+                                             accum);
                         } else {
                             tc::mma_bf16(d, ad, bd, tc::idesc_bf16(ti.half ? 64 : 128, BN, MN_MAJOR, MN_MAJOR), accum);
                         }
