@@ -50,13 +50,13 @@ def candidates(p: mok.Problem, batches: int = 1, ring_rows: int = 0, num_sms: in
     """Candidate configurations for one layer shape. With several macro-batches
     the stage kernels run batch by batch and the megakernel streams all of
     them through one ring of `ring_rows` rows (0: the library's default)."""
+    # the stage kernels' default: BF16 token tiles as 2-SM pairs, MXFP8 on single CTAs
     out = [Candidate("staged")]
     if p.dtype == mok.BF16:
-        out += [Candidate("staged, swapped-operand pair tiles", mok.FLAG_SWAPPED_TILES),
+        out += [Candidate("staged, 128-row token tiles on single CTAs", mok.FLAG_ROW_TILES),
+                Candidate("staged, swapped-operand pair tiles", mok.FLAG_SWAPPED_TILES),
                 Candidate("staged, swapped-operand pair tiles, balanced token tiles",
-                          mok.FLAG_SWAPPED_TILES | mok.FLAG_TOKEN_TILES_BALANCED),
-                Candidate("staged, 128-row token tiles", mok.FLAG_ROW_TILES),
-                Candidate("staged, 128-row token tiles as 2-SM pairs", mok.FLAG_GEMM_PAIRS)]
+                          mok.FLAG_SWAPPED_TILES | mok.FLAG_TOKEN_TILES_BALANCED)]
     elif p.dtype == mok.MXFP8:
         out += [Candidate("staged, 2-SM pairs", mok.FLAG_GEMM_PAIRS)]
     if megakernel_supported(p) and p.T > 0:
