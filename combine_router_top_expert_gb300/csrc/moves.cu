@@ -508,18 +508,22 @@ __global__ void dl_scatter_kernel(const float* __restrict__ dl, const int32_t* _
 // 32 token ranges keep about six CTAs per SM busy at T = 4096 (the work is
 // a few hundred dependent FMAs per loaded x value, so it needs warps).
 constexpr int kDwrSplits = 32;
+// Thread: two adjacent h (H is even), 32 experts at a time, the split's
+// tokens in ascending order (each (h, e) partial is one fp32 chain over its
+// token range); four tokens' x pairs are loaded before their products.
 __global__ void __launch_bounds__(256)
 dwr_partial_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ dl_full, int T, int H, int E,
                    float* __restrict__ part) {
     __shared__ float dls[64][32];
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    const int h = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
     const int split = blockIdx.y;
     const int per = ceil_div(T, kDwrSplits);
     const int ts = split * per, te = min(T, ts + per);
+    const bool live = h < H;
     for (int eg = 0; eg < E; eg += 32) {
-        float acc[32];
+        float a0[32], a1[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+        for (int e = 0; e < 32; ++e) a0[e] = a1[e] = 0.f;
         for (int t0 = ts; t0 < te; t0 += 64) {
             const int nt = min(64, te - t0);
             __syncthreads();
@@ -528,25 +532,56 @@ dwr_partial_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict_
                 dls[tt][i % 32] = (tt < nt && e < E) ? dl_full[(int64_t)(t0 + tt) * E + e] : 0.f;
             }
             __syncthreads();
-            if (h < H)
-                for (int tt = 0; tt < nt; ++tt) {
-                    const float xv = __bfloat162float(x[(int64_t)(t0 + tt) * H + h]);
+            if (!live) continue;
+            const __nv_bfloat162* xp = reinterpret_cast<const __nv_bfloat162*>(x + (int64_t)t0 * H + h);
+            const int hs = H / 2;   // row stride in pairs
+            int tt = 0;
+            for (; tt + 4 <= nt; tt += 4) {
+                __nv_bfloat162 xv[4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] = fmaf(xv, dls[tt][e], acc[e]);
+                for (int u = 0; u < 4; ++u) xv[u] = xp[(int64_t)(tt + u) * hs];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float x0 = __low2float(xv[u]), x1 = __high2float(xv[u]);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const float d = dls[tt + u][e];
+                        a0[e] = fmaf(x0, d, a0[e]);
+                        a1[e] = fmaf(x1, d, a1[e]);
+                    }
                 }
+            }
+            for (; tt < nt; ++tt) {
+                const __nv_bfloat162 xv = xp[(int64_t)tt * hs];
+                const float x0 = __low2float(xv), x1 = __high2float(xv);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float d = dls[tt][e];
+                    a0[e] = fmaf(x0, d, a0[e]);
+                    a1[e] = fmaf(x1, d, a1[e]);
+                }
+            }
         }
-        if (h < H)
-            for (int e = 0; e < 32 && eg + e < E; ++e) part[((int64_t)split * H + h) * E + eg + e] = acc[e];
+        // partials [split][e][h]: a warp's stores of one expert cover 256
+        // contiguous bytes
+        if (live) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (eg + e < E)
+                    *reinterpret_cast<float2*>(part + ((int64_t)split * E + eg + e) * H + h) = make_float2(a0[e], a1[e]);
+        }
     }
 }
 
-// dW_r[h, e] = sum over splits in ascending order.
+// dW_r[h, e] = sum over splits in ascending order (thread i: e = i / H,
+// h = i % H, so the partials are read in contiguous runs of h).
 __global__ void dwr_reduce_kernel(const float* __restrict__ part, int H, int E, float* __restrict__ dWr) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)H * E) return;
+    const int e = (int)(i / H), h = (int)(i % H);
     float s = 0.f;
-    for (int sp = 0; sp < kDwrSplits; ++sp) s += part[(int64_t)sp * H * E + i];
-    dWr[i] = s;
+    for (int sp = 0; sp < kDwrSplits; ++sp) s += part[((int64_t)sp * E + e) * H + h];
+    dWr[(int64_t)h * E + e] = s;
 }
 
 // ---------------------------------------------------------------------------
@@ -766,7 +801,7 @@ cudaError_t launch_bwd_small(const void* dY, const void* partials, const float* 
         dl_scatter_kernel<<<ceil_div(T, 128), 128, 0, s>>>(dl, idx, T, E, k, dl_full);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        dwr_partial_kernel<<<dim3(ceil_div(H, 256), kDwrSplits), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+        dwr_partial_kernel<<<dim3(ceil_div(H, 512), kDwrSplits), 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
                                                                                dl_full, T, H, E, part);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
