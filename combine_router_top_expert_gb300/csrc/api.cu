@@ -454,14 +454,15 @@ static mok_status forward_mega(const mok_problem* p, int32_t nbatch, const mok_f
         PackedLayout SL = packed_layout(1, p->H, p->I_shared, MOK_BF16);
         const char* sp = static_cast<const char*>(a[0].packed_shared);
         void* hs = ws + ML.hs;
+        const GemmCommon cs = make_common(ws, cfg, MOK_BF16);   // the shared expert is BF16 in every mode
         for (int b = 0; b < nbatch && e == cudaSuccess; ++b) {
             float* sh = reinterpret_cast<float*>(ws + ML.shared + (size_t)b * align_up((int64_t)p->T * p->H * 4, 1024));
             shared[b] = sh;
             e = gemm_gateup(false, a[b].x, nullptr, sp + SL.gu, nullptr, 1, p->H, p->I_shared, nullptr, p->T, p->T, hs,
-                            nullptr, nullptr, c, s);
+                            nullptr, nullptr, cs, s);
             if (e == cudaSuccess)
                 e = gemm_down(false, hs, nullptr, sp + SL.dn, nullptr, 1, p->H, p->I_shared, nullptr, nullptr,
-                              nullptr, p->T, p->T, sh, c, s);
+                              nullptr, p->T, p->T, sh, cs, s);
         }
         if (e != cudaSuccess) return cuda_status(e);
     }
@@ -582,11 +583,12 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
         const char* sp = static_cast<const char*>(a->packed_shared);
         shared = reinterpret_cast<float*>(ws + L.shared);
         void* hs = ws + L.hs;
+        const GemmCommon cs = make_common(ws, cfg, MOK_BF16);   // the shared expert is BF16 in every mode
         e = gemm_gateup(false, a->x, nullptr, sp + SL.gu, nullptr, 1, p->H, p->I_shared, nullptr, p->T, p->T, hs,
-                        nullptr, nullptr, c, s);
+                        nullptr, nullptr, cs, s);
         if (e == cudaSuccess)
             e = gemm_down(false, hs, nullptr, sp + SL.dn, nullptr, 1, p->H, p->I_shared, nullptr, nullptr, nullptr,
-                          p->T, p->T, shared, c, s);
+                          p->T, p->T, shared, cs, s);
     }
     if (e == cudaSuccess) e = launch_combine(partials, r.topk_w, shared, a->out, p->T, p->H, p->k, s);
     return cuda_status(e);

@@ -230,7 +230,7 @@ cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void*
     p.sf_kchunks = H / 128;
     p.n_tiles = 2 * I / BN;
     // 2-SM pairs (256-wide, grouped rows): each CTA loads half of B
-    const bool cl = c.cluster == 2 && BN == 256 && identity_rows == 0;
+    const bool cl = c.cluster == 2 && BN == 256 && (identity_rows == 0 || !mx);
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, A, a_rows, H, eb, bk, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, Bgu, (int64_t)p.E * 2 * I, H, eb, bk, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;
@@ -286,7 +286,7 @@ cudaError_t gemm_down(bool mx, const void* h, const uint8_t* h_sf, const void* B
     // BF16: 256 or 128
     const int BN = down_tile_n(H, mx);
     p.n_tiles = H / BN;
-    const bool cl = c.cluster == 2 && !mx && BN == 256 && identity_rows == 0;
+    const bool cl = c.cluster == 2 && !mx && BN == 256;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, h, a_rows, I, eb, bk, 128)) return cudaErrorInvalidValue;
     if (!make_tmap(&tb, Bdn, (int64_t)p.E * H, I, eb, bk, cl ? BN / 2 : BN)) return cudaErrorInvalidValue;

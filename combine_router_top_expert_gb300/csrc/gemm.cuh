@@ -239,7 +239,7 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const GemmParams& p, const 
         if (s.toff[mid] <= g) lo = mid; else hi = mid - 1;
     }
     const int e = lo;
-    const int cnt = p.counts[e];
+    const int cnt = p.identity_rows > 0 ? p.identity_rows : p.counts[e];
     if (p.m_fixed > 0) {
         // weight gradients: M = the fixed weight rows (a multiple of 256), in
         // pairs of 128-row tiles; K = the expert's padded token segment
