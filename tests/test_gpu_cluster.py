@@ -64,15 +64,17 @@ def test_cluster_pairs_backward_bitwise():
 
 @pytest.mark.gpu
 def test_last_tiles_of_at_most_64_rows():
-    """Experts whose last 128-row tile holds 64, 65, 1, 127, 64 and 1 rows
+    """Experts of 64, 65, 1, 127, 192, 129, 0, 320, 385 and 640 rows
     (hand-made routing, k = 1): the single-CTA kernels run an M=64 MMA for
-    last tiles of at most 64 rows; the output equals the oracle and is
-    bit-identical to the 2-SM pair kernels, which run M=256 MMAs only."""
+    last tiles of at most 64 rows; the 2-SM pair kernels run an expert's odd
+    last tile (one tile of 1-128 rows, or the third or fifth of 320 and 640
+    rows) as an M=128 pair and an even count's short last tile (385 rows)
+    inside an M=256 pair. Both equal the oracle and each other bit for bit."""
     import numpy as np
     import oracle
     from helpers import TOL, assert_close, host_bf16_f64
 
-    counts = [64, 65, 1, 127, 192, 129]
+    counts = [64, 65, 1, 127, 192, 129, 0, 320, 385, 640]
     E, T = len(counts), sum(counts)
     wl = synth.small("m64_tiles", T=T, H=512, I=256, E=E, k=1)
     inp = synth.make_inputs(wl, seed=5)
