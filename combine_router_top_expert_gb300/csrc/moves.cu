@@ -172,8 +172,9 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
             return poff[e] + slot_row[sl] - offsets[e];
         };
         const int my_pr = (k <= 32 && lane < k) ? dest(lane) : 0;
-        // lane L quantises blocks L, L + 32, ...; the next round's four
-        // 16-byte loads are issued before this round is quantised and stored
+        // lane L quantises blocks bw + L, bw + L + 32W, ...; the next
+        // iteration's four 16-byte loads are issued before this one's blocks
+        // are quantised and stored
         const uint4* xs = reinterpret_cast<const uint4*>(x + t * H);
         const int step = 32 * W;
         uint4 nv[4];
