@@ -331,8 +331,10 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
             layer.backward(x, dY, cfg=cfg, stream=stream)
             if ev is not None:
                 ev[1].record(stream)
-        # route 3, training forward 4 (dispatch, 2 GEMMs, combine), backward 12
-        launches_per_step = 3 + 4 + 12
+        # route 3; BF16: training forward 4 (dispatch, 2 GEMMs, combine), backward
+        # 12; MXFP8: forward 6 (BF16 rows, E4M3 rows, pad zeroing, 2 GEMMs,
+        # combine), backward 16 (5 quantisation passes into 3, 4 GEMMs as in BF16)
+        launches_per_step = 3 + (6 + 16 if dtype == mok.MXFP8 else 4 + 12)
         status_ws = b["ws"]
         flops = 18.0 * H * wl.I * T * wl.k
         kern = ("layer GEMMs fwd+bwd (staged; 2 fwd + 4 bwd grouped GEMM launches" +

@@ -556,14 +556,21 @@ mok_status mok_moe_forward(const mok_problem* p, const mok_fwd_args* a, const mo
         if (mx && !training)
             e = launch_dispatch_tokens(a->x, p->T, p->H, p->E, p->k, r.topk_idx, r.slot_row, r.counts, r.offsets, A,
                                        A_sf, s);
-        else if (mx)   // MXFP8 training: BF16 rows saved for the weight gradients, quantised for the GEMM
+        else if (mx) {
+            // MXFP8 training: the BF16 rows saved for the weight gradients (pads
+            // zero), and the E4M3 rows for the GEMM quantised once per token from
+            // x, their pads zeroed so the saved G|U and h of pad rows stay zero
             e = launch_dispatch(false, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, sv + L.sA,
                                 nullptr, nullptr, nullptr, s, true);
-        else
+            if (e == cudaSuccess)
+                e = launch_dispatch_tokens(a->x, p->T, p->H, p->E, p->k, r.topk_idx, r.slot_row, r.counts,
+                                           r.offsets, A, A_sf, s);
+            if (e == cudaSuccess) e = launch_zero_pad_rows_q(r.counts, rows, p->E, p->H, A, A_sf, s);
+        } else {
             e = launch_dispatch(mx, a->x, p->T, p->H, p->E, p->k, r.counts, r.offsets, r.row_src, A, A_sf, nullptr,
                                 nullptr, s, training);
+        }
     }
-    if (e == cudaSuccess && mx && training) e = launch_quantize_rows_tiled(sv + L.sA, rows_tiles(p), p->H, A, A_sf, s);
     if (e == cudaSuccess && use_swap(p, cfg, training)) {
         e = gemm_gateup_swap(A, pk + PL.gu, p->E, p->H, p->I, r.counts, rows, h, swap_policy(cfg), c, s);
         if (e == cudaSuccess)

@@ -216,6 +216,29 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
     }
 }
 
+// Pad rows of an MXFP8 expert-contiguous buffer (rows past each expert's
+// count up to its 128-row boundary): zero E4M3 codes and the scale code of an
+// all-zero block (0), the bytes a quantiser writes for zero rows. One warp
+// per padded row; routed rows are left alone.
+__global__ void __launch_bounds__(256)
+zero_pad_rows_q_kernel(const int32_t* __restrict__ counts, int E, int H, uint8_t* __restrict__ A,
+                       uint8_t* __restrict__ A_sf) {
+    __shared__ int32_t poff[kMaxE + 1];
+    padded_offsets(counts, E, poff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = poff[E];
+    const int kc_row = H / 128;
+    for (int pr = blockIdx.x * 8 + warp; pr < total; pr += gridDim.x * 8) {
+        const int e = find_expert(poff, E, pr);
+        if (pr - poff[e] < counts[e]) continue;
+        uint4* dst = reinterpret_cast<uint4*>(A + (int64_t)pr * H);
+        for (int c = lane; c < H / 16; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+        for (int q = lane; q < kc_row; q += 32)
+            *reinterpret_cast<uint32_t*>(A_sf + ((int64_t)(pr / kTileM) * kc_row + q) * 512 +
+                                         sf_chunk_offset(pr % kTileM, 0)) = 0u;
+    }
+}
+
 template <bool MX>
 __global__ void __launch_bounds__(256)
 dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const int32_t* __restrict__ counts,
@@ -623,6 +646,13 @@ cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, co
     const int blocks = (int)std::min<int64_t>(ceil_div((int64_t)T * W, 8), (int64_t)sm_count() * 8);
     dispatch_tokens_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H, E, k, W, topk_idx,
                                                   slot_row, counts, offsets, static_cast<uint8_t*>(A), A_sf);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows_q(const int32_t* counts, int64_t rows, int E, int H, void* A, uint8_t* A_sf,
+                                  cudaStream_t s) {
+    const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8));
+    zero_pad_rows_q_kernel<<<blocks, 256, 0, s>>>(counts, E, H, static_cast<uint8_t*>(A), A_sf);
     return cudaGetLastError();
 }
 

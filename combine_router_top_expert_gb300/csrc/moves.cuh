@@ -105,6 +105,10 @@ cudaError_t gemm_down_swap(const void* h, const void* Bdn, int E, int H, int I, 
 // MXFP8 quantisation of each row of x [T, H] (the codes the dispatch writes):
 // x_q [T, H] E4M3, x_sf [T, H/32] E8M0 bytes.
 cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x_sf, cudaStream_t s);
+// Zero the pad rows of an MXFP8 expert-contiguous buffer of at most `rows`
+// padded rows (codes 0, scale code 0), leaving the routed rows alone.
+cudaError_t launch_zero_pad_rows_q(const int32_t* counts, int64_t rows, int E, int H, void* A, uint8_t* A_sf,
+                                  cudaStream_t s);
 // MXFP8 pull-dispatch in one token-major pass (each token quantised once,
 // its k rows written from registers); pad rows are not written.
 cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, const int32_t* topk_idx,
