@@ -62,11 +62,12 @@ struct GemmCommon {
     int num_sms;
     int l2_prefetch;   // K blocks ahead at which the GEMM producers prefetch weight boxes into L2 (0: off)
     int cluster;   // 2: grouped GEMMs run as 2-SM CTA pairs (tcgen05 cta_group::2, B rows split
-                   // between the two CTAs, no multicast loads); 1: single CTAs
+                   // between the two CTAs, no multicast loads; the BF16 default); 1: single CTAs
 };
 // Forward gate/up GEMM + SwiGLU. A: [rows, H] (bf16 or E4M3 + tile scales);
 // packed B: [E * 2I, H] (interleaved gate/up per il = BN/2 columns).
-// identity_rows > 0: A is a plain [identity_rows, H] matrix (shared expert).
+// identity_rows > 0: A is a plain [identity_rows, H] matrix (shared expert;
+// BF16 pairs then take ceil(identity_rows / 128) row tiles as for one expert).
 cudaError_t gemm_gateup(bool mx, const void* A, const uint8_t* A_sf, const void* Bgu, const uint8_t* Bgu_sf,
                         int E, int H, int I, const int32_t* counts, int identity_rows, int64_t a_rows,
                         void* h, uint8_t* h_sf, void* gu_save, const GemmCommon& c, cudaStream_t s,
