@@ -585,7 +585,7 @@ def roofline(m, args):
     wl, dtype = m["wl"], m["dtype"]
     peaks = load_peaks()
     H = wl.H
-    # captured traffic belongs to the single-CTA stage kernels only
+    # captured traffic belongs to the default stage kernels (BF16: 2-SM pairs) only
     traffic, traffic_note = (captured_traffic(wl.name) if (m["staged"] and m["batches"] == 1 and not args.gemm_pairs
                                                            and not args.swapped_tiles and not args.single_cta)
                              else (None, "not captured for this path"))
