@@ -100,3 +100,39 @@ def test_last_tiles_of_at_most_64_rows():
     r = {"idx": idx, "w": np.ones((T, 1)), "offsets": offsets, "row_src": order}
     ref = oracle.moe_forward(inp.x, inp.Wg, inp.Wu, inp.Wd, r, mode=oracle.MODE_BF16)
     assert_close(host_bf16_f64(outs[0]), ref, TOL[mok.BF16], "M=64 last tiles")
+
+
+SWEEP = [
+    synth.small("sw_e16_t333", T=333, H=256, I=256, E=16, k=2),
+    synth.small("sw_e64_t1000", T=1000, H=512, I=128, E=64, k=4, zipf_s=1.2),
+    synth.small("sw_e4_t100", T=100, H=768, I=384, E=4, k=1),
+    synth.small("sw_e8_t777", T=777, H=512, I=512, E=8, k=3, zipf_s=0.8, shared_I=384),
+    synth.small("sw_e32_t2000", T=2000, H=256, I=256, E=32, k=8),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", SWEEP, ids=[w.name for w in SWEEP])
+def test_pairs_bitwise_sweep(wl):
+    """BF16 layers of assorted shapes and routings (uniform and Zipf, k from
+    1 to 8, 4 to 64 experts, with and without a shared expert): the default
+    2-SM pairs (odd last tiles as M=128 pairs) against single CTAs, forward
+    bit for bit, and the training step's gradients bit for bit."""
+    inp = synth.make_inputs(wl)
+    layer = layer_for(inp, mok.BF16)
+    x = to_dev_bf16(inp.x)
+    layer.route(x)
+    outs = [_staged(layer, x, wl.T, f).clone() for f in (0, mok.FLAG_ROW_TILES)]
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    if wl.shared_I:
+        return   # no backward for the shared expert
+    dY = torch.randn((wl.T, wl.H), device="cuda").to(torch.bfloat16)
+    res = []
+    for flags in (0, mok.FLAG_ROW_TILES):
+        cfg = mok.make_config(flags=flags)
+        layer.forward(x, training=True, cfg=cfg)
+        g = layer.backward(x, dY, cfg=cfg)
+        torch.cuda.synchronize()
+        res.append({n: t.clone() for n, t in g.items()})
+    for n in res[0]:
+        assert torch.equal(res[0][n].view(torch.uint8), res[1][n].view(torch.uint8)), n
