@@ -77,6 +77,28 @@ bool make_tmap_out3d(CUtensorMap* m, void* base, int E, int64_t rows, int64_t wi
     return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+// 2-D row-major [rows, cols] tensor read in unswizzled boxes of box_cols x
+// box_rows (box_cols * elem_bytes a multiple of 16); rows and columns out of
+// range read 0.
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
+                    int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(cols * elem_bytes)};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 // Clusters of two CTAs that can be resident at once for kernel `kern` with
 // launch configuration `cfg` (dynamic shared memory and block size fixed per
 // kernel), queried once per device and kernel: the occupancy query is a

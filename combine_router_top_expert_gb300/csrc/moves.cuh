@@ -5,6 +5,11 @@
 
 namespace mok {
 
+// gemm.cu: tensor map of a row-major [rows, cols] tensor read in
+// unswizzled boxes of box_cols x box_rows (out-of-range elements read 0)
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int elem_bytes, int box_cols,
+                    int box_rows);
+
 // route.cu
 size_t route_workspace_bytes(int T, int H, int E, int k);
 cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bias, int T, int H, int E, int k,

@@ -20,16 +20,17 @@ namespace mok {
 constexpr int kRouteTTMax = 32;    // tokens per CTA, at most
 constexpr int kRouteTTMin = 4;     // tokens per CTA, at least (sizes the histogram)
 constexpr int kRouteThreads = 256; // layout kernel
-constexpr int kTopkThreads = 512;  // top-k kernel: 8 expert quads x 2 token groups
-constexpr int kRouteChunk = 256;   // h values per pipeline chunk (32 lanes x 8)
+constexpr int kTopkThreads = 512;  // top-k kernel: 16 warps, two summation chains each
+constexpr int kRouteChunk = 256;   // h values per pipeline chunk (32 chains x 8)
+constexpr int kRouteRow = kRouteChunk + 4;   // padded shared-memory row (weights and fp32 x), in floats
 constexpr uint64_t kRouteTimeoutNs = 4000000000ull;   // bound on every wait of the top-k kernel
 
 // Router weights in the order the top-k kernel streams them: per 256-wide h
-// chunk c and 32-expert group g one contiguous 32 KB block [32 experts][256],
-// zero-padded past H and E, and inside each 256-wide row h = 8L + 4j + i
-// stored at j*128 + 4L + i (so lane L reads its 8 values as two conflict-free
-// 16-byte words). One bulk copy then moves a whole chunk into shared memory.
-__host__ __device__ inline int64_t router_chunk_floats() { return 32 * (int64_t)kRouteChunk; }
+// chunk c and 32-expert group g one contiguous block [32 experts][kRouteRow]
+// (h in natural order, zero past H and E, four pad floats per row so that
+// rows of consecutive experts start four banks apart). One bulk copy then
+// moves a whole chunk into shared memory.
+__host__ __device__ inline int64_t router_chunk_floats() { return 32 * (int64_t)kRouteRow; }
 __host__ __device__ inline int64_t router_copy_floats(int E, int H) {
     return (int64_t)ceil_div(H, kRouteChunk) * ceil_div(E, 32) * router_chunk_floats();
 }
@@ -42,8 +43,6 @@ int route_wr_copies(int E, int H) {
     int64_t r = one > 0 ? ((int64_t)4 << 20) / one : 1;
     return (int)(r < 1 ? 1 : r > 16 ? 16 : r);
 }
-
-__device__ __forceinline__ int router_h_pos(int hl) { return ((hl >> 2) & 1) * 128 + (hl >> 3) * 4 + (hl & 3); }
 
 // W_r [H, E] -> the chunk layout above, copy blockIdx.z. Grid: (8 * chunks,
 // expert groups, copies), block (32, 8).
@@ -58,10 +57,12 @@ __global__ void router_weight_layout_kernel(const float* __restrict__ W_r, float
         tile[i][threadIdx.x] = (h < H && e < E) ? W_r[(int64_t)h * E + e] : 0.f;
     }
     __syncthreads();
+    const int c = h0 / kRouteChunk, hl0 = h0 % kRouteChunk;
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-        const int h = h0 + threadIdx.x;   // expert e0 + i: row i of group blockIdx.y
-        const int c = h / kRouteChunk, hl = h % kRouteChunk;
-        dst[(((int64_t)c * EG + blockIdx.y) * 32 + i) * kRouteChunk + router_h_pos(hl)] = tile[threadIdx.x][i];
+        // expert e0 + i: row i of group blockIdx.y
+        float* row = dst + ((int64_t)c * EG + blockIdx.y) * router_chunk_floats() + (int64_t)i * kRouteRow;
+        row[hl0 + threadIdx.x] = tile[threadIdx.x][i];
+        if (hl0 + 32 == kRouteChunk && threadIdx.x < kRouteRow - kRouteChunk) row[kRouteChunk + threadIdx.x] = 0.f;
     }
 }
 
@@ -88,40 +89,54 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
 }
 
 
-// One CTA = TT = 2*TW tokens x all experts, 16 warps. Warp w owns experts
-// 4*(w%8) .. +3 of each 32-expert group and tokens TW*(w/8) .. +TW-1; lane
-// L owns summation chain L (h = 256*i + 8*L + m). The chunks (c, g) of the
-// router weights (one 32 KB bulk copy each, from the layout above) and the
-// matching raw x rows (one bulk copy per token) stream through a STAGES-deep
-// shared-memory ring, one mbarrier per slot; thread 0 issues the copies. x
-// is converted to fp32 once per CTA, one chunk ahead, into a double buffer,
-// so the inner loop is fused multiply-adds fed by conflict-free 16-byte
-// shared loads. Every wait is bounded: after a timeout the status block
-// records it, no thread waits again, and the CTA runs to its end (its
-// results are then garbage; the caller sees MOK_ERR_TIMEOUT).
+// One CTA = TT tokens x all experts, 16 warps. Warp w owns summation chains
+// w and w + 16 (chain L: h = 256*i + 8*L + m), for every token and expert of
+// the CTA; each lane is one (token slot tl < 4, expert slot el < 8), and a
+// thread accumulates tokens tl + 4u (u < TT/4) x experts el + 8v (v < 4) of
+// the current 32-expert group on both of its warp's chains. Each 16-byte
+// shared load (four h of one chain) thus feeds 4 or TT/4 tokens' worth of
+// FMAs, and the lanes of a warp read only 4 (x) or 8 (weights) distinct
+// rows, 16 B each, four banks apart. A 128-bit shared load costs as many
+// wavefronts as the most distinct addresses among any four aligned lanes,
+// and at least two (measured on this GPU), so lane bits 0 and 1 select one
+// bit of tl and one of el: every quad reads two x and two weight rows, and
+// both loads take the minimum of two wavefronts. The chunks
+// (c, g) of the router weights (one bulk copy each, from the layout above)
+// and the matching [TT tokens x 256 h] box of raw x (one tensor copy; tokens
+// past T and h past H read 0) stream through a STAGES-deep shared-memory
+// ring, one mbarrier per slot; thread 0 issues the copies. x is converted to fp32 once per CTA, one chunk ahead, into a double
+// buffer. After a group's last chunk the 32 chains of every (token, expert)
+// are added in the butterfly's tree: chain w + 16 into chain w in registers,
+// then warp w + d into warp w for d = 8, 4, 2, 1 through shared memory (the
+// fp32 x buffer just consumed). Every wait is bounded: after a timeout the
+// status block records it, no thread waits again, and the CTA runs to its
+// end (its results are then garbage; the caller sees MOK_ERR_TIMEOUT).
 // Dynamic shared memory:
-//   bars [STAGES] u64 (128 B) | ws [STAGES][32][256] f32 | xr [STAGES][TT][256] bf16 |
-//   xf [2][TT][256] f32 | lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
-template <int TW, int STAGES>
-__global__ void __launch_bounds__(kTopkThreads)
-route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ Wr_copies, int wr_copies,
+//   bars [STAGES] u64 (128 B) | ws [STAGES][32][kRouteRow] f32 | xr [STAGES][TT][256] bf16 |
+//   xf [2][TT][kRouteRow] f32 | lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
+template <int TT, int STAGES>
+__global__ void __launch_bounds__(kTopkThreads, 1)
+route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restrict__ Wr_copies, int wr_copies,
                   const float* __restrict__ bias, int T, int H, int E, int k, int32_t* __restrict__ topk_idx,
                   float* __restrict__ topk_w, int32_t* __restrict__ hist, StatusBlock* st, uint64_t tmo,
                   int withhold) {
-    constexpr int TT = 2 * TW;
+    constexpr int TU = TT / 4;   // token slots per thread
     constexpr int NT = kTopkThreads;
-    static_assert(TT <= kRouteTTMax && TT >= kRouteTTMin && STAGES >= 3 && STAGES <= 16, "router tile");
+    static_assert(TT % 4 == 0 && TT <= kRouteTTMax && TT >= kRouteTTMin && STAGES >= 3 && STAGES <= 16,
+                  "router tile");
+    static_assert(8 * 32 <= kRouteRow, "the chain sums of 8 warps fit one fp32 x buffer");
     extern __shared__ __align__(128) unsigned char route_smem[];
     const uint32_t bar0 = tc::smem_u32(route_smem);
     float* ws = reinterpret_cast<float*>(route_smem + 128);
-    __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(ws + STAGES * 32 * kRouteChunk);
+    __nv_bfloat16* xr = reinterpret_cast<__nv_bfloat16*>(ws + STAGES * router_chunk_floats());
     float* xf = reinterpret_cast<float*>(xr + STAGES * TT * kRouteChunk);
-    float* lg = xf + 2 * TT * kRouteChunk;
+    float* lg = xf + 2 * TT * kRouteRow;
     float* slog = lg + TT * E;
     int32_t* cnt = reinterpret_cast<int32_t*>(slog + TT * k);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 7, tg = warp >> 3;
+    // lane bits b4..b0: tl = b0 + 2*b2, el = b1 + 2*b3 + 4*b4
+    const int tl = (lane & 1) | ((lane >> 1) & 2), el = ((lane >> 1) & 1) | ((lane >> 2) & 6);
     const int t0 = blockIdx.x * TT;
     const int ntok = min(TT, T - t0);
     const int nchunks = ceil_div(H, kRouteChunk);
@@ -131,6 +146,7 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 
     for (int e = tid; e < E; e += NT) cnt[e] = 0;
     if (tid == 0) {
+        tc::prefetch_tmap(&tmx);
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(bar0 + 8u * s, 1);
         tc::fence_mbar_init();
     }
@@ -147,14 +163,11 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         issued = n + 1;
         if (hold && n == 1) return;
         const int g = n / nchunks, c = n % nchunks, slot = n % STAGES;
-        const int h0 = c * kRouteChunk, hw = min(kRouteChunk, H - h0);
         const uint32_t bar = bar0 + 8u * slot;
-        tc::mbar_expect_tx(bar, (uint32_t)(router_chunk_floats() * 4 + (int64_t)ntok * hw * 2));
-        tc::bulk_load(tc::smem_u32(ws + slot * 32 * kRouteChunk),
+        tc::mbar_expect_tx(bar, (uint32_t)(router_chunk_floats() * 4 + TT * kRouteChunk * 2));
+        tc::bulk_load(tc::smem_u32(ws + slot * router_chunk_floats()),
                       Wr + ((int64_t)c * EG + g) * router_chunk_floats(), (uint32_t)(router_chunk_floats() * 4), bar);
-        const uint32_t xd = tc::smem_u32(xr + slot * TT * kRouteChunk);
-        for (int t = 0; t < ntok; ++t)
-            tc::bulk_load(xd + t * kRouteChunk * 2, x + (int64_t)(t0 + t) * H + h0, (uint32_t)hw * 2, bar);
+        tc::tma_load_2d(tc::smem_u32(xr + slot * TT * kRouteChunk), &tmx, bar, c * kRouteChunk, t0);
     };
     auto wait = [&](int n) {
         if (ok && n < total) {
@@ -162,15 +175,15 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
             if (ok) seen = n + 1;
         }
     };
-    // raw x of slot b -> fp32 buffer d (the h order above)
+    // raw x of slot b -> fp32 buffer d (natural h order, padded rows)
     auto convert_x = [&](int b, int d) {
         const __nv_bfloat16* xb = xr + b * TT * kRouteChunk;
         for (int v = tid; v < TT * (kRouteChunk / 8); v += NT) {
             const int t = v / (kRouteChunk / 8), L = v % (kRouteChunk / 8);
             const uint4 r = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * L);
-            float* o = xf + (d * TT + t) * kRouteChunk + 4 * L;
+            float* o = xf + (d * TT + t) * kRouteRow + 8 * L;
             *reinterpret_cast<float4*>(o) = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
-            *reinterpret_cast<float4*>(o + 128) = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
+            *reinterpret_cast<float4*>(o + 4) = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
         }
     };
 
@@ -178,7 +191,7 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         for (int n = 0; n < STAGES - 1; ++n) issue(n);
     wait(0);
     convert_x(0, 0);
-    float acc[TW][4];
+    float acc[2][TU][4];
     for (int n = 0; n < total; ++n) {
         wait(n + 1);       // its x is converted below
         __syncthreads();   // x(n) converted by every thread; chunk n - 1 consumed
@@ -187,60 +200,85 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
         const int g = n / nchunks, c = n % nchunks;
         if (c == 0) {
 #pragma unroll
-            for (int t = 0; t < TW; ++t)
+            for (int ci = 0; ci < 2; ++ci)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) acc[t][q] = 0.f;
+                for (int u = 0; u < TU; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) acc[ci][u][v] = 0.f;
         }
-        const float* wb = ws + (n % STAGES) * 32 * kRouteChunk;
-        const float* xb = xf + ((n & 1) * TT + tg * TW) * kRouteChunk;
-        if (c * kRouteChunk + 8 * lane < H) {
-            float wv[4][8];
+        const float* wb = ws + (n % STAGES) * router_chunk_floats() + el * kRouteRow;
+        const float* xb = xf + ((n & 1) * TT + tl) * kRouteRow;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float* wr = wb + (4 * quad + q) * kRouteChunk + 4 * lane;
-                const float4 a = *reinterpret_cast<const float4*>(wr);
-                const float4 b = *reinterpret_cast<const float4*>(wr + 128);
-                wv[q][0] = a.x; wv[q][1] = a.y; wv[q][2] = a.z; wv[q][3] = a.w;
-                wv[q][4] = b.x; wv[q][5] = b.y; wv[q][6] = b.z; wv[q][7] = b.w;
-            }
-            // two tokens at a time, h (m) outermost: each step issues 8
-            // independent FMAs, one per (token, expert) chain; every chain
-            // accumulates its h values in ascending order
+        for (int ci = 0; ci < 2; ++ci) {
+            const int hl = 8 * (warp + 16 * ci);   // chain warp + 16*ci: h = hl .. hl + 7 of the chunk
+            if (c * kRouteChunk + hl < H) {
 #pragma unroll
-            for (int t2 = 0; t2 < TW; t2 += 2) {
-                float xv[2][8];
+                for (int s4 = 0; s4 < 8; s4 += 4) {
+                    float4 wv[4], xv[TU];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (t2 + u < TW) {
-                        const float* xr2 = xb + (t2 + u) * kRouteChunk + 4 * lane;
-                        const float4 a = *reinterpret_cast<const float4*>(xr2);
-                        const float4 b = *reinterpret_cast<const float4*>(xr2 + 128);
-                        xv[u][0] = a.x; xv[u][1] = a.y; xv[u][2] = a.z; xv[u][3] = a.w;
-                        xv[u][4] = b.x; xv[u][5] = b.y; xv[u][6] = b.z; xv[u][7] = b.w;
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        wv[v] = *reinterpret_cast<const float4*>(wb + 8 * v * kRouteRow + hl + s4);
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+                        xv[u] = *reinterpret_cast<const float4*>(xb + 4 * u * kRouteRow + hl + s4);
+                    // every (token, expert) accumulator takes its four h in
+                    // ascending order; the TU x 4 accumulators are independent
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].x, wv[v].x, acc[ci][u][v]);
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].y, wv[v].y, acc[ci][u][v]);
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].z, wv[v].z, acc[ci][u][v]);
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].w, wv[v].w, acc[ci][u][v]);
                 }
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (t2 + u < TW) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) acc[t2 + u][q] = fmaf(xv[u][m], wv[q][m], acc[t2 + u][q]);
-                        }
             }
         }
         if (c == nchunks - 1) {
-            // butterfly across the 32 chains, then the bias
+            // the butterfly's tree over the 32 chains: chain L + 16 into chain
+            // L (this thread's two chains), then chains L + 8, + 4, + 2, + 1
+            // (warp w + d into warp w), then the bias. fp32 addition is
+            // commutative, so which operand comes first does not matter.
+            float p[TU][4];
 #pragma unroll
-            for (int t = 0; t < TW; ++t)
+            for (int u = 0; u < TU; ++u)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float s = acc[t][q];
+                for (int v = 0; v < 4; ++v) p[u][v] = acc[0][u][v] + acc[1][u][v];
+            float* red = xf + (n & 1) * TT * kRouteRow;   // free until chunk n + 2 is converted into it
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) s = s + __shfl_xor_sync(0xffffffffu, s, off);
-                    const int e = 32 * g + 4 * quad + q, tt = tg * TW + t;
-                    if (lane == 0 && e < E && tt < ntok) lg[tt * E + e] = bias ? s + bias[e] : s;
+            for (int d = 8; d >= 1; d >>= 1) {
+                __syncthreads();   // red's previous readers (chunk n's x, or the level before) are done
+                if (warp >= d && warp < 2 * d) {
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) red[((warp - d) * TT + tl + 4 * u) * 32 + el + 8 * v] = p[u][v];
                 }
+                __syncthreads();
+                if (warp < d) {
+#pragma unroll
+                    for (int u = 0; u < TU; ++u)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) p[u][v] = p[u][v] + red[(warp * TT + tl + 4 * u) * 32 + el + 8 * v];
+                }
+            }
+            if (warp == 0) {
+#pragma unroll
+                for (int u = 0; u < TU; ++u)
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const int e = 32 * g + el + 8 * v, tt = tl + 4 * u;
+                        if (e < E && tt < ntok) lg[tt * E + e] = bias ? p[u][v] + bias[e] : p[u][v];
+                    }
+            }
         }
     }
     if (tid == 0 && seen < issued) {
@@ -309,8 +347,8 @@ route_topk_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__
 }
 
 size_t route_topk_smem_bytes(int TT, int STAGES, int E, int k) {
-    return (size_t)128 + (size_t)STAGES * 32 * kRouteChunk * 4 + (size_t)STAGES * TT * kRouteChunk * 2 +
-           (size_t)2 * TT * kRouteChunk * 4 + (size_t)TT * E * 4 + (size_t)TT * k * 4 + (size_t)E * 4;
+    return (size_t)128 + (size_t)STAGES * router_chunk_floats() * 4 + (size_t)STAGES * TT * kRouteChunk * 2 +
+           (size_t)2 * TT * kRouteRow * 4 + (size_t)TT * E * 4 + (size_t)TT * k * 4 + (size_t)E * 4;
 }
 
 // Counts, offsets and the stable (expert, token) permutation. CTA b handles
@@ -404,48 +442,59 @@ cudaError_t launch_router_weight_layout(const float* W_r, float* dst, int H, int
     return cudaGetLastError();
 }
 
-// Launch the top-k kernel with 2*TW tokens per CTA and a STAGES-deep ring.
-template <int TW, int STAGES>
-cudaError_t launch_topk_variant(const __nv_bfloat16* x, const float* Wr, int wr_copies, const float* bias, int T,
+// Launch the top-k kernel with TT tokens per CTA and a STAGES-deep ring.
+template <int TT, int STAGES>
+cudaError_t launch_topk_variant(const CUtensorMap& tmx, const float* Wr, int wr_copies, const float* bias, int T,
                                 int H, int E, int k, int32_t* topk_idx, float* topk_w, int32_t* hist,
                                 StatusBlock* st, uint64_t timeout_ns, int withhold, cudaStream_t s) {
-    const size_t smem = route_topk_smem_bytes(2 * TW, STAGES, E, k);
+    const size_t smem = route_topk_smem_bytes(TT, STAGES, E, k);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    auto kern = route_topk_kernel<TW, STAGES>;
+    auto kern = route_topk_kernel<TT, STAGES>;
     if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
-    kern<<<ceil_div(T, 2 * TW), kTopkThreads, smem, s>>>(x, Wr, wr_copies, bias, T, H, E, k, topk_idx, topk_w, hist,
-                                                         st, timeout_ns, withhold);
+    kern<<<ceil_div(T, TT), kTopkThreads, smem, s>>>(tmx, Wr, wr_copies, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                     timeout_ns, withhold);
     return cudaGetLastError();
 }
 
-// Tokens per CTA (2*TW, TW in {2, 4, 9, 14}). One CTA per SM; a CTA's time
-// is about (fixed cost of streaming every weight chunk, worth ~5 tokens per
-// warp) + TW, so the kernel takes about rounds x (TW + 5), rounds = CTAs
-// over SMs. Pick the cheapest that fits shared memory, larger tiles on ties.
-constexpr int kRouteStages(int tw) { return tw == 14 ? 3 : 4; }
+// Tokens per CTA: TT in {28, 20, 12, 8, 4}. One CTA per SM; a CTA's time is
+// about (a fixed cost of streaming every weight chunk, worth about one token
+// slot per thread) + TT/4, so the kernel takes about rounds x (TT/4 + 1),
+// rounds = CTAs over SMs. Pick the cheapest that fits shared memory, larger
+// tiles on ties.
+constexpr int kRouteStages(int tt) { return tt >= 20 ? 3 : 4; }
 int route_tokens_per_cta(int T, int num_sms, int E, int k) {
-    const int tws[4] = {14, 9, 4, 2};
-    int best = 2;
+    const int tts[5] = {28, 20, 12, 8, 4};
+    int best = 4;
     int64_t best_cost = -1;
-    for (int tw : tws) {
-        if (route_topk_smem_bytes(2 * tw, kRouteStages(tw), E, k) > 227 * 1024) continue;
-        const int64_t rounds = ceil_div(ceil_div(T, 2 * tw), num_sms > 0 ? num_sms : 1);
-        const int64_t cost = rounds * (tw + 5);
-        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tw; }
+    for (int tt : tts) {
+        if (route_topk_smem_bytes(tt, kRouteStages(tt), E, k) > 227 * 1024) continue;
+        const int64_t rounds = ceil_div(ceil_div(T, tt), num_sms > 0 ? num_sms : 1);
+        const int64_t cost = rounds * (tt / 4 + 1);
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tt; }
     }
-    return 2 * best;
+    return best;
 }
 
 cudaError_t launch_route_topk(const __nv_bfloat16* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                               int tt, int32_t* topk_idx, float* topk_w, int32_t* hist, StatusBlock* st,
                               uint64_t tmo, int hold, cudaStream_t s) {
     const int r = route_wr_copies(E, H);
-    if (tt == 28) return launch_topk_variant<14, kRouteStages(14)>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist,
-                                                                   st, tmo, hold, s);
-    if (tt == 18) return launch_topk_variant<9, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
-    if (tt == 8) return launch_topk_variant<4, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
-    if (tt == 4) return launch_topk_variant<2, 4>(x, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st, tmo, hold, s);
-    return cudaErrorInvalidValue;
+    // x [T, H] BF16 in boxes of 256 h x tt tokens (H % 8 == 0: 16-byte row pitch)
+    CUtensorMap tmx;
+    if (!make_tmap_rows(&tmx, x, T, H, 2, kRouteChunk, tt)) return cudaErrorInvalidValue;
+    switch (tt) {
+    case 28: return launch_topk_variant<28, kRouteStages(28)>(tmx, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                              tmo, hold, s);
+    case 20: return launch_topk_variant<20, kRouteStages(20)>(tmx, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                              tmo, hold, s);
+    case 12: return launch_topk_variant<12, kRouteStages(12)>(tmx, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                              tmo, hold, s);
+    case 8: return launch_topk_variant<8, kRouteStages(8)>(tmx, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                           tmo, hold, s);
+    case 4: return launch_topk_variant<4, kRouteStages(4)>(tmx, Wr, r, bias, T, H, E, k, topk_idx, topk_w, hist, st,
+                                                           tmo, hold, s);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 namespace {
