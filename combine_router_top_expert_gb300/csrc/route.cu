@@ -27,9 +27,11 @@ constexpr uint64_t kRouteTimeoutNs = 4000000000ull;   // bound on every wait of 
 
 // Router weights in the order the top-k kernel streams them: per 256-wide h
 // chunk c and 32-expert group g one contiguous block [32 experts][kRouteRow]
-// (h in natural order, zero past H and E, four pad floats per row so that
-// rows of consecutive experts start four banks apart). One bulk copy then
-// moves a whole chunk into shared memory.
+// (zero past H and E, four pad floats per row so that rows of consecutive
+// experts start four banks apart). Inside a row, h and h + 128 are adjacent
+// (h < 128 at 2h, h + 128 at 2h + 1): summation chains L and L + 16 then
+// advance together in one packed fp32x2 FMA. One bulk copy moves a whole
+// chunk into shared memory.
 __host__ __device__ inline int64_t router_chunk_floats() { return 32 * (int64_t)kRouteRow; }
 __host__ __device__ inline int64_t router_copy_floats(int E, int H) {
     return (int64_t)ceil_div(H, kRouteChunk) * ceil_div(E, 32) * router_chunk_floats();
@@ -61,7 +63,8 @@ __global__ void router_weight_layout_kernel(const float* __restrict__ W_r, float
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
         // expert e0 + i: row i of group blockIdx.y
         float* row = dst + ((int64_t)c * EG + blockIdx.y) * router_chunk_floats() + (int64_t)i * kRouteRow;
-        row[hl0 + threadIdx.x] = tile[threadIdx.x][i];
+        const int hl = hl0 + threadIdx.x;
+        row[2 * (hl & 127) + (hl >> 7)] = tile[threadIdx.x][i];
         if (hl0 + 32 == kRouteChunk && threadIdx.x < kRouteRow - kRouteChunk) row[kRouteChunk + threadIdx.x] = 0.f;
     }
 }
@@ -93,10 +96,13 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
 // w and w + 16 (chain L: h = 256*i + 8*L + m), for every token and expert of
 // the CTA; each lane is one (token slot tl < 4, expert slot el < 8), and a
 // thread accumulates tokens tl + 4u (u < TT/4) x experts el + 8v (v < 4) of
-// the current 32-expert group on both of its warp's chains. Each 16-byte
-// shared load (four h of one chain) thus feeds 4 or TT/4 tokens' worth of
-// FMAs, and the lanes of a warp read only 4 (x) or 8 (weights) distinct
-// rows, 16 B each, four banks apart. A 128-bit shared load costs as many
+// the current 32-expert group on both of its warp's chains, as the two
+// halves of a float2 advanced by packed fp32x2 FMAs (h of chain w and
+// h + 128 of chain w + 16 sit side by side in shared memory; each half is
+// an ordinary fp32 FMA, so every chain keeps its order and its bits). Each
+// 16-byte shared load (two h of both chains) thus feeds 4 or TT/4 tokens'
+// worth of FMAs, and the lanes of a warp read only 4 (x) or 8 (weights)
+// distinct rows, 16 B each, four banks apart. A 128-bit shared load costs as many
 // wavefronts as the most distinct addresses among any four aligned lanes,
 // and at least two (measured on this GPU), so lane bits 0 and 1 select one
 // bit of tl and one of el: every quad reads two x and two weight rows, and
@@ -104,8 +110,9 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
 // (c, g) of the router weights (one bulk copy each, from the layout above)
 // and the matching [TT tokens x 256 h] box of raw x (one tensor copy; tokens
 // past T and h past H read 0) stream through a STAGES-deep shared-memory
-// ring, one mbarrier per slot; thread 0 issues the copies. x is converted to fp32 once per CTA, one chunk ahead, into a double
-// buffer. After a group's last chunk the 32 chains of every (token, expert)
+// ring, one mbarrier per slot; thread 0 issues the copies. x is converted
+// to fp32 (in the paired h order) once per CTA, one chunk ahead, into a
+// double buffer. After a group's last chunk the 32 chains of every (token, expert)
 // are added in the butterfly's tree: chain w + 16 into chain w in registers,
 // then warp w + d into warp w for d = 8, 4, 2, 1 through shared memory (the
 // fp32 x buffer just consumed). Every wait is bounded: after a timeout the
@@ -175,15 +182,16 @@ route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restri
             if (ok) seen = n + 1;
         }
     };
-    // raw x of slot b -> fp32 buffer d (natural h order, padded rows)
+    // raw x of slot b -> fp32 buffer d (h and h + 128 side by side, padded rows)
     auto convert_x = [&](int b, int d) {
         const __nv_bfloat16* xb = xr + b * TT * kRouteChunk;
-        for (int v = tid; v < TT * (kRouteChunk / 8); v += NT) {
-            const int t = v / (kRouteChunk / 8), L = v % (kRouteChunk / 8);
-            const uint4 r = *reinterpret_cast<const uint4*>(xb + t * kRouteChunk + 8 * L);
-            float* o = xf + (d * TT + t) * kRouteRow + 8 * L;
-            *reinterpret_cast<float4*>(o) = make_float4(bf16_lo(r.x), bf16_hi(r.x), bf16_lo(r.y), bf16_hi(r.y));
-            *reinterpret_cast<float4*>(o + 4) = make_float4(bf16_lo(r.z), bf16_hi(r.z), bf16_lo(r.w), bf16_hi(r.w));
+        for (int v = tid; v < TT * 32; v += NT) {
+            const int t = v >> 5, h0 = 4 * (v & 31);
+            const uint2 lo = *reinterpret_cast<const uint2*>(xb + t * kRouteChunk + h0);
+            const uint2 hi = *reinterpret_cast<const uint2*>(xb + t * kRouteChunk + h0 + 128);
+            float* o = xf + (d * TT + t) * kRouteRow + 2 * h0;
+            *reinterpret_cast<float4*>(o) = make_float4(bf16_lo(lo.x), bf16_lo(hi.x), bf16_hi(lo.x), bf16_hi(hi.x));
+            *reinterpret_cast<float4*>(o + 4) = make_float4(bf16_lo(lo.y), bf16_lo(hi.y), bf16_hi(lo.y), bf16_hi(hi.y));
         }
     };
 
@@ -191,7 +199,7 @@ route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restri
         for (int n = 0; n < STAGES - 1; ++n) issue(n);
     wait(0);
     convert_x(0, 0);
-    float acc[2][TU][4];
+    float2 acc[TU][4];   // .x: chain warp, .y: chain warp + 16
     for (int n = 0; n < total; ++n) {
         wait(n + 1);       // its x is converted below
         __syncthreads();   // x(n) converted by every thread; chunk n - 1 consumed
@@ -200,46 +208,40 @@ route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restri
         const int g = n / nchunks, c = n % nchunks;
         if (c == 0) {
 #pragma unroll
-            for (int ci = 0; ci < 2; ++ci)
+            for (int u = 0; u < TU; ++u)
 #pragma unroll
-                for (int u = 0; u < TU; ++u)
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) acc[ci][u][v] = 0.f;
+                for (int v = 0; v < 4; ++v) acc[u][v] = make_float2(0.f, 0.f);
         }
         const float* wb = ws + (n % STAGES) * router_chunk_floats() + el * kRouteRow;
         const float* xb = xf + ((n & 1) * TT + tl) * kRouteRow;
+        // chain warp: h = hl .. hl + 7 of the chunk; chain warp + 16: the same
+        // + 128. Past H both read zeros (a chain never holds -0, so adding
+        // 0 * 0 leaves it unchanged); a step whose first chain starts past H
+        // is skipped.
+        const int hl = 8 * warp;
+        if (c * kRouteChunk + hl < H) {
+#pragma unroll(TT >= 28 ? 1 : 2)   // 28 tokens: no spills with one step in flight
+            for (int s2 = 0; s2 < 8; s2 += 2) {
+                // h = hl + s2 and hl + s2 + 1 of both chains
+                float4 wv[4], xv[TU];
 #pragma unroll
-        for (int ci = 0; ci < 2; ++ci) {
-            const int hl = 8 * (warp + 16 * ci);   // chain warp + 16*ci: h = hl .. hl + 7 of the chunk
-            if (c * kRouteChunk + hl < H) {
+                for (int v = 0; v < 4; ++v)
+                    wv[v] = *reinterpret_cast<const float4*>(wb + 8 * v * kRouteRow + 2 * (hl + s2));
 #pragma unroll
-                for (int s4 = 0; s4 < 8; s4 += 4) {
-                    float4 wv[4], xv[TU];
+                for (int u = 0; u < TU; ++u)
+                    xv[u] = *reinterpret_cast<const float4*>(xb + 4 * u * kRouteRow + 2 * (hl + s2));
+                // every (token, expert, chain) accumulator takes its h in
+                // ascending order; the TU x 4 float2 accumulators are independent
+#pragma unroll
+                for (int u = 0; u < TU; ++u)
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
-                        wv[v] = *reinterpret_cast<const float4*>(wb + 8 * v * kRouteRow + hl + s4);
+                        acc[u][v] = __ffma2_rn(make_float2(xv[u].x, xv[u].y), make_float2(wv[v].x, wv[v].y), acc[u][v]);
 #pragma unroll
-                    for (int u = 0; u < TU; ++u)
-                        xv[u] = *reinterpret_cast<const float4*>(xb + 4 * u * kRouteRow + hl + s4);
-                    // every (token, expert) accumulator takes its four h in
-                    // ascending order; the TU x 4 accumulators are independent
+                for (int u = 0; u < TU; ++u)
 #pragma unroll
-                    for (int u = 0; u < TU; ++u)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].x, wv[v].x, acc[ci][u][v]);
-#pragma unroll
-                    for (int u = 0; u < TU; ++u)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].y, wv[v].y, acc[ci][u][v]);
-#pragma unroll
-                    for (int u = 0; u < TU; ++u)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].z, wv[v].z, acc[ci][u][v]);
-#pragma unroll
-                    for (int u = 0; u < TU; ++u)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) acc[ci][u][v] = fmaf(xv[u].w, wv[v].w, acc[ci][u][v]);
-                }
+                    for (int v = 0; v < 4; ++v)
+                        acc[u][v] = __ffma2_rn(make_float2(xv[u].z, xv[u].w), make_float2(wv[v].z, wv[v].w), acc[u][v]);
             }
         }
         if (c == nchunks - 1) {
@@ -251,7 +253,7 @@ route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restri
 #pragma unroll
             for (int u = 0; u < TU; ++u)
 #pragma unroll
-                for (int v = 0; v < 4; ++v) p[u][v] = acc[0][u][v] + acc[1][u][v];
+                for (int v = 0; v < 4; ++v) p[u][v] = acc[u][v].x + acc[u][v].y;
             float* red = xf + (n & 1) * TT * kRouteRow;   // free until chunk n + 2 is converted into it
 #pragma unroll
             for (int d = 8; d >= 1; d >>= 1) {
