@@ -65,6 +65,38 @@ __device__ __forceinline__ bool abort_requested(const StatusBlock* st) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched by launch_after (below)
+// may become resident while the kernel before it on the stream is still
+// running. pdl_wait() blocks until that kernel has completed and its memory
+// writes are visible (a no-op for a plain launch), so everything before it
+// may touch only shared memory, tensor memory, barriers and kernel
+// parameters; pdl_allow_next() lets the next kernel on the stream start its
+// own launch. The next kernel's CTAs take an SM only once every CTA of this
+// grid has started, so a grid larger than one wave is never starved.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// kern<<<grid, block, smem, s>>>(args...) with the programmatic
+// stream-serialization attribute (the kernel must call pdl_wait() before it
+// reads or writes global memory that earlier work on the stream uses).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                         Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Numeric helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }

@@ -136,7 +136,7 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
     auto kern = grouped_gemm_kernel<BN, MX, MN, EPI, S, ACC, CLN>;
     ensure_smem_attr(reinterpret_cast<const void*>(kern), C::kSmemBytes);
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmemBytes;
     cfg.stream = s;
@@ -156,6 +156,13 @@ cudaError_t run(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
     }
     if (grid < 1) return cudaSuccess;
     cfg.gridDim = dim3(grid);
+    // the prologue (barriers, tensor memory, tensor-map prefetch) may overlap
+    // the end of the kernel before on the stream (the kernel waits before it
+    // reads anything that kernel writes)
+    attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs += 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, b, b2, sa, sb, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -315,7 +315,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     StatusBlock* st = p.status;
     const uint64_t tmo = p.timeout_ns;
 
-    build_sched<BN, MN_MAJOR, CLN>(p, sched);
     if (threadIdx.x == 32) {
         for (int s = 0; s < STAGES; ++s) {
             tc::mbar_init(full_bar(s), 1);
@@ -347,6 +346,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc::tmem_relinquish();
         }
     }
+    // everything above touches only shared and tensor memory: with a
+    // programmatic launch it overlaps the end of the kernel before
+    pdl_wait();
+    pdl_allow_next();
+    build_sched<BN, MN_MAJOR, CLN>(p, sched);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();

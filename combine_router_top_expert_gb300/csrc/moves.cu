@@ -158,6 +158,8 @@ dispatch_tokens_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int E,
                        const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets,
                        uint8_t* __restrict__ A, uint8_t* __restrict__ A_sf) {
     __shared__ int32_t poff[kMaxE + 1];
+    pdl_wait();
+    pdl_allow_next();
     padded_offsets(counts, E, poff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nb = H / 32, kc_row = H / 128;
@@ -246,6 +248,8 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
                 uint8_t* __restrict__ A_sf, const __nv_bfloat16* __restrict__ scale_src, const float* __restrict__ wslot,
                 int zero_pads) {
     __shared__ int32_t poff[kMaxE + 1];
+    pdl_wait();
+    pdl_allow_next();
     padded_offsets(counts, E, poff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = poff[E];
@@ -335,6 +339,8 @@ dispatch_kernel(const __nv_bfloat16* __restrict__ x, int H, int E, int k, const 
 __global__ void __launch_bounds__(128)
 combine_kernel(const __nv_bfloat16* __restrict__ partials, const float* __restrict__ w,
                const float* __restrict__ shared, __nv_bfloat16* __restrict__ out, int H, int k) {
+    pdl_wait();
+    pdl_allow_next();
     const int t = blockIdx.x;
     const int n = H / 8;
     for (int c = threadIdx.x; c < n; c += blockDim.x) {
@@ -624,15 +630,15 @@ cudaError_t launch_dispatch(bool mx, const void* x, int T, int H, int E, int k, 
     int64_t rows = padded_rows_max(T, E, k);
     int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)sm_count() * 8);
     if (blocks < 1) blocks = 1;
-    if (mx)
-        dispatch_kernel<true><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts, offsets,
-                                                     row_src, A, A_sf, nullptr, nullptr, zero_pads ? 1 : 0);
-    else
-        dispatch_kernel<false><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), H, E, k, counts,
-                                                      offsets, row_src, A, nullptr,
-                                                      static_cast<const __nv_bfloat16*>(scale_src), wslot,
-                                                      zero_pads ? 1 : 0);
-    return cudaGetLastError();
+    const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
+    const __nv_bfloat16* ss = static_cast<const __nv_bfloat16*>(scale_src);
+    const float* noslot = nullptr;
+    cudaError_t e =
+        mx ? launch_after(dispatch_kernel<true>, dim3(blocks), dim3(256), 0, s, xs, H, E, k, counts, offsets, row_src,
+                          A, A_sf, static_cast<const __nv_bfloat16*>(nullptr), noslot, zero_pads ? 1 : 0)
+           : launch_after(dispatch_kernel<false>, dim3(blocks), dim3(256), 0, s, xs, H, E, k, counts, offsets, row_src,
+                          A, static_cast<uint8_t*>(nullptr), ss, wslot, zero_pads ? 1 : 0);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, const int32_t* topk_idx,
@@ -644,9 +650,10 @@ cudaError_t launch_dispatch_tokens(const void* x, int T, int H, int E, int k, co
     // at most 27 of the ~32 warp slots an SM holds at this register count)
     const int W = (int64_t)T < (int64_t)sm_count() * 27 ? 2 : 1;
     const int blocks = (int)std::min<int64_t>(ceil_div((int64_t)T * W, 8), (int64_t)sm_count() * 8);
-    dispatch_tokens_kernel<<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), T, H, E, k, W, topk_idx,
-                                                  slot_row, counts, offsets, static_cast<uint8_t*>(A), A_sf);
-    return cudaGetLastError();
+    cudaError_t e = launch_after(dispatch_tokens_kernel, dim3(blocks), dim3(256), 0, s,
+                                 static_cast<const __nv_bfloat16*>(x), T, H, E, k, W, topk_idx, slot_row, counts,
+                                 offsets, static_cast<uint8_t*>(A), A_sf);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_zero_pad_rows_q(const int32_t* counts, int64_t rows, int E, int H, void* A, uint8_t* A_sf,
@@ -791,9 +798,10 @@ cudaError_t launch_quantize_rows(const void* x, int T, int H, void* x_q, void* x
 cudaError_t launch_combine(const void* partials, const float* w, const float* shared, void* out, int T, int H,
                            int k, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 128, 0, s>>>(static_cast<const __nv_bfloat16*>(partials), w, shared,
-                                     static_cast<__nv_bfloat16*>(out), H, k);
-    return cudaGetLastError();
+    cudaError_t e = launch_after(combine_kernel, dim3(T), dim3(128), 0, s,
+                                 static_cast<const __nv_bfloat16*>(partials), w, shared,
+                                 static_cast<__nv_bfloat16*>(out), H, k);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack(bool mx, const void* src0, const void* src1, int E, int K, int Nsrc, int il, void* dst,

@@ -157,6 +157,8 @@ route_topk_kernel(const __grid_constant__ CUtensorMap tmx, const float* __restri
         for (int s = 0; s < STAGES; ++s) tc::mbar_init(bar0 + 8u * s, 1);
         tc::fence_mbar_init();
     }
+    pdl_wait();   // the re-laid router weights are written by the kernel before
+    pdl_allow_next();
     __syncthreads();
 
     bool ok = true;
@@ -368,6 +370,8 @@ route_layout_kernel(const int32_t* __restrict__ topk_idx, const int32_t* __restr
     const int b = blockIdx.x;
     const int t0 = b * tt;
     const int ntok = min(tt, T - t0);
+    pdl_wait();
+    pdl_allow_next();
 
     // per-expert sums over blocks (before b, and over all): `per` threads
     // share one expert, then combine their partial sums
@@ -453,9 +457,9 @@ cudaError_t launch_topk_variant(const CUtensorMap& tmx, const float* Wr, int wr_
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     auto kern = route_topk_kernel<TT, STAGES>;
     if (smem > 48 * 1024) ensure_smem_attr(reinterpret_cast<const void*>(kern), (int)smem);
-    kern<<<ceil_div(T, TT), kTopkThreads, smem, s>>>(tmx, Wr, wr_copies, bias, T, H, E, k, topk_idx, topk_w, hist, st,
-                                                     timeout_ns, withhold);
-    return cudaGetLastError();
+    cudaError_t e = launch_after(kern, dim3(ceil_div(T, TT)), dim3(kTopkThreads), smem, s, tmx, Wr, wr_copies, bias, T,
+                                 H, E, k, topk_idx, topk_w, hist, st, timeout_ns, withhold);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Tokens per CTA: TT in {28, 20, 12, 8, 4}. One CTA per SM; a CTA's time is
@@ -532,9 +536,9 @@ cudaError_t launch_route_layout(const void* x, const float* W_r, const float* bi
                             hook.withhold, s);
     // the layout kernel must never run on top-k results that were not produced
     if (err != cudaSuccess) return err;
-    route_layout_kernel<<<nblocks, kRouteThreads, 0, s>>>(topk_idx, hist, T, E, k, tt, nblocks, counts, offsets,
-                                                          row_src, slot_row);
-    return cudaGetLastError();
+    err = launch_after(route_layout_kernel, dim3(nblocks), dim3(kRouteThreads), 0, s, topk_idx, hist, T, E, k, tt,
+                       nblocks, counts, offsets, row_src, slot_row);
+    return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace mok
