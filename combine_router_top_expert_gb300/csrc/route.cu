@@ -91,33 +91,39 @@ __device__ __forceinline__ bool ranks_before(float va, int ea, float vb, int eb)
     return va > vb || (va == vb && ea < eb);
 }
 
-
-// One CTA = TT tokens x all experts, 16 warps. Warp w owns summation chains
-// w and w + 16 (chain L: h = 256*i + 8*L + m), for every token and expert of
-// the CTA; each lane is one (token slot tl < 4, expert slot el < 8), and a
-// thread accumulates tokens tl + 4u (u < TT/4) x experts el + 8v (v < 4) of
-// the current 32-expert group on both of its warp's chains, as the two
-// halves of a float2 advanced by packed fp32x2 FMAs (h of chain w and
-// h + 128 of chain w + 16 sit side by side in shared memory; each half is
-// an ordinary fp32 FMA, so every chain keeps its order and its bits). Each
-// 16-byte shared load (two h of both chains) thus feeds 4 or TT/4 tokens'
-// worth of FMAs, and the lanes of a warp read only 4 (x) or 8 (weights)
-// distinct rows, 16 B each, four banks apart. A 128-bit shared load costs as many
-// wavefronts as the most distinct addresses among any four aligned lanes,
-// and at least two (measured on this GPU), so lane bits 0 and 1 select one
-// bit of tl and one of el: every quad reads two x and two weight rows, and
-// both loads take the minimum of two wavefronts. The chunks
-// (c, g) of the router weights (one bulk copy each, from the layout above)
-// and the matching [TT tokens x 256 h] box of raw x (one tensor copy; tokens
-// past T and h past H read 0) stream through a STAGES-deep shared-memory
-// ring, one mbarrier per slot; thread 0 issues the copies. x is converted
-// to fp32 (in the paired h order) once per CTA, one chunk ahead, into a
-// double buffer. After a group's last chunk the 32 chains of every (token, expert)
-// are added in the butterfly's tree: chain w + 16 into chain w in registers,
-// then warp w + d into warp w for d = 8, 4, 2, 1 through shared memory (the
-// fp32 x buffer just consumed). Every wait is bounded: after a timeout the
-// status block records it, no thread waits again, and the CTA runs to its
-// end (its results are then garbage; the caller sees MOK_ERR_TIMEOUT).
+// One CTA = TT tokens x all experts, 16 warps.
+//
+// Work split. Warp w owns summation chains w and w + 16 (chain L: h = 256*i
+// + 8*L + m) for every token and expert of the CTA. Each lane is one (token
+// slot tl < 4, expert slot el < 8) and accumulates tokens tl + 4u (u < TT/4)
+// x experts el + 8v (v < 4) of the current 32-expert group on both of its
+// warp's chains, as the two halves of a float2 advanced by packed fp32x2
+// FMAs: h of chain w and h + 128 of chain w + 16 sit side by side in shared
+// memory, and each half is an ordinary fp32 FMA, so every chain keeps its
+// order and its bits. One 16-byte load (two h of both chains) feeds 4 or
+// TT/4 tokens' FMAs.
+//
+// Shared-memory reads. The lanes of a warp read only 4 (x) or 8 (weights)
+// distinct rows, 16 B each, four banks apart. A 128-bit shared load costs as
+// many wavefronts as the most distinct addresses among any four aligned
+// lanes, and at least two (measured on this GPU), so lane bits 0 and 1 pick
+// one bit of tl and one of el: every quad reads two x and two weight rows
+// and both loads take the minimum of two wavefronts.
+//
+// Data flow. The chunks (c, g) of the router weights (one bulk copy each,
+// from the layout above) and the matching [TT tokens x 256 h] box of raw x
+// (one tensor copy; tokens past T and h past H read 0) stream through a
+// STAGES-deep ring, one mbarrier per slot; thread 0 issues the copies. x is
+// widened to fp32 (in the paired h order) once per CTA, one chunk ahead,
+// into a double buffer. After a group's last chunk the 32 chains of every
+// (token, expert) are added in the butterfly's tree: chain w + 16 into
+// chain w in registers, then warp w + d into warp w for d = 8, 4, 2, 1
+// through shared memory (the fp32 x buffer just consumed), then the bias.
+//
+// Every wait is bounded: after a timeout the status block records it, no
+// thread waits again, and the CTA runs to its end (its results are then
+// garbage; the caller sees MOK_ERR_TIMEOUT).
+//
 // Dynamic shared memory:
 //   bars [STAGES] u64 (128 B) | ws [STAGES][32][kRouteRow] f32 | xr [STAGES][TT][256] bf16 |
 //   xf [2][TT][kRouteRow] f32 | lg [TT][E] f32 | slog [TT][k] f32 | cnt [E] i32
