@@ -208,6 +208,53 @@ def test_stages_compose_to_forward():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
+def test_stages_behind_a_producer_kernel_on_the_stream(dtype):
+    """The library's kernels are launched with programmatic stream
+    serialization: each waits for the kernel before it on the stream before
+    touching memory. Here a torch kernel rewrites x on the stream right before
+    routing and the stages run, with no synchronisation in between, for
+    alternating inputs; every output must equal the one computed after a
+    full synchronisation."""
+    wl = synth.small("pdl", T=512, H=1024, I=256, E=8, k=2, dtype=dtype)
+    inp = synth.make_inputs(wl, seed=21)
+    mode = mok.MXFP8 if dtype == "mxfp8" else mok.BF16
+    layer = layer_for(inp, mode)
+    g = torch.Generator().manual_seed(3)
+    xs = [to_dev_bf16(synth._normal_bf16(g, (wl.T, wl.H), 1.0)) for _ in range(2)]
+    refs = []
+    for xv in xs:
+        refs.append(layer.forward(xv.clone()).clone())
+        torch.cuda.synchronize()
+    p = layer.problem(wl.T)
+    rt = layer.buffers(wl.T)["routing"]
+    rows = mok.padded_rows_max(wl.T, wl.E, wl.k)
+    eb = 1 if dtype == "mxfp8" else 2
+    A = mok.alloc_bytes(rows * wl.H * eb)
+    A_sf = mok.alloc_bytes(rows * wl.H // 32) if dtype == "mxfp8" else None
+    h = mok.alloc_bytes(rows * wl.I * eb)
+    h_sf = mok.alloc_bytes(rows * wl.I // 32) if dtype == "mxfp8" else None
+    part = torch.empty((wl.T * wl.k, wl.H), dtype=torch.bfloat16, device="cuda")
+    ws = mok.alloc_bytes(256)
+    x = torch.empty_like(xs[0])
+    outs = [torch.empty_like(refs[0]) for _ in range(20)]
+    for i in range(20):
+        x.copy_(xs[i % 2])                       # a torch kernel writes the input
+        layer.route(x)                            # ... and the routing reads it
+        if dtype == "mxfp8":
+            mok.dispatch_tokens(p, x, rt, A, A_sf)
+        else:
+            mok.dispatch(p, x, rt, A, None)
+        mok.expert_ffn(p, A, A_sf, layer.packed, rt, h, h_sf, part, ws)
+        mok.combine(p, part, rt["topk_w"], outs[i])
+        x.zero_()                                 # and is overwritten behind them
+    torch.cuda.synchronize()
+    assert mok.device_status(ws) == (mok.OK, 0)
+    for i in range(20):
+        assert torch.equal(outs[i].view(torch.int16), refs[i % 2].view(torch.int16)), i
+
+
+@pytest.mark.gpu
 def test_invalid_arguments_rejected_on_host():
     wl = synth.small("inv", T=16, H=256, I=128, E=4, k=2)
     inp = synth.make_inputs(wl)
