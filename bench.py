@@ -48,14 +48,20 @@ class ClockSampler:
     """nvidia-smi clock/throttle samples while the steps run; the SM clock is
     the median over samples taken under load (GPU utilisation >= 50%)."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.window = None   # host wall-clock (start, end) of the timed region
         self.path = os.path.join("/tmp", f"mok_clocks_{os.getpid()}.csv")
+
+    def mark(self, t_start, t_end):
+        """The timed region, as host wall-clock times taken right after the
+        synchronisations that bracket it."""
+        self.window = (t_start, t_end)
 
     def start(self):
         try:
@@ -83,12 +89,22 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 10:
-                rows.append(parts)
+        lines = open(self.path).read().splitlines()
         os.unlink(self.path)
+        return self.summarise(lines, self.window)
+
+    @staticmethod
+    def summarise(lines, window=None):
+        """Clock record from nvidia-smi CSV lines (the fields of Q). The
+        samples taken inside `window` (host wall-clock seconds) are the ones
+        summarised when there are any; else those at >= 50 % utilisation;
+        else all."""
+        import datetime
+        rows = []
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 11:
+                rows.append(parts)
         if not rows:
             return None
 
@@ -97,16 +113,26 @@ class ClockSampler:
                 return float(v)
             except ValueError:
                 return None
-        loaded = [r for r in rows if (num(r[4]) or 0.0) >= 50.0]
-        use = loaded or rows
-        sm = [num(r[1]) for r in use if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        pw = [num(r[3]) for r in use if num(r[3]) is not None]
+
+        def stamp(v):
+            try:
+                return datetime.datetime.strptime(v, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        timed = []
+        if window is not None:
+            timed = [r for r in rows if stamp(r[0]) is not None and window[0] <= stamp(r[0]) <= window[1]]
+        loaded = [r for r in rows if (num(r[5]) or 0.0) >= 50.0]
+        use = timed or loaded or rows
+        sm = [num(r[2]) for r in use if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        pw = [num(r[4]) for r in use if num(r[4]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in use for n, v in zip(names, r[6:10]) if v.lower().startswith("active")})
+        reasons = sorted({n for r in use for n, v in zip(names, r[7:11]) if v.lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "power_w_median": statistics.median(pw) if pw else None, "reasons": reasons,
-                "samples": len(rows), "samples_under_load": len(loaded)}
+                "samples": len(rows), "samples_under_load": len(loaded), "samples_in_timed_region": len(timed),
+                "summarised": "timed region" if timed else "under load" if loaded else "all samples"}
 
 
 def dist_env():
@@ -438,6 +464,7 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    t_timed0 = time.time()
     for i in range(steps):
         flush.zero_()
         s0, s1, g0, g1, x0 = evs[i]
@@ -445,6 +472,7 @@ def measure(args, wl, inp, layer, dev, steps, warmup, trace=False, with_e2e=True
         step((g0, g1, x0))
         s1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark(t_timed0, time.time())
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()

@@ -1,8 +1,8 @@
 """Host logic of the benchmark (CPU): the captured-traffic figure is reported
-only for the GEMM sources it was captured on, and the roofline object's
+only for the GEMM sources it was captured on, the roofline object's
 arithmetic (achieved = FLOP / time, the burst peak for short timed regions
 and the sustained one for long ones, twice the BF16 peak for MXFP8, the HBM
-bound when weights dominate)."""
+bound when weights dominate), and the clock record's choice of samples."""
 import types
 
 import pytest
@@ -57,3 +57,28 @@ def test_roofline_mxfp8_peak_and_hbm_bound(monkeypatch):
     r3 = bench.roofline(_m(small, mok.MXFP8, [0.3], 100.0), _args())
     assert r3["bound"] == "hbm" and r3["unit"] == "GB/s"
     assert r3["frac"] == pytest.approx(r3["bytes_per_step"] / 0.3e-3 / 1e9 / 6000.0)
+
+
+def test_clock_record_summarises_the_timed_region():
+    """Samples stamped inside the timed region decide the clock record; the
+    utilisation filter and then all samples are the fallbacks."""
+    import datetime
+    import bench
+
+    def line(t, mhz, util, power_cap):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        cap = "Active" if power_cap else "Not Active"
+        return (f"{ts}, 0, {mhz}, 2070, 500.0, {util}, 0x0, Not Active, Not Active, Not Active, {cap}")
+    t0 = 1_800_000_000.0
+    lines = [line(t0 + 0.00, 2070, 0, False),     # warm-up, before the window
+             line(t0 + 0.10, 1700, 10, True),     # inside the window (utilisation still lagging)
+             line(t0 + 0.12, 1650, 20, True),
+             line(t0 + 0.30, 2070, 90, False)]    # after it
+    r = bench.ClockSampler.summarise(lines, (t0 + 0.05, t0 + 0.20))
+    assert r["samples"] == 4 and r["samples_in_timed_region"] == 2 and r["summarised"] == "timed region"
+    assert r["sm_mhz"] == 1675.0 and r["sm_max_mhz"] == 2070.0 and r["reasons"] == ["sw_power_cap"]
+    r = bench.ClockSampler.summarise(lines, (t0 + 0.50, t0 + 0.60))   # no sample inside
+    assert r["summarised"] == "under load" and r["sm_mhz"] == 2070.0 and r["reasons"] == []
+    r = bench.ClockSampler.summarise(lines[:3])
+    assert r["summarised"] == "all samples" and r["samples_in_timed_region"] == 0
+    assert bench.ClockSampler.summarise([]) is None
